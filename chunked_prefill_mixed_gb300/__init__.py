@@ -1,0 +1,203 @@
+"""Python binding of libsarathi (ctypes): the mixed-batch paged-attention step
+of chunked prefill with stall-free batching on one sm_103a GPU.
+
+Argument marshalling only: every step of the path runs in the C/CUDA library
+(``csrc/``), whose ABI is ``include/sarathi.h``.  The function names match the
+C entry points.  If the shared library is missing this module raises: there is
+no fallback.  PyTorch supplies device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+OK, ERR_INVALID_ARG, ERR_CAPACITY, WARN_OVER_BUDGET_DECODES = 0, 1, 2, 3
+ERR_CUDA, ERR_UNSUPPORTED, ERR_DEVICE_CHECK = 4, 5, 6
+DECODE, PREFILL_RUNNING, PREFILL_WAITING = 0, 1, 2
+
+EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_rope_table", "sarathi_mixed_attn",
+            "sarathi_workspace_status", "sarathi_last_error", "sarathi_abi_version")
+
+
+class SarathiError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        super().__init__(f"{where}: status {status}: {msg}")
+        self.status = status
+
+
+class Request(ctypes.Structure):
+    _fields_ = [("state", ctypes.c_int32), ("prompt_len", ctypes.c_int32), ("num_computed", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("pages", ctypes.POINTER(ctypes.c_int32))]
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("n_sched", "num_decodes", "num_tokens", "nnz_pages", "n_items",
+                                             "n_partials", "n_merge", "max_kv_len")] + \
+               [("pairs", ctypes.c_int64), ("history_tokens", ctypes.c_int64)] + \
+               [(n, ctypes.c_int32) for n in ("off_req_index", "off_num_new", "off_last_chunk", "off_qo_indptr",
+                                             "off_kv_page_indptr", "off_kv_page_indices", "off_kv_last_page_len",
+                                             "off_req_aux", "off_items", "packed_ints")] + \
+               [("workspace_bytes", ctypes.c_int64)]
+
+
+class AttnArgs(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("plan", ctypes.c_void_p), ("info", ctypes.POINTER(PlanInfo)),
+                ("rope_table", ctypes.c_void_p), ("rope_max_pos", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64),
+                ("shape", Shape), ("sm_scale", ctypes.c_float)]
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libsarathi.so (building it with nvcc first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and _build.stale():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise ImportError(f"libsarathi.so not built at {_build.LIB}")
+    lib = ctypes.CDLL(_build.LIB)
+    lib.sarathi_plan_bounds.restype = ctypes.c_int32
+    lib.sarathi_plan_bounds.argtypes = [ctypes.POINTER(Request), ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.POINTER(Shape), ctypes.c_int32,
+                                        ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]
+    lib.sarathi_plan.restype = ctypes.c_int32
+    lib.sarathi_plan.argtypes = [ctypes.POINTER(Request), ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Shape),
+                                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(PlanInfo)]
+    lib.sarathi_rope_table.restype = ctypes.c_int32
+    lib.sarathi_rope_table.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                       ctypes.c_void_p]
+    lib.sarathi_mixed_attn.restype = ctypes.c_int32
+    lib.sarathi_mixed_attn.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p]
+    lib.sarathi_workspace_status.restype = ctypes.c_int32
+    lib.sarathi_workspace_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+    lib.sarathi_last_error.restype = ctypes.c_char_p
+    lib.sarathi_last_error.argtypes = []
+    lib.sarathi_abi_version.restype = ctypes.c_int32
+    lib.sarathi_abi_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def sarathi_last_error() -> str:
+    return load().sarathi_last_error().decode()
+
+
+def sarathi_abi_version() -> int:
+    return int(load().sarathi_abi_version())
+
+
+def _check(st: int, where: str, allow=(OK,)):
+    if st not in allow:
+        raise SarathiError(st, where, sarathi_last_error())
+    return st
+
+
+def make_requests(states, prompt_len, num_computed, block_tables):
+    """ctypes request array plus the int32 block tables it points into (keep both alive)."""
+    n = len(states)
+    arr = (Request * max(n, 1))()
+    keep = []
+    for i in range(n):
+        t = np.ascontiguousarray(np.asarray(block_tables[i], dtype=np.int32))
+        keep.append(t)
+        arr[i].state = int(states[i])
+        arr[i].prompt_len = int(prompt_len[i])
+        arr[i].num_computed = int(num_computed[i])
+        arr[i].num_pages = int(t.size)
+        arr[i].pages = t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    return arr, keep
+
+
+def sarathi_plan_bounds(reqs, n_reqs: int, token_budget: int, shape: Shape, num_sms: int):
+    hb, wb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(load().sarathi_plan_bounds(reqs, n_reqs, token_budget, ctypes.byref(shape), num_sms,
+                                      ctypes.byref(hb), ctypes.byref(wb)), "sarathi_plan_bounds")
+    return int(hb.value), int(wb.value)
+
+
+def sarathi_plan(reqs, n_reqs: int, token_budget: int, shape: Shape, num_sms: int,
+                 host_buf: np.ndarray | None = None):
+    """Returns (status, PlanInfo, packed int32 array).  Raises on errors; the
+    over-budget-decodes warning is returned as a status."""
+    if host_buf is None:
+        hb, _ = sarathi_plan_bounds(reqs, n_reqs, token_budget, shape, num_sms)
+        host_buf = np.zeros(hb // 4 + 4, dtype=np.int32)
+    info = PlanInfo()
+    st = load().sarathi_plan(reqs, n_reqs, token_budget, ctypes.byref(shape), num_sms,
+                             host_buf.ctypes.data, host_buf.nbytes, ctypes.byref(info))
+    _check(st, "sarathi_plan", allow=(OK, WARN_OVER_BUDGET_DECODES))
+    return st, info, host_buf[:info.packed_ints]
+
+
+def plan_arrays(info: PlanInfo, packed: np.ndarray) -> dict:
+    """Views of the packed plan buffer by name."""
+    n = info.n_sched
+
+    def view(off, count):
+        return packed[off:off + count]
+    return dict(
+        n_sched=n, num_decodes=info.num_decodes, num_tokens=info.num_tokens, nnz_pages=info.nnz_pages,
+        req_index=view(info.off_req_index, n), num_new=view(info.off_num_new, n),
+        last_chunk=view(info.off_last_chunk, n), qo_indptr=view(info.off_qo_indptr, n + 1),
+        kv_page_indptr=view(info.off_kv_page_indptr, n + 1),
+        kv_page_indices=view(info.off_kv_page_indices, info.nnz_pages),
+        kv_last_page_len=view(info.off_kv_last_page_len, n), req_aux=view(info.off_req_aux, n),
+        items=view(info.off_items, info.n_items * 8).reshape(info.n_items, 8),
+    )
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        return 0
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def sarathi_rope_table(table, max_pos: int, head_dim: int, rope_theta: float, stream=None) -> None:
+    """Fill ``table`` (torch float64 CUDA tensor of max_pos*head_dim elements)."""
+    _check(load().sarathi_rope_table(table.data_ptr(), max_pos, head_dim, rope_theta, _stream_ptr(stream)),
+           "sarathi_rope_table")
+
+
+def sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo, rope_table, rope_max_pos: int,
+                       workspace, shape: Shape, sm_scale: float, stream=None) -> None:
+    """Enqueue one step (one kernel) on ``stream`` (torch.cuda.Stream or raw handle)."""
+    a = AttnArgs()
+    a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    a.k_cache, a.v_cache, a.out = k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr()
+    a.plan = plan_dev.data_ptr()
+    a.info = ctypes.pointer(info)
+    a.rope_table = rope_table.data_ptr()
+    a.rope_max_pos = int(rope_max_pos)
+    a.num_pages = int(k_cache.shape[0])
+    a.workspace = workspace.data_ptr()
+    a.workspace_bytes = int(workspace.numel() * workspace.element_size())
+    a.shape = shape
+    a.sm_scale = float(sm_scale)
+    _check(load().sarathi_mixed_attn(ctypes.byref(a), _stream_ptr(stream)), "sarathi_mixed_attn")
+
+
+def sarathi_workspace_status(workspace, stream=None) -> int:
+    """Synchronise, read and clear the kernel's error word; returns it (0 = fine)."""
+    err = ctypes.c_int32(0)
+    st = load().sarathi_workspace_status(workspace.data_ptr(), _stream_ptr(stream), ctypes.byref(err))
+    if st not in (OK, ERR_DEVICE_CHECK):
+        _check(st, "sarathi_workspace_status")
+    return int(err.value)

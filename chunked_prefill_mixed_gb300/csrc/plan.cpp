@@ -1,0 +1,293 @@
+// plan.cpp -- host planner of libsarathi: the stall-free budgeted batch, its
+// ragged-batch metadata and the step kernel's work list.
+//
+// Budget order follows "Chunked Prefill 与 PD 分离" §3.1 (running decodes, then
+// unfinished prefill chunks, then new requests) and the per-request chunk of
+// "分块预填充与 Stall-free 调度" §六·补二 (min of the budget left and the prompt
+// left).  Several prefills may share one budget, "Sarathi-Serve 完全拆解"
+// §"一个 512-token 预算的例子".  Metadata arrays as named in "Sarathi-Serve 完全拆解"
+// §"混合批不是把两类注意力强行做成同一个形状".
+#include <algorithm>
+#include <array>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "sarathi.h"
+#include "sarathi_internal.h"
+
+namespace sarathi {
+
+static thread_local std::string g_last_error = "";
+
+void set_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
+int32_t fail(int32_t code, const char* msg) {
+    set_error(msg);
+    return code;
+}
+
+int32_t check_shape(const sarathi_shape* sh) {
+    if (!sh) return fail(SARATHI_ERR_INVALID_ARG, "shape is NULL");
+    if (sh->num_heads_q <= 0 || sh->num_heads_kv <= 0 || sh->head_dim <= 0 || sh->page_size <= 0)
+        return fail(SARATHI_ERR_INVALID_ARG, "shape fields must be positive");
+    if (sh->num_heads_q % sh->num_heads_kv != 0)
+        return fail(SARATHI_ERR_INVALID_ARG, "num_heads_q must be a multiple of num_heads_kv");
+    if (sh->page_size != kPage) return fail(SARATHI_ERR_UNSUPPORTED, "page_size must be 16");
+    if (sh->head_dim != 64 && sh->head_dim != 128)
+        return fail(SARATHI_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (sh->num_heads_q / sh->num_heads_kv > kMaxGroup)
+        return fail(SARATHI_ERR_UNSUPPORTED, "q heads per kv head must be <= 16");
+    return SARATHI_OK;
+}
+
+namespace {
+
+struct Sched {
+    int32_t req;
+    int32_t n;
+};
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int32_t validate_requests(const sarathi_request* reqs, int32_t n_reqs) {
+    if (n_reqs < 0) return fail(SARATHI_ERR_INVALID_ARG, "n_reqs < 0");
+    if (n_reqs > 0 && !reqs) return fail(SARATHI_ERR_INVALID_ARG, "reqs is NULL");
+    for (int32_t i = 0; i < n_reqs; ++i) {
+        const sarathi_request& r = reqs[i];
+        if (r.state < SARATHI_DECODE || r.state > SARATHI_PREFILL_WAITING)
+            return fail(SARATHI_ERR_INVALID_ARG, "request state out of range");
+        if (r.num_computed < 0) return fail(SARATHI_ERR_INVALID_ARG, "num_computed < 0");
+        if (r.state != SARATHI_DECODE && r.prompt_len < r.num_computed)
+            return fail(SARATHI_ERR_INVALID_ARG, "prefill with num_computed > prompt_len");
+        if (r.num_pages < 0 || (r.num_pages > 0 && !r.pages))
+            return fail(SARATHI_ERR_INVALID_ARG, "bad block table");
+    }
+    return SARATHI_OK;
+}
+
+// Rough per-SM speeds used only to order the work list (longest first).
+constexpr double kPrefillFlopPerNs = 3000.0;  // mma tile throughput per SM
+constexpr double kDecodeBytesPerNs = 40.0;    // HBM share per SM
+
+}  // namespace
+}  // namespace sarathi
+
+using namespace sarathi;
+
+extern "C" const char* sarathi_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int32_t sarathi_abi_version(void) { return SARATHI_ABI_VERSION; }
+
+extern "C" int32_t sarathi_plan_bounds(const sarathi_request* reqs, int32_t n_reqs, int32_t token_budget,
+                                       const sarathi_shape* shape, int32_t num_sms,
+                                       size_t* host_buf_bytes, size_t* device_workspace_bytes) {
+    int32_t st = check_shape(shape);
+    if (st) return st;
+    st = validate_requests(reqs, n_reqs);
+    if (st) return st;
+    if (token_budget <= 0) return fail(SARATHI_ERR_INVALID_ARG, "token_budget must be positive");
+    (void)num_sms;
+    const int64_t Hkv = shape->num_heads_kv;
+    const int group = shape->num_heads_q / shape->num_heads_kv;
+    int64_t n_dec = 0, pages = 0;
+    for (int32_t i = 0; i < n_reqs; ++i) {
+        n_dec += reqs[i].state == SARATHI_DECODE;
+        pages += reqs[i].num_pages;
+    }
+    const int64_t n = n_reqs;
+    const int64_t T = n_dec + token_budget;
+    const int64_t appends = T / kAppendTokens + n;
+    const int64_t tiles = (T / tokens_per_tile(group) + n) * Hkv;
+    const int64_t dec_items = (pages / kDecodeMinSplitPages + n) * Hkv;
+    const int64_t items = appends + tiles + dec_items;
+    const int64_t ints = 6 * n + 2 + pages + 8 + items * kItemInts;
+    if (host_buf_bytes) *host_buf_bytes = (size_t)ints * 4;
+    if (device_workspace_bytes) {
+        const int64_t n_merge = n * Hkv;
+        *device_workspace_bytes = (size_t)(partial_offset_bytes((int)n, (int)n_merge) +
+                                           dec_items * partial_slot_floats(group, shape->head_dim) * 4);
+    }
+    return SARATHI_OK;
+}
+
+extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int32_t token_budget,
+                                const sarathi_shape* shape, int32_t num_sms,
+                                int32_t* host_buf, size_t host_buf_bytes, sarathi_plan_info* info) {
+    if (!info) return fail(SARATHI_ERR_INVALID_ARG, "info is NULL");
+    std::memset(info, 0, sizeof *info);
+    int32_t st = check_shape(shape);
+    if (st) return st;
+    st = validate_requests(reqs, n_reqs);
+    if (st) return st;
+    if (token_budget <= 0) return fail(SARATHI_ERR_INVALID_ARG, "token_budget must be positive");
+    if (num_sms <= 0) return fail(SARATHI_ERR_INVALID_ARG, "num_sms must be positive");
+
+    const int Hkv = shape->num_heads_kv;
+    const int group = shape->num_heads_q / Hkv;
+    const int d = shape->head_dim;
+
+    // ---- 1. the budgeted batch: decodes, running prefills, waiting prefills
+    std::vector<Sched> sched;
+    sched.reserve(n_reqs);
+    int64_t left = token_budget;
+    int32_t decodes = 0;
+    for (int32_t i = 0; i < n_reqs; ++i)
+        if (reqs[i].state == SARATHI_DECODE) {
+            sched.push_back({i, 1});
+            ++decodes;
+            --left;
+        }
+    for (int cls = SARATHI_PREFILL_RUNNING; cls <= SARATHI_PREFILL_WAITING; ++cls)
+        for (int32_t i = 0; i < n_reqs; ++i) {
+            if (reqs[i].state != cls) continue;
+            int64_t rem = (int64_t)reqs[i].prompt_len - reqs[i].num_computed;
+            int64_t take = std::min<int64_t>(rem, std::max<int64_t>(left, 0));
+            if (take <= 0) continue;
+            sched.push_back({i, (int32_t)take});
+            left -= take;
+        }
+    const int32_t ns = (int32_t)sched.size();
+
+    // ---- 2. per-row KV extent, checked against the block tables
+    std::vector<int32_t> np(ns), hist(ns);
+    int64_t nnz = 0, T = 0, pairs = 0, history = 0;
+    int32_t max_kv = 0;
+    for (int32_t s = 0; s < ns; ++s) {
+        const sarathi_request& r = reqs[sched[s].req];
+        int64_t kv_len = (int64_t)r.num_computed + sched[s].n;
+        int64_t p = ceil_div(kv_len, kPage);
+        if (p > r.num_pages) {
+            char msg[160];
+            std::snprintf(msg, sizeof msg, "request %d needs %lld pages, block table has %d", sched[s].req,
+                          (long long)p, r.num_pages);
+            return fail(SARATHI_ERR_CAPACITY, msg);
+        }
+        np[s] = (int32_t)p;
+        hist[s] = r.num_computed;
+        nnz += p;
+        T += sched[s].n;
+        const int64_t n = sched[s].n, h = r.num_computed;
+        pairs += n * h + n * (n + 1) / 2;
+        history += h;
+        max_kv = std::max<int32_t>(max_kv, (int32_t)kv_len);
+    }
+
+    // ---- 3. work list
+    std::vector<int32_t> aux(ns, 0);
+    std::vector<std::array<int32_t, kItemInts>> appends;
+    struct Timed {
+        double ns_est;
+        std::array<int32_t, kItemInts> it;
+    };
+    std::vector<Timed> attn;
+    const int tpt = tokens_per_tile(group);
+    // decode split size from the total decode pages and the SM count
+    int64_t dec_page_heads = 0;
+    for (int32_t s = 0; s < ns; ++s)
+        if (sched[s].n == 1) dec_page_heads += (int64_t)np[s] * Hkv;
+    const int64_t target = (int64_t)num_sms * kDecodeItemsPerSm;
+    const int64_t split =
+        std::max<int64_t>(kDecodeMinSplitPages, ceil_div(std::max<int64_t>(dec_page_heads, 1), target));
+    int32_t n_partials = 0, n_merge = 0;
+    const double kv_page_bytes = 2.0 * kPage * d * 2;
+    for (int32_t s = 0; s < ns; ++s) {
+        const int32_t n = sched[s].n;
+        const int32_t h = hist[s];
+        if (n >= 2) {
+            // prefill-like: append items first, then one tile per (kv head, token block)
+            int32_t cnt = 0;
+            for (int32_t t0 = 0; t0 < n; t0 += kAppendTokens) {
+                appends.push_back({kAppend, s, 0, t0, std::min(kAppendTokens, n - t0), -1, -1, 0});
+                ++cnt;
+            }
+            aux[s] = cnt;
+            for (int g = 0; g < Hkv; ++g)
+                for (int32_t t0 = 0; t0 < n; t0 += tpt) {
+                    int32_t c = std::min(tpt, n - t0);
+                    double keys = (double)h + t0 + c;
+                    double flops = 4.0 * d * kTileRows * keys;
+                    attn.push_back({flops / kPrefillFlopPerNs, {kPrefill, s, g, t0, c, -1, -1, 0}});
+                }
+        } else {
+            // decode-like: split the pages; the item holding the last page also
+            // appends the new token's K/V for its head.
+            // (nsplit-1)*per < np always holds, so no split is empty.
+            const int64_t nsplit = ceil_div(np[s], split);
+            const int64_t per = ceil_div(np[s], nsplit);
+            for (int g = 0; g < Hkv; ++g) {
+                int32_t merge = nsplit > 1 ? n_merge++ : -1;
+                int32_t first = nsplit > 1 ? n_partials : -1;
+                if (nsplit > 1) n_partials += (int32_t)nsplit;
+                for (int64_t k = 0; k < nsplit; ++k) {
+                    int32_t p0 = (int32_t)(k * per);
+                    int32_t pc = (int32_t)std::min<int64_t>(per, np[s] - p0);
+                    attn.push_back({pc * kv_page_bytes / kDecodeBytesPerNs,
+                                    {kDecode, s, g, p0, pc, first, merge, (int32_t)nsplit}});
+                }
+            }
+        }
+    }
+    std::stable_sort(attn.begin(), attn.end(), [](const Timed& a, const Timed& b) { return a.ns_est > b.ns_est; });
+    const int64_t n_items = (int64_t)appends.size() + (int64_t)attn.size();
+
+    // ---- 4. packed layout
+    int64_t off = 0;
+    auto take = [&](int64_t count) {
+        int64_t o = off;
+        off += count;
+        return (int32_t)o;
+    };
+    info->off_req_index = take(ns);
+    info->off_num_new = take(ns);
+    info->off_last_chunk = take(ns);
+    info->off_qo_indptr = take(ns + 1);
+    info->off_kv_page_indptr = take(ns + 1);
+    info->off_kv_page_indices = take(nnz);
+    info->off_kv_last_page_len = take(ns);
+    info->off_req_aux = take(ns);
+    off = (off + 3) / 4 * 4;  // items start on a 16-byte boundary
+    info->off_items = take(n_items * kItemInts);
+    info->packed_ints = (int32_t)off;
+    info->n_sched = ns;
+    info->num_decodes = decodes;
+    info->num_tokens = (int32_t)T;
+    info->nnz_pages = (int32_t)nnz;
+    info->n_items = (int32_t)n_items;
+    info->n_partials = n_partials;
+    info->n_merge = n_merge;
+    info->max_kv_len = max_kv;
+    info->pairs = pairs;
+    info->history_tokens = history;
+    info->workspace_bytes =
+        partial_offset_bytes(ns, n_merge) + (int64_t)n_partials * partial_slot_floats(group, d) * 4;
+    if (!host_buf || host_buf_bytes < (size_t)off * 4)
+        return fail(SARATHI_ERR_CAPACITY, "host_buf too small (info->packed_ints holds the size needed)");
+
+    int32_t* b = host_buf;
+    std::memset(b, 0, (size_t)off * 4);
+    int32_t* qo = b + info->off_qo_indptr;
+    int32_t* kvp = b + info->off_kv_page_indptr;
+    int32_t* kvi = b + info->off_kv_page_indices;
+    qo[0] = 0;
+    kvp[0] = 0;
+    for (int32_t s = 0; s < ns; ++s) {
+        const sarathi_request& r = reqs[sched[s].req];
+        const int32_t n = sched[s].n;
+        b[info->off_req_index + s] = sched[s].req;
+        b[info->off_num_new + s] = n;
+        b[info->off_last_chunk + s] = (r.state == SARATHI_DECODE || r.num_computed + n == r.prompt_len) ? 1 : 0;
+        qo[s + 1] = qo[s] + n;
+        std::memcpy(kvi + kvp[s], r.pages, (size_t)np[s] * 4);
+        kvp[s + 1] = kvp[s] + np[s];
+        b[info->off_kv_last_page_len + s] = r.num_computed + n - kPage * (np[s] - 1);
+        b[info->off_req_aux + s] = aux[s];
+    }
+    int32_t* items = b + info->off_items;
+    int64_t w = 0;
+    for (auto& it : appends) std::memcpy(items + kItemInts * w++, it.data(), sizeof(int32_t) * kItemInts);
+    for (auto& t : attn) std::memcpy(items + kItemInts * w++, t.it.data(), sizeof(int32_t) * kItemInts);
+    set_error("");
+    return decodes > token_budget ? SARATHI_WARN_OVER_BUDGET_DECODES : SARATHI_OK;
+}

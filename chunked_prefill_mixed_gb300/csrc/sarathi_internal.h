@@ -1,0 +1,58 @@
+// sarathi_internal.h -- layout contract between the host planner (plan.cpp)
+// and the step kernel (mixed_attn.cu).  Not part of the public ABI.
+#pragma once
+#include <stdint.h>
+
+struct sarathi_shape;
+
+namespace sarathi {
+
+// Error helpers shared by the planner and the launcher (thread-local message).
+void set_error(const char* msg);
+int32_t fail(int32_t code, const char* msg);
+int32_t check_shape(const sarathi_shape* shape);
+
+constexpr int kPage = 16;             // tokens per KV page (the only size built)
+constexpr int kAppendTokens = 16;     // new tokens per APPEND work item
+constexpr int kTileRows = 128;        // query rows (token x head-in-group) per prefill tile
+constexpr int kMaxGroup = 16;         // q heads per kv head handled by the decode path
+constexpr int kDecodeMinSplitPages = 8;
+constexpr int kDecodeItemsPerSm = 6;  // target split-KV items per SM for the decode phase
+constexpr int kItemInts = 8;
+
+enum ItemKind : int32_t { kAppend = 0, kPrefill = 1, kDecode = 2 };
+
+// Work item, kItemInts int32:
+//   [0] kind
+//   [1] s        scheduled row (request) index
+//   [2] g        kv head (prefill / decode)
+//   [3] start    append: first token (request-local); prefill: first token of the
+//                tile (request-local); decode: first page (request-local)
+//   [4] count    tokens (append / prefill) or pages (decode)
+//   [5] slot     decode: first partial slot of its merge group (the group's
+//                splits own consecutive slots; split k = start / ceil(pages /
+//                nsplit) owns slot + k); -1 when the item is the only split
+//   [6] merge    decode: merge group, -1 when the item is the only split
+//   [7] nsplit   decode: splits in the merge group
+enum ItemField { kKind = 0, kS, kG, kStart, kCount, kSlot, kMerge, kNSplit };
+
+// Workspace: an int32 header, then fp32 partial slots from byte kPartialOffset.
+//   [0] work-queue head   [1] CTAs exited   [2] error word   [3] error detail
+//   [kHdrInts + s]             append items finished for row s
+//   [kHdrInts + n_sched + m]   arrivals in merge group m
+constexpr int kHdrInts = 16;
+constexpr int kErrWait = 1;     // a bounded wait ran out
+constexpr int kErrBounds = 2;   // a bounds check failed
+
+inline int64_t sync_ints(int n_sched, int n_merge) { return kHdrInts + (int64_t)n_sched + n_merge; }
+inline int64_t partial_offset_bytes(int n_sched, int n_merge) {
+    int64_t b = sync_ints(n_sched, n_merge) * 4;
+    return (b + 255) / 256 * 256;
+}
+// One decode split writes, for each q head of its group, o[d] (normalised by
+// its own sum), then m and l (running max and sum, base-2 logits).
+inline int64_t partial_slot_floats(int group, int d) { return (int64_t)group * (d + 2); }
+
+inline int tokens_per_tile(int group) { return group >= kTileRows ? 1 : kTileRows / group; }
+
+}  // namespace sarathi

@@ -1,0 +1,55 @@
+"""A small host-side driver around the C ABI: owns the RoPE table and the
+workspace on one device, plans a step, copies the packed plan to the device
+and enqueues the step kernel.  PyTorch is used for device memory and streams
+only; all computation runs in libsarathi."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import (PlanInfo, Shape, make_requests, sarathi_mixed_attn, sarathi_plan, sarathi_rope_table,
+               sarathi_workspace_status)
+
+
+class StepRunner:
+    def __init__(self, H_q: int, H_kv: int, d: int, max_pos: int, device="cuda", rope_theta: float = 10000.0,
+                 page_size: int = 16, stream=None):
+        self.shape = Shape(H_q, H_kv, d, page_size)
+        self.device = torch.device(device)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
+        self.sm_scale = 1.0 / math.sqrt(d)
+        self.max_pos = int(max_pos)
+        self.rope = torch.empty(self.max_pos * d, dtype=torch.float64, device=self.device)
+        sarathi_rope_table(self.rope, self.max_pos, d, rope_theta, self.stream)
+        self.workspace = torch.zeros(1 << 16, dtype=torch.uint8, device=self.device)
+
+    def plan(self, states, prompt_len, num_computed, block_tables, budget: int):
+        reqs, keep = make_requests(states, prompt_len, num_computed, block_tables)
+        return sarathi_plan(reqs, len(states), budget, self.shape, self.num_sms)
+
+    def ensure_workspace(self, nbytes: int):
+        if self.workspace.numel() < nbytes:
+            torch.cuda.current_stream(self.device).wait_stream(self.stream)
+            self.workspace = torch.zeros(max(nbytes, 2 * self.workspace.numel()), dtype=torch.uint8,
+                                         device=self.device)
+            self.stream.wait_stream(torch.cuda.current_stream(self.device))
+
+    def upload(self, packed: np.ndarray) -> torch.Tensor:
+        src = torch.from_numpy(np.ascontiguousarray(packed))
+        dev = torch.empty(src.numel() + 4, dtype=torch.int32, device=self.device)
+        dev[:src.numel()].copy_(src)
+        self.stream.wait_stream(torch.cuda.current_stream(self.device))
+        return dev
+
+    def run(self, q, k, v, k_cache, v_cache, out, plan_dev: torch.Tensor, info: PlanInfo) -> None:
+        self.ensure_workspace(int(info.workspace_bytes))
+        if info.max_kv_len > self.max_pos:
+            raise ValueError(f"RoPE table covers {self.max_pos} positions, batch needs {info.max_kv_len}")
+        sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info, self.rope, self.max_pos,
+                           self.workspace, self.shape, self.sm_scale, self.stream)
+
+    def status(self) -> int:
+        return sarathi_workspace_status(self.workspace, self.stream)

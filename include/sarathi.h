@@ -1,0 +1,189 @@
+/*
+ * sarathi.h -- C ABI of libsarathi: the mixed-batch paged-attention step of
+ * chunked prefill with stall-free batching, on one sm_103a GPU.
+ *
+ * Two calls make the step:
+ *   sarathi_plan        (host only) fills a per-iteration token budget --
+ *                       decodes first, then in-progress prefill chunks, then new
+ *                       prefills -- and emits the ragged-batch metadata
+ *                       qo_indptr / kv_page_indptr / kv_page_indices /
+ *                       kv_last_page_len plus the kernel's work list, packed in
+ *                       one int32 buffer for a single host-to-device copy.
+ *   sarathi_mixed_attn  enqueues ONE kernel on the caller's stream: RoPE at
+ *                       absolute positions and K/V append into pages, causal
+ *                       attention of every prefill chunk over history pages plus
+ *                       the chunk, split-KV decode attention and its
+ *                       log-sum-exp merge.
+ *
+ * Conventions for every function here:
+ *   - returns an int32 sarathi_status; 0 is success; nothing throws;
+ *   - sarathi_last_error() gives a thread-local message for the last failure;
+ *   - the caller owns every buffer (host and device); the library keeps no
+ *     device allocation across calls;
+ *   - "device pointer" means CUDA global memory of the current device.
+ *
+ * Sources (pages, by title):
+ *   [SS] "Sarathi-Serve 完全拆解：分块 Prefill 与无停顿批处理如何兼顾吞吐和尾延迟"
+ *   [CP] "Chunked Prefill 与 PD 分离：切片混批，还是拆开两个池"
+ *   [ST] "分块预填充与 Stall-free 调度：把 LLM 推理的吞吐-延迟权衡算清楚"
+ */
+#ifndef SARATHI_H_
+#define SARATHI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SARATHI_ABI_VERSION 1
+
+/* Status codes. */
+#define SARATHI_OK 0
+#define SARATHI_ERR_INVALID_ARG 1          /* bad pointer, size, state or metadata */
+#define SARATHI_ERR_CAPACITY 2             /* block table too short or buffer too small */
+#define SARATHI_WARN_OVER_BUDGET_DECODES 3 /* decodes alone exceed the budget; output valid */
+#define SARATHI_ERR_CUDA 4                 /* a CUDA runtime/driver call failed */
+#define SARATHI_ERR_UNSUPPORTED 5          /* head_dim / group size / page size not built */
+#define SARATHI_ERR_DEVICE_CHECK 6         /* the kernel flagged an error (see below) */
+
+/* Request states, [CP] §3.1: running decodes, in-progress prefills, new requests. */
+#define SARATHI_DECODE 0
+#define SARATHI_PREFILL_RUNNING 1
+#define SARATHI_PREFILL_WAITING 2
+
+/* One request as the scheduler sees it ([SS] §"分块不等于截断上下文": processed
+ * prompt length, block table).  The plan never writes to it; after the step the
+ * caller advances num_computed by the scheduled num_new, and a request whose
+ * last chunk ran becomes SARATHI_DECODE ([SS] §"一个 512-token 预算的例子"). */
+typedef struct sarathi_request {
+    int32_t state;          /* SARATHI_DECODE / _PREFILL_RUNNING / _PREFILL_WAITING   */
+    int32_t prompt_len;     /* prefill: total prompt tokens; decode: ignored         */
+    int32_t num_computed;   /* h: tokens already in the KV cache                      */
+    int32_t num_pages;      /* length of the block table                              */
+    const int32_t* pages;   /* host pointer: physical page ids in logical order       */
+} sarathi_request;
+
+/* Model shape of the attention layer.  Built: page_size 16, head_dim 64 or 128,
+ * num_heads_q a multiple of num_heads_kv with group size 1..16. */
+typedef struct sarathi_shape {
+    int32_t num_heads_q;
+    int32_t num_heads_kv;
+    int32_t head_dim;
+    int32_t page_size;
+} sarathi_shape;
+
+/* What sarathi_plan produced.  Offsets count int32 elements from the start of
+ * the packed buffer; the same offsets hold for its device copy. */
+typedef struct sarathi_plan_info {
+    int32_t n_sched;            /* scheduled requests = rows of qo_indptr - 1          */
+    int32_t num_decodes;        /* the first num_decodes scheduled rows are decodes   */
+    int32_t num_tokens;         /* T = qo_indptr[n_sched]                              */
+    int32_t nnz_pages;          /* entries of kv_page_indices                           */
+    int32_t n_items;            /* kernel work items                                    */
+    int32_t n_partials;         /* split-KV partial slots the kernel writes             */
+    int32_t n_merge;            /* split-KV merge groups                                */
+    int32_t max_kv_len;         /* longest h + n in the batch (RoPE table must cover it) */
+    int64_t pairs;              /* query-key pairs scored: sum n*h + n(n+1)/2           */
+    int64_t history_tokens;     /* sum of h over scheduled requests (KV read once each)  */
+    int32_t off_req_index;      /* [n_sched] caller index of each scheduled request     */
+    int32_t off_num_new;        /* [n_sched] new tokens this step                       */
+    int32_t off_last_chunk;     /* [n_sched] 1 if sampling is valid for the row         */
+    int32_t off_qo_indptr;      /* [n_sched+1]                                          */
+    int32_t off_kv_page_indptr; /* [n_sched+1]                                          */
+    int32_t off_kv_page_indices;/* [nnz_pages]                                          */
+    int32_t off_kv_last_page_len;/* [n_sched] in 1..page_size                            */
+    int32_t off_req_aux;        /* [n_sched] kernel bookkeeping (append items per row)  */
+    int32_t off_items;          /* [n_items][8] kernel work list                         */
+    int32_t packed_ints;        /* int32 elements to copy to the device                  */
+    int64_t workspace_bytes;    /* device workspace sarathi_mixed_attn needs             */
+} sarathi_plan_info;
+
+/* Upper bounds for the buffers of sarathi_plan on this request set at ANY
+ * budget <= token_budget: host packed buffer bytes and device workspace bytes.
+ * Either output pointer may be NULL. */
+int32_t sarathi_plan_bounds(const sarathi_request* reqs, int32_t n_reqs, int32_t token_budget,
+                            const sarathi_shape* shape, int32_t num_sms,
+                            size_t* host_buf_bytes, size_t* device_workspace_bytes);
+
+/* Build the step's batch.  Budget order ([CP] §3.1; [ST] §六·补二; [SS]
+ * §"一个 512-token 预算的例子"): every SARATHI_DECODE request gets 1 token (in
+ * caller order), then every SARATHI_PREFILL_RUNNING request gets
+ * min(prompt_len - num_computed, budget left), then every
+ * SARATHI_PREFILL_WAITING request likewise; requests that get 0 are left out.
+ * When the decodes alone exceed the budget all of them are still scheduled,
+ * prefills get nothing and the return is SARATHI_WARN_OVER_BUDGET_DECODES
+ * (decodes never stall, [CP] §3.1).
+ * Metadata ([SS] §"混合批不是…"): for scheduled row s with history h and n new
+ * tokens, kv_len = h + n, its pages are the first ceil(kv_len/page_size) entries
+ * of the block table, and kv_last_page_len = kv_len - page_size*(pages-1).
+ * num_sms sizes the split-KV work (pass the device's SM count).
+ * host_buf: caller-allocated, >= host_buf_bytes, 4-byte aligned.
+ * Errors: INVALID_ARG (bad state, h > prompt_len, budget <= 0, NULL pointers),
+ * CAPACITY (a block table too short, or host_buf too small: info->packed_ints
+ * then holds the size needed), UNSUPPORTED (shape not built). */
+int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int32_t token_budget,
+                     const sarathi_shape* shape, int32_t num_sms,
+                     int32_t* host_buf, size_t host_buf_bytes, sarathi_plan_info* info);
+
+/* Fill the RoPE table on the device: table[p][j] = {cos(p*f_j), sin(p*f_j)} in
+ * fp64 for p < max_pos, j < head_dim/2, f_j = rope_theta^(-2j/head_dim)
+ * (rotate-half RoPE at absolute positions, [SS] §"分块不等于截断上下文").
+ * table: device pointer to max_pos*head_dim doubles (double[max_pos][head_dim/2][2]).
+ * Asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy default stream). */
+int32_t sarathi_rope_table(double* table, int32_t max_pos, int32_t head_dim, double rope_theta,
+                           void* cuda_stream);
+
+/* Arguments of one step.  All pointers are device pointers unless noted. */
+typedef struct sarathi_attn_args {
+    const void* q;              /* bf16 [T][H_q][d]  new tokens' queries, before RoPE   */
+    const void* k;              /* bf16 [T][H_kv][d] new tokens' keys, before RoPE      */
+    const void* v;              /* bf16 [T][H_kv][d] new tokens' values                 */
+    void* k_cache;              /* bf16 [num_pages][H_kv][page_size][d], rotated keys    */
+    void* v_cache;              /* bf16 [num_pages][H_kv][page_size][d]                 */
+    void* out;                  /* bf16 [T][H_q][d] attention outputs                   */
+    const int32_t* plan;        /* device copy of the packed plan buffer                */
+    const sarathi_plan_info* info; /* HOST pointer: the info sarathi_plan returned      */
+    const double* rope_table;   /* from sarathi_rope_table, max_pos >= info->max_kv_len */
+    int32_t rope_max_pos;
+    int32_t num_pages;          /* pages in each cache pool                             */
+    void* workspace;            /* >= info->workspace_bytes, 256-byte aligned, ZEROED    */
+    int64_t workspace_bytes;    /*   once before first use; every launch leaves it so   */
+    sarathi_shape shape;
+    float sm_scale;             /* softmax scale, normally 1/sqrt(head_dim)             */
+} sarathi_attn_args;
+
+/* Enqueue the step on `cuda_stream` (a cudaStream_t): one kernel launch, no
+ * host synchronisation, no allocation.  Writes the new tokens' rotated K and V
+ * into their pages and every out row.  The history pages must already hold
+ * the earlier tokens of each request.  Attention for row i of a request with
+ * history h: softmax over keys 0..h+i of RoPE(q_i, h+i).K_j * sm_scale,
+ * weights applied to V_j ([SS] §"分块不等于截断上下文").  Keys are the bf16
+ * pages; scores and sums in fp32.
+ * Launches using one workspace must not overlap in time.  A launch that hits a
+ * device-side check (a wait that ran out, a page id outside the pool) sets an
+ * error word in the workspace; read it with sarathi_workspace_status.
+ * Errors (before anything is enqueued): INVALID_ARG, CAPACITY (workspace or
+ * RoPE table too small), UNSUPPORTED, CUDA. */
+int32_t sarathi_mixed_attn(const sarathi_attn_args* args, void* cuda_stream);
+
+/* Synchronise `cuda_stream`, then read and clear the device error word of a
+ * workspace.  *device_error receives 0 or the kernel's error code (1: a
+ * bounded wait ran out; 2: a bounds check failed).  Returns SARATHI_OK, or
+ * SARATHI_ERR_DEVICE_CHECK when the word was nonzero (the rest of the
+ * workspace must then be zeroed again before the next launch), or
+ * SARATHI_ERR_CUDA. */
+int32_t sarathi_workspace_status(void* workspace, void* cuda_stream, int32_t* device_error);
+
+/* Thread-local text of the last error; never NULL. */
+const char* sarathi_last_error(void);
+
+/* SARATHI_ABI_VERSION of the loaded library. */
+int32_t sarathi_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SARATHI_H_ */

@@ -42,7 +42,7 @@ def build(force: bool = False) -> str:
         stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
         if force or stale:
             tmp = _LIB + f".tmp{os.getpid()}"
-            cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+            cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
             subprocess.run(cmd, check=True)
             os.replace(tmp, _LIB)
     return _LIB

@@ -1,0 +1,175 @@
+"""CPU tests of the library's host side: the C ABI loads and exports every
+declared symbol; sarathi_plan's metadata equals the oracle's plan bit for bit;
+the kernel work list covers every output row, token and page exactly once."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+import chunked_prefill_mixed_gb300 as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_library_exports_every_declared_function():
+    text = open(os.path.join(ROOT, "include", "sarathi.h")).read()
+    declared = set(re.findall(r"^\s*(?:int32_t|const char\*)\s+(sarathi_\w+)\s*\(", text, re.M))
+    assert declared == set(S.EXPORTED)
+    lib = S.load()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert S.sarathi_abi_version() == 1
+
+
+def _product_plan(states, prompt, computed, tables, budget, shape, num_sms=148):
+    reqs, keep = S.make_requests(states, prompt, computed, tables)
+    st, info, packed = S.sarathi_plan(reqs, len(states), budget, S.Shape(shape.H_q, shape.H_kv, shape.d, 16), num_sms)
+    return st, info, S.plan_arrays(info, packed)
+
+
+def _compare(st_o, mo, st_p, mp):
+    assert st_o == st_p
+    for key in ("req_index", "num_new", "last_chunk", "qo_indptr", "kv_page_indptr", "kv_page_indices",
+                "kv_last_page_len"):
+        assert np.array_equal(np.asarray(mo[key]), np.asarray(mp[key])), key
+    assert mo["num_decodes"] == mp["num_decodes"] and mo["num_tokens"] == mp["num_tokens"]
+
+
+def _workload_cases():
+    yield W.tiny(0)
+    yield W.tiny(3)
+    yield W.mistral()
+    for k in range(5):
+        yield W.llama7b(chunk_step=k)
+    yield W.llama70b()
+    yield W.yi34b()
+    yield W.llama7b_prefill_only(512, 3)
+
+
+@pytest.mark.parametrize("wl", list(_workload_cases()), ids=lambda w: f"{w.name}-{w.notes}")
+def test_plan_matches_oracle_on_workloads(wl):
+    st_o, mo = oracle.plan(*wl.arrays(), wl.budget, 16)
+    st_p, info, mp = _product_plan(*wl.arrays(), wl.budget, wl.shape)
+    _compare(st_o, mo, st_p, mp)
+    _check_work_list(info, mp, wl.shape)
+    assert info.pairs == oracle.pairs(mo, 16)
+
+
+def test_plan_matches_oracle_random_request_sets():
+    rng = np.random.default_rng(123)
+    shape = W.Shape(8, 2, 64)
+    for trial in range(60):
+        n = int(rng.integers(0, 12))
+        states, prompt, computed, tables = [], [], [], []
+        for i in range(n):
+            stt = int(rng.integers(0, 3))
+            if stt == W.DECODE:
+                h = int(rng.integers(0, 300))
+                pl = 0
+                cap = h + 1
+            else:
+                pl = int(rng.integers(1, 400))
+                h = 0 if stt == W.PREFILL_WAITING and rng.random() < 0.7 else int(rng.integers(0, pl + 1))
+                cap = pl
+            npages = (cap + 15) // 16 + int(rng.integers(0, 3))
+            states.append(stt)
+            prompt.append(pl)
+            computed.append(h)
+            tables.append(rng.permutation(5000)[:npages].astype(np.int32))
+        budget = int(rng.integers(1, 600))
+        st_o, mo = oracle.plan(states, prompt, computed, tables, budget, 16)
+        st_p, info, mp = _product_plan(states, prompt, computed, tables, budget, shape,
+                                       num_sms=int(rng.integers(1, 200)))
+        _compare(st_o, mo, st_p, mp)
+        _check_work_list(info, mp, shape)
+
+
+def _check_work_list(info, m, shape):
+    """Every (row, q head) is produced once; every new token's K/V is appended
+    once per kv head; decode splits tile each decode's pages; appends come
+    before the tiles that wait on them."""
+    G = shape.H_q // shape.H_kv
+    n = m["n_sched"]
+    qo, kvp = m["qo_indptr"], m["kv_page_indptr"]
+    items = m["items"]
+    T = int(qo[-1]) if n else 0
+    covered = np.zeros((T, shape.H_q), np.int32)
+    appended = np.zeros((T, shape.H_kv), np.int32)
+    first_prefill = None
+    seen_slots = set()
+    pages_cov = {}
+    for idx, it in enumerate(items):
+        kind, s, g, start, count, slot, merge, nsplit = (int(x) for x in it)
+        nn = qo[s + 1] - qo[s]
+        np_ = kvp[s + 1] - kvp[s]
+        if kind == 0:
+            assert first_prefill is None, "append after a prefill tile"
+            assert nn >= 2
+            appended[qo[s] + start: qo[s] + start + count, :] += 1
+        elif kind == 1:
+            first_prefill = idx if first_prefill is None else first_prefill
+            assert count * G <= 128 and 0 <= start and start + count <= nn
+            for t in range(start, start + count):
+                covered[qo[s] + t, g * G:(g + 1) * G] += 1
+        else:
+            assert nn == 1
+            per = -(-np_ // nsplit)
+            pages_cov.setdefault((s, g), []).append((start, count))
+            if start + count == np_:
+                appended[qo[s], g] += 1
+                covered[qo[s], g * G:(g + 1) * G] += 1
+            if nsplit > 1:
+                k = start // per
+                assert start == k * per
+                assert (slot + k) not in seen_slots
+                seen_slots.add(slot + k)
+                assert 0 <= merge < info.n_merge
+            else:
+                assert slot == -1 and merge == -1
+    assert np.all(covered == 1)
+    assert np.all(appended == 1)
+    for (s, g), spans in pages_cov.items():
+        spans.sort()
+        pos = 0
+        for a, c in spans:
+            assert a == pos and c > 0
+            pos += c
+        assert pos == kvp[s + 1] - kvp[s]
+    assert len(seen_slots) == info.n_partials
+    aux = m["req_aux"]
+    for s in range(n):
+        nn = qo[s + 1] - qo[s]
+        assert aux[s] == (-(-nn // 16) if nn >= 2 else 0)
+
+
+def test_plan_reports_errors_and_warning():
+    shape = W.Shape(4, 4, 64)
+    t = [np.arange(2, dtype=np.int32)]
+    with pytest.raises(S.SarathiError) as e:
+        _product_plan([W.PREFILL_WAITING], [100], [0], t, 64, shape)
+    assert e.value.status == S.ERR_CAPACITY
+    with pytest.raises(S.SarathiError) as e:
+        _product_plan([W.DECODE], [0], [3], t, 0, shape)
+    assert e.value.status == S.ERR_INVALID_ARG
+    with pytest.raises(S.SarathiError) as e:
+        _product_plan([W.DECODE], [0], [3], t, 4, W.Shape(4, 4, 96))
+    assert e.value.status == S.ERR_UNSUPPORTED
+    with pytest.raises(S.SarathiError) as e:
+        _product_plan([W.DECODE], [0], [3], t, 4, W.Shape(64, 2, 128))
+    assert e.value.status == S.ERR_UNSUPPORTED
+    tables = [np.arange(4, dtype=np.int32) + 4 * i for i in range(11)]
+    st, info, m = _product_plan([W.DECODE] * 10 + [W.PREFILL_WAITING], [0] * 10 + [40], [20] * 10 + [0], tables, 8,
+                                shape)
+    assert st == S.WARN_OVER_BUDGET_DECODES and m["n_sched"] == 10
+
+
+def test_plan_bounds_cover_actual_sizes():
+    for wl in (W.mistral(), W.llama70b(), W.yi34b(), W.tiny(1)):
+        reqs, keep = S.make_requests(*wl.arrays())
+        shp = S.Shape(wl.shape.H_q, wl.shape.H_kv, wl.shape.d, 16)
+        hb, wb = S.sarathi_plan_bounds(reqs, len(wl.requests), wl.budget, shp, 148)
+        st, info, packed = S.sarathi_plan(reqs, len(wl.requests), wl.budget, shp, 148)
+        assert info.packed_ints * 4 <= hb and info.workspace_bytes <= wb
