@@ -1,0 +1,388 @@
+"""Benchmark of the mixed-batch paged-attention step (one kernel launch per step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mistral]
+                    [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  ``value`` is tokens/s over the whole job: the
+step's new tokens (decodes + prefill chunk tokens) divided by the kernel's
+device time (CUDA events on the launching stream, L2 flushed before every
+timed step).  ``e2e`` is the same metric through the public API with the
+step's inputs in pinned host memory: host planning, host->device copies, the
+kernel and the device->host read of the outputs inside the timed region.
+``--impl reference`` times the oracle (plain fp64 CPU code) on a bounded
+sample of the same workload.  Under torchrun every rank runs its own replica
+(the step needs no exchange between GPUs).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "mixed-batch paged attn: μs/step, tokens/s, % of roofline (HBM or TC)"
+UNIT = "tokens/s"
+DESCR = {
+    "mistral": "Mistral-7B-like attention layer (32 q / 8 kv heads, d 128, page 16), budget 512: "
+               "80 decodes (context U[256,4096]) + running prefill P (300 left, no history) + "
+               "running prefill Q (132 of 900 left, 768 history)",
+    "llama7b": "Llama-2-7B-like MHA layer (32/32 heads, d 128), budget 2048: 64 decodes (context U[512,8192]) "
+               "+ 1984-token chunk of an 8192-token prompt after 5952 history",
+    "llama70b": "LLaMA2-70B-like GQA layer (64 q / 8 kv, d 128), budget 1536: 200 decodes (lognormal context) + "
+                "chunks (12288,500), (4096,600), (0,236)",
+    "yi34b": "Yi-34B-like layer (56 q / 8 kv, d 128), budget 512, fragmented pages: 256 decodes (context 4096) + "
+             "256-token chunk after 3840 history",
+    "tiny": "tiny layer (4/4 heads, d 64), budget 66: 2 decodes + 64-token chunk",
+    "llama7b_oneshot": "Llama-2-7B-like MHA layer, prefill-only: one 8192-token prompt in one shot",
+    "llama7b_c512": "Llama-2-7B-like MHA layer, prefill-only: last 512-token chunk of an 8192-token prompt",
+    "llama7b_c2048": "Llama-2-7B-like MHA layer, prefill-only: last 2048-token chunk of an 8192-token prompt",
+}
+
+
+def make_workload(name: str) -> W.Workload:
+    if name == "llama7b":
+        return W.llama7b(chunk_step=3)
+    if name == "llama7b_oneshot":
+        return W.llama7b_prefill_only(8192, 0)
+    if name.startswith("llama7b_c"):
+        c = int(name[len("llama7b_c"):])
+        return W.llama7b_prefill_only(c, 8192 // c - 1)
+    return W.WORKLOADS[name]()
+
+
+def algorithmic(wl: W.Workload, meta) -> dict:
+    """Algorithmic FLOP and bytes of one step: FLOP = 4 d H_q pairs; bytes =
+    Q in + raw K,V in + K,V page writes + history K,V read once per request + O out."""
+    sh = wl.shape
+    n = np.diff(meta["qo_indptr"]).astype(np.int64)
+    kv = (np.diff(meta["kv_page_indptr"]).astype(np.int64) - 1) * 16 + meta["kv_last_page_len"].astype(np.int64)
+    h = kv - n
+    T = int(n.sum())
+    pairs = int((n * h + n * (n + 1) // 2).sum())
+    flop = 4.0 * sh.d * sh.H_q * pairs
+    byt = (2.0 * T * sh.H_q * sh.d + 4.0 * T * sh.H_kv * sh.d + 4.0 * T * sh.H_kv * sh.d
+           + 4.0 * float(h.sum()) * sh.H_kv * sh.d + 2.0 * T * sh.H_q * sh.d)
+    return {"T": T, "pairs": pairs, "flop": flop, "bytes": byt, "history": int(h.sum())}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("mixed_attn.cu", "sarathi_internal.h", "plan.cpp"):
+        h.update(open(os.path.join(ROOT, "chunked_prefill_mixed_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        e = json.load(open(p)).get(workload)
+        if e and e.get("src_sha") == kernel_source_sha():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample_time(wl: W.Workload, meta, q, k, v, kc, vc, budget_s: float, seed: int = 0):
+    """Time the oracle on a bounded sample of the step: every append plus the
+    attention of random (row, head) pairs, until ~budget_s of CPU work; scale
+    to the full step by the share of query-key pairs the sample covered.
+    Returns (estimated seconds per full step, cores, description)."""
+    import oracle
+    sh = wl.shape
+    n = np.diff(meta["qo_indptr"])
+    kvl = (np.diff(meta["kv_page_indptr"]) - 1) * 16 + meta["kv_last_page_len"]
+    h = kvl - n
+    row_keys = np.concatenate([np.arange(h[s] + 1, h[s] + n[s] + 1) for s in range(len(n))]).astype(np.int64)
+    total_pairs = int(row_keys.sum()) * sh.H_q
+    kcw, vcw = kc.copy(), vc.copy()
+    t0 = time.perf_counter()
+    oracle.append(meta, k, v, sh.H_kv, sh.d, 16, sh.rope_base, kcw, vcw)
+    t_append = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    T = int(meta["qo_indptr"][-1])
+    done_pairs, t_attn, batches = 0, 0.0, 0
+    batch = max(oracle.num_threads() * 4, 16)
+    while t_attn < budget_s and done_pairs < total_pairs:
+        rt = rng.integers(0, T, size=batch).astype(np.int32)
+        rh = rng.integers(0, sh.H_q, size=batch).astype(np.int32)
+        t1 = time.perf_counter()
+        oracle.attend(meta, q, sh.H_q, sh.H_kv, sh.d, 16, sh.rope_base, kcw, vcw, rt, rh)
+        t_attn += time.perf_counter() - t1
+        done_pairs += int(row_keys[rt].sum())
+        batches += 1
+    est = t_append + t_attn * (total_pairs / max(done_pairs, 1))
+    desc = (f"all {T} appends + {batches * batch} random (row, q-head) attention outputs "
+            f"({done_pairs / total_pairs:.2%} of the step's query-key pairs), scaled by pairs")
+    return est, oracle.num_threads(), desc
+
+
+def setup_inputs(wl: W.Workload):
+    import oracle
+    st, meta = oracle.plan(*wl.arrays(), wl.budget, 16)
+    q, k, v = W.new_token_values(meta["num_tokens"], wl.shape, wl.seed)
+    return meta, q, k, v
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step = a bounded sample of the workload."""
+    if rank != 0:
+        return None
+    wl = make_workload(args.workload)
+    meta, q, k, v = setup_inputs(wl)
+    kc, vc = W.history_cache_numpy(wl.num_pages, wl.shape, wl.seed)
+    alg = algorithmic(wl, meta)
+    per_step = max(1.0, args.ref_seconds / max(args.steps + args.warmup, 1))
+    times, cores, desc = [], 1, ""
+    for i in range(args.warmup + args.steps):
+        est, cores, desc = oracle_sample_time(wl, meta, q, k, v, kc, vc, per_step, seed=i)
+        if i >= args.warmup:
+            times.append(est)
+    sec = statistics.mean(times)
+    value = alg["T"] / sec
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": DESCR[args.workload]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import chunked_prefill_mixed_gb300 as S
+    from chunked_prefill_mixed_gb300.runner import StepRunner
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    S.load()
+    wl = make_workload(args.workload)
+    sh = wl.shape
+    meta, q, k, v = setup_inputs(wl)
+    alg = algorithmic(wl, meta)
+    T = alg["T"]
+    kc, vc = W.history_cache_torch(wl.num_pages, sh, wl.seed, dev)
+    max_kv = int(((np.diff(meta["kv_page_indptr"]) - 1) * 16 + meta["kv_last_page_len"]).max())
+    stream = torch.cuda.Stream(dev)
+    runner = StepRunner(sh.H_q, sh.H_kv, sh.d, max_kv + 16, device=dev, rope_theta=sh.rope_base, stream=stream)
+    st, info, packed = runner.plan(*wl.arrays(), wl.budget)
+    runner.ensure_workspace(int(info.workspace_bytes))
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    q_h, k_h, v_h = (bf(x).pin_memory() for x in (q, k, v))
+    q_d, k_d, v_d = (x.to(dev) for x in (q_h, k_h, v_h))
+    out = torch.empty((T, sh.H_q, sh.d), dtype=torch.bfloat16, device=dev)
+    out_h = torch.empty((T, sh.H_q, sh.d), dtype=torch.bfloat16).pin_memory()
+    plan_pin = torch.empty(info.packed_ints + 64, dtype=torch.int32).pin_memory()
+    plan_dev = torch.empty(info.packed_ints + 64, dtype=torch.int32, device=dev)
+    plan_pin[:info.packed_ints].copy_(torch.from_numpy(packed))
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        plan_dev[:info.packed_ints].copy_(plan_pin[:info.packed_ints], non_blocking=True)
+    stream.synchronize()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            runner.run(q_d, k_d, v_d, kc, vc, out, plan_dev, info)
+    if runner.status() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_wall0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.zero_()
+                starts[i].record(stream)
+                runner.run(q_d, k_d, v_d, kc, vc, out, plan_dev, info)
+                ends[i].record(stream)
+        stream.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if runner.status() != 0:
+        raise RuntimeError("device error in the timed region")
+
+    # e2e through the public API: plan on the host, pinned H2D, kernel, D2H
+    h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * 2 + info.packed_ints * 4
+    d2h = out.numel() * 2
+    e2e_times = []
+    barrier()
+    for i in range(args.steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        st2, info2, packed2 = runner.plan(*wl.arrays(), wl.budget)
+        plan_pin[:info2.packed_ints].copy_(torch.from_numpy(packed2))
+        with torch.cuda.stream(stream):
+            plan_dev[:info2.packed_ints].copy_(plan_pin[:info2.packed_ints], non_blocking=True)
+            q_d.copy_(q_h, non_blocking=True)
+            k_d.copy_(k_h, non_blocking=True)
+            v_d.copy_(v_h, non_blocking=True)
+            runner.run(q_d, k_d, v_d, kc, vc, out, plan_dev, info2)
+            out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+        e2e_times.append(time.perf_counter() - t0)
+    barrier()
+
+    ms_per = float(sum(ms)) / args.steps
+    e2e_s = float(np.mean(e2e_times))
+    if world > 1:
+        t = torch.tensor([ms_per, e2e_s], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per, e2e_s = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+    hbm, tc, tc_sus, peak_kind = load_peaks()
+    t_hbm = alg["bytes"] / (hbm * 1e9)
+    t_tc = alg["flop"] / (tc * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    sec = ms_per / 1e3
+    if bound == "hbm":
+        achieved, peak, unit_r = alg["bytes"] / sec / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit_r = alg["flop"] / sec / 1e12, tc, "TFLOP/s"
+    res = {
+        "metric": METRIC, "value": world * T / sec, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per, "us_per_step": ms_per * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "name": args.workload, "tokens_per_step": T,
+                   "l2": "flushed (512 MB write) before every timed step", "replicas": world},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit_r, "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json, burst)",
+                     "roofline_us": max(t_hbm, t_tc) * 1e6, "algorithmic_bytes": alg["bytes"],
+                     "algorithmic_flop": alg["flop"], "traffic": committed_traffic(args.workload)},
+        "e2e": {"value": world * T / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h),
+                "includes": "host plan + pinned H2D (q, k, v, plan) + kernel + D2H (out)"},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps,
+        "timing": {"kernel_ms_min": min(ms), "kernel_ms_median": statistics.median(ms), "wall_s": t_wall},
+    }
+    if not args.no_cpu_baseline:
+        kc_h = kc.view(torch.int16).cpu().numpy().view(np.uint16)
+        vc_h = vc.view(torch.int16).cpu().numpy().view(np.uint16)
+        # the device caches already hold this step's appends; the oracle
+        # re-appends the same values, so the sample sees the same state
+        est, cores, desc = oracle_sample_time(wl, meta, q, k, v, kc_h, vc_h, args.cpu_seconds)
+        res["cpu_baseline"] = {"value": T / est, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mistral", choices=sorted(DESCR))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world, local_rank)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+"""GPU parity: the CUDA step (through the C ABI) against the oracle on the same
+seeded inputs.  KV pages must match bit for bit (bf16 of the fp64 RoPE);
+outputs within max-abs 2e-2 and mean-abs 2e-3 of the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from gpu_helpers import GpuStep, assert_close, from_u16, to_u16
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_step(gs: GpuStep, rows="all", n_random=256):
+    err = gs.run()
+    assert err == 0, f"device error {err}"
+    kc, vc = gs.oracle_caches()
+    assert np.array_equal(to_u16(gs.kc_dev), kc), "K pages differ from the oracle"
+    assert np.array_equal(to_u16(gs.vc_dev), vc), "V pages differ from the oracle"
+    outd = oracle.bf16_to_double(to_u16(gs.out))
+    if rows == "all":
+        ref, rt, rh = gs.oracle_rows(kc, vc)
+    else:
+        rt, rh = gs.sample_rows(n_random)
+        ref, rt, rh = gs.oracle_rows(kc, vc, rt, rh)
+    return assert_close(outd[rt, rh], ref, gs.wl.name)
+
+
+def test_tiny_single_step():
+    _check_step(GpuStep(W.tiny(0)))
+
+
+def test_mistral_budget_512_all_rows():
+    _check_step(GpuStep(W.mistral()))
+
+
+@pytest.mark.parametrize("k", [0, 3, 4])
+def test_llama7b_budget_2048_sampled(k):
+    _check_step(GpuStep(W.llama7b(chunk_step=k)), rows="sample")
+
+
+def test_llama70b_budget_1536_sampled():
+    _check_step(GpuStep(W.llama70b()), rows="sample")
+
+
+def test_yi34b_fragmented_sampled():
+    _check_step(GpuStep(W.yi34b()), rows="sample")
+
+
+def _custom(shape, specs, budget, seed=5, permute=True, name="custom"):
+    return W._build(name, shape, budget, specs, seed, permute=permute, spare_pages=3)
+
+
+@pytest.mark.parametrize("H_q,H_kv,d", [(8, 2, 64), (7, 1, 128), (16, 1, 64), (4, 4, 128), (8, 1, 128)])
+def test_edge_shapes_ragged_chunks(H_q, H_kv, d):
+    shape = W.Shape(H_q, H_kv, d)
+    specs = [
+        (W.DECODE, 0, 0, 1),        # first decode token: attends only to itself
+        (W.DECODE, 0, 15, 16),      # fills a page exactly (last page length 16)
+        (W.DECODE, 0, 16, 17),      # opens a new page (last page length 1)
+        (W.DECODE, 0, 333, 334),
+        (W.PREFILL_RUNNING, 40, 39, 40),     # chunk of one token after history
+        (W.PREFILL_RUNNING, 100, 31, 100),   # ragged history, chunk 69
+        (W.PREFILL_RUNNING, 64, 16, 64),     # history an exact page multiple
+        (W.PREFILL_WAITING, 17, 0, 17),
+        (W.PREFILL_WAITING, 300, 0, 300),    # takes what is left (several tiles, ragged tail)
+    ]
+    _check_step(GpuStep(_custom(shape, specs, budget=400)))
+
+
+def test_repeat_launch_is_deterministic_and_leaves_workspace_clean():
+    import torch
+    gs = GpuStep(W.mistral())
+    k0, v0 = gs.kc_dev.clone(), gs.vc_dev.clone()
+    assert gs.run() == 0
+    out1, k1 = gs.out.clone(), gs.kc_dev.clone()
+    gs.kc_dev.copy_(k0)
+    gs.vc_dev.copy_(v0)
+    gs.out.fill_(float("nan"))
+    assert gs.run() == 0
+    assert np.array_equal(to_u16(gs.out), to_u16(out1))
+    assert np.array_equal(to_u16(gs.kc_dev), to_u16(k1))
+    hdr = gs.runner.workspace[:64].view(torch.int32).cpu().numpy()
+    assert np.all(hdr[:3] == 0)
+
+
+def test_tiny_chunked_schedule_equals_one_shot_and_oracle():
+    """The 200-token prompt in chunks of 64 over 4 steps next to 2 decodes, then
+    the same prompt in one shot: same KV pages, outputs within tolerance, and
+    every step matches the oracle."""
+    import torch
+    from chunked_prefill_mixed_gb300.runner import StepRunner
+    shape = W.SHAPES["tiny"]
+    L = 200
+    pq, pk, pv = W.new_token_values(L, shape, 100)
+    wl0 = W.tiny(0)
+    kc_h, vc_h = W.history_cache_numpy(wl0.num_pages, shape, 0)
+    dev = torch.device("cuda")
+    kc, vc = from_u16(kc_h, dev), from_u16(vc_h, dev)
+    okc, ovc = kc_h.copy(), vc_h.copy()
+    runner = StepRunner(shape.H_q, shape.H_kv, shape.d, 256, device=dev)
+    prompt_out = np.zeros((L, shape.H_q, shape.d))
+    done = 0
+    for s in range(4):
+        wl = W.tiny(s)
+        st, meta = oracle.plan(*wl.arrays(), wl.budget, 16)
+        n = int(meta["num_new"][2])
+        dq, dk, dv = W.new_token_values(2, shape, 200 + s)
+        q = np.concatenate([dq, pq[done:done + n]])
+        k = np.concatenate([dk, pk[done:done + n]])
+        v = np.concatenate([dv, pv[done:done + n]])
+        status, info, packed = runner.plan(*wl.arrays(), wl.budget)
+        out = torch.empty((2 + n, shape.H_q, shape.d), dtype=torch.bfloat16, device=dev)
+        runner.run(from_u16(q, dev), from_u16(k, dev), from_u16(v, dev), kc, vc, out, runner.upload(packed), info)
+        assert runner.status() == 0
+        oo = oracle.step(meta, q, k, v, shape.H_q, shape.H_kv, shape.d, 16, shape.rope_base, okc, ovc)
+        assert np.array_equal(to_u16(kc), okc) and np.array_equal(to_u16(vc), ovc)
+        assert_close(oracle.bf16_to_double(to_u16(out)), oo, f"tiny step {s}")
+        prompt_out[done:done + n] = oracle.bf16_to_double(to_u16(out))[2:]
+        done += n
+    assert done == L
+    # one shot: the same prompt into a fresh copy of the history pools
+    table = wl0.requests[2].pages
+    wl1 = W._build("tiny_oneshot", shape, L, [(W.PREFILL_WAITING, L, 0, L)], 0)
+    wl1.requests[0].pages = table
+    kc2, vc2 = from_u16(kc_h, dev), from_u16(vc_h, dev)
+    status, info, packed = runner.plan(*wl1.arrays(), L)
+    out = torch.empty((L, shape.H_q, shape.d), dtype=torch.bfloat16, device=dev)
+    runner.run(from_u16(pq, dev), from_u16(pk, dev), from_u16(pv, dev), kc2, vc2, out, runner.upload(packed), info)
+    assert runner.status() == 0
+    ptab = table[: (L + 15) // 16]
+    assert np.array_equal(to_u16(kc2)[ptab], to_u16(kc)[ptab])
+    assert np.array_equal(to_u16(vc2)[ptab], to_u16(vc)[ptab])
+    diff = np.abs(oracle.bf16_to_double(to_u16(out)) - prompt_out)
+    assert diff.max() <= 2e-2
+
+
+@pytest.mark.parametrize("chunk", [512, 2048])
+def test_llama7b_prefill_chunk_sweep_pages_equal_one_shot(chunk):
+    """Prefill-only 8192-token prompt: every chunking writes the same pages as
+    one shot, chunk outputs agree with one shot, and sampled rows of the one
+    shot match the oracle."""
+    import torch
+    L = 8192
+    one = GpuStep(W.llama7b_prefill_only(L, 0))
+    assert one.run() == 0
+    pages = one.wl.requests[0].pages
+    ref_k = to_u16(one.kc_dev)[pages]
+    ref_v = to_u16(one.vc_dev)[pages]
+    rt = np.array([0, 1, 511, 512, 513, 4095, 4096, 8190, 8191], np.int32)
+    rh = np.array([0, 31, 5, 17, 3, 9, 30, 2, 31], np.int32)
+    kc_o, vc_o = one.oracle_caches()
+    ref, _, _ = one.oracle_rows(kc_o, vc_o, rt, rh)
+    assert_close(oracle.bf16_to_double(to_u16(one.out))[rt, rh], ref, "one-shot 8192")
+    gs = GpuStep(W.llama7b_prefill_only(chunk, 0), runner=one.runner)
+    done = 0
+    while done < L:
+        wl = W.llama7b_prefill_only(chunk, done // chunk)
+        st, info, packed = gs.runner.plan(*wl.arrays(), wl.budget)
+        n = info.num_tokens
+        out = torch.empty((n, 32, 128), dtype=torch.bfloat16, device="cuda")
+        gs.runner.run(one.q_dev[done:done + n], one.k_dev[done:done + n], one.v_dev[done:done + n],
+                      gs.kc_dev, gs.vc_dev, out, gs.runner.upload(packed), info)
+        assert gs.runner.status() == 0
+        diff = (out.float() - one.out[done:done + n].float()).abs()
+        assert float(diff.max()) <= 2e-2
+        done += n
+    assert np.array_equal(to_u16(gs.kc_dev)[pages], ref_k)
+    assert np.array_equal(to_u16(gs.vc_dev)[pages], ref_v)

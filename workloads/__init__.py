@@ -224,6 +224,13 @@ def history_cache_torch(num_pages: int, shape: Shape, seed: int, device):
     g = torch.Generator(device=device)
     g.manual_seed(seed + 104729)
     dims = (num_pages, shape.H_kv, shape.page_size, shape.d)
-    k = torch.randn(dims, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
-    v = torch.randn(dims, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
-    return k, v
+    out = []
+    for _ in range(2):
+        t = torch.empty(dims, dtype=torch.bfloat16, device=device)
+        flat = t.view(num_pages, -1)
+        step = max(1, (64 << 20) // flat.shape[1])  # about 64 M elements per draw
+        for p0 in range(0, num_pages, step):
+            blk = flat[p0:p0 + step]
+            blk.copy_(torch.randn(blk.shape, generator=g, device=device, dtype=torch.float32))
+        out.append(t)
+    return out[0], out[1]
