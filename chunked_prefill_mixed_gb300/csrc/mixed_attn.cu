@@ -72,7 +72,9 @@ constexpr int kDecStageBytes = 2 * 2 * kPageHalfBytes;         // K+V page-head,
 constexpr int kSmemStages = kWarps * kDecStages * kDecStageBytes;  // 192 KB
 constexpr int kSmemDecQ = kSmemStages;                         // 16 x 128 bf16
 constexpr int kSmemStash = kSmemDecQ + 2 * kPageHalfBytes;     // new K/V (2 x 128 bf16)
-constexpr int kSmemBars = kSmemStash + 512;
+constexpr int kSmemBars = kSmemStash + 512;                   // mbarriers, initialised once
+constexpr int kDecBar0 = 0;                                    // [warp][stage] decode rings
+constexpr int kPfBar0 = kWarps * kDecStages;                   // prefill ring
 constexpr int kSmemBytes = kSmemBars + 256;
 constexpr int kSmemAlloc = kSmemBytes + 1024;                  // + alignment slack
 // prefill layout inside the stage region
@@ -192,15 +194,27 @@ __device__ __forceinline__ void raise_error(const KParams& P, int code, int deta
     *(volatile int*)s_abort = 1;
 }
 
-// Bounded wait on an mbarrier phase; returns false (and flags the CTA) on timeout.
-__device__ bool mbar_wait_bounded(const KParams& P, uint32_t bar, uint32_t parity, int* s_abort, int detail) {
+// Bounded wait on an mbarrier phase; returns false (and flags the CTA) on
+// timeout, recording the work item, the thread and the barrier's raw state in
+// header words 3..11 for the host to read.
+__device__ bool mbar_wait_bounded(const KParams& P, uint32_t bar, uint32_t parity, int* s_abort, int detail,
+                                  const int* it) {
     for (int i = 0; i < 256; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity)) {
         if (*(volatile int*)s_abort) return false;
         if (globaltimer() - t0 > kWaitNs) {
-            raise_error(P, kErrWait, detail, s_abort);
+            if (atomicCAS(&P.ws_int[2], 0, kErrWait) == 0) {
+                uint64_t raw;
+                asm volatile("ld.shared.b64 %0, [%1];" : "=l"(raw) : "r"(bar) : "memory");
+                P.ws_int[3] = detail;
+                for (int i = 0; i < 5; ++i) P.ws_int[4 + i] = it[i];
+                P.ws_int[9] = (int)threadIdx.x | ((int)parity << 16);
+                P.ws_int[10] = (int)(uint32_t)raw;
+                P.ws_int[11] = (int)(uint32_t)(raw >> 32);
+            }
+            *(volatile int*)s_abort = 1;
             return false;
         }
     }
@@ -300,7 +314,7 @@ __device__ void run_append(const KParams& P, const int* it, int* s_abort) {
 // ----------------------------------------------------------------------------
 template <int D>
 __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUtensorMap* tmV, const int* it,
-                            uint8_t* smem, int* s_abort) {
+                            uint8_t* smem, int* s_abort, uint32_t& phase) {
     constexpr int HALVES = D / 64;
     constexpr int HALF = D / 2;
     constexpr int KBLK_HALF = kPfBlockKeys * 128;  // one column half of a 64-key block
@@ -316,7 +330,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
     const int pages_hi = (kv_hi + kPage - 1) / kPage;
     uint8_t* qtile = smem;
     uint8_t* stages = smem + kPfQBytes;
-    const uint32_t bars = smem_u32(smem + kSmemBars);
+    const uint32_t bars = smem_u32(smem + kSmemBars) + 8 * kPfBar0;
 
     // 1. the chunk's K/V must be in the pages: wait for this request's APPENDs
     if (tid == 0) {
@@ -333,8 +347,6 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             }
         }
         fence_proxy_async_global();
-        for (int i = 0; i < kPfStages; ++i) mbar_init(bars + 8 * i, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     if (*(volatile int*)s_abort) return;
@@ -403,7 +415,8 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
 
     for (int b = 0; b < nblk; ++b) {
         const int stg = b % kPfStages;
-        mbar_wait_bounded(P, bars + 8 * stg, (b / kPfStages) & 1, s_abort, b);
+        mbar_wait_bounded(P, bars + 8 * stg, (phase >> stg) & 1u, s_abort, b, it);
+        phase ^= 1u << stg;
         uint8_t* kb = stages + stg * STAGE;
         uint8_t* vb = kb + K_BYTES;
         const int key0 = b * kPfBlockKeys;
@@ -523,7 +536,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
 // ----------------------------------------------------------------------------
 template <int D>
 __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUtensorMap* tmV, const int* it,
-                           uint8_t* smem, int* s_abort, int* s_flag) {
+                           uint8_t* smem, int* s_abort, int* s_flag, uint32_t& phase) {
     constexpr int HALVES = D / 64;
     constexpr int HALF = D / 2;
     constexpr int KPAGE = HALVES * kPageHalfBytes;  // one K page-head in smem
@@ -538,14 +551,9 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     uint8_t* qtile = smem + kSmemDecQ;
     uint16_t* stash = reinterpret_cast<uint16_t*>(smem + kSmemStash);
     uint8_t* wst = smem + warp * kDecStages * kDecStageBytes;
-    const uint32_t wbar = smem_u32(smem + kSmemBars) + 8 * kDecStages * warp;
+    const uint32_t wbar = smem_u32(smem + kSmemBars) + 8 * (kDecBar0 + kDecStages * warp);
     const int my_pages = pc > warp ? (pc - warp + kWarps - 1) / kWarps : 0;
 
-    if (lane == 0) {
-        for (int i = 0; i < kDecStages; ++i) mbar_init(wbar + 8 * i, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
     auto issue = [&](int k) {
         const int lp = p0 + warp + kWarps * k;
         const int page = page_id(P, R, lp, s_abort);
@@ -620,7 +628,8 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
 
     for (int k = 0; k < my_pages; ++k) {
         const int stg = k % kDecStages;
-        mbar_wait_bounded(P, wbar + 8 * stg, (k / kDecStages) & 1, s_abort, k);
+        mbar_wait_bounded(P, wbar + 8 * stg, (phase >> stg) & 1u, s_abort, k, it);
+        phase ^= 1u << stg;
         uint8_t* kb = wst + stg * kDecStageBytes;
         uint8_t* vb = kb + KPAGE;
         const int lp = p0 + warp + kWarps * k;
@@ -790,7 +799,14 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
     __shared__ int s_abort;
     __shared__ int s_flag;
     const int tid = threadIdx.x;
-    if (tid == 0) s_abort = 0;
+    if (tid == 0) {
+        s_abort = 0;
+        const uint32_t bars = smem_u32(smem + kSmemBars);
+        for (int i = 0; i < kPfBar0 + kPfStages; ++i) mbar_init(bars + 8 * i, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // completed-phase parity of each ring stage, carried across work items
+    uint32_t pf_phase = 0, dec_phase = 0;
     for (;;) {
         if (tid == 0) {
             const int idx = atomicAdd(&P.ws_int[0], 1);
@@ -817,9 +833,12 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         if (it[0] == kAppend)
             run_append<D>(P, it, &s_abort);
         else if (it[0] == kPrefill)
-            run_prefill<D>(P, &tmK, &tmV, it, smem, &s_abort);
+            run_prefill<D>(P, &tmK, &tmV, it, smem, &s_abort, pf_phase);
         else
-            run_decode<D>(P, &tmK, &tmV, it, smem, &s_abort, &s_flag);
+            run_decode<D>(P, &tmK, &tmV, it, smem, &s_abort, &s_flag, dec_phase);
+        // shared memory written through the generic proxy this item (tiles,
+        // scratch, patched rows) is next overwritten by TMA
+        fence_proxy_async_shared();
         __syncthreads();
         if (s_abort) return;  // the error word is set; the workspace must be re-zeroed
     }

@@ -61,6 +61,8 @@ class GpuStep:
         import torch
         self.runner.run(self.q_dev, self.k_dev, self.v_dev, self.kc_dev, self.vc_dev, self.out, self.plan_dev,
                         self.info)
+        torch.cuda.synchronize()
+        self.last_header = self.runner.workspace[:64].view(torch.int32).cpu().numpy().copy()
         err = self.runner.status()
         torch.cuda.synchronize()
         return err

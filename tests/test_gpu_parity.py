@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 
 def _check_step(gs: GpuStep, rows="all", n_random=256):
     err = gs.run()
-    assert err == 0, f"device error {err}"
+    assert err == 0, f"device error {err}, header {gs.last_header[:12].tolist()}"
     kc, vc = gs.oracle_caches()
     assert np.array_equal(to_u16(gs.kc_dev), kc), "K pages differ from the oracle"
     assert np.array_equal(to_u16(gs.vc_dev), vc), "V pages differ from the oracle"
