@@ -22,7 +22,7 @@ ERR_CUDA, ERR_UNSUPPORTED, ERR_DEVICE_CHECK = 4, 5, 6
 DECODE, PREFILL_RUNNING, PREFILL_WAITING = 0, 1, 2
 
 EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_rope_table", "sarathi_mixed_attn",
-            "sarathi_workspace_status", "sarathi_last_error", "sarathi_abi_version")
+            "sarathi_mixed_attn_noalloc", "sarathi_workspace_status", "sarathi_last_error", "sarathi_abi_version")
 
 
 class SarathiError(RuntimeError):
@@ -86,6 +86,8 @@ def load(build_if_missing: bool = True):
                                        ctypes.c_void_p]
     lib.sarathi_mixed_attn.restype = ctypes.c_int32
     lib.sarathi_mixed_attn.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p]
+    lib.sarathi_mixed_attn_noalloc.restype = ctypes.c_int32
+    lib.sarathi_mixed_attn_noalloc.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p]
     lib.sarathi_workspace_status.restype = ctypes.c_int32
     lib.sarathi_workspace_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.sarathi_last_error.restype = ctypes.c_char_p
@@ -192,6 +194,25 @@ def sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo,
     a.shape = shape
     a.sm_scale = float(sm_scale)
     _check(load().sarathi_mixed_attn(ctypes.byref(a), _stream_ptr(stream)), "sarathi_mixed_attn")
+
+
+def sarathi_mixed_attn_noalloc(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo, rope_table,
+                               rope_max_pos: int, shape: Shape, sm_scale: float, stream=None) -> None:
+    """Enqueue one step without a caller workspace: the library's built-in
+    scratch array is used (see include/sarathi.h for its limits)."""
+    a = AttnArgs()
+    a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    a.k_cache, a.v_cache, a.out = k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr()
+    a.plan = plan_dev.data_ptr()
+    a.info = ctypes.pointer(info)
+    a.rope_table = rope_table.data_ptr()
+    a.rope_max_pos = int(rope_max_pos)
+    a.num_pages = int(k_cache.shape[0])
+    a.workspace = None
+    a.workspace_bytes = 0
+    a.shape = shape
+    a.sm_scale = float(sm_scale)
+    _check(load().sarathi_mixed_attn_noalloc(ctypes.byref(a), _stream_ptr(stream)), "sarathi_mixed_attn_noalloc")
 
 
 def sarathi_workspace_status(workspace, stream=None) -> int:

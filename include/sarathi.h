@@ -168,6 +168,23 @@ typedef struct sarathi_attn_args {
  * RoPE table too small), UNSUPPORTED, CUDA. */
 int32_t sarathi_mixed_attn(const sarathi_attn_args* args, void* cuda_stream);
 
+/* The same step as sarathi_mixed_attn, for callers that cannot allocate device
+ * memory when they run it -- for example a plugin inside a process whose
+ * allocator already owns the GPU's memory, or a serving loop that allows no
+ * allocation after start-up.  The pages have no counterpart to this call.
+ * The scratch (args->workspace and args->workspace_bytes are ignored) comes
+ * from an 8 MiB array inside the library that every GPU loading the library
+ * holds until the process exits; a batch whose info->workspace_bytes exceeds
+ * 8 MiB is rejected with SARATHI_ERR_CAPACITY before anything is enqueued.
+ * The call allocates nothing: it clears the array's counters with
+ * cudaMemsetAsync on `cuda_stream` and enqueues the step kernel.  The first
+ * call on each device looks up the array's device address; make that first
+ * call before any stream capture.  All calls share the one array, so calls
+ * whose work overlaps on the GPU (other streams, other threads) race and give
+ * wrong results.  The device error word lives in the shared array and is not
+ * reported; use sarathi_mixed_attn with a workspace when it is needed. */
+int32_t sarathi_mixed_attn_noalloc(const sarathi_attn_args* args, void* cuda_stream);
+
 /* Synchronise `cuda_stream`, then read and clear the device error word of a
  * workspace.  *device_error receives 0 or the kernel's error code (1: a
  * bounded wait ran out; 2: a bounds check failed).  Returns SARATHI_OK, or

@@ -1,0 +1,52 @@
+"""The step entry point for callers that cannot allocate device memory.
+
+Some callers -- a plugin inside a process whose allocator already owns the
+GPU's memory, or a serving loop that forbids allocation after start-up --
+cannot provide a workspace.  sarathi_mixed_attn_noalloc runs the same step with
+the library's own fixed scratch array.  These tests check that it gives the
+same pages and outputs as the workspace entry point, on two calls in a row (the
+array keeps the previous call's contents), and that batches needing more
+scratch than the array holds are refused.  The file is named so that pytest
+collects it last."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+import chunked_prefill_mixed_gb300 as S
+
+
+def test_noalloc_refuses_batches_beyond_the_scratch_limit():
+    info = S.PlanInfo()
+    info.n_items = 1
+    info.workspace_bytes = (8 << 20) + 256
+    a = S.AttnArgs()
+    a.info = ctypes.pointer(info)
+    st = S.load().sarathi_mixed_attn_noalloc(ctypes.byref(a), None)
+    assert st == S.ERR_CAPACITY
+    assert "scratch" in S.sarathi_last_error()
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_workspace_entry_point_on_two_calls():
+    import torch
+    from gpu_helpers import GpuStep, assert_close, to_u16
+    gs = GpuStep(W.mistral())  # split decodes: the scratch holds merge tickets and partials
+    assert gs.info.n_partials > 0 and gs.info.workspace_bytes <= (8 << 20)
+    k0, v0 = gs.kc_dev.clone(), gs.vc_dev.clone()
+    assert gs.run() == 0
+    ref_out = oracle.bf16_to_double(to_u16(gs.out))
+    ref_k, ref_v = to_u16(gs.kc_dev), to_u16(gs.vc_dev)
+    r = gs.runner
+    for call in range(2):
+        gs.kc_dev.copy_(k0)
+        gs.vc_dev.copy_(v0)
+        out = torch.full_like(gs.out, float("nan"))
+        S.sarathi_mixed_attn_noalloc(gs.q_dev, gs.k_dev, gs.v_dev, gs.kc_dev, gs.vc_dev, out, gs.plan_dev, gs.info,
+                                     r.rope, r.max_pos, r.shape, r.sm_scale, r.stream)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_u16(gs.kc_dev), ref_k), f"call {call}: K pages differ"
+        assert np.array_equal(to_u16(gs.vc_dev), ref_v), f"call {call}: V pages differ"
+        assert_close(oracle.bf16_to_double(to_u16(out)), ref_out, f"no-alloc call {call}")
