@@ -64,26 +64,19 @@ struct KParams {
     int slot_floats;
 };
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kThreads = 416;                                  // 13 warps
+constexpr int kDecWarps = 8;                                   // warps that stream decode pages
 constexpr int kDecStages = 3;                                  // per-warp page ring
 constexpr int kPageHalfBytes = kPage * 128;                    // 16 rows x 64 bf16
 constexpr int kDecStageBytes = 2 * 2 * kPageHalfBytes;         // K+V page-head, d=128
-constexpr int kSmemStages = kWarps * kDecStages * kDecStageBytes;  // 192 KB
+constexpr int kSmemStages = kDecWarps * kDecStages * kDecStageBytes;  // 192 KB
 constexpr int kSmemDecQ = kSmemStages;                         // 16 x 128 bf16
 constexpr int kSmemStash = kSmemDecQ + 2 * kPageHalfBytes;     // new K/V (2 x 128 bf16)
 constexpr int kSmemBars = kSmemStash + 512;                   // mbarriers, initialised once
 constexpr int kDecBar0 = 0;                                    // [warp][stage] decode rings
-constexpr int kPfBar0 = kWarps * kDecStages;                   // prefill ring
-constexpr int kSmemBytes = kSmemBars + 256;
+constexpr int kSmemBytes = kSmemBars + 512;
 constexpr int kSmemAlloc = kSmemBytes + 1024;                  // + alignment slack
-// prefill layout inside the stage region
-constexpr int kPfBlockKeys = 64;
-constexpr int kPfStages = 3;
-constexpr int kPfQBytes = 2 * kTileRows * 128;                 // 128 rows x 128 bf16
-constexpr int kPfStageBytes = 2 * 2 * kPfBlockKeys * 128;      // K+V, 64 keys x 128
-static_assert(kPfQBytes + kPfStages * kPfStageBytes <= kSmemStages, "prefill smem");
-static_assert(kWarps * 16 * 128 * 4 + 2 * kWarps * 16 * 4 <= kSmemStages, "merge scratch");
+static_assert(kDecWarps * 16 * 128 * 4 + 2 * kDecWarps * 16 * 4 <= kSmemStages, "merge scratch");
 static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s bound on any wait
@@ -157,6 +150,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+// 2^x with the MUFU approximation (flushes subnormals; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Round a double to bf16 in ONE rounding (ties to even): round to float with
 // round-to-odd (truncate, then force the last bit to 1 when inexact), then
@@ -309,28 +308,130 @@ __device__ void run_append(const KParams& P, const int* it, int* s_abort) {
 }
 
 // ----------------------------------------------------------------------------
-// PREFILL tile: up to 128 rows (token-major, q-head-in-group minor) of one
-// chunk for one kv head, causal over history pages + the chunk.
+// tcgen05 / TMEM helpers (inline PTX)
 // ----------------------------------------------------------------------------
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, M = 128.
+__host__ __device__ constexpr uint32_t umma_idesc(int n, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Phase counters of the prefill pipeline, one set per thread, carried across
+// work items (each role only touches the counters of the barriers it waits on).
+struct PfPhase {
+    int kfill[2], vfill[2];   // producer: loads issued into each K / V stage
+    int kuse[2], vuse[2];     // MMA issuer: loads consumed from each stage
+    int pfull;                // MMA issuer: P tiles consumed
+    int suse[2], pvdone;      // softmax: S tiles consumed, P.V products completed
+    int vseen[2];             // softmax: V loads into each stage (for the last-block clean-up)
+};
+
+// ----------------------------------------------------------------------------
+// PREFILL tile on the 5th-generation tensor cores: up to 128 query rows
+// (token-major, q-head-in-group minor) of one chunk for one kv head, causal
+// over every history page and the chunk ("Sarathi-Serve 完全拆解",
+// §"分块不等于截断上下文").
+//   S = Q K^T per 128-key block: tcgen05.mma (M 128, N 128, K 16 steps), fp32
+//       accumulator in TMEM, double buffered;
+//   softmax: thread r of warps 0-3 owns query row r (= TMEM lane r); row max,
+//       lazy rescale of O (only when the max grows by more than 2^8), bf16 P
+//       written to shared memory in the 128-byte-swizzled K-major layout;
+//   O += P V: tcgen05.mma with V read as an MN-major operand straight from the
+//       TMA-loaded pages; O stays in TMEM until the end of the tile.
+// Roles: warps 8-11 are four TMA streams (K and V rings, 2 stages each, one
+// 64-column half per stream: one issuing thread sustains only ~14 boxes/us),
+// warp 12 lane 0 issues the MMAs, warps 0-7 run the softmax and the epilogue: warps w
+// and w+4 share TMEM lane quadrant w (rows 32w..32w+31) and split each block's
+// 128 key columns, exchanging row maxima through a pair barrier.
+// ----------------------------------------------------------------------------
+constexpr int kTcKeys = 128;                     // keys per block
+constexpr int kTcQ = 0;                          // Q tile: [d/64][128 rows][128 B]
+constexpr int kTcK = 32768;                      // K ring: 2 x [d/64][128 keys][128 B]
+constexpr int kTcV = kTcK + 2 * 32768;           // V ring: same
+constexpr int kTcP = kTcV + 2 * 32768;           // P tile: [2][128 rows][128 B]
+static_assert(kTcP + 32768 <= kSmemStages, "tcgen05 prefill smem");
+constexpr uint32_t kTmemCols = 512;              // S0 [0,128) S1 [128,256) O [256,256+d)
+constexpr uint32_t kTmemO = 256;
+// barrier indices (after the decode rings)
+constexpr int kBarKFull = kDecWarps * kDecStages;  // 2
+constexpr int kBarKEmpty = kBarKFull + 2;        // 2
+constexpr int kBarVFull = kBarKEmpty + 2;        // 2
+constexpr int kBarVEmpty = kBarVFull + 2;        // 2
+constexpr int kBarSFull = kBarVEmpty + 2;        // 2
+constexpr int kBarPFull = kBarSFull + 2;         // 1 (256 arrivals)
+constexpr int kBarPvDone = kBarPFull + 1;        // 1
+constexpr int kBarDrain = kBarPvDone + 1;        // 1
+constexpr int kNumBars = kBarDrain + 1;
+
 template <int D>
 __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUtensorMap* tmV, const int* it,
-                            uint8_t* smem, int* s_abort, uint32_t& phase) {
+                            uint8_t* smem, int* s_abort, PfPhase& ph, uint32_t tmem) {
     constexpr int HALVES = D / 64;
     constexpr int HALF = D / 2;
-    constexpr int KBLK_HALF = kPfBlockKeys * 128;  // one column half of a 64-key block
-    constexpr int K_BYTES = HALVES * KBLK_HALF;
-    constexpr int STAGE = 2 * K_BYTES;
+    constexpr int BLK_HALF = kTcKeys * 128;      // one 64-column half of a 128-key block
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = it[kS], g = it[kG], t0 = it[kStart], cnt = it[kCount];
     const Row R = row_geom(P, s);
     const int G = P.group;
     const int rows_valid = cnt * G;
-    const int kv_hi = R.h + t0 + cnt;                 // keys [0, kv_hi) are visible to some row
-    const int nblk = (kv_hi + kPfBlockKeys - 1) / kPfBlockKeys;
+    const int kv_hi = R.h + t0 + cnt;            // keys [0, kv_hi) are visible to some row
+    const int nblk = (kv_hi + kTcKeys - 1) / kTcKeys;
     const int pages_hi = (kv_hi + kPage - 1) / kPage;
-    uint8_t* qtile = smem;
-    uint8_t* stages = smem + kPfQBytes;
-    const uint32_t bars = smem_u32(smem + kSmemBars) + 8 * kPfBar0;
+    uint8_t* qtile = smem + kTcQ;
+    const uint32_t bars = smem_u32(smem + kSmemBars);
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
     // 1. the chunk's K/V must be in the pages: wait for this request's APPENDs
     if (tid == 0) {
@@ -348,186 +449,249 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         }
         fence_proxy_async_global();
     }
-    __syncthreads();
-    if (*(volatile int*)s_abort) return;
-
-    auto issue = [&](int b) {
-        const int stg = b % kPfStages;
-        uint8_t* kb = stages + stg * STAGE;
-        const uint32_t bar = bars + 8 * stg;
-        int npg = 0;
-        for (int i = 0; i < kPfBlockKeys / kPage; ++i) npg += (b * 4 + i < pages_hi);
-        mbar_expect_tx(bar, npg * HALVES * kPageHalfBytes * 2);
-        for (int i = 0; i < kPfBlockKeys / kPage; ++i) {
-            const int lp = b * 4 + i;
-            if (lp >= pages_hi) break;
-            const int page = page_id(P, R, lp, s_abort);
-            const int y = (page * P.Hkv + g) * kPage;
-            for (int hf = 0; hf < HALVES; ++hf) {
-                tma_load_2d(smem_u32(kb + hf * KBLK_HALF + i * kPageHalfBytes), tmK, hf * 64, y, bar);
-                tma_load_2d(smem_u32(kb + K_BYTES + hf * KBLK_HALF + i * kPageHalfBytes), tmV, hf * 64, y, bar);
-            }
-        }
-    };
-    if (tid == 0)
-        for (int b = 0; b < nblk && b < kPfStages; ++b) issue(b);
-
-    // 2. Q rows, RoPE'd in fp32 at their absolute positions, into the tile
-    for (int i = tid; i < kTileRows * HALF; i += kThreads) {
-        const int row = i / HALF, j = i % HALF;
-        float y0 = 0.f, y1 = 0.f;
+    // 2. Q rows, RoPE'd in fp32 at their absolute positions, into the swizzled
+    //    tile; one thread rotates 8 consecutive pairs (two 16-byte chunks)
+    for (int i = tid; i < kTileRows * (HALF / 8); i += kThreads) {
+        const int row = i / (HALF / 8), c = i % (HALF / 8);
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if (row < rows_valid) {
             const int t = t0 + row / G;
             const int hq = g * G + row % G;
             const int pos = R.h + t;
             const __nv_bfloat16* qr = P.q + ((size_t)(R.qo0 + t) * P.Hq + hq) * D;
-            const float x0 = __bfloat162float(qr[j]), x1 = __bfloat162float(qr[j + HALF]);
-            const double2 cs = P.rope[(size_t)pos * HALF + j];
-            const float c = (float)cs.x, sn = (float)cs.y;
-            y0 = x0 * c - x1 * sn;
-            y1 = x1 * c + x0 * sn;
+            const uint4 a = __ldg(reinterpret_cast<const uint4*>(qr) + c);
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(qr + HALF) + c);
+            const __nv_bfloat16* x0 = reinterpret_cast<const __nv_bfloat16*>(&a);
+            const __nv_bfloat16* x1 = reinterpret_cast<const __nv_bfloat16*>(&b);
+            const double2* cs = P.rope + (size_t)pos * HALF + c * 8;
+            uint32_t ylo[4], yhi[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const double2 c0 = cs[e], c1 = cs[e + 1];
+                const float a0 = __bfloat162float(x0[e]), a1 = __bfloat162float(x0[e + 1]);
+                const float b0 = __bfloat162float(x1[e]), b1 = __bfloat162float(x1[e + 1]);
+                ylo[e >> 1] = pack_bf16(a0 * (float)c0.x - b0 * (float)c0.y, a1 * (float)c1.x - b1 * (float)c1.y);
+                yhi[e >> 1] = pack_bf16(b0 * (float)c0.x + a0 * (float)c0.y, b1 * (float)c1.x + a1 * (float)c1.y);
+            }
+            lo = make_uint4(ylo[0], ylo[1], ylo[2], ylo[3]);
+            hi = make_uint4(yhi[0], yhi[1], yhi[2], yhi[3]);
         }
-        *reinterpret_cast<__nv_bfloat16*>(qtile + sw128_off(kTileRows, row, j)) = __float2bfloat16_rn(y0);
-        *reinterpret_cast<__nv_bfloat16*>(qtile + sw128_off(kTileRows, row, j + HALF)) = __float2bfloat16_rn(y1);
+        *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c)) = lo;
+        *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c + HALF / 8)) = hi;
     }
+    fence_proxy_async_shared();  // Q is read by the tensor cores (async proxy)
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    if (*(volatile int*)s_abort) return;
 
-    const int wrow0 = warp * 16;
-    const bool active = wrow0 < rows_valid;
-    const int mi = lane >> 3;
-    uint32_t qa[D / 16][4];
-    {
-        const int row = wrow0 + (mi & 1) * 8 + (lane & 7);
+    if (warp >= 8 && warp < 12) {
+        // ---------------- TMA producers: warp 8+2v+hf loads column half hf of ring v ----------------
+        const int stream = warp - 8;
+        const bool is_v = stream >= 2;
+        const int hf = stream & 1;
+        if (lane == 0 && hf < HALVES) {
+            const CUtensorMap* map = is_v ? tmV : tmK;
+            const int full0 = is_v ? kBarVFull : kBarKFull;
+            const int empty0 = is_v ? kBarVEmpty : kBarKEmpty;
+            int* fill = is_v ? ph.vfill : ph.kfill;
+            uint8_t* ring = smem + (is_v ? kTcV : kTcK) + hf * BLK_HALF;
+            const int32_t* kvi = P.plan + P.off_kvi + R.kvp0;
+            int ids[8], nxt[8];
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-            ldsm_x4(smem_u32(qtile + sw128_chunk(kTileRows, row, 2 * kk + (mi >> 1))), qa[kk][0], qa[kk][1],
-                    qa[kk][2], qa[kk][3]);
-    }
-    // absolute positions of this thread's two rows (invalid rows mimic the last)
-    const int rA = wrow0 + (lane >> 2), rB = rA + 8;
-    const int posA = R.h + t0 + (rA < rows_valid ? rA / G : cnt - 1);
-    const int posB = R.h + t0 + (rB < rows_valid ? rB / G : cnt - 1);
-    const int pos_min = R.h + t0 + wrow0 / G;
-    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
-    float o[D / 8][4];
+            for (int i = 0; i < 8; ++i) ids[i] = i < pages_hi ? kvi[i] : 0;
+            for (int j = 0; j < nblk; ++j) {
+                const int st = j & 1;
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-
-    for (int b = 0; b < nblk; ++b) {
-        const int stg = b % kPfStages;
-        mbar_wait_bounded(P, bars + 8 * stg, (phase >> stg) & 1u, s_abort, b, it);
-        phase ^= 1u << stg;
-        uint8_t* kb = stages + stg * STAGE;
-        uint8_t* vb = kb + K_BYTES;
-        const int key0 = b * kPfBlockKeys;
-        if (key0 + kPfBlockKeys > kv_hi) {
-            // keys past kv_hi hold stale bytes: zero them so 0-weight x V stays 0
-            const int first = kv_hi - key0;
-            const int nbytes = (kPfBlockKeys - first) * 128;
-            for (int hf = 0; hf < 2 * HALVES; ++hf) {
-                uint8_t* base = kb + hf * KBLK_HALF + first * 128;
-                for (int i = tid * 16; i < nbytes; i += kThreads * 16)
-                    *reinterpret_cast<uint4*>(base + i) = make_uint4(0, 0, 0, 0);
-            }
-            __syncthreads();
-        }
-        if (active) {
-            float sc[8][4];
+                for (int i = 0; i < 8; ++i) nxt[i] = (j + 1) * 8 + i < pages_hi ? kvi[(j + 1) * 8 + i] : 0;
+                int npg = 0;
+                for (int i = 0; i < kTcKeys / kPage; ++i) npg += (j * 8 + i < pages_hi);
+                uint8_t* dstb = ring + st * 32768;
+                if (fill[st] > 0)
+                    mbar_wait_bounded(P, bar(empty0 + st), (fill[st] - 1) & 1, s_abort, (is_v ? 2000 : 1000) + j, it);
+                mbar_expect_tx(bar(full0 + st), (uint32_t)npg * kPageHalfBytes);
 #pragma unroll
-            for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-                for (int np2 = 0; np2 < 4; ++np2) {
-                    const int key = np2 * 16 + (mi >> 1) * 8 + (lane & 7);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(smem_u32(kb + sw128_chunk(kPfBlockKeys, key, 2 * kk + (mi & 1))), b0, b1, b2, b3);
-                    mma_bf16(sc[2 * np2], qa[kk], b0, b1);
-                    mma_bf16(sc[2 * np2 + 1], qa[kk], b2, b3);
-                }
-            }
-            const bool need_mask = key0 + kPfBlockKeys - 1 > pos_min;
-            float mxA = -INFINITY, mxB = -INFINITY;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float v = sc[n][e] * P.scale_log2;
-                    if (need_mask) {
-                        const int key = key0 + n * 8 + 2 * (lane & 3) + (e & 1);
-                        if (key > (e < 2 ? posA : posB)) v = -INFINITY;
+                for (int i = 0; i < kTcKeys / kPage; ++i) {
+                    if (j * 8 + i >= pages_hi) break;
+                    int page = ids[i];
+                    if (page < 0 || page >= P.num_pages) {
+                        raise_error(P, kErrBounds, page, s_abort);
+                        page = 0;
                     }
-                    sc[n][e] = v;
+                    tma_load_2d(smem_u32(dstb + i * kPageHalfBytes), map, hf * 64, (page * P.Hkv + g) * kPage,
+                                bar(full0 + st));
                 }
-                mxA = fmaxf(mxA, fmaxf(sc[n][0], sc[n][1]));
-                mxB = fmaxf(mxB, fmaxf(sc[n][2], sc[n][3]));
-            }
-            mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
-            mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
-            mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
-            mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
-            const float nmA = fmaxf(mA, mxA), nmB = fmaxf(mB, mxB);
-            // a row sees no key of a block only when it already saw block 0
-            const float baseA = nmA == -INFINITY ? 0.f : nmA;
-            const float baseB = nmB == -INFINITY ? 0.f : nmB;
-            const float alA = exp2f(mA - baseA), alB = exp2f(mB - baseB);
-            mA = nmA;
-            mB = nmB;
-            float sumA = 0.f, sumB = 0.f;
-            uint32_t pa[4][4];
+                ++fill[st];
 #pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                const float p0 = exp2f(sc[n][0] - baseA), p1 = exp2f(sc[n][1] - baseA);
-                const float p2 = exp2f(sc[n][2] - baseB), p3 = exp2f(sc[n][3] - baseB);
-                sumA += p0 + p1;
-                sumB += p2 + p3;
-                pa[n >> 1][(n & 1) * 2 + 0] = pack_bf16(p0, p1);
-                pa[n >> 1][(n & 1) * 2 + 1] = pack_bf16(p2, p3);
-            }
-            lA = lA * alA + sumA;
-            lB = lB * alB + sumB;
-#pragma unroll
-            for (int n = 0; n < D / 8; ++n) {
-                o[n][0] *= alA;
-                o[n][1] *= alA;
-                o[n][2] *= alB;
-                o[n][3] *= alB;
-            }
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-                for (int np2 = 0; np2 < D / 16; ++np2) {
-                    const int key = ks * 16 + (mi & 1) * 8 + (lane & 7);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(smem_u32(vb + sw128_chunk(kPfBlockKeys, key, 2 * np2 + (mi >> 1))), b0, b1, b2, b3);
-                    mma_bf16(o[2 * np2], pa[ks], b0, b1);
-                    mma_bf16(o[2 * np2 + 1], pa[ks], b2, b3);
-                }
+                for (int i = 0; i < 8; ++i) ids[i] = nxt[i];
             }
         }
-        __syncthreads();
-        if (tid == 0 && b + kPfStages < nblk) {
+    } else if (warp == 12) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = umma_idesc(kTcKeys, false);
+            constexpr uint32_t idesc_o = umma_idesc(D, true);
+            const uint32_t q_addr = smem_u32(qtile);
+            auto issue_qk = [&](int j) {
+                const int st = j & 1;
+                mbar_wait_bounded(P, bar(kBarKFull + st), ph.kuse[st] & 1, s_abort, 3000 + j, it);
+                ++ph.kuse[st];
+                tc_fence_after();
+                const uint32_t k_addr = smem_u32(smem + kTcK + st * 32768);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)((kk >> 2) * kTileRows * 128 + (kk & 3) * 32);
+                    const uint32_t koff = (uint32_t)((kk >> 2) * BLK_HALF + (kk & 3) * 32);
+                    umma_f16(tmem + (uint32_t)(st * kTcKeys), umma_desc(q_addr + off, 16, 1024),
+                             umma_desc(k_addr + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(kBarKEmpty + st));
+                umma_commit(bar(kBarSFull + st));
+            };
+            issue_qk(0);
+            if (nblk > 1) issue_qk(1);
+            const uint32_t p_addr = smem_u32(smem + kTcP);
+            for (int j = 0; j < nblk; ++j) {
+                const int st = j & 1;
+                mbar_wait_bounded(P, bar(kBarPFull), ph.pfull & 1, s_abort, 4000 + j, it);
+                ++ph.pfull;
+                mbar_wait_bounded(P, bar(kBarVFull + st), ph.vuse[st] & 1, s_abort, 5000 + j, it);
+                ++ph.vuse[st];
+                tc_fence_after();
+                const uint32_t v_addr = smem_u32(smem + kTcV + st * 32768);
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                    // A = P (K-major over keys); B = V (MN-major: d contiguous, keys as rows)
+                    const uint32_t poff = (uint32_t)((kk >> 2) * kTileRows * 128 + (kk & 3) * 32);
+                    const uint32_t voff = (uint32_t)(kk * 16 * 128);
+                    umma_f16(tmem + kTmemO, umma_desc(p_addr + poff, 16, 1024),
+                             umma_desc(v_addr + voff, BLK_HALF, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(bar(kBarVEmpty + st));
+                umma_commit(bar(kBarPvDone));
+                if (j + 2 < nblk) issue_qk(j + 2);
+            }
+        }
+    } else if (warp < 8) {
+        // ---------------- softmax + epilogue (warps 0-7) ----------------
+        const int quad = warp & 3, ch = warp >> 2;   // lane quadrant, key-column half
+        const int r = quad * 32 + lane;              // query row = TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const int pos_r = R.h + t0 + (r < rows_valid ? r / G : cnt - 1);
+        const float sl2 = P.scale_log2;
+        const int pair_bar = 1 + quad;
+        float* red = reinterpret_cast<float*>(smem + kSmemDecQ);  // [2 parity][2 half][128] maxima, [2][128] sums
+        float m_run = -INFINITY, l_run = 0.f;
+        uint8_t* prow = smem + kTcP + ch * kTileRows * 128;
+        for (int j = 0; j < nblk; ++j) {
+            const int st = j & 1;
+            const int kb0 = j * kTcKeys + ch * 64;   // first key of this thread's 64 columns
+            mbar_wait_bounded(P, bar(kBarSFull + st), ph.suse[st] & 1, s_abort, 6000 + j, it);
+            ++ph.suse[st];
+            tc_fence_after();
+            float v[64];
+            {
+                float* v0 = v;
+                float* v1 = v + 32;
+                tmem_ld32(lane_base + (uint32_t)(st * kTcKeys + ch * 64), *reinterpret_cast<float(*)[32]>(v0));
+                tmem_ld32(lane_base + (uint32_t)(st * kTcKeys + ch * 64 + 32), *reinterpret_cast<float(*)[32]>(v1));
+            }
+            float mx = -INFINITY;
+            if (kb0 + 63 > pos_r) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    v[e] = kb0 + e <= pos_r ? v[e] * sl2 : -INFINITY;
+                    mx = fmaxf(mx, v[e]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    v[e] *= sl2;
+                    mx = fmaxf(mx, v[e]);
+                }
+            }
+            red[((j & 1) * 2 + ch) * 128 + r] = mx;
+            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+            mx = fmaxf(mx, red[((j & 1) * 2 + (ch ^ 1)) * 128 + r]);
+            // lazy rescale: move the exponent base only when the max grows by > 2^8
+            const bool grow = mx > m_run + 8.f;
+            const float m_new = grow ? mx : m_run;
+            const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
+            // P and O are in use until the previous block's P.V has completed
+            if (j > 0) {
+                mbar_wait_bounded(P, bar(kBarPvDone), ph.pvdone & 1, s_abort, 7000 + j, it);
+                ++ph.pvdone;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 64; ++c) {
+                        float o[32];
+                        const uint32_t oc = lane_base + kTmemO + (uint32_t)(ch * (D / 2) + c * 32);
+                        tmem_ld32(oc, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st32(oc, o);
+                    }
+                }
+            }
+            l_run *= alpha;
+            m_run = m_new;
+            // P = 2^(s - m) in bf16 into this half of the K-major swizzled P tile
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const float p0 = ex2_approx(v[8 * q + e] - m_run);
+                    const float p1 = ex2_approx(v[8 * q + e + 1] - m_run);
+                    sum += p0 + p1;
+                    pk[e >> 1] = pack_bf16(p0, p1);
+                }
+                *reinterpret_cast<uint4*>(prow + r * 128 + ((q ^ (r & 7)) << 4)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            l_run += sum;
+            // last block: V rows past kv_hi hold stale bytes; zero them so 0 x V stays 0
+            const int vs = ph.vseen[st]++;
+            const int key0 = j * kTcKeys;
+            if (j == nblk - 1 && key0 + kTcKeys > kv_hi) {
+                mbar_wait_bounded(P, bar(kBarVFull + st), vs & 1, s_abort, 8000 + j, it);
+                uint8_t* vb = smem + kTcV + st * 32768;
+                const int first = kv_hi - key0;
+                for (int hf = 0; hf < HALVES; ++hf)
+                    for (int i = first * 128 + tid * 16; i < kTcKeys * 128; i += 256 * 16)
+                        *reinterpret_cast<uint4*>(vb + hf * BLK_HALF + i) = make_uint4(0, 0, 0, 0);
+            }
             fence_proxy_async_shared();
-            issue(b + kPfStages);
+            tc_fence_before();
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull)) : "memory");
         }
-    }
-    if (!active) return;
-    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
-    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
-    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
-    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
-    const float invA = 1.f / lA, invB = 1.f / lB;
-    if (rA < rows_valid) {
-        __nv_bfloat16* dst = P.out + ((size_t)(R.qo0 + t0 + rA / G) * P.Hq + g * G + rA % G) * D;
+        // epilogue: O / l -> bf16; each warp of the pair writes half of the columns
+        mbar_wait_bounded(P, bar(kBarPvDone), ph.pvdone & 1, s_abort, 9000, it);
+        ++ph.pvdone;
+        tc_fence_after();
+        red[512 + ch * 128 + r] = l_run;
+        asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+        const float inv = 1.f / (l_run + red[512 + (ch ^ 1) * 128 + r]);
+        __nv_bfloat16* dst =
+            r < rows_valid ? P.out + ((size_t)(R.qo0 + t0 + r / G) * P.Hq + g * G + r % G) * D + ch * (D / 2)
+                           : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+            float o[32];
+            tmem_ld32(lane_base + kTmemO + (uint32_t)(ch * (D / 2) + c * 32), o);
+            if (dst) {
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n)
-            *reinterpret_cast<uint32_t*>(dst + n * 8 + 2 * (lane & 3)) = pack_bf16(o[n][0] * invA, o[n][1] * invA);
-    }
-    if (rB < rows_valid) {
-        __nv_bfloat16* dst = P.out + ((size_t)(R.qo0 + t0 + rB / G) * P.Hq + g * G + rB % G) * D;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n)
-            *reinterpret_cast<uint32_t*>(dst + n * 8 + 2 * (lane & 3)) = pack_bf16(o[n][2] * invB, o[n][3] * invB);
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) =
+                        make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                   pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                   pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                   pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+            }
+        }
+        tc_fence_before();
     }
 }
 
@@ -552,11 +716,16 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     uint16_t* stash = reinterpret_cast<uint16_t*>(smem + kSmemStash);
     uint8_t* wst = smem + warp * kDecStages * kDecStageBytes;
     const uint32_t wbar = smem_u32(smem + kSmemBars) + 8 * (kDecBar0 + kDecStages * warp);
-    const int my_pages = pc > warp ? (pc - warp + kWarps - 1) / kWarps : 0;
+    const int my_pages = (warp < kDecWarps && pc > warp) ? (pc - warp + kDecWarps - 1) / kDecWarps : 0;
 
-    auto issue = [&](int k) {
-        const int lp = p0 + warp + kWarps * k;
-        const int page = page_id(P, R, lp, s_abort);
+    // lane l holds the page id of this warp's page (32*window + l), so that
+    // lane 0 never waits on a global load right before a TMA issue
+    auto load_ids = [&](int base) -> int {
+        const int k = base + lane;
+        return k < my_pages ? page_id(P, R, p0 + warp + kDecWarps * k, s_abort) : 0;
+    };
+    int ids = load_ids(0);
+    auto issue = [&](int k, int page) {
         const int stg = k % kDecStages;
         const uint32_t dst = smem_u32(wst + stg * kDecStageBytes);
         const uint32_t bar = wbar + 8 * stg;
@@ -567,8 +736,10 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
             tma_load_2d(dst + KPAGE + hf * kPageHalfBytes, tmV, hf * 64, y, bar);
         }
     };
-    if (lane == 0)
-        for (int k = 0; k < my_pages && k < kDecStages; ++k) issue(k);
+    for (int k = 0; k < my_pages && k < kDecStages; ++k) {
+        const int pid = __shfl_sync(0xffffffffu, ids, k);
+        if (lane == 0) issue(k, pid);
+    }
 
     // Q rows of the group, RoPE'd in fp32, rows >= G zero
     for (int i = tid; i < 16 * HALF; i += kThreads) {
@@ -632,7 +803,7 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         phase ^= 1u << stg;
         uint8_t* kb = wst + stg * kDecStageBytes;
         uint8_t* vb = kb + KPAGE;
-        const int lp = p0 + warp + kWarps * k;
+        const int lp = p0 + warp + kDecWarps * k;
         const int key0 = lp * kPage;
         if (lp == R.np - 1) {
             // last page: put the new token in its slot, zero the slots past it
@@ -700,9 +871,14 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
             mma_bf16(o[2 * np2 + 1], pa, b2, b3);
         }
         __syncwarp();
-        if (lane == 0 && k + kDecStages < my_pages) {
-            fence_proxy_async_shared();
-            issue(k + kDecStages);
+        const int kn = k + kDecStages;
+        if (kn < my_pages) {
+            if ((kn & 31) == 0) ids = load_ids(kn);
+            const int pid = __shfl_sync(0xffffffffu, ids, kn & 31);
+            if (lane == 0) {
+                fence_proxy_async_shared();
+                issue(kn, pid);
+            }
         }
     }
     lA += __shfl_xor_sync(0xffffffffu, lA, 1);
@@ -713,9 +889,9 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     // in-CTA merge of the warps' (m, l, o) through the (now idle) stage memory
     __syncthreads();
     float* so = reinterpret_cast<float*>(smem);                 // [warp][16][D]
-    float* sm = so + kWarps * 16 * D;                           // [warp][16]
-    float* sl = sm + kWarps * 16;                               // [warp][16]
-    {
+    float* sm = so + kDecWarps * 16 * D;                        // [warp][16]
+    float* sl = sm + kDecWarps * 16;                            // [warp][16]
+    if (warp < kDecWarps) {
         const int rA = lane >> 2, rB = rA + 8;
         float* ow = so + warp * 16 * D;
 #pragma unroll
@@ -738,9 +914,9 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     for (int i = tid; i < G * D; i += kThreads) {
         const int row = i / D, col = i % D;
         float M = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm[w * 16 + row]);
+        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm[w * 16 + row]);
         float L = 0.f, acc = 0.f;
-        for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < kDecWarps; ++w) {
             const float mw = sm[w * 16 + row];
             if (mw == -INFINITY) continue;
             const float sc = exp2f(mw - M);
@@ -798,15 +974,34 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
     __shared__ int s_item[kItemInts];
     __shared__ int s_abort;
     __shared__ int s_flag;
+    __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x;
+    const uint32_t bars = smem_u32(smem + kSmemBars);
     if (tid == 0) {
         s_abort = 0;
-        const uint32_t bars = smem_u32(smem + kSmemBars);
-        for (int i = 0; i < kPfBar0 + kPfStages; ++i) mbar_init(bars + 8 * i, 1);
+        for (int i = 0; i < kNumBars; ++i) {
+            uint32_t count = 1;
+            if (i == kBarPFull) count = 256;
+            if (i >= kBarKFull && i < kBarKFull + 2) count = D / 64;
+            if (i >= kBarVFull && i < kBarVFull + 2) count = D / 64;
+            mbar_init(bars + 8 * i, count);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // completed-phase parity of each ring stage, carried across work items
-    uint32_t pf_phase = 0, dec_phase = 0;
+    if (tid < 32) {
+        // one CTA per SM: take the whole tensor memory for the prefill tiles
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    // completed-phase parities / counters, carried across work items
+    uint32_t dec_phase = 0;
+    PfPhase pf_phase = {};
     for (;;) {
         if (tid == 0) {
             const int idx = atomicAdd(&P.ws_int[0], 1);
@@ -833,15 +1028,30 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         if (it[0] == kAppend)
             run_append<D>(P, it, &s_abort);
         else if (it[0] == kPrefill)
-            run_prefill<D>(P, &tmK, &tmV, it, smem, &s_abort, pf_phase);
+            run_prefill<D>(P, &tmK, &tmV, it, smem, &s_abort, pf_phase, tmem);
         else
             run_decode<D>(P, &tmK, &tmV, it, smem, &s_abort, &s_flag, dec_phase);
         // shared memory written through the generic proxy this item (tiles,
         // scratch, patched rows) is next overwritten by TMA
         fence_proxy_async_shared();
+        tc_fence_before();
         __syncthreads();
-        if (s_abort) return;  // the error word is set; the workspace must be re-zeroed
+        tc_fence_after();
+        if (s_abort) break;  // the error word is set; the workspace must be re-zeroed
     }
+    // no tensor-core work may be in flight when the tensor memory is released
+    if (tid == 12 * 32) {
+        umma_commit(bars + 8 * kBarDrain);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(bars + 8 * kBarDrain, 0))
+            if (globaltimer() - t0 > kWaitNs) break;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid < 32)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    if (s_abort) return;
     // the last CTA out leaves the counters at zero for the next launch
     if (tid == 0) {
         __threadfence();

@@ -68,7 +68,7 @@ int32_t validate_requests(const sarathi_request* reqs, int32_t n_reqs) {
 }
 
 // Rough per-SM speeds used only to order the work list (longest first).
-constexpr double kPrefillFlopPerNs = 3000.0;  // mma tile throughput per SM
+constexpr double kPrefillFlopPerNs = 5000.0;  // tensor-core tile throughput per SM
 constexpr double kDecodeBytesPerNs = 40.0;    // HBM share per SM
 
 }  // namespace
@@ -181,7 +181,7 @@ extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int
         double ns_est;
         std::array<int32_t, kItemInts> it;
     };
-    std::vector<Timed> attn;
+    std::vector<Timed> tiles, decs;
     const int tpt = tokens_per_tile(group);
     // decode split size from the total decode pages and the SM count
     int64_t dec_page_heads = 0;
@@ -203,12 +203,14 @@ extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int
                 ++cnt;
             }
             aux[s] = cnt;
+            // one (request, kv head) at a time, costliest tile first: the tiles
+            // that read the same history pages run side by side and share L2
             for (int g = 0; g < Hkv; ++g)
-                for (int32_t t0 = 0; t0 < n; t0 += tpt) {
+                for (int32_t t0 = (n - 1) / tpt * tpt; t0 >= 0; t0 -= tpt) {
                     int32_t c = std::min(tpt, n - t0);
                     double keys = (double)h + t0 + c;
                     double flops = 4.0 * d * kTileRows * keys;
-                    attn.push_back({flops / kPrefillFlopPerNs, {kPrefill, s, g, t0, c, -1, -1, 0}});
+                    tiles.push_back({flops / kPrefillFlopPerNs, {kPrefill, s, g, t0, c, -1, -1, 0}});
                 }
         } else {
             // decode-like: split the pages; the item holding the last page also
@@ -223,13 +225,36 @@ extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int
                 for (int64_t k = 0; k < nsplit; ++k) {
                     int32_t p0 = (int32_t)(k * per);
                     int32_t pc = (int32_t)std::min<int64_t>(per, np[s] - p0);
-                    attn.push_back({pc * kv_page_bytes / kDecodeBytesPerNs,
+                    decs.push_back({pc * kv_page_bytes / kDecodeBytesPerNs,
                                     {kDecode, s, g, p0, pc, first, merge, (int32_t)nsplit}});
                 }
             }
         }
     }
-    std::stable_sort(attn.begin(), attn.end(), [](const Timed& a, const Timed& b) { return a.ns_est > b.ns_est; });
+    // Longest first.  The tiles of one (request, kv head) read the same pages,
+    // so they stay contiguous: the group sorts by its costliest tile.
+    struct Keyed {
+        double key;
+        int64_t group;
+        Timed t;
+    };
+    std::vector<Keyed> keyed;
+    keyed.reserve(tiles.size() + decs.size());
+    for (size_t i = 0; i < tiles.size();) {
+        size_t e = i;
+        const int32_t s0 = tiles[i].it[kS], g0 = tiles[i].it[kG];
+        double mx = 0;
+        while (e < tiles.size() && tiles[e].it[kS] == s0 && tiles[e].it[kG] == g0) mx = std::max(mx, tiles[e++].ns_est);
+        for (; i < e; ++i) keyed.push_back({mx, (int64_t)s0 * Hkv + g0, tiles[i]});
+    }
+    for (auto& t : decs) keyed.push_back({t.ns_est, -1, t});
+    std::stable_sort(keyed.begin(), keyed.end(), [](const Keyed& a, const Keyed& b) {
+        if (a.key != b.key) return a.key > b.key;
+        return a.group < b.group;
+    });
+    std::vector<Timed> attn;
+    attn.reserve(keyed.size());
+    for (auto& k : keyed) attn.push_back(k.t);
     const int64_t n_items = (int64_t)appends.size() + (int64_t)attn.size();
 
     // ---- 4. packed layout

@@ -17,7 +17,7 @@ constexpr int kAppendTokens = 16;     // new tokens per APPEND work item
 constexpr int kTileRows = 128;        // query rows (token x head-in-group) per prefill tile
 constexpr int kMaxGroup = 16;         // q heads per kv head handled by the decode path
 constexpr int kDecodeMinSplitPages = 8;
-constexpr int kDecodeItemsPerSm = 6;  // target split-KV items per SM for the decode phase
+constexpr int kDecodeItemsPerSm = 2;  // target split-KV items per SM for the decode phase
 constexpr int kItemInts = 8;
 
 enum ItemKind : int32_t { kAppend = 0, kPrefill = 1, kDecode = 2 };

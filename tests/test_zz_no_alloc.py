@@ -33,7 +33,12 @@ def test_noalloc_refuses_batches_beyond_the_scratch_limit():
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
     import torch
     from gpu_helpers import GpuStep, assert_close, to_u16
-    gs = GpuStep(W.mistral())  # split decodes: the scratch holds merge tickets and partials
+    # a few very long decodes are split across CTAs, so the scratch holds merge
+    # tickets and partial results; the prefill chunk uses the append counters
+    shape = W.SHAPES["mistral"]
+    specs = [(W.DECODE, 0, 12000 + 37 * i, 12001 + 37 * i) for i in range(6)]
+    specs.append((W.PREFILL_RUNNING, 900, 700, 900))
+    gs = GpuStep(W._build("noalloc", shape, 256, specs, 7))
     assert gs.info.n_partials > 0 and gs.info.workspace_bytes <= (8 << 20)
     k0, v0 = gs.kc_dev.clone(), gs.vc_dev.clone()
     assert gs.run() == 0
