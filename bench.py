@@ -270,8 +270,10 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(args.warmup):
             flush.zero_()
             runner.run(q_d, k_d, v_d, kc, vc, out, plan_dev, info)
+    torch.cuda.synchronize(dev)
+    hdr = runner.workspace[:64].view(torch.int32).cpu().tolist()
     if runner.status() != 0:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError(f"device error during warm-up: workspace header {hdr[:12]}")
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -288,8 +290,10 @@ def run_ours(args, rank, world, local_rank):
         t_wall = time.perf_counter() - t_wall0
     barrier()
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    torch.cuda.synchronize(dev)
+    hdr = runner.workspace[:64].view(torch.int32).cpu().tolist()
     if runner.status() != 0:
-        raise RuntimeError("device error in the timed region")
+        raise RuntimeError(f"device error in the timed region: workspace header {hdr[:12]}")
 
     # e2e through the public API: plan on the host, pinned H2D, kernel, D2H
     h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * 2 + info.packed_ints * 4

@@ -329,6 +329,15 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Same with the A operand read from tensor memory.
+__device__ __forceinline__ void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
@@ -373,8 +382,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 struct PfPhase {
     int kfill[2], vfill[2];   // producer: loads issued into each K / V stage
     int kuse[2], vuse[2];     // MMA issuer: loads consumed from each stage
-    int pfull;                // MMA issuer: P tiles consumed
-    int suse[2], pvdone;      // softmax: S tiles consumed, P.V products completed
+    int pfull[2];             // MMA issuer: P tiles consumed from each buffer
+    int suse[2];              // softmax: S tiles consumed
+    int pvd[2];               // softmax: completions of each P.V barrier before this item
     int vseen[2];             // softmax: V loads into each stage (for the last-block clean-up)
 };
 
@@ -400,19 +410,21 @@ constexpr int kTcKeys = 128;                     // keys per block
 constexpr int kTcQ = 0;                          // Q tile: [d/64][128 rows][128 B]
 constexpr int kTcK = 32768;                      // K ring: 2 x [d/64][128 keys][128 B]
 constexpr int kTcV = kTcK + 2 * 32768;           // V ring: same
-constexpr int kTcP = kTcV + 2 * 32768;           // P tile: [2][128 rows][128 B]
-static_assert(kTcP + 32768 <= kSmemStages, "tcgen05 prefill smem");
-constexpr uint32_t kTmemCols = 512;              // S0 [0,128) S1 [128,256) O [256,256+d)
+static_assert(kTcV + 2 * 32768 <= kSmemStages, "tcgen05 prefill smem");
+// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512);
+// P (bf16, two per 32-bit column) is the A operand of O += P V, read from TMEM
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 384;
 // barrier indices (after the decode rings)
 constexpr int kBarKFull = kDecWarps * kDecStages;  // 2
 constexpr int kBarKEmpty = kBarKFull + 2;        // 2
 constexpr int kBarVFull = kBarKEmpty + 2;        // 2
 constexpr int kBarVEmpty = kBarVFull + 2;        // 2
 constexpr int kBarSFull = kBarVEmpty + 2;        // 2
-constexpr int kBarPFull = kBarSFull + 2;         // 1 (256 arrivals)
-constexpr int kBarPvDone = kBarPFull + 1;        // 1
-constexpr int kBarDrain = kBarPvDone + 1;        // 1
+constexpr int kBarPFull = kBarSFull + 2;         // 2 (one per P buffer, 256 arrivals each)
+constexpr int kBarPvDone = kBarPFull + 2;        // 2 (one per P buffer)
+constexpr int kBarDrain = kBarPvDone + 2;        // 1
 constexpr int kNumBars = kBarDrain + 1;
 
 template <int D>
@@ -550,25 +562,27 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             };
             issue_qk(0);
             if (nblk > 1) issue_qk(1);
-            const uint32_t p_addr = smem_u32(smem + kTcP);
             for (int j = 0; j < nblk; ++j) {
                 const int st = j & 1;
-                mbar_wait_bounded(P, bar(kBarPFull), ph.pfull & 1, s_abort, 4000 + j, it);
-                ++ph.pfull;
+                // one barrier per P buffer: softmax may finish block j+1 before
+                // this thread sees block j, and a single barrier would then
+                // have moved two phases
+                mbar_wait_bounded(P, bar(kBarPFull + st), ph.pfull[st] & 1, s_abort, 4000 + j, it);
+                ++ph.pfull[st];
                 mbar_wait_bounded(P, bar(kBarVFull + st), ph.vuse[st] & 1, s_abort, 5000 + j, it);
                 ++ph.vuse[st];
                 tc_fence_after();
                 const uint32_t v_addr = smem_u32(smem + kTcV + st * 32768);
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                    // A = P (K-major over keys); B = V (MN-major: d contiguous, keys as rows)
-                    const uint32_t poff = (uint32_t)((kk >> 2) * kTileRows * 128 + (kk & 3) * 32);
+                    // A = P from TMEM (16 keys = 8 columns per step); B = V (MN-major:
+                    // d contiguous, keys as rows) straight from the TMA-loaded pages
                     const uint32_t voff = (uint32_t)(kk * 16 * 128);
-                    umma_f16(tmem + kTmemO, umma_desc(p_addr + poff, 16, 1024),
-                             umma_desc(v_addr + voff, BLK_HALF, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_f16_ts(tmem + kTmemO, tmem + kTmemP + (uint32_t)(st * 64 + kk * 8),
+                                umma_desc(v_addr + voff, BLK_HALF, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(bar(kBarVEmpty + st));
-                umma_commit(bar(kBarPvDone));
+                umma_commit(bar(kBarPvDone + st));
                 if (j + 2 < nblk) issue_qk(j + 2);
             }
         }
@@ -582,7 +596,8 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         const int pair_bar = 1 + quad;
         float* red = reinterpret_cast<float*>(smem + kSmemDecQ);  // [2 parity][2 half][128] maxima, [2][128] sums
         float m_run = -INFINITY, l_run = 0.f;
-        uint8_t* prow = smem + kTcP + ch * kTileRows * 128;
+        // P.V of block k completes phase pvd[k&1] + k/2 of barrier kBarPvDone + (k&1)
+        auto pv_parity = [&](int k) { return (uint32_t)((ph.pvd[k & 1] + k / 2) & 1); };
         for (int j = 0; j < nblk; ++j) {
             const int st = j & 1;
             const int kb0 = j * kTcKeys + ch * 64;   // first key of this thread's 64 columns
@@ -617,12 +632,16 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             const bool grow = mx > m_run + 8.f;
             const float m_new = grow ? mx : m_run;
             const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
-            // P and O are in use until the previous block's P.V has completed
-            if (j > 0) {
-                mbar_wait_bounded(P, bar(kBarPvDone), ph.pvdone & 1, s_abort, 7000 + j, it);
-                ++ph.pvdone;
+            // P buffer j&1 is free once P.V of block j-2 is done; O may be
+            // rescaled only after P.V of block j-1
+            if (j >= 2) {
+                mbar_wait_bounded(P, bar(kBarPvDone + st), pv_parity(j - 2), s_abort, 7000 + j, it);
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, grow)) {
+            }
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                mbar_wait_bounded(P, bar(kBarPvDone + (st ^ 1)), pv_parity(j - 1), s_abort, 7500 + j, it);
+                tc_fence_after();
+                {
 #pragma unroll 1
                     for (int c = 0; c < D / 64; ++c) {
                         float o[32];
@@ -636,21 +655,17 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             }
             l_run *= alpha;
             m_run = m_new;
-            // P = 2^(s - m) in bf16 into this half of the K-major swizzled P tile
+            // P = 2^(s - m) in bf16, two keys per TMEM column of P buffer j&1
             float sum = 0.f;
+            float pk[32];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const float p0 = ex2_approx(v[8 * q + e] - m_run);
-                    const float p1 = ex2_approx(v[8 * q + e + 1] - m_run);
-                    sum += p0 + p1;
-                    pk[e >> 1] = pack_bf16(p0, p1);
-                }
-                *reinterpret_cast<uint4*>(prow + r * 128 + ((q ^ (r & 7)) << 4)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int e = 0; e < 64; e += 2) {
+                const float p0 = ex2_approx(v[e] - m_run);
+                const float p1 = ex2_approx(v[e + 1] - m_run);
+                sum += p0 + p1;
+                pk[e >> 1] = __uint_as_float(pack_bf16(p0, p1));
             }
+            tmem_st32(lane_base + kTmemP + (uint32_t)(st * 64 + ch * 32), pk);
             l_run += sum;
             // last block: V rows past kv_hi hold stale bytes; zero them so 0 x V stays 0
             const int vs = ph.vseen[st]++;
@@ -662,15 +677,16 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 for (int hf = 0; hf < HALVES; ++hf)
                     for (int i = first * 128 + tid * 16; i < kTcKeys * 128; i += 256 * 16)
                         *reinterpret_cast<uint4*>(vb + hf * BLK_HALF + i) = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_shared();
             }
-            fence_proxy_async_shared();
             tc_fence_before();
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull)) : "memory");
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull + st)) : "memory");
         }
         // epilogue: O / l -> bf16; each warp of the pair writes half of the columns
-        mbar_wait_bounded(P, bar(kBarPvDone), ph.pvdone & 1, s_abort, 9000, it);
-        ++ph.pvdone;
+        mbar_wait_bounded(P, bar(kBarPvDone + ((nblk - 1) & 1)), pv_parity(nblk - 1), s_abort, 9000, it);
         tc_fence_after();
+        ph.pvd[0] += (nblk + 1) / 2;
+        ph.pvd[1] += nblk / 2;
         red[512 + ch * 128 + r] = l_run;
         asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
         const float inv = 1.f / (l_run + red[512 + (ch ^ 1) * 128 + r]);
@@ -981,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         s_abort = 0;
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == kBarPFull) count = 256;
+            if (i == kBarPFull || i == kBarPFull + 1) count = 256;
             if (i >= kBarKFull && i < kBarKFull + 2) count = D / 64;
             if (i >= kBarVFull && i < kBarVFull + 2) count = D / 64;
             mbar_init(bars + 8 * i, count);

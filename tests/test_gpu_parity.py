@@ -167,3 +167,20 @@ def test_llama7b_prefill_chunk_sweep_pages_equal_one_shot(chunk):
         done += n
     assert np.array_equal(to_u16(gs.kc_dev)[pages], ref_k)
     assert np.array_equal(to_u16(gs.vc_dev)[pages], ref_v)
+
+
+def test_repeated_launches_with_long_prefill_tiles():
+    """Several launches in a row of a step whose prefill tiles run ~100 key
+    blocks (the softmax warps can then run a block ahead of the MMA issuer):
+    every launch ends without a device error and gives the same bits."""
+    gs = GpuStep(W.llama70b())
+    k0, v0 = gs.kc_dev.clone(), gs.vc_dev.clone()
+    outs = []
+    for _ in range(4):
+        gs.kc_dev.copy_(k0)
+        gs.vc_dev.copy_(v0)
+        err = gs.run()
+        assert err == 0, f"device error {err}, header {gs.last_header[:12].tolist()}"
+        outs.append(to_u16(gs.out))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
