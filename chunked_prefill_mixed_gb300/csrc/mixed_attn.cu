@@ -196,8 +196,8 @@ __device__ __forceinline__ void raise_error(const KParams& P, int code, int deta
 // Bounded wait on an mbarrier phase; returns false (and flags the CTA) on
 // timeout, recording the work item, the thread and the barrier's raw state in
 // header words 3..11 for the host to read.
-__device__ bool mbar_wait_bounded(const KParams& P, uint32_t bar, uint32_t parity, int* s_abort, int detail,
-                                  const int* it) {
+__device__ __noinline__ bool mbar_wait_slow(const KParams& P, uint32_t bar, uint32_t parity, int* s_abort,
+                                            int detail, const int* it) {
     for (int i = 0; i < 256; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
@@ -218,6 +218,11 @@ __device__ bool mbar_wait_bounded(const KParams& P, uint32_t bar, uint32_t parit
         }
     }
     return true;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(const KParams& P, uint32_t bar, uint32_t parity, int* s_abort,
+                                                  int detail, const int* it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(P, bar, parity, s_abort, detail, it);
 }
 
 struct Row {
@@ -380,12 +385,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 // Phase counters of the prefill pipeline, one set per thread, carried across
 // work items (each role only touches the counters of the barriers it waits on).
 struct PfPhase {
-    int kfill[2], vfill[2];   // producer: loads issued into each K / V stage
-    int kuse[2], vuse[2];     // MMA issuer: loads consumed from each stage
+    int kfill[3], vfill[3];   // producer: loads issued into each K / V stage
+    int kuse[2], vuse[3];     // MMA issuer: loads consumed from each stage
     int pfull[2];             // MMA issuer: P tiles consumed from each buffer
     int suse[2];              // softmax: S tiles consumed
     int pvd[2];               // softmax: completions of each P.V barrier before this item
-    int vseen[2];             // softmax: V loads into each stage (for the last-block clean-up)
+    int vseen[3];             // softmax: V loads into each stage (for the last-block clean-up)
 };
 
 // ----------------------------------------------------------------------------
@@ -409,8 +414,9 @@ struct PfPhase {
 constexpr int kTcKeys = 128;                     // keys per block
 constexpr int kTcQ = 0;                          // Q tile: [d/64][128 rows][128 B]
 constexpr int kTcK = 32768;                      // K ring: 2 x [d/64][128 keys][128 B]
-constexpr int kTcV = kTcK + 2 * 32768;           // V ring: same
-static_assert(kTcV + 2 * 32768 <= kSmemStages, "tcgen05 prefill smem");
+constexpr int kKStages = 2, kVStages = 3;        // V is needed later than K: deeper ring
+constexpr int kTcV = kTcK + kKStages * 32768;    // V ring: 3 x [d/64][128 keys][128 B]
+static_assert(kTcV + kVStages * 32768 <= kSmemStages, "tcgen05 prefill smem");
 // TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512);
 // P (bf16, two per 32-bit column) is the A operand of O += P V, read from TMEM
 constexpr uint32_t kTmemCols = 512;
@@ -419,9 +425,9 @@ constexpr uint32_t kTmemP = 384;
 // barrier indices (after the decode rings)
 constexpr int kBarKFull = kDecWarps * kDecStages;  // 2
 constexpr int kBarKEmpty = kBarKFull + 2;        // 2
-constexpr int kBarVFull = kBarKEmpty + 2;        // 2
-constexpr int kBarVEmpty = kBarVFull + 2;        // 2
-constexpr int kBarSFull = kBarVEmpty + 2;        // 2
+constexpr int kBarVFull = kBarKEmpty + 2;        // 3
+constexpr int kBarVEmpty = kBarVFull + 3;        // 3
+constexpr int kBarSFull = kBarVEmpty + 3;        // 2
 constexpr int kBarPFull = kBarSFull + 2;         // 2 (one per P buffer, 256 arrivals each)
 constexpr int kBarPvDone = kBarPFull + 2;        // 2 (one per P buffer)
 constexpr int kBarDrain = kBarPvDone + 2;        // 1
@@ -502,40 +508,36 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         const int stream = warp - 8;
         const bool is_v = stream >= 2;
         const int hf = stream & 1;
-        if (lane == 0 && hf < HALVES) {
+        if (hf < HALVES) {
+            // lanes 0-7 each issue one page's box in the same instruction
             const CUtensorMap* map = is_v ? tmV : tmK;
+            const int nst = is_v ? kVStages : kKStages;
             const int full0 = is_v ? kBarVFull : kBarKFull;
             const int empty0 = is_v ? kBarVEmpty : kBarKEmpty;
             int* fill = is_v ? ph.vfill : ph.kfill;
             uint8_t* ring = smem + (is_v ? kTcV : kTcK) + hf * BLK_HALF;
             const int32_t* kvi = P.plan + P.off_kvi + R.kvp0;
-            int ids[8], nxt[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ids[i] = i < pages_hi ? kvi[i] : 0;
+            int id = (lane < 8 && lane < pages_hi) ? kvi[lane] : 0;
             for (int j = 0; j < nblk; ++j) {
-                const int st = j & 1;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) nxt[i] = (j + 1) * 8 + i < pages_hi ? kvi[(j + 1) * 8 + i] : 0;
-                int npg = 0;
-                for (int i = 0; i < kTcKeys / kPage; ++i) npg += (j * 8 + i < pages_hi);
-                uint8_t* dstb = ring + st * 32768;
+                const int st = j % nst;
+                const int nxt = (lane < 8 && (j + 1) * 8 + lane < pages_hi) ? kvi[(j + 1) * 8 + lane] : 0;
+                const int npg = min(kTcKeys / kPage, pages_hi - j * 8);
                 if (fill[st] > 0)
                     mbar_wait_bounded(P, bar(empty0 + st), (fill[st] - 1) & 1, s_abort, (is_v ? 2000 : 1000) + j, it);
-                mbar_expect_tx(bar(full0 + st), (uint32_t)npg * kPageHalfBytes);
-#pragma unroll
-                for (int i = 0; i < kTcKeys / kPage; ++i) {
-                    if (j * 8 + i >= pages_hi) break;
-                    int page = ids[i];
+                if (lane == 0) mbar_expect_tx(bar(full0 + st), (uint32_t)npg * kPageHalfBytes);
+                __syncwarp();
+                if (lane < npg) {
+                    int page = id;
                     if (page < 0 || page >= P.num_pages) {
                         raise_error(P, kErrBounds, page, s_abort);
                         page = 0;
                     }
-                    tma_load_2d(smem_u32(dstb + i * kPageHalfBytes), map, hf * 64, (page * P.Hkv + g) * kPage,
-                                bar(full0 + st));
+                    tma_load_2d(smem_u32(ring + st * 32768 + lane * kPageHalfBytes), map, hf * 64,
+                                (page * P.Hkv + g) * kPage, bar(full0 + st));
                 }
+                __syncwarp();
                 ++fill[st];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) ids[i] = nxt[i];
+                id = nxt;
             }
         }
     } else if (warp == 12) {
@@ -543,19 +545,20 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         if (lane == 0) {
             constexpr uint32_t idesc_s = umma_idesc(kTcKeys, false);
             constexpr uint32_t idesc_o = umma_idesc(D, true);
-            const uint32_t q_addr = smem_u32(qtile);
+            const uint64_t qd = umma_desc(smem_u32(qtile), 16, 1024);
             auto issue_qk = [&](int j) {
                 const int st = j & 1;
                 mbar_wait_bounded(P, bar(kBarKFull + st), ph.kuse[st] & 1, s_abort, 3000 + j, it);
                 ++ph.kuse[st];
                 tc_fence_after();
-                const uint32_t k_addr = smem_u32(smem + kTcK + st * 32768);
+                const uint64_t kd = umma_desc(smem_u32(smem + kTcK + st * 32768), 16, 1024);
+                const uint32_t sd = tmem + (uint32_t)(st * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk >> 2) * kTileRows * 128 + (kk & 3) * 32);
-                    const uint32_t koff = (uint32_t)((kk >> 2) * BLK_HALF + (kk & 3) * 32);
-                    umma_f16(tmem + (uint32_t)(st * kTcKeys), umma_desc(q_addr + off, 16, 1024),
-                             umma_desc(k_addr + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                    // start addresses advance in 16-byte units inside the descriptors
+                    const uint64_t off = (uint64_t)(((kk >> 2) * kTileRows * 128 + (kk & 3) * 32) >> 4);
+                    const uint64_t koff = (uint64_t)(((kk >> 2) * BLK_HALF + (kk & 3) * 32) >> 4);
+                    umma_f16(sd, qd + off, kd + koff, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(kBarKEmpty + st));
                 umma_commit(bar(kBarSFull + st));
@@ -569,19 +572,20 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 // have moved two phases
                 mbar_wait_bounded(P, bar(kBarPFull + st), ph.pfull[st] & 1, s_abort, 4000 + j, it);
                 ++ph.pfull[st];
-                mbar_wait_bounded(P, bar(kBarVFull + st), ph.vuse[st] & 1, s_abort, 5000 + j, it);
-                ++ph.vuse[st];
+                const int vst = j % kVStages;
+                mbar_wait_bounded(P, bar(kBarVFull + vst), ph.vuse[vst] & 1, s_abort, 5000 + j, it);
+                ++ph.vuse[vst];
                 tc_fence_after();
-                const uint32_t v_addr = smem_u32(smem + kTcV + st * 32768);
+                const uint64_t vd = umma_desc(smem_u32(smem + kTcV + vst * 32768), BLK_HALF, 1024);
+                const uint32_t pa = tmem + kTmemP + (uint32_t)(st * 64);
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
                     // A = P from TMEM (16 keys = 8 columns per step); B = V (MN-major:
                     // d contiguous, keys as rows) straight from the TMA-loaded pages
-                    const uint32_t voff = (uint32_t)(kk * 16 * 128);
-                    umma_f16_ts(tmem + kTmemO, tmem + kTmemP + (uint32_t)(st * 64 + kk * 8),
-                                umma_desc(v_addr + voff, BLK_HALF, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_f16_ts(tmem + kTmemO, pa + (uint32_t)(kk * 8), vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                                (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(bar(kBarVEmpty + st));
+                umma_commit(bar(kBarVEmpty + vst));
                 umma_commit(bar(kBarPvDone + st));
                 if (j + 2 < nblk) issue_qk(j + 2);
             }
@@ -611,23 +615,21 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 tmem_ld32(lane_base + (uint32_t)(st * kTcKeys + ch * 64), *reinterpret_cast<float(*)[32]>(v0));
                 tmem_ld32(lane_base + (uint32_t)(st * kTcKeys + ch * 64 + 32), *reinterpret_cast<float(*)[32]>(v1));
             }
+            // raw scores here; the softmax scale (> 0) is applied in the exponent
             float mx = -INFINITY;
             if (kb0 + 63 > pos_r) {
 #pragma unroll
                 for (int e = 0; e < 64; ++e) {
-                    v[e] = kb0 + e <= pos_r ? v[e] * sl2 : -INFINITY;
+                    v[e] = kb0 + e <= pos_r ? v[e] : -INFINITY;
                     mx = fmaxf(mx, v[e]);
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    v[e] *= sl2;
-                    mx = fmaxf(mx, v[e]);
-                }
+                for (int e = 0; e < 64; ++e) mx = fmaxf(mx, v[e]);
             }
             red[((j & 1) * 2 + ch) * 128 + r] = mx;
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-            mx = fmaxf(mx, red[((j & 1) * 2 + (ch ^ 1)) * 128 + r]);
+            mx = fmaxf(mx, red[((j & 1) * 2 + (ch ^ 1)) * 128 + r]) * sl2;
             // lazy rescale: move the exponent base only when the max grows by > 2^8
             const bool grow = mx > m_run + 8.f;
             const float m_new = grow ? mx : m_run;
@@ -658,21 +660,23 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             // P = 2^(s - m) in bf16, two keys per TMEM column of P buffer j&1
             float sum = 0.f;
             float pk[32];
+            const float nm = -m_run;
 #pragma unroll
             for (int e = 0; e < 64; e += 2) {
-                const float p0 = ex2_approx(v[e] - m_run);
-                const float p1 = ex2_approx(v[e + 1] - m_run);
+                const float p0 = ex2_approx(fmaf(v[e], sl2, nm));
+                const float p1 = ex2_approx(fmaf(v[e + 1], sl2, nm));
                 sum += p0 + p1;
                 pk[e >> 1] = __uint_as_float(pack_bf16(p0, p1));
             }
             tmem_st32(lane_base + kTmemP + (uint32_t)(st * 64 + ch * 32), pk);
             l_run += sum;
             // last block: V rows past kv_hi hold stale bytes; zero them so 0 x V stays 0
-            const int vs = ph.vseen[st]++;
+            const int vst = j % kVStages;
+            const int vs = ph.vseen[vst]++;
             const int key0 = j * kTcKeys;
             if (j == nblk - 1 && key0 + kTcKeys > kv_hi) {
-                mbar_wait_bounded(P, bar(kBarVFull + st), vs & 1, s_abort, 8000 + j, it);
-                uint8_t* vb = smem + kTcV + st * 32768;
+                mbar_wait_bounded(P, bar(kBarVFull + vst), vs & 1, s_abort, 8000 + j, it);
+                uint8_t* vb = smem + kTcV + vst * 32768;
                 const int first = kv_hi - key0;
                 for (int hf = 0; hf < HALVES; ++hf)
                     for (int i = first * 128 + tid * 16; i < kTcKeys * 128; i += 256 * 16)
@@ -999,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
             uint32_t count = 1;
             if (i == kBarPFull || i == kBarPFull + 1) count = 256;
             if (i >= kBarKFull && i < kBarKFull + 2) count = D / 64;
-            if (i >= kBarVFull && i < kBarVFull + 2) count = D / 64;
+            if (i >= kBarVFull && i < kBarVFull + kVStages) count = D / 64;
             mbar_init(bars + 8 * i, count);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
