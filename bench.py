@@ -162,6 +162,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_max(values, world: int, device=None):
+    """Max over ranks of per-rank timings (all_reduce MAX); the job is as slow
+    as its slowest replica."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tokens_per_s(tokens_per_step: int, world: int, seconds_per_step: float) -> float:
+    """Whole-job throughput: every replica processes its own step's tokens."""
+    return world * tokens_per_step / seconds_per_step
+
+
 def oracle_sample_time(wl: W.Workload, meta, q, k, v, kc, vc, budget_s: float, seed: int = 0):
     """Time the oracle on a bounded sample of the step: every append plus the
     attention of random (row, head) pairs, until ~budget_s of CPU work; scale
@@ -318,12 +335,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_times.append(time.perf_counter() - t0)
     barrier()
 
-    ms_per = float(sum(ms)) / args.steps
-    e2e_s = float(np.mean(e2e_times))
-    if world > 1:
-        t = torch.tensor([ms_per, e2e_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per, e2e_s = float(t[0]), float(t[1])
+    ms_per, e2e_s = reduce_max([float(sum(ms)) / args.steps, float(np.mean(e2e_times))], world, device=dev)
     if rank != 0:
         return None
     hbm, tc, tc_sus, peak_kind = load_peaks()
@@ -336,7 +348,7 @@ def run_ours(args, rank, world, local_rank):
     else:
         achieved, peak, unit_r = alg["flop"] / sec / 1e12, tc, "TFLOP/s"
     res = {
-        "metric": METRIC, "value": world * T / sec, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": job_tokens_per_s(T, world, sec), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per, "us_per_step": ms_per * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": DESCR[args.workload], "name": args.workload, "tokens_per_step": T,
@@ -345,7 +357,7 @@ def run_ours(args, rank, world, local_rank):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json, burst)",
                      "roofline_us": max(t_hbm, t_tc) * 1e6, "algorithmic_bytes": alg["bytes"],
                      "algorithmic_flop": alg["flop"], "traffic": committed_traffic(args.workload)},
-        "e2e": {"value": world * T / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": job_tokens_per_s(T, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
                 "includes": "host plan + pinned H2D (q, k, v, plan) + kernel + D2H (out)"},
         "clocks": clk.summary(),
@@ -362,6 +374,77 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
+def run_sweep(args):
+    """Whole-prompt prefill of the 8192-token Llama-2-7B-like prompt in chunks
+    of 512 / 1024 / 2048 and in one shot (the history re-read of chunked
+    prefill), and single chunks of 128/129, 256/257, 512/513 tokens after
+    4096 tokens of history (tile quantisation).  Kernel time per step: CUDA
+    events, L2 flushed before each timed launch, median of 5."""
+    import torch
+    import chunked_prefill_mixed_gb300 as S
+    from chunked_prefill_mixed_gb300.runner import StepRunner
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    S.load()
+    sh = W.SHAPES["llama7b"]
+    L = 8192
+    base = W.llama7b_prefill_only(L, 0)
+    kc, vc = W.history_cache_torch(base.num_pages, sh, base.seed, dev)
+    q, k, v = W.new_token_values(L, sh, base.seed)
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+    qd, kd, vd = bf(q), bf(k), bf(v)
+    runner = StepRunner(sh.H_q, sh.H_kv, sh.d, L + 64, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def time_step(wl, t0):
+        st, info, packed = runner.plan(*wl.arrays(), wl.budget)
+        pd = runner.upload(packed)
+        n = info.num_tokens
+        out = torch.empty((n, sh.H_q, sh.d), dtype=torch.bfloat16, device=dev)
+        ms = []
+        for i in range(7):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            runner.run(qd[t0:t0 + n], kd[t0:t0 + n], vd[t0:t0 + n], kc, vc, out, pd, info)
+            b.record()
+            b.synchronize()
+            if i >= 2:
+                ms.append(a.elapsed_time(b))
+        if runner.status() != 0:
+            raise RuntimeError("device error in the sweep")
+        return statistics.median(ms), n, info
+
+    chunks = {}
+    for c in (512, 1024, 2048, L):
+        done, steps, reread = 0, [], 0
+        while done < L:
+            wl = W.llama7b_prefill_only(c, done // c)
+            ms, n, info = time_step(wl, done)
+            steps.append(ms)
+            reread += info.history_tokens
+            done += n
+        chunks[c] = {"prompt_us": 1e3 * sum(steps), "steps": len(steps), "history_tokens_reread": int(reread),
+                     "reread_bytes": int(reread) * 4 * sh.H_kv * sh.d, "step_us": [round(1e3 * x, 1) for x in steps]}
+    one = chunks[L]["prompt_us"]
+    for c in chunks:
+        chunks[c]["overhead_vs_one_shot"] = chunks[c]["prompt_us"] / one - 1.0
+    tq = {}
+    for n in (128, 129, 256, 257, 512, 513):
+        wl = W._build("tq", sh, n, [(W.PREFILL_RUNNING, 4096 + n, 4096, 4096 + n)], base.seed)
+        ms, _, _ = time_step(wl, 0)
+        tq[n] = round(1e3 * ms, 2)
+    res = {"sweep": "chunked prefill of one 8192-token prompt (Llama-2-7B-like layer, 32/32 heads, d 128)",
+           "chunks": {str(c): v for c, v in chunks.items()},
+           "tile_quantisation_us_after_4096_history": {str(k): v for k, v in tq.items()},
+           "ratio_257_over_256": tq[257] / tq[256], "ratio_129_over_128": tq[129] / tq[128],
+           "ratio_513_over_512": tq[513] / tq[512]}
+    print(json.dumps(res), flush=True)
+    return None
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -372,6 +455,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="chunk-size / tile-quantisation sweep (own JSON line)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -380,6 +464,9 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
+    if args.sweep:
+        run_sweep(args)
+        return
     res = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world, local_rank)
     if res is not None:
         print(json.dumps(res), flush=True)

@@ -173,7 +173,7 @@ def _stream_ptr(stream) -> int:
 
 
 def sarathi_rope_table(table, max_pos: int, head_dim: int, rope_theta: float, stream=None) -> None:
-    """Fill ``table`` (torch float64 CUDA tensor of max_pos*head_dim elements)."""
+    """Fill ``table`` (torch float64 CUDA tensor of 2*max_pos*head_dim elements)."""
     _check(load().sarathi_rope_table(table.data_ptr(), max_pos, head_dim, rope_theta, _stream_ptr(stream)),
            "sarathi_rope_table")
 

@@ -55,7 +55,8 @@ struct KParams {
     const int32_t* plan;
     int off_qo, off_kvp, off_kvi, off_last, off_aux, off_items;
     int n_items, n_sched;
-    const double2* rope;  // [max_pos][d/2] {cos, sin}
+    const double2* rope;  // [max_pos][d/2] {cos, sin} in fp64
+    const float4* ropef;  // [max_pos][d/2] {cos_hi, cos_lo, sin_hi, sin_lo}: cos = cos_hi + cos_lo to ~2^-48
     int rope_max_pos;
     int32_t* ws_int;      // header, append counters, merge tickets
     float* ws_part;       // split partials
@@ -250,14 +251,49 @@ __device__ __forceinline__ int page_id(const KParams& P, const Row& R, int lp, i
     return page;
 }
 
-// Rotate (x0, x1) = (k_j, k_{j+d/2}) by the table angle in fp64, one rounding
-// per product and sum (no contraction), exactly as written:
-//   y0 = x0 cos - x1 sin,  y1 = x1 cos + x0 sin.
-__device__ __forceinline__ void rope_pair_fp64(double x0, double x1, double2 cs, uint16_t& y0, uint16_t& y1) {
-    double a = __dsub_rn(__dmul_rn(x0, cs.x), __dmul_rn(x1, cs.y));
-    double b = __dadd_rn(__dmul_rn(x1, cs.x), __dmul_rn(x0, cs.y));
-    y0 = bf16_from_double(a);
-    y1 = bf16_from_double(b);
+// bf16 of y = a*p + b*q where the fp64 evaluation rounds each product and
+// the sum once (no contraction) and then rounds once to bf16 -- the RoPE of a
+// key at an absolute position (y0 = x0 cos - x1 sin, y1 = x1 cos + x0 sin).
+//
+// Fast path in fp32: with p = p_hi + p_lo, q = q_hi + q_lo, the products
+// a*p_hi and b*q_hi are split exactly by FMA (a, b have 8 significant bits)
+// and summed by TwoSum, so y = S + small with an error below 2^-46 (|a p| +
+// |b q|).  The fp64 evaluation differs from the exact value by at most about
+// 2^-52 (|a p| + |b q|).  When S + small lies farther than 2^-34 (|a p| +
+// |b q|) from both bf16 rounding boundaries around its nearest bf16 value w,
+// every value within those errors rounds to w, so w is the answer.  Otherwise
+// (about one element in 10^8) the fp64 evaluation runs as written.
+__device__ __forceinline__ uint16_t rope_bf16(float a, float b, float p_hi, float p_lo, float q_hi, float q_lo,
+                                             double p, double q) {
+    const float P1 = a * p_hi, E1 = fmaf(a, p_hi, -P1);
+    const float P2 = b * q_hi, E2 = fmaf(b, q_hi, -P2);
+    const float S = P1 + P2;
+    const float bb = S - P1;
+    const float T = (P1 - (S - bb)) + (P2 - bb);
+    const float small = ((E1 + E2) + T) + fmaf(a, p_lo, b * q_lo);
+    const float u = S + small;
+    const float mag = fabsf(P1) + fabsf(P2);
+    const uint32_t ub = __float_as_uint(u);
+    const uint16_t w = (uint16_t)((ub + 0x7FFFu + ((ub >> 16) & 1u)) >> 16);
+    const uint32_t wb = (uint32_t)w;
+    const float wf = __uint_as_float(wb << 16);
+    const float awf = fabsf(wf);
+    if (mag > 0.f && awf > 1e-30f && awf < 1e30f) {
+        // neighbours of w toward +inf and -inf (w away from zero and inf)
+        const uint32_t up = (wb & 0x8000u) ? wb - 1u : wb + 1u;
+        const uint32_t dn = (wb & 0x8000u) ? wb + 1u : wb - 1u;
+        const float m1 = 0.5f * (wf + __uint_as_float(up << 16));   // exact: short significands
+        const float m0 = 0.5f * (wf + __uint_as_float(dn << 16));
+        const float margin = mag * 0x1p-34f;
+        const float d1 = (m1 - S) - small;   // m1 - S is exact (Sterbenz)
+        const float d0 = (S - m0) + small;
+        if (d1 > margin && d0 > margin) return w;
+    }
+    return bf16_from_double(__dadd_rn(__dmul_rn((double)a, p), __dmul_rn((double)b, q)));
+}
+__device__ __forceinline__ void rope_pair(float x0, float x1, float4 cf, double2 cs, uint16_t& y0, uint16_t& y1) {
+    y0 = rope_bf16(x0, -x1, cf.x, cf.y, cf.z, cf.w, cs.x, cs.y);
+    y1 = rope_bf16(x1, x0, cf.x, cf.y, cf.z, cf.w, cs.x, cs.y);
 }
 
 // ----------------------------------------------------------------------------
@@ -286,8 +322,8 @@ __device__ void run_append(const KParams& P, const int* it, int* s_abort) {
         }
         const uint16_t* kr = kin + ((size_t)(R.qo0 + t) * Hkv + g) * D;
         uint16_t y0, y1;
-        rope_pair_fp64((double)bf16_bits_to_float(kr[j]), (double)bf16_bits_to_float(kr[j + HALF]),
-                       P.rope[(size_t)pos * HALF + j], y0, y1);
+        const size_t ti = (size_t)pos * HALF + j;
+        rope_pair(bf16_bits_to_float(kr[j]), bf16_bits_to_float(kr[j + HALF]), P.ropef[ti], P.rope[ti], y0, y1);
         uint16_t* dst = kc + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D;
         dst[j] = y0;
         dst[j + HALF] = y1;
@@ -481,15 +517,15 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             const uint4 b = __ldg(reinterpret_cast<const uint4*>(qr + HALF) + c);
             const __nv_bfloat16* x0 = reinterpret_cast<const __nv_bfloat16*>(&a);
             const __nv_bfloat16* x1 = reinterpret_cast<const __nv_bfloat16*>(&b);
-            const double2* cs = P.rope + (size_t)pos * HALF + c * 8;
+            const float4* cs = P.ropef + (size_t)pos * HALF + c * 8;
             uint32_t ylo[4], yhi[4];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-                const double2 c0 = cs[e], c1 = cs[e + 1];
+                const float4 c0 = cs[e], c1 = cs[e + 1];
                 const float a0 = __bfloat162float(x0[e]), a1 = __bfloat162float(x0[e + 1]);
                 const float b0 = __bfloat162float(x1[e]), b1 = __bfloat162float(x1[e + 1]);
-                ylo[e >> 1] = pack_bf16(a0 * (float)c0.x - b0 * (float)c0.y, a1 * (float)c1.x - b1 * (float)c1.y);
-                yhi[e >> 1] = pack_bf16(b0 * (float)c0.x + a0 * (float)c0.y, b1 * (float)c1.x + a1 * (float)c1.y);
+                ylo[e >> 1] = pack_bf16(a0 * c0.x - b0 * c0.z, a1 * c1.x - b1 * c1.z);
+                yhi[e >> 1] = pack_bf16(b0 * c0.x + a0 * c0.z, b1 * c1.x + a1 * c1.z);
             }
             lo = make_uint4(ylo[0], ylo[1], ylo[2], ylo[3]);
             hi = make_uint4(yhi[0], yhi[1], yhi[2], yhi[3]);
@@ -768,8 +804,8 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         if (row < G) {
             const __nv_bfloat16* qr = P.q + ((size_t)R.qo0 * P.Hq + g * G + row) * D;
             const float x0 = __bfloat162float(qr[j]), x1 = __bfloat162float(qr[j + HALF]);
-            const double2 cs = P.rope[(size_t)pos * HALF + j];
-            const float c = (float)cs.x, sn = (float)cs.y;
+            const float4 cs = P.ropef[(size_t)pos * HALF + j];
+            const float c = cs.x, sn = cs.z;
             y0 = x0 * c - x1 * sn;
             y1 = x1 * c + x0 * sn;
         }
@@ -786,8 +822,9 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         for (int j = tid; j < HALF; j += kThreads) {
             uint16_t y0 = 0, y1 = 0;
             if (ok) {
-                rope_pair_fp64((double)bf16_bits_to_float(kr[j]), (double)bf16_bits_to_float(kr[j + HALF]),
-                               P.rope[(size_t)pos * HALF + j], y0, y1);
+                const size_t ti = (size_t)pos * HALF + j;
+                rope_pair(bf16_bits_to_float(kr[j]), bf16_bits_to_float(kr[j + HALF]), P.ropef[ti], P.rope[ti], y0,
+                          y1);
                 reinterpret_cast<uint16_t*>(P.k_cache)[off + j] = y0;
                 reinterpret_cast<uint16_t*>(P.k_cache)[off + j + HALF] = y1;
             }
@@ -1096,7 +1133,7 @@ struct InvFreq {
     double v[64];
 };
 
-__global__ void rope_table_kernel(double2* table, int max_pos, int half, const InvFreq f) {
+__global__ void rope_table_kernel(double2* table, float4* split, int max_pos, int half, const InvFreq f) {
     const int64_t total = (int64_t)max_pos * half;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int p = (int)(i / half), j = (int)(i % half);
@@ -1104,6 +1141,8 @@ __global__ void rope_table_kernel(double2* table, int max_pos, int half, const I
         double sn, cs;
         sincos(th, &sn, &cs);
         table[i] = make_double2(cs, sn);
+        const float ch = __double2float_rn(cs), sh = __double2float_rn(sn);
+        split[i] = make_float4(ch, __double2float_rn(cs - (double)ch), sh, __double2float_rn(sn - (double)sh));
     }
 }
 
@@ -1177,8 +1216,9 @@ extern "C" int32_t sarathi_rope_table(double* table, int32_t max_pos, int32_t he
     for (int j = 0; j < head_dim / 2; ++j) f.v[j] = std::pow(rope_theta, -(2.0 * (double)j) / (double)head_dim);
     const int64_t total = (int64_t)max_pos * (head_dim / 2);
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, 8192);
-    rope_table_kernel<<<blocks, 256, 0, (cudaStream_t)cuda_stream>>>(reinterpret_cast<double2*>(table), max_pos,
-                                                                      head_dim / 2, f);
+    rope_table_kernel<<<blocks, 256, 0, (cudaStream_t)cuda_stream>>>(
+        reinterpret_cast<double2*>(table), reinterpret_cast<float4*>(table + (size_t)max_pos * head_dim), max_pos,
+        head_dim / 2, f);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "rope_table launch");
     return SARATHI_OK;
@@ -1253,6 +1293,7 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
     P.n_items = in->n_items;
     P.n_sched = in->n_sched;
     P.rope = reinterpret_cast<const double2*>(a->rope_table);
+    P.ropef = reinterpret_cast<const float4*>(a->rope_table + (size_t)a->rope_max_pos * d);
     P.rope_max_pos = a->rope_max_pos;
     P.ws_int = static_cast<int32_t*>(a->workspace);
     P.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) +

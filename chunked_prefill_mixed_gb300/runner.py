@@ -22,7 +22,7 @@ class StepRunner:
         self.num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         self.sm_scale = 1.0 / math.sqrt(d)
         self.max_pos = int(max_pos)
-        self.rope = torch.empty(self.max_pos * d, dtype=torch.float64, device=self.device)
+        self.rope = torch.empty(2 * self.max_pos * d, dtype=torch.float64, device=self.device)
         sarathi_rope_table(self.rope, self.max_pos, d, rope_theta, self.stream)
         self.workspace = torch.zeros(1 << 16, dtype=torch.uint8, device=self.device)
 

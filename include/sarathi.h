@@ -127,10 +127,12 @@ int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int32_t token_
                      const sarathi_shape* shape, int32_t num_sms,
                      int32_t* host_buf, size_t host_buf_bytes, sarathi_plan_info* info);
 
-/* Fill the RoPE table on the device: table[p][j] = {cos(p*f_j), sin(p*f_j)} in
- * fp64 for p < max_pos, j < head_dim/2, f_j = rope_theta^(-2j/head_dim)
- * (rotate-half RoPE at absolute positions, [SS] §"分块不等于截断上下文").
- * table: device pointer to max_pos*head_dim doubles (double[max_pos][head_dim/2][2]).
+/* Fill the RoPE table on the device: {cos(p*f_j), sin(p*f_j)} in fp64 for
+ * p < max_pos, j < head_dim/2, f_j = rope_theta^(-2j/head_dim) (rotate-half
+ * RoPE at absolute positions, [SS] §"分块不等于截断上下文"), followed by the same
+ * values split into float pairs (hi + lo) for the kernel's fp32 fast path.
+ * table: device pointer to 2*max_pos*head_dim doubles (16*max_pos*head_dim
+ * bytes): double[max_pos][head_dim/2][2], then float[max_pos][head_dim/2][4].
  * Asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy default stream). */
 int32_t sarathi_rope_table(double* table, int32_t max_pos, int32_t head_dim, double rope_theta,
                            void* cuda_stream);
@@ -145,7 +147,7 @@ typedef struct sarathi_attn_args {
     void* out;                  /* bf16 [T][H_q][d] attention outputs                   */
     const int32_t* plan;        /* device copy of the packed plan buffer                */
     const sarathi_plan_info* info; /* HOST pointer: the info sarathi_plan returned      */
-    const double* rope_table;   /* from sarathi_rope_table, max_pos >= info->max_kv_len */
+    const double* rope_table;   /* from sarathi_rope_table, max_pos >= info->max_kv_len  */
     int32_t rope_max_pos;
     int32_t num_pages;          /* pages in each cache pool                             */
     void* workspace;            /* >= info->workspace_bytes, 256-byte aligned, ZEROED    */
