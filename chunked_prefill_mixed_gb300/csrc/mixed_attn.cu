@@ -116,6 +116,13 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+// Plain (untiled) bulk copy global -> shared; both addresses 16-byte aligned,
+// size a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ int ld_acquire(const int* p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -264,7 +271,7 @@ __device__ __forceinline__ int page_id(const KParams& P, const Row& R, int lp, i
 // every value within those errors rounds to w, so w is the answer.  Otherwise
 // (about one element in 10^8) the fp64 evaluation runs as written.
 __device__ __forceinline__ uint16_t rope_bf16(float a, float b, float p_hi, float p_lo, float q_hi, float q_lo,
-                                             double p, double q) {
+                                             const double2* pq) {
     const float P1 = a * p_hi, E1 = fmaf(a, p_hi, -P1);
     const float P2 = b * q_hi, E2 = fmaf(b, q_hi, -P2);
     const float S = P1 + P2;
@@ -289,63 +296,111 @@ __device__ __forceinline__ uint16_t rope_bf16(float a, float b, float p_hi, floa
         const float d0 = (S - m0) + small;
         if (d1 > margin && d0 > margin) return w;
     }
-    return bf16_from_double(__dadd_rn(__dmul_rn((double)a, p), __dmul_rn((double)b, q)));
+    const double2 c = *pq;  // fp64 {cos, sin}: read only on this rare path
+    return bf16_from_double(__dadd_rn(__dmul_rn((double)a, c.x), __dmul_rn((double)b, c.y)));
 }
-__device__ __forceinline__ void rope_pair(float x0, float x1, float4 cf, double2 cs, uint16_t& y0, uint16_t& y1) {
-    y0 = rope_bf16(x0, -x1, cf.x, cf.y, cf.z, cf.w, cs.x, cs.y);
-    y1 = rope_bf16(x1, x0, cf.x, cf.y, cf.z, cf.w, cs.x, cs.y);
+__device__ __forceinline__ void rope_pair(float x0, float x1, float4 cf, const double2* cs, uint16_t& y0,
+                                          uint16_t& y1) {
+    y0 = rope_bf16(x0, -x1, cf.x, cf.y, cf.z, cf.w, cs);
+    y1 = rope_bf16(x1, x0, cf.x, cf.y, cf.z, cf.w, cs);
 }
 
 // ----------------------------------------------------------------------------
 // APPEND: rotate + store the K/V of up to kAppendTokens prefill tokens
 // ----------------------------------------------------------------------------
+// The item's K and V rows ([token][kv_head][d], contiguous) and the fp32 RoPE
+// rows of its positions (contiguous) come into shared memory with three bulk
+// copies, so a pass costs one memory round trip however loaded HBM is.  A
+// pass holds as many tokens as fit in the stage area: all 16 up to 10 kv heads
+// of d = 128 (two passes for 32 heads).
 template <int D>
-__device__ void run_append(const KParams& P, const int* it, int* s_abort) {
+__device__ void run_append(const KParams& P, const int* it, uint8_t* smem, uint32_t bar, uint32_t* s_phase,
+                           int* s_abort) {
     const int tid = threadIdx.x;
+    uint32_t phase = *s_phase;  // passes this CTA has waited for; kept in shared memory, not a loop register
     const int s = it[kS], t0 = it[kStart], cnt = it[kCount];
     const Row R = row_geom(P, s);
     const int Hkv = P.Hkv;
-    constexpr int HALF = D / 2;
+    constexpr int HALF = D / 2, C8 = D / 8, H8 = HALF / 8;
+    const int row_bytes = Hkv * D * 2;                // one token's K (or V), every kv head
+    const int tok_bytes = 2 * row_bytes + HALF * 16;  // its K, V and fp32 RoPE row
+    const int tpp = min(cnt, kSmemStages / tok_bytes);
     const uint16_t* kin = reinterpret_cast<const uint16_t*>(P.k);
     uint16_t* kc = reinterpret_cast<uint16_t*>(P.k_cache);
-    const int totk = cnt * Hkv * HALF;
-    for (int i = tid; i < totk; i += kThreads) {
-        const int j = i % HALF;
-        const int rest = i / HALF;
-        const int g = rest % Hkv;
-        const int t = t0 + rest / Hkv;
-        const int pos = R.h + t;
-        const int page = P.plan[P.off_kvi + R.kvp0 + pos / kPage];
-        if (page < 0 || page >= P.num_pages || pos >= P.rope_max_pos) {
-            raise_error(P, kErrBounds, page, s_abort);
-            continue;
+    const int32_t* pages = P.plan + P.off_kvi + R.kvp0;
+    if (R.h + t0 + cnt > P.rope_max_pos) {
+        if (tid == 0) raise_error(P, kErrBounds, R.h + t0 + cnt - 1, s_abort);
+    } else {
+        for (int p0 = 0; p0 < cnt; p0 += tpp) {
+            const int n = min(tpp, cnt - p0);
+            const int ta = t0 + p0;  // first chunk token of this pass
+            const uint32_t kbytes = (uint32_t)(n * row_bytes);
+            if (tid == 0) {
+                const uint32_t rbytes = (uint32_t)(n * HALF * 16);
+                const size_t row0 = (size_t)(R.qo0 + ta) * Hkv * D;
+                mbar_expect_tx(bar, 2 * kbytes + rbytes);
+                bulk_load(smem_u32(smem), kin + row0, kbytes, bar);
+                bulk_load(smem_u32(smem + kbytes), P.v + row0, kbytes, bar);
+                bulk_load(smem_u32(smem + 2 * kbytes), P.ropef + (size_t)(R.h + ta) * HALF, rbytes, bar);
+            }
+            if (!mbar_wait_bounded(P, bar, phase & 1, s_abort, 10000 + p0, it)) return;
+            ++phase;
+            const uint16_t* ks = reinterpret_cast<const uint16_t*>(smem);
+            const uint4* vs = reinterpret_cast<const uint4*>(smem + kbytes);
+            const float4* rs = reinterpret_cast<const float4*>(smem + 2 * kbytes);
+            const int totv = n * Hkv * C8;
+            for (int i = tid; i < totv; i += kThreads) {
+                const int c = i % C8, rest = i / C8, g = rest % Hkv, pos = R.h + ta + rest / Hkv;
+                const int page = __ldg(pages + pos / kPage);
+                if (page < 0 || page >= P.num_pages) continue;  // reported by the K loop below
+                reinterpret_cast<uint4*>(P.v_cache + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D)[c] = vs[i];
+            }
+            const int totk = n * H8 * Hkv;
+            for (int i = tid; i < totk; i += kThreads) {
+                // kv head fastest: neighbouring threads share a RoPE row
+                const int g = i % Hkv, rest = i / Hkv, j8 = rest % H8, tl = rest / H8;
+                const int pos = R.h + ta + tl;
+                const int page = __ldg(pages + pos / kPage);
+                if (page < 0 || page >= P.num_pages) {
+                    raise_error(P, kErrBounds, page, s_abort);
+                    continue;
+                }
+                const uint16_t* kr = ks + ((size_t)tl * Hkv + g) * D + j8 * 8;
+                const uint4 a = *reinterpret_cast<const uint4*>(kr);
+                const uint4 b = *reinterpret_cast<const uint4*>(kr + HALF);
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+                const double2* fb = P.rope + (size_t)pos * HALF + j8 * 8;
+                const float4* cf = rs + tl * HALF + j8 * 8;
+                uint32_t w0[4], w1[4];
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    uint16_t lo0, lo1, hi0, hi1;
+                    rope_pair(__uint_as_float(aw[e2] << 16), __uint_as_float(bw[e2] << 16), cf[2 * e2], fb + 2 * e2,
+                              lo0, lo1);
+                    rope_pair(__uint_as_float(aw[e2] & 0xFFFF0000u), __uint_as_float(bw[e2] & 0xFFFF0000u),
+                              cf[2 * e2 + 1], fb + 2 * e2 + 1, hi0, hi1);
+                    w0[e2] = (uint32_t)lo0 | ((uint32_t)hi0 << 16);
+                    w1[e2] = (uint32_t)lo1 | ((uint32_t)hi1 << 16);
+                }
+                uint16_t* dst = kc + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D + j8 * 8;
+                *reinterpret_cast<uint4*>(dst) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+                *reinterpret_cast<uint4*>(dst + HALF) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+            }
+            if (p0 + tpp < cnt) {
+                // the next pass's bulk copies overwrite what was just read
+                fence_proxy_async_shared();
+                __syncthreads();
+            }
         }
-        const uint16_t* kr = kin + ((size_t)(R.qo0 + t) * Hkv + g) * D;
-        uint16_t y0, y1;
-        const size_t ti = (size_t)pos * HALF + j;
-        rope_pair(bf16_bits_to_float(kr[j]), bf16_bits_to_float(kr[j + HALF]), P.ropef[ti], P.rope[ti], y0, y1);
-        uint16_t* dst = kc + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D;
-        dst[j] = y0;
-        dst[j + HALF] = y1;
-    }
-    const int totv = cnt * Hkv * (D / 8);
-    for (int i = tid; i < totv; i += kThreads) {
-        const int c = i % (D / 8);
-        const int rest = i / (D / 8);
-        const int g = rest % Hkv;
-        const int t = t0 + rest / Hkv;
-        const int pos = R.h + t;
-        const int page = P.plan[P.off_kvi + R.kvp0 + pos / kPage];
-        if (page < 0 || page >= P.num_pages) continue;
-        const uint4* src = reinterpret_cast<const uint4*>(P.v + ((size_t)(R.qo0 + t) * Hkv + g) * D) + c;
-        uint4* dst = reinterpret_cast<uint4*>(P.v_cache + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D) + c;
-        *dst = __ldg(src);
     }
     // publish: the pages are read next by TMA (async proxy) in other CTAs
     fence_proxy_async_global();
     __threadfence();
     __syncthreads();
-    if (tid == 0) atomicAdd(&P.ws_int[kHdrInts + s], 1);
+    if (tid == 0) {
+        atomicAdd(&P.ws_int[kHdrInts + s], 1);
+        *s_phase = phase;
+    }
 }
 
 // ----------------------------------------------------------------------------
@@ -418,16 +473,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Phase counters of the prefill pipeline, one set per thread, carried across
-// work items (each role only touches the counters of the barriers it waits on).
+// Phase parities of the prefill pipeline, one word per thread, carried across
+// work items; each role only flips the bits of the barriers it waits on.  Only
+// parities are needed: a barrier's n-th completion is waited for with parity
+// n & 1, and a fresh barrier passes a wait on parity 1 at once (the phase
+// before its first), which is how a producer's first wait on an empty slot
+// returns.
 struct PfPhase {
-    int kfill[3], vfill[3];   // producer: loads issued into each K / V stage
-    int kuse[2], vuse[3];     // MMA issuer: loads consumed from each stage
-    int pfull[2];             // MMA issuer: P tiles consumed from each buffer
-    int suse[2];              // softmax: S tiles consumed
-    int pvd[2];               // softmax: completions of each P.V barrier before this item
-    int vseen[3];             // softmax: V loads into each stage (for the last-block clean-up)
+    uint32_t bits;
 };
+constexpr int kPhKFill = 0;   // 2: producer, loads issued into each K stage
+constexpr int kPhVFill = 2;   // 3: producer, loads issued into each V stage
+constexpr int kPhKUse = 5;    // 2: MMA issuer, K loads consumed
+constexpr int kPhVUse = 7;    // 3: MMA issuer, V loads consumed
+constexpr int kPhPFull = 10;  // 2: MMA issuer, P tiles consumed from each buffer
+constexpr int kPhSUse = 12;   // 2: softmax, S tiles consumed
+constexpr int kPhPvd = 14;    // 2: softmax, completions of each P.V barrier before this item
+constexpr int kPhVSeen = 16;  // 3: softmax, V loads into each stage (last-block clean-up)
+__device__ __forceinline__ uint32_t ph_get(const PfPhase& ph, int bit) { return (ph.bits >> bit) & 1u; }
+__device__ __forceinline__ void ph_flip(PfPhase& ph, int bit) { ph.bits ^= 1u << bit; }
 
 // ----------------------------------------------------------------------------
 // PREFILL tile on the 5th-generation tensor cores: up to 128 query rows
@@ -467,7 +531,9 @@ constexpr int kBarSFull = kBarVEmpty + 3;        // 2
 constexpr int kBarPFull = kBarSFull + 2;         // 2 (one per P buffer, 256 arrivals each)
 constexpr int kBarPvDone = kBarPFull + 2;        // 2 (one per P buffer)
 constexpr int kBarDrain = kBarPvDone + 2;        // 1
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kBarAppend = kBarDrain + 1;        // 1 (APPEND bulk copies)
+constexpr int kNumBars = kBarAppend + 1;
+static_assert(kNumBars * 8 <= 512, "barrier area");
 
 template <int D>
 __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUtensorMap* tmV, const int* it,
@@ -550,7 +616,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             const int nst = is_v ? kVStages : kKStages;
             const int full0 = is_v ? kBarVFull : kBarKFull;
             const int empty0 = is_v ? kBarVEmpty : kBarKEmpty;
-            int* fill = is_v ? ph.vfill : ph.kfill;
+            const int fill = is_v ? kPhVFill : kPhKFill;
             uint8_t* ring = smem + (is_v ? kTcV : kTcK) + hf * BLK_HALF;
             const int32_t* kvi = P.plan + P.off_kvi + R.kvp0;
             int id = (lane < 8 && lane < pages_hi) ? kvi[lane] : 0;
@@ -558,8 +624,8 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 const int st = j % nst;
                 const int nxt = (lane < 8 && (j + 1) * 8 + lane < pages_hi) ? kvi[(j + 1) * 8 + lane] : 0;
                 const int npg = min(kTcKeys / kPage, pages_hi - j * 8);
-                if (fill[st] > 0)
-                    mbar_wait_bounded(P, bar(empty0 + st), (fill[st] - 1) & 1, s_abort, (is_v ? 2000 : 1000) + j, it);
+                mbar_wait_bounded(P, bar(empty0 + st), ph_get(ph, fill + st) ^ 1u, s_abort, (is_v ? 2000 : 1000) + j,
+                                  it);
                 if (lane == 0) mbar_expect_tx(bar(full0 + st), (uint32_t)npg * kPageHalfBytes);
                 __syncwarp();
                 if (lane < npg) {
@@ -572,7 +638,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                                 (page * P.Hkv + g) * kPage, bar(full0 + st));
                 }
                 __syncwarp();
-                ++fill[st];
+                ph_flip(ph, fill + st);
                 id = nxt;
             }
         }
@@ -584,8 +650,8 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             const uint64_t qd = umma_desc(smem_u32(qtile), 16, 1024);
             auto issue_qk = [&](int j) {
                 const int st = j & 1;
-                mbar_wait_bounded(P, bar(kBarKFull + st), ph.kuse[st] & 1, s_abort, 3000 + j, it);
-                ++ph.kuse[st];
+                mbar_wait_bounded(P, bar(kBarKFull + st), ph_get(ph, kPhKUse + st), s_abort, 3000 + j, it);
+                ph_flip(ph, kPhKUse + st);
                 tc_fence_after();
                 const uint64_t kd = umma_desc(smem_u32(smem + kTcK + st * 32768), 16, 1024);
                 const uint32_t sd = tmem + (uint32_t)(st * kTcKeys);
@@ -606,11 +672,11 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 // one barrier per P buffer: softmax may finish block j+1 before
                 // this thread sees block j, and a single barrier would then
                 // have moved two phases
-                mbar_wait_bounded(P, bar(kBarPFull + st), ph.pfull[st] & 1, s_abort, 4000 + j, it);
-                ++ph.pfull[st];
+                mbar_wait_bounded(P, bar(kBarPFull + st), ph_get(ph, kPhPFull + st), s_abort, 4000 + j, it);
+                ph_flip(ph, kPhPFull + st);
                 const int vst = j % kVStages;
-                mbar_wait_bounded(P, bar(kBarVFull + vst), ph.vuse[vst] & 1, s_abort, 5000 + j, it);
-                ++ph.vuse[vst];
+                mbar_wait_bounded(P, bar(kBarVFull + vst), ph_get(ph, kPhVUse + vst), s_abort, 5000 + j, it);
+                ph_flip(ph, kPhVUse + vst);
                 tc_fence_after();
                 const uint64_t vd = umma_desc(smem_u32(smem + kTcV + vst * 32768), BLK_HALF, 1024);
                 const uint32_t pa = tmem + kTmemP + (uint32_t)(st * 64);
@@ -637,12 +703,12 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         float* red = reinterpret_cast<float*>(smem + kSmemDecQ);  // [2 parity][2 half][128] maxima, [2][128] sums
         float m_run = -INFINITY, l_run = 0.f;
         // P.V of block k completes phase pvd[k&1] + k/2 of barrier kBarPvDone + (k&1)
-        auto pv_parity = [&](int k) { return (uint32_t)((ph.pvd[k & 1] + k / 2) & 1); };
+        auto pv_parity = [&](int k) { return ph_get(ph, kPhPvd + (k & 1)) ^ (uint32_t)((k / 2) & 1); };
         for (int j = 0; j < nblk; ++j) {
             const int st = j & 1;
             const int kb0 = j * kTcKeys + ch * 64;   // first key of this thread's 64 columns
-            mbar_wait_bounded(P, bar(kBarSFull + st), ph.suse[st] & 1, s_abort, 6000 + j, it);
-            ++ph.suse[st];
+            mbar_wait_bounded(P, bar(kBarSFull + st), ph_get(ph, kPhSUse + st), s_abort, 6000 + j, it);
+            ph_flip(ph, kPhSUse + st);
             tc_fence_after();
             float v[64];
             {
@@ -708,7 +774,8 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             l_run += sum;
             // last block: V rows past kv_hi hold stale bytes; zero them so 0 x V stays 0
             const int vst = j % kVStages;
-            const int vs = ph.vseen[vst]++;
+            const uint32_t vs = ph_get(ph, kPhVSeen + vst);
+            ph_flip(ph, kPhVSeen + vst);
             const int key0 = j * kTcKeys;
             if (j == nblk - 1 && key0 + kTcKeys > kv_hi) {
                 mbar_wait_bounded(P, bar(kBarVFull + vst), vs & 1, s_abort, 8000 + j, it);
@@ -725,8 +792,8 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         // epilogue: O / l -> bf16; each warp of the pair writes half of the columns
         mbar_wait_bounded(P, bar(kBarPvDone + ((nblk - 1) & 1)), pv_parity(nblk - 1), s_abort, 9000, it);
         tc_fence_after();
-        ph.pvd[0] += (nblk + 1) / 2;
-        ph.pvd[1] += nblk / 2;
+        if (((nblk + 1) / 2) & 1) ph_flip(ph, kPhPvd);
+        if ((nblk / 2) & 1) ph_flip(ph, kPhPvd + 1);
         red[512 + ch * 128 + r] = l_run;
         asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
         const float inv = 1.f / (l_run + red[512 + (ch ^ 1) * 128 + r]);
@@ -823,7 +890,7 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
             uint16_t y0 = 0, y1 = 0;
             if (ok) {
                 const size_t ti = (size_t)pos * HALF + j;
-                rope_pair(bf16_bits_to_float(kr[j]), bf16_bits_to_float(kr[j + HALF]), P.ropef[ti], P.rope[ti], y0,
+                rope_pair(bf16_bits_to_float(kr[j]), bf16_bits_to_float(kr[j + HALF]), P.ropef[ti], P.rope + ti, y0,
                           y1);
                 reinterpret_cast<uint16_t*>(P.k_cache)[off + j] = y0;
                 reinterpret_cast<uint16_t*>(P.k_cache)[off + j + HALF] = y1;
@@ -841,14 +908,10 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     __syncthreads();
 
     const int mi = lane >> 3;
-    uint32_t qa[D / 16][4];
-    {
-        const int row = (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-            ldsm_x4(smem_u32(qtile + sw128_chunk(16, row, 2 * kk + (mi >> 1))), qa[kk][0], qa[kk][1], qa[kk][2],
-                    qa[kk][3]);
-    }
+    // Q fragments are re-read from shared memory for every page (4 KB per
+    // 8 KB page) rather than held: the accumulator alone takes D / 2
+    // registers a thread
+    const int qrow = (mi & 1) * 8 + (lane & 7);
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
     float o[D / 8][4];
 #pragma unroll
@@ -881,10 +944,11 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int key = (mi >> 1) * 8 + (lane & 7);
-            uint32_t b0, b1, b2, b3;
+            uint32_t qa[4], b0, b1, b2, b3;
+            ldsm_x4(smem_u32(qtile + sw128_chunk(16, qrow, 2 * kk + (mi >> 1))), qa[0], qa[1], qa[2], qa[3]);
             ldsm_x4(smem_u32(kb + sw128_chunk(kPage, key, 2 * kk + (mi & 1))), b0, b1, b2, b3);
-            mma_bf16(sc[0], qa[kk], b0, b1);
-            mma_bf16(sc[1], qa[kk], b2, b3);
+            mma_bf16(sc[0], qa, b0, b1);
+            mma_bf16(sc[1], qa, b2, b3);
         }
         float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll
@@ -1032,10 +1096,12 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
     __shared__ int s_abort;
     __shared__ int s_flag;
     __shared__ uint32_t s_tmem;
+    __shared__ uint32_t s_app_phase;
     const int tid = threadIdx.x;
     const uint32_t bars = smem_u32(smem + kSmemBars);
     if (tid == 0) {
         s_abort = 0;
+        s_app_phase = 0;
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
             if (i == kBarPFull || i == kBarPFull + 1) count = 256;
@@ -1083,7 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         for (int i = 0; i < kItemInts; ++i) it[i] = s_item[i];
         if (it[0] < 0) break;
         if (it[0] == kAppend)
-            run_append<D>(P, it, &s_abort);
+            run_append<D>(P, it, smem, bars + 8 * kBarAppend, &s_app_phase, &s_abort);
         else if (it[0] == kPrefill)
             run_prefill<D>(P, &tmK, &tmV, it, smem, &s_abort, pf_phase, tmem);
         else
@@ -1235,7 +1301,8 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
         !a->workspace)
         return fail(SARATHI_ERR_INVALID_ARG, "NULL device pointer");
     if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->out, 16) ||
-        !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->plan, 16) || !aligned(a->workspace, 256))
+        !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->plan, 16) || !aligned(a->rope_table, 16) ||
+        !aligned(a->workspace, 256))
         return fail(SARATHI_ERR_INVALID_ARG, "misaligned pointer (tensors 16 B, workspace 256 B)");
     if (a->num_pages <= 0) return fail(SARATHI_ERR_INVALID_ARG, "num_pages must be positive");
     if (a->rope_max_pos < in->max_kv_len) return fail(SARATHI_ERR_CAPACITY, "RoPE table shorter than max_kv_len");
@@ -1266,6 +1333,13 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
                          : cudaFuncSetAttribute(mixed_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                 kSmemAlloc);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+            int resident = 0;
+            e = d == 128 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, mixed_step_kernel<128>, kThreads,
+                                                                         kSmemAlloc)
+                         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, mixed_step_kernel<64>, kThreads,
+                                                                         kSmemAlloc);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+            if (resident < 1) return fail(SARATHI_ERR_CUDA, "step kernel does not fit one SM (registers/shared memory)");
             ds.smem_set[di] = true;
         }
         sms = ds.sms;
