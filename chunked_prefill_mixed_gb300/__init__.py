@@ -20,6 +20,8 @@ _lib = None
 OK, ERR_INVALID_ARG, ERR_CAPACITY, WARN_OVER_BUDGET_DECODES = 0, 1, 2, 3
 ERR_CUDA, ERR_UNSUPPORTED, ERR_DEVICE_CHECK = 4, 5, 6
 DECODE, PREFILL_RUNNING, PREFILL_WAITING = 0, 1, 2
+ABI_VERSION = 2   # SARATHI_ABI_VERSION of include/sarathi.h
+ITEM_INTS = 24    # SARATHI_ITEM_INTS
 
 EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_rope_table", "sarathi_mixed_attn",
             "sarathi_mixed_attn_noalloc", "sarathi_workspace_status", "sarathi_last_error", "sarathi_abi_version")
@@ -162,7 +164,7 @@ def plan_arrays(info: PlanInfo, packed: np.ndarray) -> dict:
         kv_page_indptr=view(info.off_kv_page_indptr, n + 1),
         kv_page_indices=view(info.off_kv_page_indices, info.nnz_pages),
         kv_last_page_len=view(info.off_kv_last_page_len, n), req_aux=view(info.off_req_aux, n),
-        items=view(info.off_items, info.n_items * 8).reshape(info.n_items, 8),
+        items=view(info.off_items, info.n_items * ITEM_INTS).reshape(info.n_items, ITEM_INTS),
     )
 
 

@@ -236,19 +236,27 @@ __device__ __forceinline__ bool mbar_wait_bounded(const KParams& P, uint32_t bar
 struct Row {
     int qo0, n, kvp0, np, kv_len, h;
 };
-__device__ __forceinline__ Row row_geom(const KParams& P, int s) {
+// The row's geometry travels in the item (a copy of its metadata), so the
+// first page can be fetched one load after the item is claimed.
+__device__ __forceinline__ Row row_geom(const int* it) {
     Row r;
-    const int32_t* pl = P.plan;
-    r.qo0 = pl[P.off_qo + s];
-    r.n = pl[P.off_qo + s + 1] - r.qo0;
-    r.kvp0 = pl[P.off_kvp + s];
-    r.np = pl[P.off_kvp + s + 1] - r.kvp0;
-    r.kv_len = (r.np - 1) * kPage + pl[P.off_last + s];
+    r.qo0 = it[kQo0];
+    r.n = it[kNNew];
+    r.kvp0 = it[kKvp0];
+    r.np = it[kNp];
+    r.kv_len = it[kKvLen];
     r.h = r.kv_len - r.n;
     return r;
 }
 
 // Physical page id of a request-local page, checked against the pool.
+__device__ __forceinline__ int checked_page(const KParams& P, int page, int* s_abort) {
+    if (page < 0 || page >= P.num_pages) {
+        raise_error(P, kErrBounds, page, s_abort);
+        return 0;
+    }
+    return page;
+}
 __device__ __forceinline__ int page_id(const KParams& P, const Row& R, int lp, int* s_abort) {
     const int page = P.plan[P.off_kvi + R.kvp0 + lp];
     if (page < 0 || page >= P.num_pages) {
@@ -319,7 +327,7 @@ __device__ void run_append(const KParams& P, const int* it, uint8_t* smem, uint3
     const int tid = threadIdx.x;
     uint32_t phase = *s_phase;  // passes this CTA has waited for; kept in shared memory, not a loop register
     const int s = it[kS], t0 = it[kStart], cnt = it[kCount];
-    const Row R = row_geom(P, s);
+    const Row R = row_geom(it);
     const int Hkv = P.Hkv;
     constexpr int HALF = D / 2, C8 = D / 8, H8 = HALF / 8;
     const int row_bytes = Hkv * D * 2;                // one token's K (or V), every kv head
@@ -543,7 +551,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
     constexpr int BLK_HALF = kTcKeys * 128;      // one 64-column half of a 128-key block
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = it[kS], g = it[kG], t0 = it[kStart], cnt = it[kCount];
-    const Row R = row_geom(P, s);
+    const Row R = row_geom(it);
     const int G = P.group;
     const int rows_valid = cnt * G;
     const int kv_hi = R.h + t0 + cnt;            // keys [0, kv_hi) are visible to some row
@@ -553,25 +561,15 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
     const uint32_t bars = smem_u32(smem + kSmemBars);
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
-    // 1. the chunk's K/V must be in the pages: wait for this request's APPENDs
-    if (tid == 0) {
-        const int need = P.plan[P.off_aux + s];
-        const int* ctr = &P.ws_int[kHdrInts + s];
-        if (ld_acquire(ctr) < need) {
-            const uint64_t w0 = globaltimer();
-            while (ld_acquire(ctr) < need) {
-                if (globaltimer() - w0 > kWaitNs) {
-                    raise_error(P, kErrWait, -1 - s, s_abort);
-                    break;
-                }
-                __nanosleep(100);
-            }
-        }
-        fence_proxy_async_global();
-    }
-    // 2. Q rows, RoPE'd in fp32 at their absolute positions, into the swizzled
-    //    tile; one thread rotates 8 consecutive pairs (two 16-byte chunks)
-    for (int i = tid; i < kTileRows * (HALF / 8); i += kThreads) {
+    // The TMA producers (warps 8-11) start on the history pages at once; only
+    // the blocks holding the chunk's own keys wait for this request's APPENDs.
+    // Meanwhile warps 0-7 and 12 write the Q tile and meet on named barrier 5.
+    const bool q_writer = warp < 8 || warp == 12;
+    const int qtid = warp == 12 ? 256 + lane : tid;
+    constexpr int kQThreads = 288;
+    // Q rows, RoPE'd in fp32 at their absolute positions, into the swizzled
+    // tile; one thread rotates 8 consecutive pairs (two 16-byte chunks)
+    for (int i = q_writer ? qtid : kTileRows * (HALF / 8); i < kTileRows * (HALF / 8); i += kQThreads) {
         const int row = i / (HALF / 8), c = i % (HALF / 8);
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if (row < rows_valid) {
@@ -599,11 +597,12 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c)) = lo;
         *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c + HALF / 8)) = hi;
     }
-    fence_proxy_async_shared();  // Q is read by the tensor cores (async proxy)
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (*(volatile int*)s_abort) return;
+    if (q_writer) {
+        fence_proxy_async_shared();  // Q is read by the tensor cores (async proxy)
+        tc_fence_before();
+        asm volatile("bar.sync 5, %0;" ::"n"(kQThreads) : "memory");
+        tc_fence_after();
+    }
 
     if (warp >= 8 && warp < 12) {
         // ---------------- TMA producers: warp 8+2v+hf loads column half hf of ring v ----------------
@@ -619,8 +618,28 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             const int fill = is_v ? kPhVFill : kPhKFill;
             uint8_t* ring = smem + (is_v ? kTcV : kTcK) + hf * BLK_HALF;
             const int32_t* kvi = P.plan + P.off_kvi + R.kvp0;
-            int id = (lane < 8 && lane < pages_hi) ? kvi[lane] : 0;
+            int id = (lane < 8 && lane < pages_hi) ? it[kIds + lane] : 0;  // block 0's ids come with the item
+            const int j_chunk = R.h / kTcKeys;  // first block with a key of the chunk
             for (int j = 0; j < nblk; ++j) {
+                if (j == j_chunk) {
+                    // the chunk's K/V must be in the pages: this request's APPENDs
+                    const int need = P.plan[P.off_aux + s];
+                    const int* ctr = &P.ws_int[kHdrInts + s];
+                    if (lane == 0 && ld_acquire(ctr) < need) {
+                        const uint64_t w0 = globaltimer();
+                        while (ld_acquire(ctr) < need) {
+                            if (globaltimer() - w0 > kWaitNs / 2) {  // first to give up: names the cause
+                                raise_error(P, kErrWait, -1 - s, s_abort);
+                                break;
+                            }
+                            __nanosleep(100);
+                        }
+                    }
+                    __syncwarp();
+                    (void)ld_acquire(ctr);      // every issuing lane acquires for itself
+                    fence_proxy_async_global();  // ... and orders the TMA reads after it
+                }
+                if (*(volatile int*)s_abort) break;
                 const int st = j % nst;
                 const int nxt = (lane < 8 && (j + 1) * 8 + lane < pages_hi) ? kvi[(j + 1) * 8 + lane] : 0;
                 const int npg = min(kTcKeys / kPage, pages_hi - j * 8);
@@ -829,9 +848,9 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     constexpr int KPAGE = HALVES * kPageHalfBytes;  // one K page-head in smem
     constexpr int STAGE = 2 * KPAGE;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int s = it[kS], g = it[kG], p0 = it[kStart], pc = it[kCount];
+    const int g = it[kG], p0 = it[kStart], pc = it[kCount];
     const int slot_first = it[kSlot], merge = it[kMerge], nsplit = it[kNSplit];
-    const Row R = row_geom(P, s);
+    const Row R = row_geom(it);
     const int G = P.group;
     const int pos = R.kv_len - 1;   // the decode token's absolute position
     const bool last_owner = (p0 + pc == R.np);
@@ -859,7 +878,9 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
             tma_load_2d(dst + KPAGE + hf * kPageHalfBytes, tmV, hf * 64, y, bar);
         }
     };
-    for (int k = 0; k < my_pages && k < kDecStages; ++k) {
+    // the first page id of every warp comes with the item: no load before it
+    if (my_pages > 0 && lane == 0) issue(0, checked_page(P, it[kIds + warp], s_abort));
+    for (int k = 1; k < my_pages && k < kDecStages; ++k) {
         const int pid = __shfl_sync(0xffffffffu, ids, k);
         if (lane == 0) issue(k, pid);
     }
@@ -1092,7 +1113,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ int s_item[kItemInts];
+    __shared__ __align__(16) int s_item[kItemInts];
     __shared__ int s_abort;
     __shared__ int s_flag;
     __shared__ uint32_t s_tmem;
@@ -1130,23 +1151,17 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
             const int idx = atomicAdd(&P.ws_int[0], 1);
             if (idx < P.n_items) {
                 const int4* src = reinterpret_cast<const int4*>(P.plan + P.off_items + (size_t)idx * kItemInts);
-                const int4 a = src[0], b = src[1];
-                s_item[0] = a.x;
-                s_item[1] = a.y;
-                s_item[2] = a.z;
-                s_item[3] = a.w;
-                s_item[4] = b.x;
-                s_item[5] = b.y;
-                s_item[6] = b.z;
-                s_item[7] = b.w;
+                int4 v[kItemInts / 4];
+#pragma unroll
+                for (int i = 0; i < kItemInts / 4; ++i) v[i] = src[i];
+#pragma unroll
+                for (int i = 0; i < kItemInts / 4; ++i) reinterpret_cast<int4*>(s_item)[i] = v[i];
             } else {
                 s_item[0] = -1;
             }
         }
         __syncthreads();
-        int it[kItemInts];
-#pragma unroll
-        for (int i = 0; i < kItemInts; ++i) it[i] = s_item[i];
+        const int* it = s_item;  // rewritten only after the end-of-item barrier
         if (it[0] < 0) break;
         if (it[0] == kAppend)
             run_append<D>(P, it, smem, bars + 8 * kBarAppend, &s_app_phase, &s_abort);

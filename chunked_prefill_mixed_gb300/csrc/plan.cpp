@@ -67,9 +67,15 @@ int32_t validate_requests(const sarathi_request* reqs, int32_t n_reqs) {
     return SARATHI_OK;
 }
 
-// Rough per-SM speeds used only to order the work list (longest first).
-constexpr double kPrefillFlopPerNs = 5000.0;  // tensor-core tile throughput per SM
-constexpr double kDecodeBytesPerNs = 40.0;    // HBM share per SM
+// Per-SM cost model used only to order the work list (longest first), fitted
+// to per-item times of the step kernel on GB300 with every SM busy: a prefill
+// tile costs a fixed start (Q fill, first loads, epilogue) plus its 128-key
+// blocks at tensor-core speed; a decode split a fixed start plus its pages at
+// an equal share of HBM bandwidth.
+constexpr double kPrefillFixedNs = 8000.0;
+constexpr double kPrefillFlopPerNs = 6000.0;
+constexpr double kDecodeFixedNs = 2000.0;
+constexpr double kDecodeBytesPerNs = 40.0;
 
 }  // namespace
 }  // namespace sarathi
@@ -88,7 +94,7 @@ extern "C" int32_t sarathi_plan_bounds(const sarathi_request* reqs, int32_t n_re
     st = validate_requests(reqs, n_reqs);
     if (st) return st;
     if (token_budget <= 0) return fail(SARATHI_ERR_INVALID_ARG, "token_budget must be positive");
-    (void)num_sms;
+    if (num_sms <= 0) return fail(SARATHI_ERR_INVALID_ARG, "num_sms must be positive");
     const int64_t Hkv = shape->num_heads_kv;
     const int group = shape->num_heads_q / shape->num_heads_kv;
     int64_t n_dec = 0, pages = 0;
@@ -100,7 +106,11 @@ extern "C" int32_t sarathi_plan_bounds(const sarathi_request* reqs, int32_t n_re
     const int64_t T = n_dec + token_budget;
     const int64_t appends = T / kAppendTokens + n;
     const int64_t tiles = (T / tokens_per_tile(group) + n) * Hkv;
-    const int64_t dec_items = (pages / kDecodeMinSplitPages + n) * Hkv;
+    // decode splits: sum over decodes and kv heads of ceil(np / split) with
+    // split >= decode page-heads / (num_sms * kDecodeItemsPerSm), so at most
+    // num_sms * kDecodeItemsPerSm + (decodes x kv heads) items
+    const int64_t dec_items =
+        std::min<int64_t>((pages / kDecodeMinSplitPages + n) * Hkv, (int64_t)num_sms * kDecodeItemsPerSm + n_dec * Hkv);
     const int64_t items = appends + tiles + dec_items;
     const int64_t ints = 6 * n + 2 + pages + 8 + items * kItemInts;
     if (host_buf_bytes) *host_buf_bytes = (size_t)ints * 4;
@@ -208,9 +218,10 @@ extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int
             for (int g = 0; g < Hkv; ++g)
                 for (int32_t t0 = (n - 1) / tpt * tpt; t0 >= 0; t0 -= tpt) {
                     int32_t c = std::min(tpt, n - t0);
-                    double keys = (double)h + t0 + c;
-                    double flops = 4.0 * d * kTileRows * keys;
-                    tiles.push_back({flops / kPrefillFlopPerNs, {kPrefill, s, g, t0, c, -1, -1, 0}});
+                    const double keys = (double)ceil_div((int64_t)h + t0 + c, kTileRows) * kTileRows;
+                    const double flops = 4.0 * d * kTileRows * keys;
+                    tiles.push_back(
+                        {kPrefillFixedNs + flops / kPrefillFlopPerNs, {kPrefill, s, g, t0, c, -1, -1, 0}});
                 }
         } else {
             // decode-like: split the pages; the item holding the last page also
@@ -225,7 +236,7 @@ extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int
                 for (int64_t k = 0; k < nsplit; ++k) {
                     int32_t p0 = (int32_t)(k * per);
                     int32_t pc = (int32_t)std::min<int64_t>(per, np[s] - p0);
-                    decs.push_back({pc * kv_page_bytes / kDecodeBytesPerNs,
+                    decs.push_back({kDecodeFixedNs + pc * kv_page_bytes / kDecodeBytesPerNs,
                                     {kDecode, s, g, p0, pc, first, merge, (int32_t)nsplit}});
                 }
             }
@@ -311,8 +322,24 @@ extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int
     }
     int32_t* items = b + info->off_items;
     int64_t w = 0;
-    for (auto& it : appends) std::memcpy(items + kItemInts * w++, it.data(), sizeof(int32_t) * kItemInts);
-    for (auto& t : attn) std::memcpy(items + kItemInts * w++, t.it.data(), sizeof(int32_t) * kItemInts);
+    auto put = [&](const std::array<int32_t, kItemInts>& src) {
+        int32_t* it = items + kItemInts * w++;
+        std::memcpy(it, src.data(), sizeof(int32_t) * kItemInts);
+        const int32_t s = it[kS];
+        it[kQo0] = qo[s];
+        it[kNNew] = qo[s + 1] - qo[s];
+        it[kKvp0] = kvp[s];
+        it[kNp] = np[s];
+        it[kKvLen] = kPage * (np[s] - 1) + b[info->off_kv_last_page_len + s];
+        if (it[kKind] == kDecode) {
+            for (int k = 0; k < kItemIds; ++k)
+                it[kIds + k] = k < it[kCount] ? kvi[kvp[s] + it[kStart] + k] : 0;
+        } else if (it[kKind] == kPrefill) {
+            for (int k = 0; k < kItemIds; ++k) it[kIds + k] = k < np[s] ? kvi[kvp[s] + k] : 0;
+        }
+    };
+    for (auto& it : appends) put(it);
+    for (auto& t : attn) put(t.it);
     set_error("");
     return decodes > token_budget ? SARATHI_WARN_OVER_BUDGET_DECODES : SARATHI_OK;
 }

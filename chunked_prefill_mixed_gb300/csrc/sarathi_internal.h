@@ -18,11 +18,12 @@ constexpr int kTileRows = 128;        // query rows (token x head-in-group) per 
 constexpr int kMaxGroup = 16;         // q heads per kv head handled by the decode path
 constexpr int kDecodeMinSplitPages = 8;
 constexpr int kDecodeItemsPerSm = 2;  // target split-KV items per SM for the decode phase
-constexpr int kItemInts = 8;
+constexpr int kItemInts = 24;
+constexpr int kItemIds = 8;           // page ids carried in an item (one per decode warp)
 
 enum ItemKind : int32_t { kAppend = 0, kPrefill = 1, kDecode = 2 };
 
-// Work item, kItemInts int32:
+// Work item, kItemInts int32 (96 bytes, 16-byte aligned):
 //   [0] kind
 //   [1] s        scheduled row (request) index
 //   [2] g        kv head (prefill / decode)
@@ -34,7 +35,15 @@ enum ItemKind : int32_t { kAppend = 0, kPrefill = 1, kDecode = 2 };
 //                nsplit) owns slot + k); -1 when the item is the only split
 //   [6] merge    decode: merge group, -1 when the item is the only split
 //   [7] nsplit   decode: splits in the merge group
-enum ItemField { kKind = 0, kS, kG, kStart, kCount, kSlot, kMerge, kNSplit };
+//   [8..12]      row s: qo_indptr[s], new tokens, kv_page_indptr[s], pages,
+//                kv length -- copies of the metadata, so that an item needs
+//                one load before its first page can be fetched
+//   [13..15]     zero
+//   [16..23]     decode: the page id of page start + w for decode warp w (0
+//                past the item's pages); prefill: the ids of the request's
+//                pages 0..7 (0 past its pages); append: zero
+enum ItemField { kKind = 0, kS, kG, kStart, kCount, kSlot, kMerge, kNSplit, kQo0, kNNew, kKvp0, kNp, kKvLen,
+                 kIds = 16 };
 
 // Workspace: an int32 header, then fp32 partial slots from byte kPartialOffset.
 //   [0] work-queue head   [1] CTAs exited   [2] error word   [3] error detail

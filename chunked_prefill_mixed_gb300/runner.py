@@ -9,8 +9,8 @@ import math
 import numpy as np
 import torch
 
-from . import (PlanInfo, Shape, make_requests, sarathi_mixed_attn, sarathi_plan, sarathi_rope_table,
-               sarathi_workspace_status)
+from . import (PlanInfo, Shape, make_requests, sarathi_mixed_attn, sarathi_plan, sarathi_plan_bounds,
+               sarathi_rope_table, sarathi_workspace_status)
 
 
 class StepRunner:
@@ -25,10 +25,17 @@ class StepRunner:
         self.rope = torch.empty(2 * self.max_pos * d, dtype=torch.float64, device=self.device)
         sarathi_rope_table(self.rope, self.max_pos, d, rope_theta, self.stream)
         self.workspace = torch.zeros(1 << 16, dtype=torch.uint8, device=self.device)
+        self._host_buf = np.zeros(0, dtype=np.int32)
 
     def plan(self, states, prompt_len, num_computed, block_tables, budget: int):
+        """Plans into a host buffer the runner keeps (grown when a batch needs
+        more); the returned packed array is a view of it, valid until the
+        next call."""
         reqs, keep = make_requests(states, prompt_len, num_computed, block_tables)
-        return sarathi_plan(reqs, len(states), budget, self.shape, self.num_sms)
+        hb, _ = sarathi_plan_bounds(reqs, len(states), budget, self.shape, self.num_sms)
+        if self._host_buf.nbytes < hb:
+            self._host_buf = np.zeros(max(hb // 4 + 4, 2 * self._host_buf.size), dtype=np.int32)
+        return sarathi_plan(reqs, len(states), budget, self.shape, self.num_sms, self._host_buf)
 
     def ensure_workspace(self, nbytes: int):
         if self.workspace.numel() < nbytes:

@@ -37,7 +37,11 @@
 extern "C" {
 #endif
 
-#define SARATHI_ABI_VERSION 1
+#define SARATHI_ABI_VERSION 2
+/* int32 words of one kernel work item in the packed plan.  Items are kernel
+ * bookkeeping: their layout is private to the library and may change with
+ * SARATHI_ABI_VERSION; callers copy the packed plan as a whole. */
+#define SARATHI_ITEM_INTS 24
 
 /* Status codes. */
 #define SARATHI_OK 0
@@ -95,7 +99,7 @@ typedef struct sarathi_plan_info {
     int32_t off_kv_page_indices;/* [nnz_pages]                                          */
     int32_t off_kv_last_page_len;/* [n_sched] in 1..page_size                            */
     int32_t off_req_aux;        /* [n_sched] kernel bookkeeping (append items per row)  */
-    int32_t off_items;          /* [n_items][8] kernel work list                         */
+    int32_t off_items;          /* [n_items][SARATHI_ITEM_INTS] kernel work list         */
     int32_t packed_ints;        /* int32 elements to copy to the device                  */
     int64_t workspace_bytes;    /* device workspace sarathi_mixed_attn needs             */
 } sarathi_plan_info;
@@ -147,7 +151,8 @@ typedef struct sarathi_attn_args {
     void* out;                  /* bf16 [T][H_q][d] attention outputs                   */
     const int32_t* plan;        /* device copy of the packed plan buffer                */
     const sarathi_plan_info* info; /* HOST pointer: the info sarathi_plan returned      */
-    const double* rope_table;   /* from sarathi_rope_table, max_pos >= info->max_kv_len  */
+    const double* rope_table;   /* from sarathi_rope_table, max_pos >= info->max_kv_len, */
+                                /*   16-byte aligned                                    */
     int32_t rope_max_pos;
     int32_t num_pages;          /* pages in each cache pool                             */
     void* workspace;            /* >= info->workspace_bytes, 256-byte aligned, ZEROED    */
@@ -163,6 +168,7 @@ typedef struct sarathi_attn_args {
  * history h: softmax over keys 0..h+i of RoPE(q_i, h+i).K_j * sm_scale,
  * weights applied to V_j ([SS] §"分块不等于截断上下文").  Keys are the bf16
  * pages; scores and sums in fp32.
+ * q, k, v, out, k_cache, v_cache, plan and rope_table must be 16-byte aligned.
  * Launches using one workspace must not overlap in time.  A launch that hits a
  * device-side check (a wait that ran out, a page id outside the pool) sets an
  * error word in the workspace; read it with sarathi_workspace_status.

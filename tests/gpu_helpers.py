@@ -46,6 +46,7 @@ class GpuStep:
         self.runner = runner or StepRunner(sh.H_q, sh.H_kv, sh.d, max_pos or self._max_pos(), device=self.dev,
                                            rope_theta=sh.rope_base)
         self.status, self.info, self.packed = self.runner.plan(*wl.arrays(), wl.budget)
+        self.packed = self.packed.copy()  # the runner's buffer is reused by its next plan
         self.plan_dev = self.runner.upload(self.packed)
         self.q_dev, self.k_dev, self.v_dev = (from_u16(x, self.dev) for x in (self.q, self.k, self.v))
         self.out = torch.full((T, sh.H_q, sh.d), float("nan"), dtype=torch.bfloat16, device=self.dev)

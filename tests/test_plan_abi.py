@@ -21,7 +21,9 @@ def test_library_exports_every_declared_function():
     lib = S.load()
     for name in declared:
         assert hasattr(lib, name), name
-    assert S.sarathi_abi_version() == 1
+    assert S.sarathi_abi_version() == S.ABI_VERSION
+    for name, value in (("SARATHI_ABI_VERSION", S.ABI_VERSION), ("SARATHI_ITEM_INTS", S.ITEM_INTS)):
+        assert re.search(rf"#define {name} {value}\b", text), name
 
 
 def _product_plan(states, prompt, computed, tables, budget, shape, num_sms=148):
@@ -101,10 +103,23 @@ def _check_work_list(info, m, shape):
     first_prefill = None
     seen_slots = set()
     pages_cov = {}
+    kvi, last = m["kv_page_indices"], m["kv_last_page_len"]
     for idx, it in enumerate(items):
-        kind, s, g, start, count, slot, merge, nsplit = (int(x) for x in it)
+        kind, s, g, start, count, slot, merge, nsplit = (int(x) for x in it[:8])
         nn = qo[s + 1] - qo[s]
         np_ = kvp[s + 1] - kvp[s]
+        # the row's metadata copied into the item, and the page ids it carries
+        assert list(it[8:13]) == [qo[s], nn, kvp[s], np_, 16 * (np_ - 1) + last[s]]
+        assert not it[13:16].any()
+        ids = it[16:24]
+        if kind == 0:
+            assert not ids.any()
+        elif kind == 1:
+            k = min(8, np_)
+            assert list(ids[:k]) == list(kvi[kvp[s]:kvp[s] + k]) and not ids[k:].any()
+        else:
+            k = min(8, count)
+            assert list(ids[:k]) == list(kvi[kvp[s] + start:kvp[s] + start + k]) and not ids[k:].any()
         if kind == 0:
             assert first_prefill is None, "append after a prefill tile"
             assert nn >= 2
