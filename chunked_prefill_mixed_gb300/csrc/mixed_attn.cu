@@ -490,90 +490,136 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 struct PfPhase {
     uint32_t bits;
 };
-constexpr int kPhKFill = 0;   // 2: producer, loads issued into each K stage
-constexpr int kPhVFill = 2;   // 3: producer, loads issued into each V stage
-constexpr int kPhKUse = 5;    // 2: MMA issuer, K loads consumed
-constexpr int kPhVUse = 7;    // 3: MMA issuer, V loads consumed
-constexpr int kPhPFull = 10;  // 2: MMA issuer, P tiles consumed from each buffer
-constexpr int kPhSUse = 12;   // 2: softmax, S tiles consumed
-constexpr int kPhPvd = 14;    // 2: softmax, completions of each P.V barrier before this item
-constexpr int kPhVSeen = 16;  // 3: softmax, V loads into each stage (last-block clean-up)
+constexpr int kPfStagesMax = 4;
+constexpr int kPhKFill = 0;    // 4: producer, loads issued into each K stage
+constexpr int kPhVFill = 4;    // 4: producer, loads issued into each V stage
+constexpr int kPhKUse = 8;     // 4: MMA issuer, K loads consumed
+constexpr int kPhVUse = 12;    // 4: MMA issuer, V loads consumed
+constexpr int kPhPFull = 16;   // 2: MMA issuer, P of each Q tile consumed
+constexpr int kPhSUse = 18;    // 2: softmax, S of its Q tile consumed
+constexpr int kPhODone = 20;   // 2: softmax, final P.V of its Q tile
+constexpr int kPhVSeen = 22;   // 4: softmax, V loads into each stage (last-block clean-up)
 __device__ __forceinline__ uint32_t ph_get(const PfPhase& ph, int bit) { return (ph.bits >> bit) & 1u; }
 __device__ __forceinline__ void ph_flip(PfPhase& ph, int bit) { ph.bits ^= 1u << bit; }
 
+// TMEM loads without the wait, so that two can be in flight; tmem_wait_ld
+// then also pins the destination registers after the wait.
+__device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, float* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7]),
+          "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]), "=f"(v[14]), "=f"(v[15]),
+          "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]), "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]),
+          "=f"(v[24]), "=f"(v[25]), "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
+        : "r"(taddr));
+}
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld(float (&v)[N]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]));
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane; completes at tmem_wait_st.
+__device__ __forceinline__ void tmem_st16_nw(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ----------------------------------------------------------------------------
-// PREFILL tile on the 5th-generation tensor cores: up to 128 query rows
-// (token-major, q-head-in-group minor) of one chunk for one kv head, causal
-// over every history page and the chunk ("Sarathi-Serve 完全拆解",
-// §"分块不等于截断上下文").
-//   S = Q K^T per 128-key block: tcgen05.mma (M 128, N 128, K 16 steps), fp32
-//       accumulator in TMEM, double buffered;
-//   softmax: thread r of warps 0-3 owns query row r (= TMEM lane r); row max,
-//       lazy rescale of O (only when the max grows by more than 2^8), bf16 P
-//       written to shared memory in the 128-byte-swizzled K-major layout;
-//   O += P V: tcgen05.mma with V read as an MN-major operand straight from the
-//       TMA-loaded pages; O stays in TMEM until the end of the tile.
-// Roles: warps 8-11 are four TMA streams (K and V rings, 2 stages each, one
-// 64-column half per stream: one issuing thread sustains only ~14 boxes/us),
-// warp 12 lane 0 issues the MMAs, warps 0-7 run the softmax and the epilogue: warps w
-// and w+4 share TMEM lane quadrant w (rows 32w..32w+31) and split each block's
-// 128 key columns, exchanging row maxima through a pair barrier.
+// PREFILL item on the 5th-generation tensor cores: two Q tiles (A, B) of up to
+// 128 query rows each (token-major, q-head-in-group minor) of one chunk for
+// one kv head, causal over every history page and the chunk
+// ("Sarathi-Serve 完全拆解", §"分块不等于截断上下文").  Both tiles read the
+// same 128-key K/V blocks, so each block's TMA boxes (one per page and
+// 64-column half: 16-token pages allow no larger box in the swizzled layout
+// the tensor cores read) serve 256 query rows.
+//   S_T = Q_T K^T per block: tcgen05.mma (M 128, N 128, K 16 steps), fp32 in
+//       TMEM columns [128 T, 128 T + 128);
+//   softmax (warps 4T..4T+3, thread = query row = TMEM lane): a max pass and
+//       an exponent pass over the row's 128 scores, lazy rescale of O (only
+//       when the max grows by more than 2^8), bf16 P written over the first
+//       64 columns of S_T;
+//   O_T += P_T V: tcgen05.mma with A = P from TMEM and V read as an MN-major
+//       operand straight from the TMA-loaded pages; O_T in TMEM columns
+//       256 + T d until the end of the item.
+// MMAs issued by one thread run in order, so when S_T(j+1) is complete the
+// P.V of block j has read P_T and finished with O_T: the softmax needs no
+// other wait before it overwrites S_T or rescales O_T.
+// Roles: warps 8-11 are four TMA streams (K and V rings, one 64-column half
+// per stream: one issuing thread sustains only ~14 boxes/us), warp 12 lane 0
+// issues the MMAs, warps 0-7 run the two softmaxes and epilogues.
 // ----------------------------------------------------------------------------
 constexpr int kTcKeys = 128;                     // keys per block
-constexpr int kTcQ = 0;                          // Q tile: [d/64][128 rows][128 B]
-constexpr int kTcK = 32768;                      // K ring: 2 x [d/64][128 keys][128 B]
-constexpr int kKStages = 2, kVStages = 3;        // V is needed later than K: deeper ring
-constexpr int kTcV = kTcK + kKStages * 32768;    // V ring: 3 x [d/64][128 keys][128 B]
-static_assert(kTcV + kVStages * 32768 <= kSmemStages, "tcgen05 prefill smem");
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,256+d) P0 [384,448) P1 [448,512);
-// P (bf16, two per 32-bit column) is the A operand of O += P V, read from TMEM
+constexpr int kTcTiles = kTilesPerItem;          // Q tiles per prefill item
+static_assert(kTcKeys == kTileRows, "a K/V block and a Q tile have the same shape");
+template <int D>
+struct PfLayout {
+    static constexpr int kTile = kTileRows * D * 2;   // bytes of one Q tile or one K/V block
+    static constexpr int kStages = D == 128 ? 2 : 4;  // depth of the K ring and of the V ring
+    static constexpr int kQ = 0;                      // Q tiles A, B: [d/64][128 rows][128 B] each
+    static constexpr int kK = kTcTiles * kTile;
+    static constexpr int kV = kK + kStages * kTile;
+    static_assert(kV + kStages * kTile <= kSmemStages, "prefill shared memory");
+    static_assert(kStages <= kPfStagesMax, "phase bits");
+};
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;
-constexpr uint32_t kTmemP = 384;
-// barrier indices (after the decode rings)
-constexpr int kBarKFull = kDecWarps * kDecStages;  // 2
-constexpr int kBarKEmpty = kBarKFull + 2;        // 2
-constexpr int kBarVFull = kBarKEmpty + 2;        // 3
-constexpr int kBarVEmpty = kBarVFull + 3;        // 3
-constexpr int kBarSFull = kBarVEmpty + 3;        // 2
-constexpr int kBarPFull = kBarSFull + 2;         // 2 (one per P buffer, 256 arrivals each)
-constexpr int kBarPvDone = kBarPFull + 2;        // 2 (one per P buffer)
-constexpr int kBarDrain = kBarPvDone + 2;        // 1
-constexpr int kBarAppend = kBarDrain + 1;        // 1 (APPEND bulk copies)
+constexpr uint32_t kTmemS = 0;     // S (then P) of tile T at 128 T
+constexpr uint32_t kTmemO = 256;   // O of tile T at 256 + T d
+constexpr int kBarKFull = kDecWarps * kDecStages;   // kPfStagesMax
+constexpr int kBarKEmpty = kBarKFull + kPfStagesMax;
+constexpr int kBarVFull = kBarKEmpty + kPfStagesMax;
+constexpr int kBarVEmpty = kBarVFull + kPfStagesMax;
+constexpr int kBarSFull = kBarVEmpty + kPfStagesMax;  // 2 (per Q tile)
+constexpr int kBarPFull = kBarSFull + 2;               // 2 (per Q tile, 128 arrivals each)
+constexpr int kBarODone = kBarPFull + 2;               // 2 (per Q tile)
+constexpr int kBarDrain = kBarODone + 2;               // 1
+constexpr int kBarAppend = kBarDrain + 1;              // 1 (APPEND bulk copies)
 constexpr int kNumBars = kBarAppend + 1;
 static_assert(kNumBars * 8 <= 512, "barrier area");
 
 template <int D>
 __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUtensorMap* tmV, const int* it,
                             uint8_t* smem, int* s_abort, PfPhase& ph, uint32_t tmem) {
+    using L = PfLayout<D>;
     constexpr int HALVES = D / 64;
     constexpr int HALF = D / 2;
+    constexpr int NST = L::kStages;
     constexpr int BLK_HALF = kTcKeys * 128;      // one 64-column half of a 128-key block
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = it[kS], g = it[kG], t0 = it[kStart], cnt = it[kCount];
     const Row R = row_geom(it);
     const int G = P.group;
-    const int rows_valid = cnt * G;
+    const int tpt = kTileRows / G;               // tokens per Q tile
+    const int cA = min(cnt, tpt), cB = cnt - cA; // tokens of tiles A and B
+    const int ntile = cB > 0 ? 2 : 1;
     const int kv_hi = R.h + t0 + cnt;            // keys [0, kv_hi) are visible to some row
     const int nblk = (kv_hi + kTcKeys - 1) / kTcKeys;
+    const int nblkA = (R.h + t0 + cA + kTcKeys - 1) / kTcKeys;  // blocks tile A reads (a prefix)
     const int pages_hi = (kv_hi + kPage - 1) / kPage;
-    uint8_t* qtile = smem + kTcQ;
     const uint32_t bars = smem_u32(smem + kSmemBars);
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
     // The TMA producers (warps 8-11) start on the history pages at once; only
     // the blocks holding the chunk's own keys wait for this request's APPENDs.
-    // Meanwhile warps 0-7 and 12 write the Q tile and meet on named barrier 5.
+    // Meanwhile warps 0-7 and 12 write the Q tiles and meet on named barrier 5.
     const bool q_writer = warp < 8 || warp == 12;
     const int qtid = warp == 12 ? 256 + lane : tid;
     constexpr int kQThreads = 288;
+    constexpr int kQUnits = kTileRows * (HALF / 8);  // per tile
     // Q rows, RoPE'd in fp32 at their absolute positions, into the swizzled
-    // tile; one thread rotates 8 consecutive pairs (two 16-byte chunks)
-    for (int i = q_writer ? qtid : kTileRows * (HALF / 8); i < kTileRows * (HALF / 8); i += kQThreads) {
-        const int row = i / (HALF / 8), c = i % (HALF / 8);
+    // tiles; one thread rotates 8 consecutive pairs (two 16-byte chunks)
+    for (int i = q_writer ? qtid : ntile * kQUnits; i < ntile * kQUnits; i += kQThreads) {
+        const int T = i / kQUnits, rem = i % kQUnits;
+        const int row = rem / (HALF / 8), c = rem % (HALF / 8);
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-        if (row < rows_valid) {
-            const int t = t0 + row / G;
+        if (row < (T == 0 ? cA : cB) * G) {
+            const int t = t0 + T * tpt + row / G;
             const int hq = g * G + row % G;
             const int pos = R.h + t;
             const __nv_bfloat16* qr = P.q + ((size_t)(R.qo0 + t) * P.Hq + hq) * D;
@@ -594,6 +640,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             lo = make_uint4(ylo[0], ylo[1], ylo[2], ylo[3]);
             hi = make_uint4(yhi[0], yhi[1], yhi[2], yhi[3]);
         }
+        uint8_t* qtile = smem + L::kQ + T * L::kTile;
         *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c)) = lo;
         *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c + HALF / 8)) = hi;
     }
@@ -612,11 +659,10 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         if (hf < HALVES) {
             // lanes 0-7 each issue one page's box in the same instruction
             const CUtensorMap* map = is_v ? tmV : tmK;
-            const int nst = is_v ? kVStages : kKStages;
             const int full0 = is_v ? kBarVFull : kBarKFull;
             const int empty0 = is_v ? kBarVEmpty : kBarKEmpty;
             const int fill = is_v ? kPhVFill : kPhKFill;
-            uint8_t* ring = smem + (is_v ? kTcV : kTcK) + hf * BLK_HALF;
+            uint8_t* ring = smem + (is_v ? L::kV : L::kK) + hf * BLK_HALF;
             const int32_t* kvi = P.plan + P.off_kvi + R.kvp0;
             int id = (lane < 8 && lane < pages_hi) ? it[kIds + lane] : 0;  // block 0's ids come with the item
             const int j_chunk = R.h / kTcKeys;  // first block with a key of the chunk
@@ -640,7 +686,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                     fence_proxy_async_global();  // ... and orders the TMA reads after it
                 }
                 if (*(volatile int*)s_abort) break;
-                const int st = j % nst;
+                const int st = j % NST;
                 const int nxt = (lane < 8 && (j + 1) * 8 + lane < pages_hi) ? kvi[(j + 1) * 8 + lane] : 0;
                 const int npg = min(kTcKeys / kPage, pages_hi - j * 8);
                 mbar_wait_bounded(P, bar(empty0 + st), ph_get(ph, fill + st) ^ 1u, s_abort, (is_v ? 2000 : 1000) + j,
@@ -653,7 +699,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                         raise_error(P, kErrBounds, page, s_abort);
                         page = 0;
                     }
-                    tma_load_2d(smem_u32(ring + st * 32768 + lane * kPageHalfBytes), map, hf * 64,
+                    tma_load_2d(smem_u32(ring + st * L::kTile + lane * kPageHalfBytes), map, hf * 64,
                                 (page * P.Hkv + g) * kPage, bar(full0 + st));
                 }
                 __syncwarp();
@@ -666,14 +712,20 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         if (lane == 0) {
             constexpr uint32_t idesc_s = umma_idesc(kTcKeys, false);
             constexpr uint32_t idesc_o = umma_idesc(D, true);
-            const uint64_t qd = umma_desc(smem_u32(qtile), 16, 1024);
-            auto issue_qk = [&](int j) {
-                const int st = j & 1;
-                mbar_wait_bounded(P, bar(kBarKFull + st), ph_get(ph, kPhKUse + st), s_abort, 3000 + j, it);
-                ph_flip(ph, kPhKUse + st);
-                tc_fence_after();
-                const uint64_t kd = umma_desc(smem_u32(smem + kTcK + st * 32768), 16, 1024);
-                const uint32_t sd = tmem + (uint32_t)(st * kTcKeys);
+            const uint64_t qd0 = umma_desc(smem_u32(smem + L::kQ), 16, 1024);
+            const uint64_t qd1 = umma_desc(smem_u32(smem + L::kQ + L::kTile), 16, 1024);
+            int k_have = -1, v_have = -1;  // last block whose K / V load this thread has waited for
+            auto issue_qk = [&](int T, int j) {
+                const int st = j % NST;
+                if (k_have < j) {
+                    mbar_wait_bounded(P, bar(kBarKFull + st), ph_get(ph, kPhKUse + st), s_abort, 3000 + j, it);
+                    ph_flip(ph, kPhKUse + st);
+                    tc_fence_after();
+                    k_have = j;
+                }
+                const uint64_t kd = umma_desc(smem_u32(smem + L::kK + st * L::kTile), 16, 1024);
+                const uint64_t qd = T ? qd1 : qd0;
+                const uint32_t sd = tmem + kTmemS + (uint32_t)(T * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     // start addresses advance in 16-byte units inside the descriptors
@@ -681,159 +733,169 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                     const uint64_t koff = (uint64_t)(((kk >> 2) * BLK_HALF + (kk & 3) * 32) >> 4);
                     umma_f16(sd, qd + off, kd + koff, idesc_s, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(bar(kBarKEmpty + st));
-                umma_commit(bar(kBarSFull + st));
+                umma_commit(bar(kBarSFull + T));
+                if (T == ntile - 1) umma_commit(bar(kBarKEmpty + st));  // its last reader
             };
-            issue_qk(0);
-            if (nblk > 1) issue_qk(1);
+            issue_qk(0, 0);
+            if (ntile > 1) issue_qk(1, 0);
             for (int j = 0; j < nblk; ++j) {
-                const int st = j & 1;
-                // one barrier per P buffer: softmax may finish block j+1 before
-                // this thread sees block j, and a single barrier would then
-                // have moved two phases
-                mbar_wait_bounded(P, bar(kBarPFull + st), ph_get(ph, kPhPFull + st), s_abort, 4000 + j, it);
-                ph_flip(ph, kPhPFull + st);
-                const int vst = j % kVStages;
-                mbar_wait_bounded(P, bar(kBarVFull + vst), ph_get(ph, kPhVUse + vst), s_abort, 5000 + j, it);
-                ph_flip(ph, kPhVUse + vst);
-                tc_fence_after();
-                const uint64_t vd = umma_desc(smem_u32(smem + kTcV + vst * 32768), BLK_HALF, 1024);
-                const uint32_t pa = tmem + kTmemP + (uint32_t)(st * 64);
+                const int vst = j % NST;
+                for (int T = 0; T < ntile; ++T) {
+                    if (j >= (T == 0 ? nblkA : nblk)) continue;
+                    mbar_wait_bounded(P, bar(kBarPFull + T), ph_get(ph, kPhPFull + T), s_abort, 4000 + j, it);
+                    ph_flip(ph, kPhPFull + T);
+                    if (v_have < j) {
+                        mbar_wait_bounded(P, bar(kBarVFull + vst), ph_get(ph, kPhVUse + vst), s_abort, 5000 + j, it);
+                        ph_flip(ph, kPhVUse + vst);
+                        v_have = j;
+                    }
+                    tc_fence_after();
+                    const uint64_t vd = umma_desc(smem_u32(smem + L::kV + vst * L::kTile), BLK_HALF, 1024);
+                    const uint32_t pa = tmem + kTmemS + (uint32_t)(T * kTcKeys);
 #pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                    // A = P from TMEM (16 keys = 8 columns per step); B = V (MN-major:
-                    // d contiguous, keys as rows) straight from the TMA-loaded pages
-                    umma_f16_ts(tmem + kTmemO, pa + (uint32_t)(kk * 8), vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                        // A = P from TMEM (16 keys = 8 columns per step); B = V (MN-major:
+                        // d contiguous, keys as rows) straight from the TMA-loaded pages
+                        umma_f16_ts(tmem + kTmemO + (uint32_t)(T * D), pa + (uint32_t)(kk * 8),
+                                    vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (T == ntile - 1) umma_commit(bar(kBarVEmpty + vst));  // its last reader
+                    if (j + 1 < (T == 0 ? nblkA : nblk))
+                        issue_qk(T, j + 1);
+                    else
+                        umma_commit(bar(kBarODone + T));
                 }
-                umma_commit(bar(kBarVEmpty + vst));
-                umma_commit(bar(kBarPvDone + st));
-                if (j + 2 < nblk) issue_qk(j + 2);
             }
         }
     } else if (warp < 8) {
-        // ---------------- softmax + epilogue (warps 0-7) ----------------
-        const int quad = warp & 3, ch = warp >> 2;   // lane quadrant, key-column half
+        // ---------------- softmax + epilogue: warps 4T..4T+3 own Q tile T ----------------
+        const int T = warp >> 2;
+        const int quad = warp & 3;
         const int r = quad * 32 + lane;              // query row = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        const int pos_r = R.h + t0 + (r < rows_valid ? r / G : cnt - 1);
-        const float sl2 = P.scale_log2;
-        const int pair_bar = 1 + quad;
-        float* red = reinterpret_cast<float*>(smem + kSmemDecQ);  // [2 parity][2 half][128] maxima, [2][128] sums
-        float m_run = -INFINITY, l_run = 0.f;
-        // P.V of block k completes phase pvd[k&1] + k/2 of barrier kBarPvDone + (k&1)
-        auto pv_parity = [&](int k) { return ph_get(ph, kPhPvd + (k & 1)) ^ (uint32_t)((k / 2) & 1); };
-        for (int j = 0; j < nblk; ++j) {
-            const int st = j & 1;
-            const int kb0 = j * kTcKeys + ch * 64;   // first key of this thread's 64 columns
-            mbar_wait_bounded(P, bar(kBarSFull + st), ph_get(ph, kPhSUse + st), s_abort, 6000 + j, it);
-            ph_flip(ph, kPhSUse + st);
-            tc_fence_after();
-            float v[64];
-            {
-                float* v0 = v;
-                float* v1 = v + 32;
-                tmem_ld32(lane_base + (uint32_t)(st * kTcKeys + ch * 64), *reinterpret_cast<float(*)[32]>(v0));
-                tmem_ld32(lane_base + (uint32_t)(st * kTcKeys + ch * 64 + 32), *reinterpret_cast<float(*)[32]>(v1));
-            }
-            // raw scores here; the softmax scale (> 0) is applied in the exponent
-            float mx = -INFINITY;
-            if (kb0 + 63 > pos_r) {
-#pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    v[e] = kb0 + e <= pos_r ? v[e] : -INFINITY;
-                    mx = fmaxf(mx, v[e]);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 64; ++e) mx = fmaxf(mx, v[e]);
-            }
-            red[((j & 1) * 2 + ch) * 128 + r] = mx;
-            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-            mx = fmaxf(mx, red[((j & 1) * 2 + (ch ^ 1)) * 128 + r]) * sl2;
-            // lazy rescale: move the exponent base only when the max grows by > 2^8
-            const bool grow = mx > m_run + 8.f;
-            const float m_new = grow ? mx : m_run;
-            const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
-            // P buffer j&1 is free once P.V of block j-2 is done; O may be
-            // rescaled only after P.V of block j-1
-            if (j >= 2) {
-                mbar_wait_bounded(P, bar(kBarPvDone + st), pv_parity(j - 2), s_abort, 7000 + j, it);
+        // the last block's stale V rows are zeroed by the tile that reads it first
+        const int zero_tile = nblkA == nblk ? 0 : 1;
+        if (T < ntile) {
+            const int cT = T == 0 ? cA : cB;
+            const int rows_valid = cT * G;
+            const int tt = T * tpt + (r < rows_valid ? r / G : cT - 1);  // item-local token of the row
+            const int pos_r = R.h + t0 + tt;
+            const int nT = T == 0 ? nblkA : nblk;
+            const uint32_t s_col = kTmemS + (uint32_t)(T * kTcKeys);
+            const uint32_t o_col = kTmemO + (uint32_t)(T * D);
+            const float sl2 = P.scale_log2;
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < nT; ++j) {
+                const int kb0 = j * kTcKeys;
+                mbar_wait_bounded(P, bar(kBarSFull + T), ph_get(ph, kPhSUse + T), s_abort, 6000 + j, it);
+                ph_flip(ph, kPhSUse + T);
                 tc_fence_after();
-            }
-            if (j > 0 && __any_sync(0xffffffffu, grow)) {
-                mbar_wait_bounded(P, bar(kBarPvDone + (st ^ 1)), pv_parity(j - 1), s_abort, 7500 + j, it);
-                tc_fence_after();
-                {
+                // pass 1: the row max of the raw scores (the scale > 0 is applied after)
+                float mx = -INFINITY;
 #pragma unroll 1
-                    for (int c = 0; c < D / 64; ++c) {
-                        float o[32];
-                        const uint32_t oc = lane_base + kTmemO + (uint32_t)(ch * (D / 2) + c * 32);
-                        tmem_ld32(oc, o);
+                for (int h = 0; h < 2; ++h) {
+                    float v[64];
+                    tmem_ld32_nw(lane_base + s_col + (uint32_t)(h * 64), v);
+                    tmem_ld32_nw(lane_base + s_col + (uint32_t)(h * 64 + 32), v + 32);
+                    tmem_wait_ld(v);
+                    const int kc = kb0 + h * 64;
+                    if (kc + 63 > pos_r) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tmem_st32(oc, o);
+                        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, kc + e <= pos_r ? v[e] : -INFINITY);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, v[e]);
                     }
                 }
-            }
-            l_run *= alpha;
-            m_run = m_new;
-            // P = 2^(s - m) in bf16, two keys per TMEM column of P buffer j&1
-            float sum = 0.f;
-            float pk[32];
-            const float nm = -m_run;
+                // lazy rescale: move the exponent base only when the max grows by > 2^8
+                const float mxs = mx * sl2;
+                const bool grow = mxs > m_run + 8.f;
+                const float m_new = grow ? mxs : m_run;
+                const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
+                if (j > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(lane_base + o_col + (uint32_t)(c * 32), o);
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-                const float p0 = ex2_approx(fmaf(v[e], sl2, nm));
-                const float p1 = ex2_approx(fmaf(v[e + 1], sl2, nm));
-                sum += p0 + p1;
-                pk[e >> 1] = __uint_as_float(pack_bf16(p0, p1));
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st32(lane_base + o_col + (uint32_t)(c * 32), o);
+                    }
+                }
+                // pass 2: P = 2^(s - m) in bf16, two keys per column, over the first
+                // 64 columns of S (columns of half h are written only after half h
+                // and every column below it have been read)
+                float sum = 0.f;
+                const float nm = -m_new;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float v[64];
+                    tmem_ld32_nw(lane_base + s_col + (uint32_t)(h * 64), v);
+                    tmem_ld32_nw(lane_base + s_col + (uint32_t)(h * 64 + 32), v + 32);
+                    tmem_wait_ld(v);
+                    const int kc = kb0 + h * 64;
+                    if (kc + 63 > pos_r) {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) v[e] = kc + e <= pos_r ? v[e] : -INFINITY;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float p0 = ex2_approx(fmaf(v[q * 32 + e], sl2, nm));
+                            const float p1 = ex2_approx(fmaf(v[q * 32 + e + 1], sl2, nm));
+                            sum += p0 + p1;
+                            pk[e >> 1] = pack_bf16(p0, p1);
+                        }
+                        tmem_st16_nw(lane_base + s_col + (uint32_t)(h * 32 + q * 16), pk);
+                    }
+                }
+                tmem_wait_st();
+                l_run = l_run * alpha + sum;
+                m_run = m_new;
+                // last block: V rows past kv_hi hold stale bytes; zero them so 0 x V stays 0
+                if (T == zero_tile && j == nblk - 1 && kb0 + kTcKeys > kv_hi) {
+                    const int vst = j % NST;
+                    mbar_wait_bounded(P, bar(kBarVFull + vst), ph_get(ph, kPhVSeen + vst) ^ (uint32_t)((j / NST) & 1),
+                                      s_abort, 8000 + j, it);
+                    uint8_t* vb = smem + L::kV + vst * L::kTile;
+                    const int first = kv_hi - kb0;
+                    for (int hf = 0; hf < HALVES; ++hf)
+                        for (int i = first * 128 + (tid & 127) * 16; i < kTcKeys * 128; i += 128 * 16)
+                            *reinterpret_cast<uint4*>(vb + hf * BLK_HALF + i) = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_shared();
+                }
+                tc_fence_before();
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull + T)) : "memory");
             }
-            tmem_st32(lane_base + kTmemP + (uint32_t)(st * 64 + ch * 32), pk);
-            l_run += sum;
-            // last block: V rows past kv_hi hold stale bytes; zero them so 0 x V stays 0
-            const int vst = j % kVStages;
-            const uint32_t vs = ph_get(ph, kPhVSeen + vst);
-            ph_flip(ph, kPhVSeen + vst);
-            const int key0 = j * kTcKeys;
-            if (j == nblk - 1 && key0 + kTcKeys > kv_hi) {
-                mbar_wait_bounded(P, bar(kBarVFull + vst), vs & 1, s_abort, 8000 + j, it);
-                uint8_t* vb = smem + kTcV + vst * 32768;
-                const int first = kv_hi - key0;
-                for (int hf = 0; hf < HALVES; ++hf)
-                    for (int i = first * 128 + tid * 16; i < kTcKeys * 128; i += 256 * 16)
-                        *reinterpret_cast<uint4*>(vb + hf * BLK_HALF + i) = make_uint4(0, 0, 0, 0);
-                fence_proxy_async_shared();
+            // epilogue: O / l -> bf16, one row per thread
+            mbar_wait_bounded(P, bar(kBarODone + T), ph_get(ph, kPhODone + T), s_abort, 9000, it);
+            ph_flip(ph, kPhODone + T);
+            tc_fence_after();
+            const float inv = 1.f / l_run;
+            __nv_bfloat16* dst =
+                r < rows_valid ? P.out + ((size_t)(R.qo0 + t0 + tt) * P.Hq + g * G + r % G) * D : nullptr;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                tmem_ld32(lane_base + o_col + (uint32_t)(c * 32), o);
+                if (dst) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) =
+                            make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                       pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                       pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                       pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+                }
             }
             tc_fence_before();
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull + st)) : "memory");
         }
-        // epilogue: O / l -> bf16; each warp of the pair writes half of the columns
-        mbar_wait_bounded(P, bar(kBarPvDone + ((nblk - 1) & 1)), pv_parity(nblk - 1), s_abort, 9000, it);
-        tc_fence_after();
-        if (((nblk + 1) / 2) & 1) ph_flip(ph, kPhPvd);
-        if ((nblk / 2) & 1) ph_flip(ph, kPhPvd + 1);
-        red[512 + ch * 128 + r] = l_run;
-        asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-        const float inv = 1.f / (l_run + red[512 + (ch ^ 1) * 128 + r]);
-        __nv_bfloat16* dst =
-            r < rows_valid ? P.out + ((size_t)(R.qo0 + t0 + r / G) * P.Hq + g * G + r % G) * D + ch * (D / 2)
-                           : nullptr;
-#pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-            float o[32];
-            tmem_ld32(lane_base + kTmemO + (uint32_t)(ch * (D / 2) + c * 32), o);
-            if (dst) {
+        // every softmax thread keeps count of the item's V loads per stage
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) =
-                        make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
-                                   pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                                   pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                                   pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
-            }
-        }
-        tc_fence_before();
+        for (int st = 0; st < NST; ++st)
+            if (((nblk - st + NST - 1) / NST) & 1) ph_flip(ph, kPhVSeen + st);
     }
 }
 
@@ -1125,9 +1187,9 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         s_app_phase = 0;
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == kBarPFull || i == kBarPFull + 1) count = 256;
-            if (i >= kBarKFull && i < kBarKFull + 2) count = D / 64;
-            if (i >= kBarVFull && i < kBarVFull + kVStages) count = D / 64;
+            if (i == kBarPFull || i == kBarPFull + 1) count = 128;  // the tile's softmax threads
+            if (i >= kBarKFull && i < kBarKFull + kPfStagesMax) count = D / 64;
+            if (i >= kBarVFull && i < kBarVFull + kPfStagesMax) count = D / 64;
             mbar_init(bars + 8 * i, count);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

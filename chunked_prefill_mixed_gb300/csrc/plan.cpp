@@ -193,6 +193,7 @@ extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int
     };
     std::vector<Timed> tiles, decs;
     const int tpt = tokens_per_tile(group);
+    const int tpi = tokens_per_item(group);
     // decode split size from the total decode pages and the SM count
     int64_t dec_page_heads = 0;
     for (int32_t s = 0; s < ns; ++s)
@@ -213,13 +214,13 @@ extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int
                 ++cnt;
             }
             aux[s] = cnt;
-            // one (request, kv head) at a time, costliest tile first: the tiles
+            // one (request, kv head) at a time, costliest item first: the items
             // that read the same history pages run side by side and share L2
             for (int g = 0; g < Hkv; ++g)
-                for (int32_t t0 = (n - 1) / tpt * tpt; t0 >= 0; t0 -= tpt) {
-                    int32_t c = std::min(tpt, n - t0);
+                for (int32_t t0 = (n - 1) / tpi * tpi; t0 >= 0; t0 -= tpi) {
+                    int32_t c = std::min(tpi, n - t0);
                     const double keys = (double)ceil_div((int64_t)h + t0 + c, kTileRows) * kTileRows;
-                    const double flops = 4.0 * d * kTileRows * keys;
+                    const double flops = 4.0 * d * kTileRows * ceil_div(c, tpt) * keys;
                     tiles.push_back(
                         {kPrefillFixedNs + flops / kPrefillFlopPerNs, {kPrefill, s, g, t0, c, -1, -1, 0}});
                 }

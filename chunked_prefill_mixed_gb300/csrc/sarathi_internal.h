@@ -28,7 +28,7 @@ enum ItemKind : int32_t { kAppend = 0, kPrefill = 1, kDecode = 2 };
 //   [1] s        scheduled row (request) index
 //   [2] g        kv head (prefill / decode)
 //   [3] start    append: first token (request-local); prefill: first token of the
-//                tile (request-local); decode: first page (request-local)
+//                item's first Q tile (request-local); decode: first page (request-local)
 //   [4] count    tokens (append / prefill) or pages (decode)
 //   [5] slot     decode: first partial slot of its merge group (the group's
 //                splits own consecutive slots; split k = start / ceil(pages /
@@ -63,5 +63,8 @@ inline int64_t partial_offset_bytes(int n_sched, int n_merge) {
 inline int64_t partial_slot_floats(int group, int d) { return (int64_t)group * (d + 2); }
 
 inline int tokens_per_tile(int group) { return group >= kTileRows ? 1 : kTileRows / group; }
+// A prefill item holds up to kTilesPerItem Q tiles that share each K/V block.
+constexpr int kTilesPerItem = 2;
+inline int tokens_per_item(int group) { return kTilesPerItem * tokens_per_tile(group); }
 
 }  // namespace sarathi

@@ -126,7 +126,9 @@ def _check_work_list(info, m, shape):
             appended[qo[s] + start: qo[s] + start + count, :] += 1
         elif kind == 1:
             first_prefill = idx if first_prefill is None else first_prefill
-            assert count * G <= 128 and 0 <= start and start + count <= nn
+            # up to two Q tiles of 128 // G tokens, starting on an item boundary
+            tpi = 2 * (128 // G)
+            assert 0 < count <= tpi and start % tpi == 0 and start + count <= nn
             for t in range(start, start + count):
                 covered[qo[s] + t, g * G:(g + 1) * G] += 1
         else:
