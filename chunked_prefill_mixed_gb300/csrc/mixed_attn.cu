@@ -116,6 +116,14 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+// 3-D box: coordinates {x, y, z} innermost first.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
 // Plain (untiled) bulk copy global -> shared; both addresses 16-byte aligned,
 // size a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -312,6 +320,23 @@ __device__ __forceinline__ void rope_pair(float x0, float x1, float4 cf, const d
     y0 = rope_bf16(x0, -x1, cf.x, cf.y, cf.z, cf.w, cs);
     y1 = rope_bf16(x1, x0, cf.x, cf.y, cf.z, cf.w, cs);
 }
+// Eight consecutive pairs (x0 = a, x1 = b, 8 bf16 each) of one key row:
+// lo = first-half outputs, hi = second-half outputs.
+__device__ __forceinline__ void rope8(uint4 a, uint4 b, const float4* cf, const double2* fb, uint4& lo, uint4& hi) {
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+    uint32_t w0[4], w1[4];
+#pragma unroll
+    for (int e2 = 0; e2 < 4; ++e2) {
+        uint16_t lo0, lo1, hi0, hi1;
+        rope_pair(__uint_as_float(aw[e2] << 16), __uint_as_float(bw[e2] << 16), cf[2 * e2], fb + 2 * e2, lo0, lo1);
+        rope_pair(__uint_as_float(aw[e2] & 0xFFFF0000u), __uint_as_float(bw[e2] & 0xFFFF0000u), cf[2 * e2 + 1],
+                  fb + 2 * e2 + 1, hi0, hi1);
+        w0[e2] = (uint32_t)lo0 | ((uint32_t)hi0 << 16);
+        w1[e2] = (uint32_t)lo1 | ((uint32_t)hi1 << 16);
+    }
+    lo = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+    hi = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+}
 
 // ----------------------------------------------------------------------------
 // APPEND: rotate + store the K/V of up to kAppendTokens prefill tokens
@@ -374,25 +399,12 @@ __device__ void run_append(const KParams& P, const int* it, uint8_t* smem, uint3
                     continue;
                 }
                 const uint16_t* kr = ks + ((size_t)tl * Hkv + g) * D + j8 * 8;
-                const uint4 a = *reinterpret_cast<const uint4*>(kr);
-                const uint4 b = *reinterpret_cast<const uint4*>(kr + HALF);
-                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-                const double2* fb = P.rope + (size_t)pos * HALF + j8 * 8;
-                const float4* cf = rs + tl * HALF + j8 * 8;
-                uint32_t w0[4], w1[4];
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    uint16_t lo0, lo1, hi0, hi1;
-                    rope_pair(__uint_as_float(aw[e2] << 16), __uint_as_float(bw[e2] << 16), cf[2 * e2], fb + 2 * e2,
-                              lo0, lo1);
-                    rope_pair(__uint_as_float(aw[e2] & 0xFFFF0000u), __uint_as_float(bw[e2] & 0xFFFF0000u),
-                              cf[2 * e2 + 1], fb + 2 * e2 + 1, hi0, hi1);
-                    w0[e2] = (uint32_t)lo0 | ((uint32_t)hi0 << 16);
-                    w1[e2] = (uint32_t)lo1 | ((uint32_t)hi1 << 16);
-                }
+                uint4 lo, hi;
+                rope8(*reinterpret_cast<const uint4*>(kr), *reinterpret_cast<const uint4*>(kr + HALF),
+                      rs + tl * HALF + j8 * 8, P.rope + (size_t)pos * HALF + j8 * 8, lo, hi);
                 uint16_t* dst = kc + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D + j8 * 8;
-                *reinterpret_cast<uint4*>(dst) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-                *reinterpret_cast<uint4*>(dst + HALF) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                *reinterpret_cast<uint4*>(dst) = lo;
+                *reinterpret_cast<uint4*>(dst + HALF) = hi;
             }
             if (p0 + tpp < cnt) {
                 // the next pass's bulk copies overwrite what was just read
@@ -935,9 +947,14 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         const uint32_t bar = wbar + 8 * stg;
         mbar_expect_tx(bar, STAGE);
         const int y = (page * P.Hkv + g) * kPage;
-        for (int hf = 0; hf < HALVES; ++hf) {
-            tma_load_2d(dst + hf * kPageHalfBytes, tmK, hf * 64, y, bar);
-            tma_load_2d(dst + KPAGE + hf * kPageHalfBytes, tmV, hf * 64, y, bar);
+        if (HALVES == 2) {
+            // one box per page-head: {64 columns, 16 rows, 2 halves} lands as
+            // [half][16 rows][128 B], the same swizzled image as two 2-D boxes
+            tma_load_3d(dst, tmK, 0, y, 0, bar);
+            tma_load_3d(dst + KPAGE, tmV, 0, y, 0, bar);
+        } else {
+            tma_load_2d(dst, tmK, 0, y, bar);
+            tma_load_2d(dst + KPAGE, tmV, 0, y, bar);
         }
     };
     // the first page id of every warp comes with the item: no load before it
@@ -947,20 +964,34 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         if (lane == 0) issue(k, pid);
     }
 
-    // Q rows of the group, RoPE'd in fp32, rows >= G zero
-    for (int i = tid; i < 16 * HALF; i += kThreads) {
-        const int row = i / HALF, j = i % HALF;
-        float y0 = 0.f, y1 = 0.f;
+    // Q rows of the group, RoPE'd in fp32, rows >= G zero: threads [0, QU) each
+    // rotate 8 consecutive pairs (one round trip for the whole tile).
+    constexpr int QU = 16 * (HALF / 8);
+    static_assert(QU <= kThreads, "decode prologue threads");
+    if (tid < QU) {
+        const int row = tid / (HALF / 8), c = tid % (HALF / 8);
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if (row < G) {
             const __nv_bfloat16* qr = P.q + ((size_t)R.qo0 * P.Hq + g * G + row) * D;
-            const float x0 = __bfloat162float(qr[j]), x1 = __bfloat162float(qr[j + HALF]);
-            const float4 cs = P.ropef[(size_t)pos * HALF + j];
-            const float c = cs.x, sn = cs.z;
-            y0 = x0 * c - x1 * sn;
-            y1 = x1 * c + x0 * sn;
+            const uint4 a = __ldg(reinterpret_cast<const uint4*>(qr) + c);
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(qr + HALF) + c);
+            const __nv_bfloat16* x0 = reinterpret_cast<const __nv_bfloat16*>(&a);
+            const __nv_bfloat16* x1 = reinterpret_cast<const __nv_bfloat16*>(&b);
+            const float4* cs = P.ropef + (size_t)pos * HALF + c * 8;
+            uint32_t ylo[4], yhi[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const float4 c0 = cs[e], c1 = cs[e + 1];
+                const float a0 = __bfloat162float(x0[e]), a1 = __bfloat162float(x0[e + 1]);
+                const float b0 = __bfloat162float(x1[e]), b1 = __bfloat162float(x1[e + 1]);
+                ylo[e >> 1] = pack_bf16(a0 * c0.x - b0 * c0.z, a1 * c1.x - b1 * c1.z);
+                yhi[e >> 1] = pack_bf16(b0 * c0.x + a0 * c0.z, b1 * c1.x + a1 * c1.z);
+            }
+            lo = make_uint4(ylo[0], ylo[1], ylo[2], ylo[3]);
+            hi = make_uint4(yhi[0], yhi[1], yhi[2], yhi[3]);
         }
-        *reinterpret_cast<__nv_bfloat16*>(qtile + sw128_off(16, row, j)) = __float2bfloat16_rn(y0);
-        *reinterpret_cast<__nv_bfloat16*>(qtile + sw128_off(16, row, j + HALF)) = __float2bfloat16_rn(y1);
+        *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c)) = lo;
+        *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c + HALF / 8)) = hi;
     }
     // the decode token's own K (fp64 RoPE, one rounding) and V: stash + page
     if (last_owner) {
@@ -1172,7 +1203,9 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_constant__ KParams P,
                                                                  const __grid_constant__ CUtensorMap tmK,
-                                                                 const __grid_constant__ CUtensorMap tmV) {
+                                                                 const __grid_constant__ CUtensorMap tmV,
+                                                                 const __grid_constant__ CUtensorMap tmK3,
+                                                                 const __grid_constant__ CUtensorMap tmV3) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(16) int s_item[kItemInts];
@@ -1230,7 +1263,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         else if (it[0] == kPrefill)
             run_prefill<D>(P, &tmK, &tmV, it, smem, &s_abort, pf_phase, tmem);
         else
-            run_decode<D>(P, &tmK, &tmV, it, smem, &s_abort, &s_flag, dec_phase);
+            run_decode<D>(P, &tmK3, &tmV3, it, smem, &s_abort, &s_flag, dec_phase);
         // shared memory written through the generic proxy this item (tiles,
         // scratch, patched rows) is next overwritten by TMA
         fence_proxy_async_shared();
@@ -1334,6 +1367,26 @@ int32_t make_page_map(CUtensorMap* m, void* base, int num_pages, int Hkv, int d)
     return SARATHI_OK;
 }
 
+// 3-D view of the same pool for d = 128: {64 columns, rows, 2 halves}, the
+// halves 128 bytes apart.  Box = 64 x 16 x 2: one page-head (4 KB) per copy.
+int32_t make_page_map3(CUtensorMap* m, void* base, int num_pages, int Hkv, int d) {
+    auto enc = encode_fn();
+    if (!enc) return fail(SARATHI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[3] = {64, (cuuint64_t)num_pages * Hkv * kPage, (cuuint64_t)(d / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)kPage, (cuuint32_t)(d / 64)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[128];
+        std::snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled (3-D page view) failed (%d)", (int)r);
+        return fail(SARATHI_ERR_CUDA, msg);
+    }
+    return SARATHI_OK;
+}
+
 struct DevState {
     int sms = 0;
     bool smem_set[2] = {false, false};
@@ -1426,6 +1479,13 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
     if (st) return st;
     st = make_page_map(&tmV, a->v_cache, a->num_pages, Hkv, d);
     if (st) return st;
+    CUtensorMap tmK3 = tmK, tmV3 = tmV;
+    if (d == 128) {
+        st = make_page_map3(&tmK3, a->k_cache, a->num_pages, Hkv, d);
+        if (st) return st;
+        st = make_page_map3(&tmV3, a->v_cache, a->num_pages, Hkv, d);
+        if (st) return st;
+    }
 
     KParams P;
     P.q = static_cast<const __nv_bfloat16*>(a->q);
@@ -1459,9 +1519,9 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
     const int grid = std::min(sms, in->n_items);
     cudaStream_t stream = (cudaStream_t)cuda_stream;
     if (d == 128)
-        mixed_step_kernel<128><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV);
+        mixed_step_kernel<128><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
     else
-        mixed_step_kernel<64><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV);
+        mixed_step_kernel<64><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "mixed_step_kernel launch");
     return SARATHI_OK;
