@@ -64,6 +64,11 @@ def _load():
     lib.oracle_plan.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _i32p,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p]
+    lib.oracle_plan_policy.restype = ctypes.c_int
+    lib.oracle_plan_policy.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _i32p,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int,
+                                       _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p]
     lib.oracle_append.restype = None
     lib.oracle_append.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _u16p, _u16p,
                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
@@ -113,9 +118,15 @@ def rope(x, pos: int, base: float = 10000.0) -> np.ndarray:
     return out
 
 
-def plan(states, prompt_len, num_computed, block_tables, budget: int, page_size: int):
-    """Stall-free budgeted batch: decodes, then running prefills, then waiting
-    prefills; returns (status, dict of metadata arrays)."""
+STALL_FREE, DECODE_MAXIMAL = 0, 1
+
+
+def plan(states, prompt_len, num_computed, block_tables, budget: int, page_size: int,
+         policy: int | None = None, max_batch: int = 0, align: int = 1):
+    """Budgeted batch; returns (status, dict of metadata arrays).  policy None:
+    stall-free through oracle_plan; otherwise oracle_plan_policy with the given
+    policy (STALL_FREE / DECODE_MAXIMAL: budget = chunk size), max_batch (B,
+    decode-maximal only, 0 = no limit) and chunk alignment."""
     lib = _load()
     n = len(states)
     bt_indptr = np.zeros(n + 1, dtype=np.int32)
@@ -133,11 +144,14 @@ def plan(states, prompt_len, num_computed, block_tables, budget: int, page_size:
     kvi = np.zeros(cap_pages, np.int32)
     last = np.zeros(max(n, 1), np.int32)
     counts = np.zeros(4, np.int32)
-    st = lib.oracle_plan(n, _i32(states) if n else np.zeros(1, np.int32),
-                         _i32(prompt_len) if n else np.zeros(1, np.int32),
-                         _i32(num_computed) if n else np.zeros(1, np.int32),
-                         bt_indptr, bt, int(budget), int(page_size), cap_pages,
-                         req_index, num_new, last_chunk, qo, kvp, kvi, last, counts)
+    reqs = (_i32(states) if n else np.zeros(1, np.int32), _i32(prompt_len) if n else np.zeros(1, np.int32),
+            _i32(num_computed) if n else np.zeros(1, np.int32), bt_indptr, bt)
+    outs = (req_index, num_new, last_chunk, qo, kvp, kvi, last, counts)
+    if policy is None:
+        st = lib.oracle_plan(n, *reqs, int(budget), int(page_size), cap_pages, *outs)
+    else:
+        st = lib.oracle_plan_policy(n, *reqs, int(policy), int(budget), int(max_batch), int(align),
+                                    int(page_size), cap_pages, *outs)
     ns = int(counts[0])
     meta = dict(
         n_sched=ns, num_decodes=int(counts[1]), nnz_pages=int(counts[2]), num_tokens=int(counts[3]),

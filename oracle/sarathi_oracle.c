@@ -12,9 +12,17 @@
  *   [SS]  "Sarathi-Serve 完全拆解：分块 Prefill 与无停顿批处理如何兼顾吞吐和尾延迟"
  *   [CP]  "Chunked Prefill 与 PD 分离：切片混批，还是拆开两个池"
  *   [ST]  "分块预填充与 Stall-free 调度：把 LLM 推理的吞吐-延迟权衡算清楚"
+ *   [SA]  "Sarathi：让解码搭上 prefill 的顺风车"
  *
  * Functions and the passages they restate:
- *   oracle_plan       [CP] §3.1 (decode -> in-progress chunk -> new request);
+ *   oracle_plan_policy  the two batch policies:
+ *                     stall-free [CP] §3.1 (decode -> in-progress chunk -> new
+ *                     request, the budget shared by several chunks);
+ *                     decode-maximal [SA] §"Decode-maximal batching：顺车的账本"
+ *                     (one prefill chunk plus as many decodes as fit, at most
+ *                     B - 1 of them); optional chunk alignment, [SS] §"257 为什么
+ *                     可能比 256 慢 32%" (candidate sizes aligned to 32).
+ *   oracle_plan       stall-free without alignment:
  *                     [SS] §"一个 512-token 预算的例子" (budget filled in turn,
  *                     several chunks per batch allowed);
  *                     [ST] §六·补二 (chunk = min(remaining budget, remaining prompt));
@@ -53,6 +61,9 @@
 #define ORC_DECODE 0
 #define ORC_PREFILL_RUNNING 1
 #define ORC_PREFILL_WAITING 2
+
+#define ORC_POLICY_STALL_FREE 0
+#define ORC_POLICY_DECODE_MAXIMAL 1
 
 /* ------------------------------------------------------------------------- */
 /* bf16 <-> double                                                            */
@@ -129,40 +140,82 @@ void oracle_rope(const double* x, int d, int64_t pos, double base, double* out) 
  *   counts[3] = tokens scheduled.
  * Returns ORC_OK, ORC_OVER_BUDGET_DECODES (output valid), ORC_CAPACITY,
  * ORC_INVALID. */
-int oracle_plan(int n_reqs, const int32_t* state, const int32_t* prompt_len,
-                const int32_t* num_computed, const int32_t* bt_indptr, const int32_t* bt,
-                int budget, int page_size, int cap_pages,
-                int32_t* req_index, int32_t* num_new, int32_t* last_chunk,
-                int32_t* qo_indptr, int32_t* kv_page_indptr, int32_t* kv_page_indices,
-                int32_t* kv_last_page_len, int32_t* counts) {
-    if (n_reqs < 0 || budget <= 0 || page_size <= 0) return ORC_INVALID;
+/* A chunk that does not finish its prompt is cut down to a multiple of
+ * `align` tokens (align 1: no cut); the final chunk of a prompt keeps its size.
+ * [SS] §"257 为什么可能比 256 慢 32%": the official code aligns candidate chunk
+ * sizes to multiples of 32 -- an execution-shape choice, not a semantic one. */
+static int aligned_take(int take, int rem, int align) {
+    if (align > 1 && take < rem) take -= take % align;
+    return take;
+}
+
+int oracle_plan_policy(int n_reqs, const int32_t* state, const int32_t* prompt_len,
+                       const int32_t* num_computed, const int32_t* bt_indptr, const int32_t* bt,
+                       int policy, int budget, int max_batch, int align, int page_size, int cap_pages,
+                       int32_t* req_index, int32_t* num_new, int32_t* last_chunk,
+                       int32_t* qo_indptr, int32_t* kv_page_indptr, int32_t* kv_page_indices,
+                       int32_t* kv_last_page_len, int32_t* counts) {
+    if (n_reqs < 0 || budget <= 0 || page_size <= 0 || align < 1 || max_batch < 0) return ORC_INVALID;
+    if (policy != ORC_POLICY_STALL_FREE && policy != ORC_POLICY_DECODE_MAXIMAL) return ORC_INVALID;
     for (int i = 0; i < n_reqs; ++i) {
         if (state[i] < ORC_DECODE || state[i] > ORC_PREFILL_WAITING) return ORC_INVALID;
         if (num_computed[i] < 0) return ORC_INVALID;
         if (state[i] != ORC_DECODE && prompt_len[i] < num_computed[i]) return ORC_INVALID;
         if (bt_indptr[i + 1] < bt_indptr[i]) return ORC_INVALID;
     }
-    int left = budget;
     int n = 0, decodes = 0;
-    /* 1) every running decode: one token each, [CP] §3.1 first class */
-    for (int i = 0; i < n_reqs; ++i) {
-        if (state[i] != ORC_DECODE) continue;
-        req_index[n] = i; num_new[n] = 1; last_chunk[n] = 1;
-        ++n; ++decodes; left -= 1;
-    }
-    /* 2) in-progress prefills, then 3) new prefills: min(remaining prompt,
-     *    remaining budget) each, [ST] §六·补二; several chunks may share the
-     *    budget, [SS] §"一个 512-token 预算的例子". */
-    for (int cls = ORC_PREFILL_RUNNING; cls <= ORC_PREFILL_WAITING; ++cls) {
+    if (policy == ORC_POLICY_STALL_FREE) {
+        int left = budget;
+        /* 1) every running decode: one token each, [CP] §3.1 first class */
         for (int i = 0; i < n_reqs; ++i) {
-            if (state[i] != cls) continue;
-            int rem = prompt_len[i] - num_computed[i];
-            int room = left > 0 ? left : 0;
-            int take = rem < room ? rem : room;
-            if (take <= 0) continue;
-            req_index[n] = i; num_new[n] = take;
-            last_chunk[n] = (num_computed[i] + take == prompt_len[i]) ? 1 : 0;
-            ++n; left -= take;
+            if (state[i] != ORC_DECODE) continue;
+            req_index[n] = i; num_new[n] = 1; last_chunk[n] = 1;
+            ++n; ++decodes; left -= 1;
+        }
+        /* 2) in-progress prefills, then 3) new prefills: min(remaining prompt,
+         *    remaining budget) each, [ST] §六·补二; several chunks may share the
+         *    budget, [SS] §"一个 512-token 预算的例子". */
+        for (int cls = ORC_PREFILL_RUNNING; cls <= ORC_PREFILL_WAITING; ++cls) {
+            for (int i = 0; i < n_reqs; ++i) {
+                if (state[i] != cls) continue;
+                int rem = prompt_len[i] - num_computed[i];
+                int room = left > 0 ? left : 0;
+                int take = aligned_take(rem < room ? rem : room, rem, align);
+                if (take <= 0) continue;
+                req_index[n] = i; num_new[n] = take;
+                last_chunk[n] = (num_computed[i] + take == prompt_len[i]) ? 1 : 0;
+                ++n; left -= take;
+            }
+        }
+    } else {
+        /* decode-maximal, [SA] §"Decode-maximal batching：顺车的账本": the batch
+         * holds ONE prefill chunk of min(chunk size, remaining prompt) tokens --
+         * from the first in-progress prefill, else the first new one -- and then
+         * as many decodes as fit: at most B - 1 next to a chunk (its KV takes a
+         * slot too), at most B without one; B = max_batch, 0 for no limit.
+         * Decodes are listed first, in caller order, like every plan here. */
+        int chunk_req = -1, chunk_take = 0;
+        for (int cls = ORC_PREFILL_RUNNING; cls <= ORC_PREFILL_WAITING && chunk_req < 0; ++cls) {
+            for (int i = 0; i < n_reqs; ++i) {
+                if (state[i] != cls) continue;
+                int rem = prompt_len[i] - num_computed[i];
+                if (rem <= 0) continue;
+                chunk_req = i;
+                chunk_take = aligned_take(rem < budget ? rem : budget, rem, align);
+                break;
+            }
+        }
+        if (chunk_take <= 0) chunk_req = -1;
+        int cap = max_batch > 0 ? max_batch - (chunk_req >= 0 ? 1 : 0) : n_reqs;
+        for (int i = 0; i < n_reqs && decodes < cap; ++i) {
+            if (state[i] != ORC_DECODE) continue;
+            req_index[n] = i; num_new[n] = 1; last_chunk[n] = 1;
+            ++n; ++decodes;
+        }
+        if (chunk_req >= 0) {
+            req_index[n] = chunk_req; num_new[n] = chunk_take;
+            last_chunk[n] = (num_computed[chunk_req] + chunk_take == prompt_len[chunk_req]) ? 1 : 0;
+            ++n;
         }
     }
     /* metadata: kv_len = h + n, pages = ceil(kv_len / page), last-page length */
@@ -183,7 +236,20 @@ int oracle_plan(int n_reqs, const int32_t* state, const int32_t* prompt_len,
         kv_page_indptr[s + 1] = pages_out;
     }
     counts[0] = n; counts[1] = decodes; counts[2] = pages_out; counts[3] = tokens;
-    return decodes > budget ? ORC_OVER_BUDGET_DECODES : ORC_OK;
+    return (policy == ORC_POLICY_STALL_FREE && decodes > budget) ? ORC_OVER_BUDGET_DECODES : ORC_OK;
+}
+
+/* Stall-free with no alignment: [CP] §3.1, [ST] §六·补二, [SS] §"一个 512-token
+ * 预算的例子". */
+int oracle_plan(int n_reqs, const int32_t* state, const int32_t* prompt_len,
+                const int32_t* num_computed, const int32_t* bt_indptr, const int32_t* bt,
+                int budget, int page_size, int cap_pages,
+                int32_t* req_index, int32_t* num_new, int32_t* last_chunk,
+                int32_t* qo_indptr, int32_t* kv_page_indptr, int32_t* kv_page_indices,
+                int32_t* kv_last_page_len, int32_t* counts) {
+    return oracle_plan_policy(n_reqs, state, prompt_len, num_computed, bt_indptr, bt, ORC_POLICY_STALL_FREE,
+                              budget, 0, 1, page_size, cap_pages, req_index, num_new, last_chunk, qo_indptr,
+                              kv_page_indptr, kv_page_indices, kv_last_page_len, counts);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -315,3 +315,141 @@ def test_reread_closed_form_8192(c, expect):
         total += oracle.reread_tokens(m, 16)
         done += int(m["num_new"][0])
     assert total == expect
+
+
+# ---------------------------------------------------------------- plan policies
+# Decode-maximal batching ("Sarathi：让解码搭上 prefill 的顺风车", section
+# "Decode-maximal batching：顺车的账本") and chunk alignment ("Sarathi-Serve
+# 完全拆解", section "257 为什么可能比 256 慢 32%").
+
+def _random_request_set(rng, n_dec_max=12, n_pf_max=4):
+    n_dec = int(rng.integers(0, n_dec_max + 1))
+    n_pf = int(rng.integers(0, n_pf_max + 1))
+    states, prompt, computed = [], [], []
+    for _ in range(n_dec):
+        states.append(W.DECODE); prompt.append(0); computed.append(int(rng.integers(0, 3000)))
+    for _ in range(n_pf):
+        st = W.PREFILL_RUNNING if rng.random() < 0.5 else W.PREFILL_WAITING
+        L = int(rng.integers(1, 2500))
+        h = int(rng.integers(1, L + 1)) - 1 if st == W.PREFILL_RUNNING else 0
+        states.append(st); prompt.append(L); computed.append(h)
+    order = rng.permutation(len(states))
+    states = [states[i] for i in order]; prompt = [prompt[i] for i in order]; computed = [computed[i] for i in order]
+    tables = [np.arange(300, dtype=np.int32) + 300 * i for i in range(len(states))]
+    return states, prompt, computed, tables
+
+
+def test_decode_maximal_table2_example():
+    g = json.load(open(os.path.join(GOLDEN, "decode_maximal_table2.json")))
+    B, C, L, ctx = g["batch_size_B"], g["chunk_tokens"], g["prompt_len"], g["decode_context"]
+    # more decodes are waiting than fit: the batch takes the first B - 1 of them
+    states = [W.DECODE] * 2 + [W.PREFILL_WAITING] + [W.DECODE] * 3
+    prompt = [0, 0, L, 0, 0, 0]
+    computed = [ctx, ctx, 0, ctx, ctx, ctx]
+    tables = [np.arange(100, dtype=np.int32) + 100 * i for i in range(6)]
+    st, m = oracle.plan(states, prompt, computed, tables, C, 16, policy=oracle.DECODE_MAXIMAL, max_batch=B)
+    assert st == oracle.OK
+    e = g["expect"]
+    assert m["num_decodes"] == e["decodes"] and list(m["req_index"][:3]) == [0, 1, 3]
+    assert m["req_index"][3] == 2 and m["num_new"][3] == e["chunk"] and m["last_chunk"][3] == 0
+    assert m["num_tokens"] == e["total_tokens"]
+    # next step: the prompt's last 3 tokens ride with 3 decodes
+    computed2 = [ctx + 1, ctx + 1, C, ctx + 1, ctx, ctx]
+    states2 = [W.DECODE, W.DECODE, W.PREFILL_RUNNING, W.DECODE, W.DECODE, W.DECODE]
+    st, m2 = oracle.plan(states2, prompt, computed2, tables, C, 16, policy=oracle.DECODE_MAXIMAL, max_batch=B)
+    n = g["next_step"]
+    assert m2["num_new"][-1] == n["chunk"] and m2["last_chunk"][-1] == 1
+    assert m2["num_decodes"] == n["decodes"] and m2["num_tokens"] == n["total_tokens"]
+
+
+def test_decode_maximal_one_chunk_and_decode_cap_on_random_sets():
+    rng = np.random.default_rng(21)
+    for _ in range(300):
+        states, prompt, computed, tables = _random_request_set(rng)
+        C = int(rng.integers(1, 1500))
+        B = int(rng.integers(0, 10))
+        st, m = oracle.plan(states, prompt, computed, tables, C, 16, policy=oracle.DECODE_MAXIMAL, max_batch=B)
+        assert st == oracle.OK
+        pending = [i for c in (W.PREFILL_RUNNING, W.PREFILL_WAITING) for i in range(len(states))
+                   if states[i] == c and prompt[i] > computed[i]]
+        rows = list(m["req_index"])
+        chunks = [s for s, i in enumerate(rows) if states[i] != W.DECODE]
+        # exactly one chunk when a prompt is pending: the first in-progress one, else the first new one
+        assert len(chunks) == (1 if pending else 0)
+        if pending:
+            s = chunks[0]
+            assert s == len(rows) - 1 and rows[s] == pending[0]
+            assert m["num_new"][s] == min(C, prompt[pending[0]] - computed[pending[0]])
+        decs = [i for i in range(len(states)) if states[i] == W.DECODE]
+        cap = len(decs) if B == 0 else min(len(decs), B - (1 if pending else 0))
+        assert rows[:m["num_decodes"]] == decs[:cap] and m["num_decodes"] == cap
+
+
+def test_decode_maximal_with_one_prompt_equals_stall_free():
+    # one pending prompt and no batch limit: the stall-free plan with budget
+    # decodes + C schedules exactly the same rows
+    rng = np.random.default_rng(22)
+    for _ in range(200):
+        states, prompt, computed, tables = _random_request_set(rng, n_pf_max=0)
+        L = int(rng.integers(1, 2500)); h = int(rng.integers(0, L))
+        pos = int(rng.integers(0, len(states) + 1))
+        states.insert(pos, W.PREFILL_RUNNING if h else W.PREFILL_WAITING)
+        prompt.insert(pos, L); computed.insert(pos, h)
+        tables = [np.arange(300, dtype=np.int32) + 300 * i for i in range(len(states))]
+        C = int(rng.integers(1, 1500))
+        n_dec = sum(1 for s in states if s == W.DECODE)
+        st1, a = oracle.plan(states, prompt, computed, tables, C, 16, policy=oracle.DECODE_MAXIMAL, max_batch=0)
+        st2, b = oracle.plan(states, prompt, computed, tables, n_dec + C, 16)
+        assert st1 == st2 == oracle.OK
+        for key in ("req_index", "num_new", "last_chunk", "qo_indptr", "kv_page_indptr", "kv_page_indices",
+                    "kv_last_page_len"):
+            assert np.array_equal(a[key], b[key]), key
+
+
+def test_alignment_one_changes_nothing():
+    rng = np.random.default_rng(23)
+    for _ in range(200):
+        states, prompt, computed, tables = _random_request_set(rng)
+        budget = int(rng.integers(1, 3000))
+        st1, a = oracle.plan(states, prompt, computed, tables, budget, 16)
+        st2, b = oracle.plan(states, prompt, computed, tables, budget, 16, policy=oracle.STALL_FREE, align=1)
+        assert st1 == st2
+        for key in ("req_index", "num_new", "kv_page_indices"):
+            assert np.array_equal(a[key], b[key]), key
+
+
+def test_aligned_worked_example_512_by_hand():
+    # the 512-token example with chunks aligned to 32: P's 300 tokens finish its
+    # prompt and keep their size; Q's min(900, 132) = 132 is cut to 128
+    ctx = np.random.default_rng(5).integers(256, 4096, size=80, endpoint=True)
+    states = [W.DECODE] * 80 + [W.PREFILL_RUNNING, W.PREFILL_RUNNING]
+    prompt = [0] * 80 + [300, 768 + 900]
+    computed = list(ctx) + [0, 768]
+    tables = [np.arange(2000, dtype=np.int32) + 2000 * i for i in range(82)]
+    st, m = oracle.plan(states, prompt, computed, tables, 512, 16, policy=oracle.STALL_FREE, align=32)
+    assert st == oracle.OK
+    assert list(m["num_new"][80:]) == [300, 128] and list(m["last_chunk"][80:]) == [1, 0]
+    assert m["num_tokens"] == 508
+    # decode-maximal with the same alignment: C = 1021 leaves a 992-token chunk
+    st, m = oracle.plan([W.PREFILL_WAITING], [1024], [0], [np.arange(100, dtype=np.int32)], 1021, 16,
+                        policy=oracle.DECODE_MAXIMAL, align=32)
+    assert list(m["num_new"]) == [992]
+
+
+def test_aligned_chunks_are_multiples_unless_final():
+    rng = np.random.default_rng(24)
+    for _ in range(300):
+        states, prompt, computed, tables = _random_request_set(rng)
+        budget = int(rng.integers(1, 3000))
+        align = int(rng.choice([8, 16, 32, 128]))
+        for pol in (oracle.STALL_FREE, oracle.DECODE_MAXIMAL):
+            st, m = oracle.plan(states, prompt, computed, tables, budget, 16, policy=pol, align=align)
+            for s, i in enumerate(m["req_index"]):
+                if states[i] == W.DECODE:
+                    continue
+                n = int(m["num_new"][s])
+                assert n > 0
+                assert m["last_chunk"][s] == 1 or n % align == 0
+            n_dec = m["num_decodes"]
+            if pol == oracle.STALL_FREE and n_dec <= budget:
+                assert m["num_tokens"] <= budget
