@@ -374,6 +374,51 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
+def policy_sweep(dev, flush):
+    """The Mistral-7B-like request set (80 decodes, prefills P and Q) planned by
+    each batch policy: the stall-free 512-token budget, the same with chunks
+    aligned to 32, and decode-maximal batching with one 432-token chunk (no
+    batch limit) or one 256-token chunk beside at most 47 decodes (B = 48).
+    Step time: CUDA events, L2 flushed before each launch, median of 5."""
+    import torch
+    import chunked_prefill_mixed_gb300 as S
+    from chunked_prefill_mixed_gb300.runner import StepRunner
+    wl = W.mistral()
+    sh = wl.shape
+    kc, vc = W.history_cache_torch(wl.num_pages, sh, wl.seed, dev)
+    runner = StepRunner(sh.H_q, sh.H_kv, sh.d, 8192, device=dev)
+    res = {}
+    for label, pol in (("stall_free_512", S.PlanPolicy(S.POLICY_STALL_FREE, 512, 0, 1)),
+                       ("stall_free_512_align32", S.PlanPolicy(S.POLICY_STALL_FREE, 512, 0, 32)),
+                       ("decode_maximal_c432", S.PlanPolicy(S.POLICY_DECODE_MAXIMAL, 432, 0, 1)),
+                       ("decode_maximal_c256_b48", S.PlanPolicy(S.POLICY_DECODE_MAXIMAL, 256, 48, 1))):
+        st, info, packed = runner.plan(*wl.arrays(), 0, policy=pol)
+        pd = runner.upload(packed)
+        n = info.num_tokens
+        q, k, v = W.new_token_values(n, sh, wl.seed)
+
+        def bf(x):
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+        qd, kd, vd = bf(q), bf(k), bf(v)
+        out = torch.empty((n, sh.H_q, sh.d), dtype=torch.bfloat16, device=dev)
+        ms = []
+        for i in range(7):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            runner.run(qd, kd, vd, kc, vc, out, pd, info)
+            b.record()
+            b.synchronize()
+            if i >= 2:
+                ms.append(a.elapsed_time(b))
+        if runner.status() != 0:
+            raise RuntimeError("device error in the policy sweep")
+        us = 1e3 * statistics.median(ms)
+        res[label] = {"tokens": n, "decodes": info.num_decodes, "prefill_tokens": n - info.num_decodes,
+                      "us": round(us, 1), "tokens_per_s": round(n / us * 1e6)}
+    return res
+
+
 def run_sweep(args):
     """Whole-prompt prefill of the 8192-token Llama-2-7B-like prompt in chunks
     of 512 / 1024 / 2048 and in one shot (the history re-read of chunked
@@ -440,7 +485,8 @@ def run_sweep(args):
            "chunks": {str(c): v for c, v in chunks.items()},
            "tile_quantisation_us_after_4096_history": {str(k): v for k, v in tq.items()},
            "ratio_257_over_256": tq[257] / tq[256], "ratio_129_over_128": tq[129] / tq[128],
-           "ratio_513_over_512": tq[513] / tq[512]}
+           "ratio_513_over_512": tq[513] / tq[512],
+           "plan_policies": policy_sweep(dev, flush)}
     print(json.dumps(res), flush=True)
     return None
 

@@ -23,7 +23,7 @@ DECODE, PREFILL_RUNNING, PREFILL_WAITING = 0, 1, 2
 ABI_VERSION = 2   # SARATHI_ABI_VERSION of include/sarathi.h
 ITEM_INTS = 24    # SARATHI_ITEM_INTS
 
-EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_rope_table", "sarathi_mixed_attn",
+EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_plan_ex", "sarathi_rope_table", "sarathi_mixed_attn",
             "sarathi_mixed_attn_noalloc", "sarathi_workspace_status", "sarathi_last_error", "sarathi_abi_version")
 
 
@@ -36,6 +36,14 @@ class SarathiError(RuntimeError):
 class Request(ctypes.Structure):
     _fields_ = [("state", ctypes.c_int32), ("prompt_len", ctypes.c_int32), ("num_computed", ctypes.c_int32),
                 ("num_pages", ctypes.c_int32), ("pages", ctypes.POINTER(ctypes.c_int32))]
+
+
+POLICY_STALL_FREE, POLICY_DECODE_MAXIMAL = 0, 1
+
+
+class PlanPolicy(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("token_budget", ctypes.c_int32), ("max_batch", ctypes.c_int32),
+                ("chunk_align", ctypes.c_int32)]
 
 
 class Shape(ctypes.Structure):
@@ -83,6 +91,10 @@ def load(build_if_missing: bool = True):
     lib.sarathi_plan.restype = ctypes.c_int32
     lib.sarathi_plan.argtypes = [ctypes.POINTER(Request), ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Shape),
                                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(PlanInfo)]
+    lib.sarathi_plan_ex.restype = ctypes.c_int32
+    lib.sarathi_plan_ex.argtypes = [ctypes.POINTER(Request), ctypes.c_int32, ctypes.POINTER(PlanPolicy),
+                                    ctypes.POINTER(Shape), ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
+                                    ctypes.POINTER(PlanInfo)]
     lib.sarathi_rope_table.restype = ctypes.c_int32
     lib.sarathi_rope_table.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
                                        ctypes.c_void_p]
@@ -148,6 +160,18 @@ def sarathi_plan(reqs, n_reqs: int, token_budget: int, shape: Shape, num_sms: in
     st = load().sarathi_plan(reqs, n_reqs, token_budget, ctypes.byref(shape), num_sms,
                              host_buf.ctypes.data, host_buf.nbytes, ctypes.byref(info))
     _check(st, "sarathi_plan", allow=(OK, WARN_OVER_BUDGET_DECODES))
+    return st, info, host_buf[:info.packed_ints]
+
+def sarathi_plan_ex(reqs, n_reqs: int, policy: PlanPolicy, shape: Shape, num_sms: int,
+                    host_buf: np.ndarray | None = None):
+    """sarathi_plan with a batch policy; returns (status, PlanInfo, packed int32 array)."""
+    if host_buf is None:
+        hb, _ = sarathi_plan_bounds(reqs, n_reqs, policy.token_budget, shape, num_sms)
+        host_buf = np.zeros(hb // 4 + 4, dtype=np.int32)
+    info = PlanInfo()
+    st = load().sarathi_plan_ex(reqs, n_reqs, ctypes.byref(policy), ctypes.byref(shape), num_sms,
+                                host_buf.ctypes.data, host_buf.nbytes, ctypes.byref(info))
+    _check(st, "sarathi_plan_ex", allow=(OK, WARN_OVER_BUDGET_DECODES))
     return st, info, host_buf[:info.packed_ints]
 
 

@@ -106,11 +106,12 @@ extern "C" int32_t sarathi_plan_bounds(const sarathi_request* reqs, int32_t n_re
     const int64_t T = n_dec + token_budget;
     const int64_t appends = T / kAppendTokens + n;
     const int64_t tiles = (T / tokens_per_tile(group) + n) * Hkv;
-    // decode splits: sum over decodes and kv heads of ceil(np / split) with
-    // split >= decode page-heads / (num_sms * kDecodeItemsPerSm), so at most
-    // num_sms * kDecodeItemsPerSm + (decodes x kv heads) items
+    // decode splits: sum over one-token rows (decodes, and prefill chunks of one
+    // token) and kv heads of ceil(np / split) with split >= their page-heads /
+    // (num_sms * kDecodeItemsPerSm), so at most num_sms * kDecodeItemsPerSm +
+    // (rows x kv heads) items
     const int64_t dec_items =
-        std::min<int64_t>((pages / kDecodeMinSplitPages + n) * Hkv, (int64_t)num_sms * kDecodeItemsPerSm + n_dec * Hkv);
+        std::min<int64_t>((pages / kDecodeMinSplitPages + n) * Hkv, (int64_t)num_sms * kDecodeItemsPerSm + n * Hkv);
     const int64_t items = appends + tiles + dec_items;
     const int64_t ints = 6 * n + 2 + pages + 8 + items * kItemInts;
     if (host_buf_bytes) *host_buf_bytes = (size_t)ints * 4;
@@ -122,42 +123,91 @@ extern "C" int32_t sarathi_plan_bounds(const sarathi_request* reqs, int32_t n_re
     return SARATHI_OK;
 }
 
+// A chunk that does not finish its prompt is cut down to a multiple of align
+// ("Sarathi-Serve 完全拆解", §"257 为什么可能比 256 慢 32%"); a prompt's final
+// chunk keeps its size.
+inline int64_t aligned_take(int64_t take, int64_t rem, int32_t align) {
+    return (align > 1 && take < rem) ? take - take % align : take;
+}
+
 extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int32_t token_budget,
                                 const sarathi_shape* shape, int32_t num_sms,
                                 int32_t* host_buf, size_t host_buf_bytes, sarathi_plan_info* info) {
+    const sarathi_plan_policy policy = {SARATHI_POLICY_STALL_FREE, token_budget, 0, 1};
+    return sarathi_plan_ex(reqs, n_reqs, &policy, shape, num_sms, host_buf, host_buf_bytes, info);
+}
+
+extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, const sarathi_plan_policy* policy,
+                                   const sarathi_shape* shape, int32_t num_sms,
+                                   int32_t* host_buf, size_t host_buf_bytes, sarathi_plan_info* info) {
     if (!info) return fail(SARATHI_ERR_INVALID_ARG, "info is NULL");
     std::memset(info, 0, sizeof *info);
+    if (!policy) return fail(SARATHI_ERR_INVALID_ARG, "policy is NULL");
     int32_t st = check_shape(shape);
     if (st) return st;
     st = validate_requests(reqs, n_reqs);
     if (st) return st;
+    const int32_t token_budget = policy->token_budget;
+    if (policy->kind != SARATHI_POLICY_STALL_FREE && policy->kind != SARATHI_POLICY_DECODE_MAXIMAL)
+        return fail(SARATHI_ERR_INVALID_ARG, "unknown policy kind");
     if (token_budget <= 0) return fail(SARATHI_ERR_INVALID_ARG, "token_budget must be positive");
+    if (policy->chunk_align < 1) return fail(SARATHI_ERR_INVALID_ARG, "chunk_align must be >= 1");
+    if (policy->max_batch < 0 || (policy->kind == SARATHI_POLICY_STALL_FREE && policy->max_batch != 0))
+        return fail(SARATHI_ERR_INVALID_ARG, "max_batch must be 0 (stall-free) or >= 0 (decode-maximal)");
     if (num_sms <= 0) return fail(SARATHI_ERR_INVALID_ARG, "num_sms must be positive");
 
     const int Hkv = shape->num_heads_kv;
     const int group = shape->num_heads_q / Hkv;
     const int d = shape->head_dim;
 
-    // ---- 1. the budgeted batch: decodes, running prefills, waiting prefills
+    // ---- 1. the batch
     std::vector<Sched> sched;
     sched.reserve(n_reqs);
-    int64_t left = token_budget;
     int32_t decodes = 0;
-    for (int32_t i = 0; i < n_reqs; ++i)
-        if (reqs[i].state == SARATHI_DECODE) {
-            sched.push_back({i, 1});
-            ++decodes;
-            --left;
-        }
-    for (int cls = SARATHI_PREFILL_RUNNING; cls <= SARATHI_PREFILL_WAITING; ++cls)
-        for (int32_t i = 0; i < n_reqs; ++i) {
-            if (reqs[i].state != cls) continue;
-            int64_t rem = (int64_t)reqs[i].prompt_len - reqs[i].num_computed;
-            int64_t take = std::min<int64_t>(rem, std::max<int64_t>(left, 0));
-            if (take <= 0) continue;
-            sched.push_back({i, (int32_t)take});
-            left -= take;
-        }
+    const int32_t align = policy->chunk_align;
+    if (policy->kind == SARATHI_POLICY_STALL_FREE) {
+        // decodes, running prefills, waiting prefills, each chunk as large as
+        // the budget left allows
+        int64_t left = token_budget;
+        for (int32_t i = 0; i < n_reqs; ++i)
+            if (reqs[i].state == SARATHI_DECODE) {
+                sched.push_back({i, 1});
+                ++decodes;
+                --left;
+            }
+        for (int cls = SARATHI_PREFILL_RUNNING; cls <= SARATHI_PREFILL_WAITING; ++cls)
+            for (int32_t i = 0; i < n_reqs; ++i) {
+                if (reqs[i].state != cls) continue;
+                int64_t rem = (int64_t)reqs[i].prompt_len - reqs[i].num_computed;
+                int64_t take = aligned_take(std::min<int64_t>(rem, std::max<int64_t>(left, 0)), rem, align);
+                if (take <= 0) continue;
+                sched.push_back({i, (int32_t)take});
+                left -= take;
+            }
+    } else {
+        // decode-maximal ("Sarathi：让解码搭上 prefill 的顺风车", §"Decode-maximal
+        // batching：顺车的账本"): one chunk, then up to B - 1 decodes beside it
+        int32_t chunk_req = -1;
+        int64_t chunk_take = 0;
+        for (int cls = SARATHI_PREFILL_RUNNING; cls <= SARATHI_PREFILL_WAITING && chunk_req < 0; ++cls)
+            for (int32_t i = 0; i < n_reqs; ++i) {
+                if (reqs[i].state != cls) continue;
+                int64_t rem = (int64_t)reqs[i].prompt_len - reqs[i].num_computed;
+                if (rem <= 0) continue;
+                chunk_req = i;
+                chunk_take = aligned_take(std::min<int64_t>(rem, token_budget), rem, align);
+                break;
+            }
+        if (chunk_take <= 0) chunk_req = -1;
+        const int64_t cap =
+            policy->max_batch > 0 ? (int64_t)policy->max_batch - (chunk_req >= 0 ? 1 : 0) : (int64_t)n_reqs;
+        for (int32_t i = 0; i < n_reqs && decodes < cap; ++i)
+            if (reqs[i].state == SARATHI_DECODE) {
+                sched.push_back({i, 1});
+                ++decodes;
+            }
+        if (chunk_req >= 0) sched.push_back({chunk_req, (int32_t)chunk_take});
+    }
     const int32_t ns = (int32_t)sched.size();
 
     // ---- 2. per-row KV extent, checked against the block tables
@@ -342,5 +392,6 @@ extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int
     for (auto& it : appends) put(it);
     for (auto& t : attn) put(t.it);
     set_error("");
-    return decodes > token_budget ? SARATHI_WARN_OVER_BUDGET_DECODES : SARATHI_OK;
+    return (policy->kind == SARATHI_POLICY_STALL_FREE && decodes > token_budget) ? SARATHI_WARN_OVER_BUDGET_DECODES
+                                                                                 : SARATHI_OK;
 }

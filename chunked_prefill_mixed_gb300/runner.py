@@ -9,8 +9,8 @@ import math
 import numpy as np
 import torch
 
-from . import (PlanInfo, Shape, make_requests, sarathi_mixed_attn, sarathi_plan, sarathi_plan_bounds,
-               sarathi_rope_table, sarathi_workspace_status)
+from . import (PlanInfo, PlanPolicy, Shape, make_requests, sarathi_mixed_attn, sarathi_plan, sarathi_plan_bounds,
+               sarathi_plan_ex, sarathi_rope_table, sarathi_workspace_status)
 
 
 class StepRunner:
@@ -27,14 +27,18 @@ class StepRunner:
         self.workspace = torch.zeros(1 << 16, dtype=torch.uint8, device=self.device)
         self._host_buf = np.zeros(0, dtype=np.int32)
 
-    def plan(self, states, prompt_len, num_computed, block_tables, budget: int):
+    def plan(self, states, prompt_len, num_computed, block_tables, budget: int, policy: PlanPolicy | None = None):
         """Plans into a host buffer the runner keeps (grown when a batch needs
         more); the returned packed array is a view of it, valid until the
-        next call."""
+        next call.  policy: a PlanPolicy for sarathi_plan_ex (its token_budget
+        is used); None plans with sarathi_plan and `budget`."""
         reqs, keep = make_requests(states, prompt_len, num_computed, block_tables)
-        hb, _ = sarathi_plan_bounds(reqs, len(states), budget, self.shape, self.num_sms)
+        tb = policy.token_budget if policy is not None else budget
+        hb, _ = sarathi_plan_bounds(reqs, len(states), tb, self.shape, self.num_sms)
         if self._host_buf.nbytes < hb:
             self._host_buf = np.zeros(max(hb // 4 + 4, 2 * self._host_buf.size), dtype=np.int32)
+        if policy is not None:
+            return sarathi_plan_ex(reqs, len(states), policy, self.shape, self.num_sms, self._host_buf)
         return sarathi_plan(reqs, len(states), budget, self.shape, self.num_sms, self._host_buf)
 
     def ensure_workspace(self, nbytes: int):

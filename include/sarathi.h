@@ -26,6 +26,7 @@
  *   [SS] "Sarathi-Serve 完全拆解：分块 Prefill 与无停顿批处理如何兼顾吞吐和尾延迟"
  *   [CP] "Chunked Prefill 与 PD 分离：切片混批，还是拆开两个池"
  *   [ST] "分块预填充与 Stall-free 调度：把 LLM 推理的吞吐-延迟权衡算清楚"
+ *   [SA] "Sarathi：让解码搭上 prefill 的顺风车"
  */
 #ifndef SARATHI_H_
 #define SARATHI_H_
@@ -130,6 +131,38 @@ int32_t sarathi_plan_bounds(const sarathi_request* reqs, int32_t n_reqs, int32_t
 int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int32_t token_budget,
                      const sarathi_shape* shape, int32_t num_sms,
                      int32_t* host_buf, size_t host_buf_bytes, sarathi_plan_info* info);
+
+/* Batch policies for sarathi_plan_ex. */
+#define SARATHI_POLICY_STALL_FREE 0     /* the rule of sarathi_plan above              */
+#define SARATHI_POLICY_DECODE_MAXIMAL 1 /* [SA] §"Decode-maximal batching：顺车的账本"  */
+
+typedef struct sarathi_plan_policy {
+    int32_t kind;          /* SARATHI_POLICY_*                                          */
+    int32_t token_budget;  /* stall-free: tokens per step; decode-maximal: chunk size  */
+    int32_t max_batch;     /* decode-maximal: B, requests per batch (0 = no limit);    */
+                           /*   stall-free: must be 0                                  */
+    int32_t chunk_align;   /* >= 1: a chunk that does not finish its prompt is cut     */
+                           /*   down to a multiple of this ([SS] §"257 为什么可能比 256 */
+                           /*   慢 32%": candidate sizes aligned to 32); 1 = no cut     */
+} sarathi_plan_policy;
+
+/* sarathi_plan with a choice of batch policy.
+ * SARATHI_POLICY_STALL_FREE: exactly sarathi_plan, except that chunks are
+ *   aligned as chunk_align says (a request whose aligned share is 0 is left out).
+ * SARATHI_POLICY_DECODE_MAXIMAL ([SA] §"Decode-maximal batching：顺车的账本"):
+ *   ONE prefill chunk of min(token_budget, prompt_len - num_computed) tokens,
+ *   aligned, from the first SARATHI_PREFILL_RUNNING request with tokens left,
+ *   else the first SARATHI_PREFILL_WAITING one; then as many SARATHI_DECODE
+ *   requests as fit, in caller order: at most max_batch - 1 next to a chunk,
+ *   max_batch without one (0: all).  Decodes that do not fit are left out
+ *   for this step.  Rows are listed decodes first, then the chunk.
+ * Metadata, buffers and errors are those of sarathi_plan (INVALID_ARG also for
+ * an unknown kind, chunk_align < 1, max_batch < 0, or max_batch != 0 with
+ * stall-free).  sarathi_plan_bounds with token_budget = policy->token_budget
+ * bounds the buffers of either policy. */
+int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, const sarathi_plan_policy* policy,
+                        const sarathi_shape* shape, int32_t num_sms,
+                        int32_t* host_buf, size_t host_buf_bytes, sarathi_plan_info* info);
 
 /* Fill the RoPE table on the device: {cos(p*f_j), sin(p*f_j)} in fp64 for
  * p < max_pos, j < head_dim/2, f_j = rope_theta^(-2j/head_dim) (rotate-half

@@ -25,13 +25,20 @@ class GpuStep:
     """One workload step on the GPU: history caches, new-token values, plan."""
 
     def __init__(self, wl: W.Workload, runner=None, seed_offset: int = 0, host_history: bool | None = None,
-                 max_pos: int | None = None):
+                 max_pos: int | None = None, policy: tuple | None = None):
+        """policy: (kind, token_budget, max_batch, chunk_align) to plan with
+        sarathi_plan_ex (and the oracle's same policy) instead of the workload's
+        stall-free budget."""
         import torch
         from chunked_prefill_mixed_gb300.runner import StepRunner
         self.wl = wl
         sh = wl.shape
         self.dev = torch.device("cuda")
-        self.st_o, self.meta = oracle.plan(*wl.arrays(), wl.budget, sh.page_size)
+        if policy is None:
+            self.st_o, self.meta = oracle.plan(*wl.arrays(), wl.budget, sh.page_size)
+        else:
+            kind, tb, mb, al = policy
+            self.st_o, self.meta = oracle.plan(*wl.arrays(), tb, sh.page_size, policy=kind, max_batch=mb, align=al)
         T = self.meta["num_tokens"]
         self.q, self.k, self.v = W.new_token_values(T, sh, wl.seed + seed_offset)
         elems = wl.num_pages * sh.H_kv * sh.page_size * sh.d
@@ -45,7 +52,11 @@ class GpuStep:
             self.kc0, self.vc0 = to_u16(self.kc_dev), to_u16(self.vc_dev)
         self.runner = runner or StepRunner(sh.H_q, sh.H_kv, sh.d, max_pos or self._max_pos(), device=self.dev,
                                            rope_theta=sh.rope_base)
-        self.status, self.info, self.packed = self.runner.plan(*wl.arrays(), wl.budget)
+        if policy is None:
+            self.status, self.info, self.packed = self.runner.plan(*wl.arrays(), wl.budget)
+        else:
+            from chunked_prefill_mixed_gb300 import PlanPolicy
+            self.status, self.info, self.packed = self.runner.plan(*wl.arrays(), 0, policy=PlanPolicy(*policy))
         self.packed = self.packed.copy()  # the runner's buffer is reused by its next plan
         self.plan_dev = self.runner.upload(self.packed)
         self.q_dev, self.k_dev, self.v_dev = (from_u16(x, self.dev) for x in (self.q, self.k, self.v))

@@ -34,6 +34,20 @@ def test_mistral_budget_512_all_rows():
     _check_step(GpuStep(W.mistral()))
 
 
+@pytest.mark.parametrize("policy", [(1, 256, 48, 32), (0, 512, 0, 32)], ids=["decode_maximal", "aligned"])
+def test_mistral_request_set_under_other_plan_policies(policy):
+    """The same requests planned by decode-maximal batching (one 256-token
+    chunk, at most 47 decodes) and by the stall-free rule with 32-aligned
+    chunks: the kernel follows whatever metadata the plan emits."""
+    gs = GpuStep(W.mistral(), policy=policy)
+    m = gs.meta
+    if policy[0] == 1:
+        assert m["num_decodes"] == 47 and list(m["num_new"][47:]) == [256]
+    else:
+        assert list(m["num_new"][80:]) == [300, 128]
+    _check_step(gs)
+
+
 @pytest.mark.parametrize("k", [0, 3, 4])
 def test_llama7b_budget_2048_sampled(k):
     _check_step(GpuStep(W.llama7b(chunk_step=k)), rows="sample")

@@ -1,6 +1,7 @@
 """CPU tests of the library's host side: the C ABI loads and exports every
 declared symbol; sarathi_plan's metadata equals the oracle's plan bit for bit;
 the kernel work list covers every output row, token and page exactly once."""
+import ctypes
 import os
 import re
 
@@ -190,3 +191,73 @@ def test_plan_bounds_cover_actual_sizes():
         hb, wb = S.sarathi_plan_bounds(reqs, len(wl.requests), wl.budget, shp, 148)
         st, info, packed = S.sarathi_plan(reqs, len(wl.requests), wl.budget, shp, 148)
         assert info.packed_ints * 4 <= hb and info.workspace_bytes <= wb
+
+
+# ------------------------------------------------------------ plan policies
+
+def _random_policy_set(rng):
+    n = int(rng.integers(0, 14))
+    states, prompt, computed, tables = [], [], [], []
+    for i in range(n):
+        stt = int(rng.integers(0, 3))
+        if stt == W.DECODE:
+            h, pl, cap = int(rng.integers(0, 300)), 0, 0
+            cap = h + 1
+        else:
+            pl = int(rng.integers(1, 700))
+            h = 0 if stt == W.PREFILL_WAITING and rng.random() < 0.7 else int(rng.integers(0, pl + 1))
+            cap = pl
+        states.append(stt)
+        prompt.append(pl)
+        computed.append(h)
+        tables.append(rng.permutation(5000)[:(cap + 15) // 16 + int(rng.integers(0, 3))].astype(np.int32))
+    return states, prompt, computed, tables
+
+
+def test_plan_policies_match_oracle_random_request_sets():
+    rng = np.random.default_rng(321)
+    shape = W.Shape(8, 2, 64)
+    shp = S.Shape(8, 2, 64, 16)
+    for trial in range(200):
+        states, prompt, computed, tables = _random_policy_set(rng)
+        kind = int(rng.integers(0, 2))
+        budget = int(rng.integers(1, 600))
+        max_batch = int(rng.integers(0, 8)) if kind == S.POLICY_DECODE_MAXIMAL else 0
+        align = int(rng.choice([1, 1, 8, 32, 128]))
+        st_o, mo = oracle.plan(states, prompt, computed, tables, budget, 16, policy=kind, max_batch=max_batch,
+                               align=align)
+        reqs, keep = S.make_requests(states, prompt, computed, tables)
+        pol = S.PlanPolicy(kind, budget, max_batch, align)
+        hb, wb = S.sarathi_plan_bounds(reqs, len(states), budget, shp, 148)
+        st_p, info, packed = S.sarathi_plan_ex(reqs, len(states), pol, shp, int(rng.integers(1, 200)))
+        mp = S.plan_arrays(info, packed)
+        _compare(st_o, mo, st_p, mp)
+        _check_work_list(info, mp, shape)
+        assert info.packed_ints * 4 <= hb
+
+
+@pytest.mark.parametrize("wl", [W.mistral(), W.llama70b(), W.yi34b()], ids=lambda w: w.name)
+def test_plan_policies_match_oracle_on_workloads(wl):
+    shp = S.Shape(wl.shape.H_q, wl.shape.H_kv, wl.shape.d, 16)
+    reqs, keep = S.make_requests(*wl.arrays())
+    for kind, budget, B, align in ((S.POLICY_STALL_FREE, wl.budget, 0, 32),
+                                   (S.POLICY_DECODE_MAXIMAL, 256, 0, 1),
+                                   (S.POLICY_DECODE_MAXIMAL, 512, 64, 32)):
+        st_o, mo = oracle.plan(*wl.arrays(), budget, 16, policy=kind, max_batch=B, align=align)
+        st_p, info, packed = S.sarathi_plan_ex(reqs, len(wl.requests), S.PlanPolicy(kind, budget, B, align), shp, 148)
+        mp = S.plan_arrays(info, packed)
+        _compare(st_o, mo, st_p, mp)
+        _check_work_list(info, mp, wl.shape)
+
+
+def test_plan_ex_rejects_bad_policies():
+    wl = W.tiny(0)
+    shp = S.Shape(wl.shape.H_q, wl.shape.H_kv, wl.shape.d, 16)
+    reqs, keep = S.make_requests(*wl.arrays())
+    buf = np.zeros(1 << 16, np.int32)
+    for pol in (S.PlanPolicy(2, 64, 0, 1), S.PlanPolicy(0, 64, 3, 1), S.PlanPolicy(1, 64, -1, 1),
+                S.PlanPolicy(0, 64, 0, 0), S.PlanPolicy(1, 0, 4, 1)):
+        info = S.PlanInfo()
+        st = S.load().sarathi_plan_ex(reqs, len(wl.requests), ctypes.byref(pol), ctypes.byref(shp), 148,
+                                      buf.ctypes.data, buf.nbytes, ctypes.byref(info))
+        assert st == S.ERR_INVALID_ARG, (pol.kind, pol.token_budget, pol.max_batch, pol.chunk_align)
