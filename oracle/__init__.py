@@ -64,6 +64,8 @@ def _load():
     lib.oracle_plan.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _i32p,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p]
+    lib.oracle_advance.restype = ctypes.c_int
+    lib.oracle_advance.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, ctypes.c_int, _i32p, _i32p]
     lib.oracle_plan_policy.restype = ctypes.c_int
     lib.oracle_plan_policy.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _i32p,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -160,6 +162,21 @@ def plan(states, prompt_len, num_computed, block_tables, budget: int, page_size:
         kv_page_indices=kvi[:int(counts[2])].copy(), kv_last_page_len=last[:ns].copy(),
     )
     return int(st), meta
+
+
+def advance(states, prompt_len, num_computed, meta):
+    """Request state after the step the plan `meta` describes: returns (status,
+    new states, new num_computed) as lists."""
+    lib = _load()
+    n = len(states)
+    st_a = _i32(states).copy() if n else np.zeros(1, np.int32)
+    pl = _i32(prompt_len) if n else np.zeros(1, np.int32)
+    nc = _i32(num_computed).copy() if n else np.zeros(1, np.int32)
+    ns = int(meta["n_sched"])
+    ri = _i32(meta["req_index"]) if ns else np.zeros(1, np.int32)
+    nn = _i32(meta["num_new"]) if ns else np.zeros(1, np.int32)
+    st = lib.oracle_advance(n, st_a, pl, nc, ns, ri, nn)
+    return int(st), st_a[:n].tolist(), nc[:n].tolist()
 
 
 def _meta_arrays(meta):

@@ -28,6 +28,8 @@
  *                     [ST] §六·补二 (chunk = min(remaining budget, remaining prompt));
  *                     [SS] §"混合批不是…" (qo_indptr / kv_page_indptr /
  *                     kv_page_indices / kv_last_page_len).
+ *   oracle_advance    the request state after a step, [SS] §"一个 512-token 预算的
+ *                     例子" and [CP] §3.1.
  *   oracle_rope       RoPE at the ABSOLUTE position, [SS] §"分块不等于截断上下文"
  *                     and §"先验证数值与状态正确性" (positions never restart per
  *                     chunk).  The pages never spell RoPE out; the reading used is
@@ -250,6 +252,24 @@ int oracle_plan(int n_reqs, const int32_t* state, const int32_t* prompt_len,
     return oracle_plan_policy(n_reqs, state, prompt_len, num_computed, bt_indptr, bt, ORC_POLICY_STALL_FREE,
                               budget, 0, 1, page_size, cap_pages, req_index, num_new, last_chunk, qo_indptr,
                               kv_page_indptr, kv_page_indices, kv_last_page_len, counts);
+}
+
+/* After the step: every scheduled request has num_new more tokens in its KV
+ * cache; a prefill whose last chunk ran becomes a decode, one that ran a
+ * chunk but has prompt left is in progress.  [SS] §"一个 512-token 预算的例子"
+ * (P, finished, decodes in the next step; Q continues), [CP] §3.1 (the three
+ * request classes). */
+int oracle_advance(int n_reqs, int32_t* state, const int32_t* prompt_len, int32_t* num_computed,
+                   int n_sched, const int32_t* req_index, const int32_t* num_new) {
+    for (int s = 0; s < n_sched; ++s) {
+        int i = req_index[s];
+        if (i < 0 || i >= n_reqs || num_new[s] <= 0) return ORC_INVALID;
+        num_computed[i] += num_new[s];
+        if (state[i] == ORC_DECODE) continue;
+        if (num_computed[i] > prompt_len[i]) return ORC_INVALID;
+        state[i] = num_computed[i] == prompt_len[i] ? ORC_DECODE : ORC_PREFILL_RUNNING;
+    }
+    return ORC_OK;
 }
 
 /* ------------------------------------------------------------------------- */

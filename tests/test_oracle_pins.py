@@ -453,3 +453,35 @@ def test_aligned_chunks_are_multiples_unless_final():
             n_dec = m["num_decodes"]
             if pol == oracle.STALL_FREE and n_dec <= budget:
                 assert m["num_tokens"] <= budget
+
+
+# ---------------------------------------------------------------- state after a step
+
+def test_advance_turns_worked_example_step1_into_step2():
+    """The 512-token example: after step 1, P (finished) decodes and Q continues,
+    giving step 2's 81 decodes and Q's 431-token chunk (golden fixture)."""
+    g = json.load(open(os.path.join(GOLDEN, "worked_example_512.json")))
+    ctx = np.random.default_rng(5).integers(256, 4096, size=80, endpoint=True)
+    states = [W.PREFILL_RUNNING] + [W.DECODE] * 40 + [W.PREFILL_RUNNING] + [W.DECODE] * 40
+    prompt = [300] + [0] * 40 + [768 + 900] + [0] * 40
+    computed = [0] + list(ctx[:40]) + [768] + list(ctx[40:])
+    tables = [np.arange(2000, dtype=np.int32) + 2000 * i for i in range(len(states))]
+    st, m1 = _plan_from_lists(states, prompt, computed, tables, g["budget"])
+    st, states2, computed2 = oracle.advance(states, prompt, computed, m1)
+    assert st == oracle.OK
+    assert states2[0] == W.DECODE and computed2[0] == 300
+    assert states2[41] == W.PREFILL_RUNNING and computed2[41] == 768 + 132
+    assert computed2[1:41] == list(ctx[:40] + 1)
+    st, m2 = _plan_from_lists(states2, prompt, computed2, tables, g["budget"])
+    s2 = g["step2"]
+    assert m2["num_decodes"] == s2["decodes"] and m2["num_new"][-1] == s2["Q"]["expect_new"]
+    assert m2["num_tokens"] == s2["expect_total"]
+
+
+def test_advance_waiting_prompt_runs_then_decodes():
+    states, prompt, computed = [W.PREFILL_WAITING], [100], [0]
+    tables = [np.arange(10, dtype=np.int32)]
+    for expect_state, expect_h in ((W.PREFILL_RUNNING, 64), (W.DECODE, 100), (W.DECODE, 101)):
+        st, m = oracle.plan(states, prompt, computed, tables, 64, 16)
+        st, states, computed = oracle.advance(states, prompt, computed, m)
+        assert st == oracle.OK and states == [expect_state] and computed == [expect_h]
