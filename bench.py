@@ -419,6 +419,62 @@ def policy_sweep(dev, flush):
     return res
 
 
+def run_serve(args):
+    """Many steps over an arrival trace (chunked_prefill_mixed_gb300.driver):
+    the Mistral-7B-like layer under Sarathi-Serve's stall-free 512-token
+    budget, under mixed batching with no chunking (a budget no prompt
+    reaches), and under decode-maximal batching with 512-token chunks.  Per
+    iteration the step kernel is timed with CUDA events (inputs already on the
+    device); reported: distribution of iteration times and tokens/s over the
+    whole trace."""
+    import torch
+    import chunked_prefill_mixed_gb300 as S
+    from chunked_prefill_mixed_gb300.driver import MultiStepDriver
+    from chunked_prefill_mixed_gb300.runner import StepRunner
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    S.load()
+    sh = W.SHAPES["mistral"]
+    num_pages = 30000
+    gen = torch.Generator(device=dev)
+
+    def values(it, T):
+        gen.manual_seed(5000 + it)
+        mk = lambda h: torch.randn((T, h, sh.d), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        return mk(sh.H_q), mk(sh.H_kv), mk(sh.H_kv)
+
+    out = {"serve": "Mistral-7B-like attention layer (32 q / 8 kv heads, d 128), synthetic arrival traces",
+           "traces": {}}
+    for kind, n_req, gap in (("chat", 48, 3.0), ("summarization", 24, 8.0)):
+        trace = W.arrival_trace(kind, n_req, gap, seed=11)
+        res = {}
+        for label, budget, pol in (("sarathi_serve_budget512", 512, None),
+                                   ("mixed_no_chunking", 1 << 20, None),
+                                   ("decode_maximal_chunk512", 0, S.PlanPolicy(S.POLICY_DECODE_MAXIMAL, 512, 0, 1))):
+            # every page a step reads was written earlier in the trace: zeroed pools
+            dims = (num_pages, sh.H_kv, sh.page_size, sh.d)
+            kc = torch.zeros(dims, dtype=torch.bfloat16, device=dev)
+            vc = torch.zeros(dims, dtype=torch.bfloat16, device=dev)
+            runner = StepRunner(sh.H_q, sh.H_kv, sh.d, 16384 + 1024, device=dev)
+            drv = MultiStepDriver(runner, kc, vc, num_pages, trace, values, budget=budget, policy=pol)
+            recs = []
+            while not drv.finished() and len(recs) < 5000:
+                recs.append(drv.step())
+            us = np.array([r.kernel_us for r in recs if r.tokens > 0])
+            toks = sum(r.tokens for r in recs)
+            res[label] = {"iterations": len(recs), "tokens": int(toks),
+                          "us_mean": round(float(us.mean()), 1), "us_p50": round(float(np.percentile(us, 50)), 1),
+                          "us_p99": round(float(np.percentile(us, 99)), 1), "us_max": round(float(us.max()), 1),
+                          "us_cv": round(float(us.std() / us.mean()), 3),
+                          "tokens_per_s": round(toks / (us.sum() * 1e-6)),
+                          "max_prefill_tokens_in_a_step": int(max(r.prefill_tokens for r in recs))}
+            del kc, vc, runner, drv
+            torch.cuda.empty_cache()
+        out["traces"][kind] = {"requests": n_req, "mean_gap_steps": gap, "policies": res}
+    print(json.dumps(out), flush=True)
+    return None
+
+
 def run_sweep(args):
     """Whole-prompt prefill of the 8192-token Llama-2-7B-like prompt in chunks
     of 512 / 1024 / 2048 and in one shot (the history re-read of chunked
@@ -502,6 +558,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="chunk-size / tile-quantisation sweep (own JSON line)")
+    ap.add_argument("--serve", action="store_true", help="multi-step loop over arrival traces (own JSON line)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -512,6 +569,9 @@ def main():
         torch.distributed.init_process_group("nccl")
     if args.sweep:
         run_sweep(args)
+        return
+    if args.serve:
+        run_serve(args)
         return
     res = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world, local_rank)
     if res is not None:

@@ -23,7 +23,8 @@ DECODE, PREFILL_RUNNING, PREFILL_WAITING = 0, 1, 2
 ABI_VERSION = 2   # SARATHI_ABI_VERSION of include/sarathi.h
 ITEM_INTS = 24    # SARATHI_ITEM_INTS
 
-EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_plan_ex", "sarathi_rope_table", "sarathi_mixed_attn",
+EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_plan_ex", "sarathi_advance", "sarathi_rope_table",
+            "sarathi_mixed_attn",
             "sarathi_mixed_attn_noalloc", "sarathi_workspace_status", "sarathi_last_error", "sarathi_abi_version")
 
 
@@ -91,6 +92,9 @@ def load(build_if_missing: bool = True):
     lib.sarathi_plan.restype = ctypes.c_int32
     lib.sarathi_plan.argtypes = [ctypes.POINTER(Request), ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Shape),
                                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(PlanInfo)]
+    lib.sarathi_advance.restype = ctypes.c_int32
+    lib.sarathi_advance.argtypes = [ctypes.POINTER(Request), ctypes.c_int32, ctypes.POINTER(PlanInfo),
+                                    ctypes.c_void_p]
     lib.sarathi_plan_ex.restype = ctypes.c_int32
     lib.sarathi_plan_ex.argtypes = [ctypes.POINTER(Request), ctypes.c_int32, ctypes.POINTER(PlanPolicy),
                                     ctypes.POINTER(Shape), ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
@@ -161,6 +165,12 @@ def sarathi_plan(reqs, n_reqs: int, token_budget: int, shape: Shape, num_sms: in
                              host_buf.ctypes.data, host_buf.nbytes, ctypes.byref(info))
     _check(st, "sarathi_plan", allow=(OK, WARN_OVER_BUDGET_DECODES))
     return st, info, host_buf[:info.packed_ints]
+
+def sarathi_advance(reqs, n_reqs: int, info: PlanInfo, packed: np.ndarray) -> None:
+    """Apply the step's plan to the ctypes request array in place."""
+    packed = np.ascontiguousarray(packed, dtype=np.int32)
+    _check(load().sarathi_advance(reqs, n_reqs, ctypes.byref(info), packed.ctypes.data), "sarathi_advance")
+
 
 def sarathi_plan_ex(reqs, n_reqs: int, policy: PlanPolicy, shape: Shape, num_sms: int,
                     host_buf: np.ndarray | None = None):

@@ -395,3 +395,21 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     return (policy->kind == SARATHI_POLICY_STALL_FREE && decodes > token_budget) ? SARATHI_WARN_OVER_BUDGET_DECODES
                                                                                  : SARATHI_OK;
 }
+
+extern "C" int32_t sarathi_advance(sarathi_request* reqs, int32_t n_reqs, const sarathi_plan_info* info,
+                                   const int32_t* host_buf) {
+    if (!info || !host_buf || (n_reqs > 0 && !reqs)) return fail(SARATHI_ERR_INVALID_ARG, "NULL pointer");
+    const int32_t* req_index = host_buf + info->off_req_index;
+    const int32_t* num_new = host_buf + info->off_num_new;
+    for (int32_t s = 0; s < info->n_sched; ++s) {
+        const int32_t i = req_index[s], n = num_new[s];
+        if (i < 0 || i >= n_reqs || n <= 0) return fail(SARATHI_ERR_INVALID_ARG, "plan row out of range");
+        sarathi_request& r = reqs[i];
+        r.num_computed += n;
+        if (r.state == SARATHI_DECODE) continue;
+        if (r.num_computed > r.prompt_len) return fail(SARATHI_ERR_INVALID_ARG, "chunk past the prompt");
+        r.state = r.num_computed == r.prompt_len ? SARATHI_DECODE : SARATHI_PREFILL_RUNNING;
+    }
+    set_error("");
+    return SARATHI_OK;
+}

@@ -164,6 +164,17 @@ int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, const sarat
                         const sarathi_shape* shape, int32_t num_sms,
                         int32_t* host_buf, size_t host_buf_bytes, sarathi_plan_info* info);
 
+/* Apply a step's plan to the requests ([SS] §"一个 512-token 预算的例子";
+ * [CP] §3.1): every scheduled request's num_computed grows by its num_new; a
+ * prefill whose last chunk ran becomes SARATHI_DECODE, one with prompt left
+ * becomes SARATHI_PREFILL_RUNNING.  reqs: the array (same order) the plan was
+ * made from, updated in place.  host_buf / info: the packed plan and the info
+ * that sarathi_plan or sarathi_plan_ex returned.  Host only.
+ * Errors: INVALID_ARG (NULL pointer, a row index out of range, a chunk past
+ * its prompt); on error reqs may be partly updated. */
+int32_t sarathi_advance(sarathi_request* reqs, int32_t n_reqs, const sarathi_plan_info* info,
+                        const int32_t* host_buf);
+
 /* Fill the RoPE table on the device: {cos(p*f_j), sin(p*f_j)} in fp64 for
  * p < max_pos, j < head_dim/2, f_j = rope_theta^(-2j/head_dim) (rotate-half
  * RoPE at absolute positions, [SS] §"分块不等于截断上下文"), followed by the same

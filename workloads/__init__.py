@@ -234,3 +234,36 @@ def history_cache_torch(num_pages: int, shape: Shape, seed: int, device):
             blk.copy_(torch.randn(blk.shape, generator=g, device=device, dtype=torch.float32))
         out.append(t)
     return out[0], out[1]
+
+
+# ---------------------------------------------------------------- arrival traces
+# Stand-ins for the pages' two request-length distributions (a chat set and a
+# summarisation set, whose prompts are much longer and outputs shorter): the
+# datasets are not used; lengths are drawn lognormal with the medians below.
+TRACE_KINDS = {
+    #               prompt median, sigma, clip        output median, sigma, clip
+    "chat": ((800, 0.8, (32, 6000)), (150, 0.8, (8, 600))),
+    "summarization": ((5000, 0.5, (1000, 14000)), (100, 0.5, (16, 400))),
+}
+
+
+@dataclass
+class Arrival:
+    iteration: int      # step at which the request becomes visible to the scheduler
+    prompt_len: int
+    max_new: int        # output tokens (the first comes with the last prefill chunk)
+
+
+def arrival_trace(kind: str, n: int, mean_gap: float, seed: int) -> list[Arrival]:
+    """n requests; gaps between arrivals (in steps) exponential with the given
+    mean, rounded down; lengths as TRACE_KINDS[kind]."""
+    (pm, ps, (plo, phi)), (om, os_, (olo, ohi)) = TRACE_KINDS[kind]
+    rng = np.random.default_rng(seed + 65537)
+    t = 0.0
+    out = []
+    for _ in range(n):
+        pl = int(np.clip(np.exp(np.log(pm) + ps * rng.standard_normal()), plo, phi))
+        mn = int(np.clip(np.exp(np.log(om) + os_ * rng.standard_normal()), olo, ohi))
+        out.append(Arrival(int(t), pl, mn))
+        t += rng.exponential(mean_gap)
+    return out
