@@ -60,6 +60,8 @@ def _load():
     lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_rope.restype = None
     lib.oracle_rope.argtypes = [_f64p, ctypes.c_int, ctypes.c_int64, ctypes.c_double, _f64p]
+    lib.oracle_rope_styled.restype = None
+    lib.oracle_rope_styled.argtypes = [_f64p, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_int, _f64p]
     lib.oracle_plan.restype = ctypes.c_int
     lib.oracle_plan.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _i32p,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -71,15 +73,24 @@ def _load():
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int,
                                        _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p]
+    lib.oracle_append_styled.restype = None
     lib.oracle_append.restype = None
     lib.oracle_append.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _u16p, _u16p,
                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                   _u16p, _u16p]
+    lib.oracle_attend_styled.restype = None
     lib.oracle_attend.restype = None
     lib.oracle_attend.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _u16p,
                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_double, _u16p, _u16p, ctypes.c_int, _i32p, _i32p,
                                   _f64p, _f64p]
+    lib.oracle_append_styled.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _u16p, _u16p,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                         _u16p, _u16p]
+    lib.oracle_attend_styled.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _u16p,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_double, ctypes.c_int, _u16p, _u16p, ctypes.c_int, _i32p, _i32p,
+                                         _f64p, _f64p]
     lib.oracle_pairs.restype = ctypes.c_int64
     lib.oracle_pairs.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, ctypes.c_int]
     lib.oracle_reread_tokens.restype = ctypes.c_int64
@@ -111,12 +122,19 @@ def bf16_to_double(bits) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def rope(x, pos: int, base: float = 10000.0) -> np.ndarray:
-    """RoPE (rotate-half) of one vector at absolute position ``pos``, fp64."""
+ROTATE_HALF, INTERLEAVED = 0, 1
+
+
+def rope(x, pos: int, base: float = 10000.0, style: int = ROTATE_HALF) -> np.ndarray:
+    """RoPE of one vector at absolute position ``pos``, fp64; style ROTATE_HALF
+    pairs (j, j + d/2), INTERLEAVED pairs (2j, 2j + 1)."""
     lib = _load()
     xv = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
     out = np.empty_like(xv)
-    lib.oracle_rope(xv, xv.size, int(pos), float(base), out)
+    if style == ROTATE_HALF:
+        lib.oracle_rope(xv, xv.size, int(pos), float(base), out)
+    else:
+        lib.oracle_rope_styled(xv, xv.size, int(pos), float(base), int(style), out)
     return out
 
 
@@ -191,7 +209,7 @@ def _meta_arrays(meta):
 
 
 def append(meta, k_bits, v_bits, H_kv: int, d: int, page_size: int, base: float,
-           k_cache: np.ndarray, v_cache: np.ndarray) -> None:
+           k_cache: np.ndarray, v_cache: np.ndarray, style: int = ROTATE_HALF) -> None:
     """Write the step's new K (rotated, bf16) and V into the caches, in place.
     Caches: uint16 [num_pages][H_kv][page_size][d]."""
     lib = _load()
@@ -202,12 +220,12 @@ def append(meta, k_bits, v_bits, H_kv: int, d: int, page_size: int, base: float,
     vb = np.ascontiguousarray(v_bits, dtype=np.uint16).reshape(-1)
     if kb.size == 0:
         return
-    lib.oracle_append(ns, qo, kvp, kvi, last, kb, vb, H_kv, d, page_size, float(base),
+    lib.oracle_append_styled(ns, qo, kvp, kvi, last, kb, vb, H_kv, d, page_size, float(base), int(style),
                       k_cache.reshape(-1), v_cache.reshape(-1))
 
 
 def attend(meta, q_bits, H_q: int, H_kv: int, d: int, page_size: int, base: float,
-           k_cache: np.ndarray, v_cache: np.ndarray, rows_t=None, rows_hq=None):
+           k_cache: np.ndarray, v_cache: np.ndarray, rows_t=None, rows_hq=None, style: int = ROTATE_HALF):
     """fp64 attention outputs for (row, q-head) pairs (all pairs if None).
     Returns (out [n_pairs][d], lse [n_pairs], rows_t, rows_hq)."""
     lib = _load()
@@ -223,18 +241,18 @@ def attend(meta, q_bits, H_q: int, H_kv: int, d: int, page_size: int, base: floa
     lse = np.zeros(max(n, 1), np.float64)
     if n:
         qb = np.ascontiguousarray(q_bits, dtype=np.uint16).reshape(-1)
-        lib.oracle_attend(ns, qo, kvp, kvi, last, qb, H_q, H_kv, d, page_size, float(base),
+        lib.oracle_attend_styled(ns, qo, kvp, kvi, last, qb, H_q, H_kv, d, page_size, float(base), int(style),
                           np.ascontiguousarray(k_cache).reshape(-1), np.ascontiguousarray(v_cache).reshape(-1),
                           n, rows_t, rows_hq, out.reshape(-1), lse)
     return out[:n], lse[:n], rows_t, rows_hq
 
 
 def step(meta, q_bits, k_bits, v_bits, H_q: int, H_kv: int, d: int, page_size: int,
-         base: float, k_cache: np.ndarray, v_cache: np.ndarray):
+         base: float, k_cache: np.ndarray, v_cache: np.ndarray, style: int = ROTATE_HALF):
     """One whole step: append every new token, then attend every (row, q head).
     Returns out [T][H_q][d] (fp64); the caches are updated in place."""
-    append(meta, k_bits, v_bits, H_kv, d, page_size, base, k_cache, v_cache)
-    out, _, _, _ = attend(meta, q_bits, H_q, H_kv, d, page_size, base, k_cache, v_cache)
+    append(meta, k_bits, v_bits, H_kv, d, page_size, base, k_cache, v_cache, style)
+    out, _, _, _ = attend(meta, q_bits, H_q, H_kv, d, page_size, base, k_cache, v_cache, style=style)
     T = int(meta["qo_indptr"][-1])
     return out.reshape(T, H_q, d)
 

@@ -30,7 +30,7 @@
  *                     kv_page_indices / kv_last_page_len).
  *   oracle_advance    the request state after a step, [SS] §"一个 512-token 预算的
  *                     例子" and [CP] §3.1.
- *   oracle_rope       RoPE at the ABSOLUTE position, [SS] §"分块不等于截断上下文"
+ *   oracle_rope(_styled)  RoPE at the ABSOLUTE position, [SS] §"分块不等于截断上下文"
  *                     and §"先验证数值与状态正确性" (positions never restart per
  *                     chunk).  The pages never spell RoPE out; the reading used is
  *                     rotate-half with theta_j = base^(-2j/d).
@@ -116,16 +116,24 @@ uint16_t oracle_bf16_rne(double x) {
  *   out_j       = x_j cos theta - x_{j+d/2} sin theta
  *   out_{j+d/2} = x_{j+d/2} cos theta + x_j sin theta
  * in fp64.  x and out may not alias. */
-void oracle_rope(const double* x, int d, int64_t pos, double base, double* out) {
+/* style 0, rotate-half: pair j is (x[j], x[j + d/2]).  style 1, interleaved:
+ * pair j is (x[2j], x[2j+1]), the pairing of the original RoPE formulation
+ * (Su et al., RoFormer, 2021, section 3.4.2).  Both rotate pair j by
+ * pos * base^(-2j/d). */
+void oracle_rope_styled(const double* x, int d, int64_t pos, double base, int style, double* out) {
     int half = d / 2;
     for (int j = 0; j < half; ++j) {
         double inv_freq = pow(base, -(2.0 * (double)j) / (double)d);
         double theta = (double)pos * inv_freq;
         double c = cos(theta), s = sin(theta);
-        double x0 = x[j], x1 = x[j + half];
-        out[j] = x0 * c - x1 * s;
-        out[j + half] = x1 * c + x0 * s;
+        int i0 = style ? 2 * j : j, i1 = style ? 2 * j + 1 : j + half;
+        double x0 = x[i0], x1 = x[i1];
+        out[i0] = x0 * c - x1 * s;
+        out[i1] = x1 * c + x0 * s;
     }
+}
+void oracle_rope(const double* x, int d, int64_t pos, double base, double* out) {
+    oracle_rope_styled(x, d, pos, base, 0, out);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -285,10 +293,10 @@ static size_t cache_off(int page, int g, int slot, int H_kv, int page_size, int 
 /* Write every scheduled new token's K (rotated at its absolute position, then
  * rounded once to bf16) and V (copied) into page kv_page_indices[...][pos/page]
  * at slot pos%page, for every kv head.  k, v: bf16 bits [T][H_kv][d]. */
-void oracle_append(int n_sched, const int32_t* qo_indptr, const int32_t* kv_page_indptr,
-                   const int32_t* kv_page_indices, const int32_t* kv_last_page_len,
-                   const uint16_t* k, const uint16_t* v, int H_kv, int d, int page_size,
-                   double rope_base, uint16_t* k_cache, uint16_t* v_cache) {
+void oracle_append_styled(int n_sched, const int32_t* qo_indptr, const int32_t* kv_page_indptr,
+                          const int32_t* kv_page_indices, const int32_t* kv_last_page_len,
+                          const uint16_t* k, const uint16_t* v, int H_kv, int d, int page_size,
+                          double rope_base, int rope_style, uint16_t* k_cache, uint16_t* v_cache) {
     double* x = (double*)malloc(sizeof(double) * (size_t)d * 2);
     double* xr = x + d;
     for (int s = 0; s < n_sched; ++s) {
@@ -305,7 +313,7 @@ void oracle_append(int n_sched, const int32_t* qo_indptr, const int32_t* kv_page
                 const uint16_t* kr = k + ((size_t)t * H_kv + g) * d;
                 const uint16_t* vr = v + ((size_t)t * H_kv + g) * d;
                 for (int e = 0; e < d; ++e) x[e] = oracle_bf16_to_double(kr[e]);
-                oracle_rope(x, d, pos, rope_base, xr);
+                oracle_rope_styled(x, d, pos, rope_base, rope_style, xr);
                 size_t off = cache_off(page, g, slot, H_kv, page_size, d);
                 for (int e = 0; e < d; ++e) {
                     k_cache[off + e] = oracle_bf16_rne(xr[e]);
@@ -325,12 +333,12 @@ void oracle_append(int n_sched, const int32_t* qo_indptr, const int32_t* kv_page
  * kv head of hq: g = hq / (H_q / H_kv) (contiguous GQA groups).
  * out: double [n_pairs][d]; lse (optional): double [n_pairs] = m + log(sum).
  * Rows are independent; OpenMP (if enabled) splits the list. */
-void oracle_attend(int n_sched, const int32_t* qo_indptr, const int32_t* kv_page_indptr,
-                   const int32_t* kv_page_indices, const int32_t* kv_last_page_len,
-                   const uint16_t* q, int H_q, int H_kv, int d, int page_size, double rope_base,
-                   const uint16_t* k_cache, const uint16_t* v_cache,
-                   int n_pairs, const int32_t* row_t, const int32_t* row_hq,
-                   double* out, double* lse) {
+void oracle_attend_styled(int n_sched, const int32_t* qo_indptr, const int32_t* kv_page_indptr,
+                          const int32_t* kv_page_indices, const int32_t* kv_last_page_len,
+                          const uint16_t* q, int H_q, int H_kv, int d, int page_size, double rope_base,
+                          int rope_style, const uint16_t* k_cache, const uint16_t* v_cache,
+                          int n_pairs, const int32_t* row_t, const int32_t* row_hq,
+                          double* out, double* lse) {
     int T = qo_indptr[n_sched];
     int group = H_q / H_kv;
     double scale = 1.0 / sqrt((double)d);
@@ -360,7 +368,7 @@ void oracle_attend(int n_sched, const int32_t* qo_indptr, const int32_t* kv_page
             int g = hq / group;
             const uint16_t* qrow = q + ((size_t)t * H_q + hq) * d;
             for (int e = 0; e < d; ++e) qx[e] = oracle_bf16_to_double(qrow[e]);
-            oracle_rope(qx, d, p, rope_base, qr);
+            oracle_rope_styled(qx, d, p, rope_base, rope_style, qr);
             if ((size_t)(p + 1) > cap) {
                 cap = (size_t)(p + 1);
                 sc = (double*)realloc(sc, sizeof(double) * cap);
@@ -389,6 +397,23 @@ void oracle_attend(int n_sched, const int32_t* qo_indptr, const int32_t* kv_page
         free(qx);
         free(sc);
     }
+}
+
+void oracle_append(int n_sched, const int32_t* qo_indptr, const int32_t* kv_page_indptr,
+                   const int32_t* kv_page_indices, const int32_t* kv_last_page_len,
+                   const uint16_t* k, const uint16_t* v, int H_kv, int d, int page_size,
+                   double rope_base, uint16_t* k_cache, uint16_t* v_cache) {
+    oracle_append_styled(n_sched, qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, k, v, H_kv, d,
+                         page_size, rope_base, 0, k_cache, v_cache);
+}
+void oracle_attend(int n_sched, const int32_t* qo_indptr, const int32_t* kv_page_indptr,
+                   const int32_t* kv_page_indices, const int32_t* kv_last_page_len,
+                   const uint16_t* q, int H_q, int H_kv, int d, int page_size, double rope_base,
+                   const uint16_t* k_cache, const uint16_t* v_cache,
+                   int n_pairs, const int32_t* row_t, const int32_t* row_hq,
+                   double* out, double* lse) {
+    oracle_attend_styled(n_sched, qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, q, H_q, H_kv, d,
+                         page_size, rope_base, 0, k_cache, v_cache, n_pairs, row_t, row_hq, out, lse);
 }
 
 /* ------------------------------------------------------------------------- */

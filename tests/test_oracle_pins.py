@@ -485,3 +485,59 @@ def test_advance_waiting_prompt_runs_then_decodes():
         st, m = oracle.plan(states, prompt, computed, tables, 64, 16)
         st, states, computed = oracle.advance(states, prompt, computed, m)
         assert st == oracle.OK and states == [expect_state] and computed == [expect_h]
+
+
+# ---------------------------------------------------------------- interleaved RoPE
+# The interleaved pairing (2j, 2j+1) of the original RoPE formulation (Su et
+# al., RoFormer), as an option next to rotate-half.
+
+def _perm_interleaved_to_half(d):
+    # position 2j -> j, 2j+1 -> j + d/2
+    p = np.empty(d, dtype=np.int64)
+    p[0::2] = np.arange(d // 2)
+    p[1::2] = np.arange(d // 2) + d // 2
+    return p
+
+
+def test_interleaved_rope_is_rotate_half_after_pairing_permutation():
+    rng = np.random.default_rng(31)
+    for d in (64, 128):
+        perm = _perm_interleaved_to_half(d)
+        for pos in (0, 1, 77, 4096, 16383):
+            x = rng.standard_normal(d)
+            xh = np.empty(d); xh[perm] = x          # x in rotate-half order
+            yh = oracle.rope(xh, pos)
+            yi = oracle.rope(x, pos, style=oracle.INTERLEAVED)
+            assert np.array_equal(yi, yh[perm])
+
+
+def test_interleaved_rope_closed_form_unit_vectors():
+    d, pos, base = 64, 37, 10000.0
+    for j in (0, 5, 31):
+        x = np.zeros(d); x[2 * j] = 1.0
+        th = pos * base ** (-2.0 * j / d)
+        y = oracle.rope(x, pos, base, style=oracle.INTERLEAVED)
+        expect = np.zeros(d); expect[2 * j] = np.cos(th); expect[2 * j + 1] = np.sin(th)
+        assert np.max(np.abs(y - expect)) < 1e-15
+
+
+def test_interleaved_step_equals_rotate_half_step_on_permuted_heads():
+    """A whole step with interleaved RoPE equals the rotate-half step on inputs
+    whose head dimensions were permuted, with the pages permuted back."""
+    wl = W.tiny(1)
+    sh = wl.shape
+    st, m = oracle.plan(*wl.arrays(), wl.budget, 16)
+    T = m["num_tokens"]
+    q, k, v = W.new_token_values(T, sh, 5)
+    kc, vc = W.history_cache_numpy(wl.num_pages, sh, wl.seed)
+    perm = _perm_interleaved_to_half(sh.d)
+    inv = np.argsort(perm)
+    # interleaved step on (q, k, v) and caches as given
+    kc_i, vc_i = kc.copy(), vc.copy()
+    out_i = oracle.step(m, q, k, v, sh.H_q, sh.H_kv, sh.d, 16, sh.rope_base, kc_i, vc_i, style=oracle.INTERLEAVED)
+    # rotate-half step on the same data with head dims reordered
+    reord = lambda a: np.ascontiguousarray(a[..., inv])
+    kc_h, vc_h = reord(kc), reord(vc)
+    out_h = oracle.step(m, reord(q), reord(k), reord(v), sh.H_q, sh.H_kv, sh.d, 16, sh.rope_base, kc_h, vc_h)
+    assert np.array_equal(kc_h[..., perm], kc_i) and np.array_equal(vc_h[..., perm], vc_i)
+    assert np.max(np.abs(out_h[..., perm] - out_i)) < 1e-12
