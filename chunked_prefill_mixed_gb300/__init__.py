@@ -20,7 +20,8 @@ _lib = None
 OK, ERR_INVALID_ARG, ERR_CAPACITY, WARN_OVER_BUDGET_DECODES = 0, 1, 2, 3
 ERR_CUDA, ERR_UNSUPPORTED, ERR_DEVICE_CHECK = 4, 5, 6
 DECODE, PREFILL_RUNNING, PREFILL_WAITING = 0, 1, 2
-ABI_VERSION = 2   # SARATHI_ABI_VERSION of include/sarathi.h
+ABI_VERSION = 3   # SARATHI_ABI_VERSION of include/sarathi.h
+ROPE_ROTATE_HALF, ROPE_INTERLEAVED = 0, 1
 ITEM_INTS = 24    # SARATHI_ITEM_INTS
 
 EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_plan_ex", "sarathi_advance", "sarathi_rope_table",
@@ -68,7 +69,7 @@ class AttnArgs(ctypes.Structure):
                 ("plan", ctypes.c_void_p), ("info", ctypes.POINTER(PlanInfo)),
                 ("rope_table", ctypes.c_void_p), ("rope_max_pos", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64),
-                ("shape", Shape), ("sm_scale", ctypes.c_float)]
+                ("shape", Shape), ("sm_scale", ctypes.c_float), ("rope_style", ctypes.c_int32)]
 
 
 def lib_path() -> str:
@@ -215,7 +216,7 @@ def sarathi_rope_table(table, max_pos: int, head_dim: int, rope_theta: float, st
 
 
 def sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo, rope_table, rope_max_pos: int,
-                       workspace, shape: Shape, sm_scale: float, stream=None) -> None:
+                       workspace, shape: Shape, sm_scale: float, stream=None, rope_style: int = ROPE_ROTATE_HALF) -> None:
     """Enqueue one step (one kernel) on ``stream`` (torch.cuda.Stream or raw handle)."""
     a = AttnArgs()
     a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
@@ -229,11 +230,13 @@ def sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo,
     a.workspace_bytes = int(workspace.numel() * workspace.element_size())
     a.shape = shape
     a.sm_scale = float(sm_scale)
+    a.rope_style = int(rope_style)
     _check(load().sarathi_mixed_attn(ctypes.byref(a), _stream_ptr(stream)), "sarathi_mixed_attn")
 
 
 def sarathi_mixed_attn_noalloc(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo, rope_table,
-                               rope_max_pos: int, shape: Shape, sm_scale: float, stream=None) -> None:
+                               rope_max_pos: int, shape: Shape, sm_scale: float, stream=None,
+                               rope_style: int = ROPE_ROTATE_HALF) -> None:
     """Enqueue one step without a caller workspace: the library's built-in
     scratch array is used (see include/sarathi.h for its limits)."""
     a = AttnArgs()
@@ -248,6 +251,7 @@ def sarathi_mixed_attn_noalloc(q, k, v, k_cache, v_cache, out, plan_dev, info: P
     a.workspace_bytes = 0
     a.shape = shape
     a.sm_scale = float(sm_scale)
+    a.rope_style = int(rope_style)
     _check(load().sarathi_mixed_attn_noalloc(ctypes.byref(a), _stream_ptr(stream)), "sarathi_mixed_attn_noalloc")
 
 

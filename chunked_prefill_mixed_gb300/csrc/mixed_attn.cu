@@ -320,6 +320,21 @@ __device__ __forceinline__ void rope_pair(float x0, float x1, float4 cf, const d
     y0 = rope_bf16(x0, -x1, cf.x, cf.y, cf.z, cf.w, cs);
     y1 = rope_bf16(x1, x0, cf.x, cf.y, cf.z, cf.w, cs);
 }
+// Interleaved pairing: a holds dims 2j0..2j0+7 (pairs j0..j0+3), b the next
+// eight (pairs j0+4..j0+7); the outputs replace them in place.
+__device__ __forceinline__ void rope8_interleaved(uint4 a, uint4 b, const float4* cf, const double2* fb, uint4& oa,
+                                                  uint4& ob) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        uint16_t y0, y1;
+        rope_pair(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xFFFF0000u), cf[p], fb + p, y0, y1);
+        o[p] = (uint32_t)y0 | ((uint32_t)y1 << 16);
+    }
+    oa = make_uint4(o[0], o[1], o[2], o[3]);
+    ob = make_uint4(o[4], o[5], o[6], o[7]);
+}
 // Eight consecutive pairs (x0 = a, x1 = b, 8 bf16 each) of one key row:
 // lo = first-half outputs, hi = second-half outputs.
 __device__ __forceinline__ void rope8(uint4 a, uint4 b, const float4* cf, const double2* fb, uint4& lo, uint4& hi) {
@@ -338,6 +353,37 @@ __device__ __forceinline__ void rope8(uint4 a, uint4 b, const float4* cf, const 
     hi = make_uint4(w1[0], w1[1], w1[2], w1[3]);
 }
 
+// Eight pairs of one query row in fp32, rounded to bf16 (Q feeds the MMA in
+// bf16; its rotation needs no certified rounding).  Rotate-half: a = x0 and
+// b = x1 of pairs j0..j0+7, lo / hi = their outputs.  Interleaved: a = dims
+// 2j0..2j0+7, b = the next eight, outputs in place.  cs: table rows j0..j0+7.
+__device__ __forceinline__ void rope_q8(uint4 a, uint4 b, const float4* cs, bool interleaved, uint4& lo, uint4& hi) {
+    const __nv_bfloat16* xa = reinterpret_cast<const __nv_bfloat16*>(&a);
+    const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&b);
+    uint32_t ylo[4], yhi[4];
+    if (!interleaved) {
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const float4 c0 = cs[e], c1 = cs[e + 1];
+            const float a0 = __bfloat162float(xa[e]), a1 = __bfloat162float(xa[e + 1]);
+            const float b0 = __bfloat162float(xb[e]), b1 = __bfloat162float(xb[e + 1]);
+            ylo[e >> 1] = pack_bf16(a0 * c0.x - b0 * c0.z, a1 * c1.x - b1 * c1.z);
+            yhi[e >> 1] = pack_bf16(b0 * c0.x + a0 * c0.z, b1 * c1.x + a1 * c1.z);
+        }
+    } else {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float4 ca = cs[p], cb = cs[p + 4];
+            const float x0 = __bfloat162float(xa[2 * p]), x1 = __bfloat162float(xa[2 * p + 1]);
+            const float z0 = __bfloat162float(xb[2 * p]), z1 = __bfloat162float(xb[2 * p + 1]);
+            ylo[p] = pack_bf16(x0 * ca.x - x1 * ca.z, x1 * ca.x + x0 * ca.z);
+            yhi[p] = pack_bf16(z0 * cb.x - z1 * cb.z, z1 * cb.x + z0 * cb.z);
+        }
+    }
+    lo = make_uint4(ylo[0], ylo[1], ylo[2], ylo[3]);
+    hi = make_uint4(yhi[0], yhi[1], yhi[2], yhi[3]);
+}
+
 // ----------------------------------------------------------------------------
 // APPEND: rotate + store the K/V of up to kAppendTokens prefill tokens
 // ----------------------------------------------------------------------------
@@ -346,7 +392,7 @@ __device__ __forceinline__ void rope8(uint4 a, uint4 b, const float4* cf, const 
 // copies, so a pass costs one memory round trip however loaded HBM is.  A
 // pass holds as many tokens as fit in the stage area: all 16 up to 10 kv heads
 // of d = 128 (two passes for 32 heads).
-template <int D>
+template <int D, bool IL>
 __device__ void run_append(const KParams& P, const int* it, uint8_t* smem, uint32_t bar, uint32_t* s_phase,
                            int* s_abort) {
     const int tid = threadIdx.x;
@@ -398,13 +444,22 @@ __device__ void run_append(const KParams& P, const int* it, uint8_t* smem, uint3
                     raise_error(P, kErrBounds, page, s_abort);
                     continue;
                 }
-                const uint16_t* kr = ks + ((size_t)tl * Hkv + g) * D + j8 * 8;
+                const uint16_t* krow = ks + ((size_t)tl * Hkv + g) * D;
+                uint16_t* drow = kc + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D;
+                const float4* cf = rs + tl * HALF + j8 * 8;
+                const double2* fb = P.rope + (size_t)pos * HALF + j8 * 8;
+                // pairs 8 j8 .. 8 j8 + 7: dims (j, j + d/2), or (2j, 2j + 1) interleaved
+                const int d0 = IL ? 16 * j8 : 8 * j8;
+                const int d1 = IL ? 16 * j8 + 8 : HALF + 8 * j8;
                 uint4 lo, hi;
-                rope8(*reinterpret_cast<const uint4*>(kr), *reinterpret_cast<const uint4*>(kr + HALF),
-                      rs + tl * HALF + j8 * 8, P.rope + (size_t)pos * HALF + j8 * 8, lo, hi);
-                uint16_t* dst = kc + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D + j8 * 8;
-                *reinterpret_cast<uint4*>(dst) = lo;
-                *reinterpret_cast<uint4*>(dst + HALF) = hi;
+                if (IL)
+                    rope8_interleaved(*reinterpret_cast<const uint4*>(krow + d0),
+                                      *reinterpret_cast<const uint4*>(krow + d1), cf, fb, lo, hi);
+                else
+                    rope8(*reinterpret_cast<const uint4*>(krow + d0), *reinterpret_cast<const uint4*>(krow + d1), cf,
+                          fb, lo, hi);
+                *reinterpret_cast<uint4*>(drow + d0) = lo;
+                *reinterpret_cast<uint4*>(drow + d1) = hi;
             }
             if (p0 + tpp < cnt) {
                 // the next pass's bulk copies overwrite what was just read
@@ -595,7 +650,7 @@ constexpr int kBarAppend = kBarDrain + 1;              // 1 (APPEND bulk copies)
 constexpr int kNumBars = kBarAppend + 1;
 static_assert(kNumBars * 8 <= 512, "barrier area");
 
-template <int D>
+template <int D, bool IL>
 __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUtensorMap* tmV, const int* it,
                             uint8_t* smem, int* s_abort, PfPhase& ph, uint32_t tmem) {
     using L = PfLayout<D>;
@@ -629,32 +684,20 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
     for (int i = q_writer ? qtid : ntile * kQUnits; i < ntile * kQUnits; i += kQThreads) {
         const int T = i / kQUnits, rem = i % kQUnits;
         const int row = rem / (HALF / 8), c = rem % (HALF / 8);
+        // 16-byte chunks holding pairs 8c..8c+7, and where their outputs go
+        const int c0 = IL ? 2 * c : c, c1 = IL ? 2 * c + 1 : c + HALF / 8;
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if (row < (T == 0 ? cA : cB) * G) {
             const int t = t0 + T * tpt + row / G;
             const int hq = g * G + row % G;
             const int pos = R.h + t;
             const __nv_bfloat16* qr = P.q + ((size_t)(R.qo0 + t) * P.Hq + hq) * D;
-            const uint4 a = __ldg(reinterpret_cast<const uint4*>(qr) + c);
-            const uint4 b = __ldg(reinterpret_cast<const uint4*>(qr + HALF) + c);
-            const __nv_bfloat16* x0 = reinterpret_cast<const __nv_bfloat16*>(&a);
-            const __nv_bfloat16* x1 = reinterpret_cast<const __nv_bfloat16*>(&b);
-            const float4* cs = P.ropef + (size_t)pos * HALF + c * 8;
-            uint32_t ylo[4], yhi[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const float4 c0 = cs[e], c1 = cs[e + 1];
-                const float a0 = __bfloat162float(x0[e]), a1 = __bfloat162float(x0[e + 1]);
-                const float b0 = __bfloat162float(x1[e]), b1 = __bfloat162float(x1[e + 1]);
-                ylo[e >> 1] = pack_bf16(a0 * c0.x - b0 * c0.z, a1 * c1.x - b1 * c1.z);
-                yhi[e >> 1] = pack_bf16(b0 * c0.x + a0 * c0.z, b1 * c1.x + a1 * c1.z);
-            }
-            lo = make_uint4(ylo[0], ylo[1], ylo[2], ylo[3]);
-            hi = make_uint4(yhi[0], yhi[1], yhi[2], yhi[3]);
+            const uint4* qv = reinterpret_cast<const uint4*>(qr);
+            rope_q8(__ldg(qv + c0), __ldg(qv + c1), P.ropef + (size_t)pos * HALF + c * 8, IL, lo, hi);
         }
         uint8_t* qtile = smem + L::kQ + T * L::kTile;
-        *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c)) = lo;
-        *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c + HALF / 8)) = hi;
+        *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c0)) = lo;
+        *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c1)) = hi;
     }
     if (q_writer) {
         fence_proxy_async_shared();  // Q is read by the tensor cores (async proxy)
@@ -914,7 +957,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
 // ----------------------------------------------------------------------------
 // DECODE split: pages [p0, p0+pc) of one decode for kv head g, all G q heads
 // ----------------------------------------------------------------------------
-template <int D>
+template <int D, bool IL>
 __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUtensorMap* tmV, const int* it,
                            uint8_t* smem, int* s_abort, int* s_flag, uint32_t& phase) {
     constexpr int HALVES = D / 64;
@@ -970,28 +1013,14 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     static_assert(QU <= kThreads, "decode prologue threads");
     if (tid < QU) {
         const int row = tid / (HALF / 8), c = tid % (HALF / 8);
+        const int c0 = IL ? 2 * c : c, c1 = IL ? 2 * c + 1 : c + HALF / 8;
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if (row < G) {
-            const __nv_bfloat16* qr = P.q + ((size_t)R.qo0 * P.Hq + g * G + row) * D;
-            const uint4 a = __ldg(reinterpret_cast<const uint4*>(qr) + c);
-            const uint4 b = __ldg(reinterpret_cast<const uint4*>(qr + HALF) + c);
-            const __nv_bfloat16* x0 = reinterpret_cast<const __nv_bfloat16*>(&a);
-            const __nv_bfloat16* x1 = reinterpret_cast<const __nv_bfloat16*>(&b);
-            const float4* cs = P.ropef + (size_t)pos * HALF + c * 8;
-            uint32_t ylo[4], yhi[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const float4 c0 = cs[e], c1 = cs[e + 1];
-                const float a0 = __bfloat162float(x0[e]), a1 = __bfloat162float(x0[e + 1]);
-                const float b0 = __bfloat162float(x1[e]), b1 = __bfloat162float(x1[e + 1]);
-                ylo[e >> 1] = pack_bf16(a0 * c0.x - b0 * c0.z, a1 * c1.x - b1 * c1.z);
-                yhi[e >> 1] = pack_bf16(b0 * c0.x + a0 * c0.z, b1 * c1.x + a1 * c1.z);
-            }
-            lo = make_uint4(ylo[0], ylo[1], ylo[2], ylo[3]);
-            hi = make_uint4(yhi[0], yhi[1], yhi[2], yhi[3]);
+            const uint4* qv = reinterpret_cast<const uint4*>(P.q + ((size_t)R.qo0 * P.Hq + g * G + row) * D);
+            rope_q8(__ldg(qv + c0), __ldg(qv + c1), P.ropef + (size_t)pos * HALF + c * 8, IL, lo, hi);
         }
-        *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c)) = lo;
-        *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c + HALF / 8)) = hi;
+        *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c0)) = lo;
+        *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c1)) = hi;
     }
     // the decode token's own K (fp64 RoPE, one rounding) and V: stash + page
     if (last_owner) {
@@ -1001,16 +1030,16 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         const uint16_t* kr = reinterpret_cast<const uint16_t*>(P.k) + ((size_t)R.qo0 * P.Hkv + g) * D;
         const uint16_t* vr = reinterpret_cast<const uint16_t*>(P.v) + ((size_t)R.qo0 * P.Hkv + g) * D;
         for (int j = tid; j < HALF; j += kThreads) {
+            const int i0 = IL ? 2 * j : j, i1 = IL ? 2 * j + 1 : j + HALF;
             uint16_t y0 = 0, y1 = 0;
             if (ok) {
                 const size_t ti = (size_t)pos * HALF + j;
-                rope_pair(bf16_bits_to_float(kr[j]), bf16_bits_to_float(kr[j + HALF]), P.ropef[ti], P.rope + ti, y0,
-                          y1);
-                reinterpret_cast<uint16_t*>(P.k_cache)[off + j] = y0;
-                reinterpret_cast<uint16_t*>(P.k_cache)[off + j + HALF] = y1;
+                rope_pair(bf16_bits_to_float(kr[i0]), bf16_bits_to_float(kr[i1]), P.ropef[ti], P.rope + ti, y0, y1);
+                reinterpret_cast<uint16_t*>(P.k_cache)[off + i0] = y0;
+                reinterpret_cast<uint16_t*>(P.k_cache)[off + i1] = y1;
             }
-            stash[j] = y0;
-            stash[j + HALF] = y1;
+            stash[i0] = y0;
+            stash[i1] = y1;
         }
         for (int e = tid; e < D; e += kThreads) {
             const uint16_t vv = vr[e];
@@ -1200,7 +1229,8 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
 // ----------------------------------------------------------------------------
 // The persistent step kernel
 // ----------------------------------------------------------------------------
-template <int D>
+// IL: interleaved RoPE pairing (x[2j], x[2j+1]) instead of rotate-half.
+template <int D, bool IL>
 __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_constant__ KParams P,
                                                                  const __grid_constant__ CUtensorMap tmK,
                                                                  const __grid_constant__ CUtensorMap tmV,
@@ -1259,11 +1289,11 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         const int* it = s_item;  // rewritten only after the end-of-item barrier
         if (it[0] < 0) break;
         if (it[0] == kAppend)
-            run_append<D>(P, it, smem, bars + 8 * kBarAppend, &s_app_phase, &s_abort);
+            run_append<D, IL>(P, it, smem, bars + 8 * kBarAppend, &s_app_phase, &s_abort);
         else if (it[0] == kPrefill)
-            run_prefill<D>(P, &tmK, &tmV, it, smem, &s_abort, pf_phase, tmem);
+            run_prefill<D, IL>(P, &tmK, &tmV, it, smem, &s_abort, pf_phase, tmem);
         else
-            run_decode<D>(P, &tmK3, &tmV3, it, smem, &s_abort, &s_flag, dec_phase);
+            run_decode<D, IL>(P, &tmK3, &tmV3, it, smem, &s_abort, &s_flag, dec_phase);
         // shared memory written through the generic proxy this item (tiles,
         // scratch, patched rows) is next overwritten by TMA
         fence_proxy_async_shared();
@@ -1387,9 +1417,16 @@ int32_t make_page_map3(CUtensorMap* m, void* base, int num_pages, int Hkv, int d
     return SARATHI_OK;
 }
 
+// The step kernel instantiation for a head size and RoPE pairing.
+const void* kernel_for(int d, int rope_style) {
+    const bool il = rope_style == SARATHI_ROPE_INTERLEAVED;
+    if (d == 128) return il ? (const void*)mixed_step_kernel<128, true> : (const void*)mixed_step_kernel<128, false>;
+    return il ? (const void*)mixed_step_kernel<64, true> : (const void*)mixed_step_kernel<64, false>;
+}
+
 struct DevState {
     int sms = 0;
-    bool smem_set[2] = {false, false};
+    bool smem_set[4] = {false, false, false, false};  // [d == 128][interleaved]
 };
 std::mutex g_mu;
 DevState g_dev[128];
@@ -1434,6 +1471,8 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
         !aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->plan, 16) || !aligned(a->rope_table, 16) ||
         !aligned(a->workspace, 256))
         return fail(SARATHI_ERR_INVALID_ARG, "misaligned pointer (tensors 16 B, workspace 256 B)");
+    if (a->rope_style != SARATHI_ROPE_ROTATE_HALF && a->rope_style != SARATHI_ROPE_INTERLEAVED)
+        return fail(SARATHI_ERR_INVALID_ARG, "rope_style must be SARATHI_ROPE_ROTATE_HALF or _INTERLEAVED");
     if (a->num_pages <= 0) return fail(SARATHI_ERR_INVALID_ARG, "num_pages must be positive");
     if (a->rope_max_pos < in->max_kv_len) return fail(SARATHI_ERR_CAPACITY, "RoPE table shorter than max_kv_len");
     if (a->workspace_bytes < in->workspace_bytes) return fail(SARATHI_ERR_CAPACITY, "workspace too small");
@@ -1456,18 +1495,13 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
             e = cudaDeviceGetAttribute(&ds.sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
         }
-        const int di = d == 128 ? 1 : 0;
+        const int di = (d == 128 ? 2 : 0) + (a->rope_style == SARATHI_ROPE_INTERLEAVED ? 1 : 0);
         if (!ds.smem_set[di]) {
-            e = d == 128 ? cudaFuncSetAttribute(mixed_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                kSmemAlloc)
-                         : cudaFuncSetAttribute(mixed_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                kSmemAlloc);
+            const void* fn = kernel_for(d, a->rope_style);
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
             int resident = 0;
-            e = d == 128 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, mixed_step_kernel<128>, kThreads,
-                                                                         kSmemAlloc)
-                         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, mixed_step_kernel<64>, kThreads,
-                                                                         kSmemAlloc);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, fn, kThreads, kSmemAlloc);
             if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
             if (resident < 1) return fail(SARATHI_ERR_CUDA, "step kernel does not fit one SM (registers/shared memory)");
             ds.smem_set[di] = true;
@@ -1518,10 +1552,15 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
 
     const int grid = std::min(sms, in->n_items);
     cudaStream_t stream = (cudaStream_t)cuda_stream;
-    if (d == 128)
-        mixed_step_kernel<128><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
+    const bool il = a->rope_style == SARATHI_ROPE_INTERLEAVED;
+    if (d == 128 && !il)
+        mixed_step_kernel<128, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
+    else if (d == 128)
+        mixed_step_kernel<128, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
+    else if (!il)
+        mixed_step_kernel<64, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
     else
-        mixed_step_kernel<64><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
+        mixed_step_kernel<64, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "mixed_step_kernel launch");
     return SARATHI_OK;

@@ -15,12 +15,13 @@ from . import (PlanInfo, PlanPolicy, Shape, make_requests, sarathi_mixed_attn, s
 
 class StepRunner:
     def __init__(self, H_q: int, H_kv: int, d: int, max_pos: int, device="cuda", rope_theta: float = 10000.0,
-                 page_size: int = 16, stream=None):
+                 page_size: int = 16, stream=None, rope_style: int = 0):
         self.shape = Shape(H_q, H_kv, d, page_size)
         self.device = torch.device(device)
         self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
         self.num_sms = torch.cuda.get_device_properties(self.device).multi_processor_count
         self.sm_scale = 1.0 / math.sqrt(d)
+        self.rope_style = rope_style  # 0 rotate-half, 1 interleaved
         self.max_pos = int(max_pos)
         self.rope = torch.empty(2 * self.max_pos * d, dtype=torch.float64, device=self.device)
         sarathi_rope_table(self.rope, self.max_pos, d, rope_theta, self.stream)
@@ -60,7 +61,7 @@ class StepRunner:
         if info.max_kv_len > self.max_pos:
             raise ValueError(f"RoPE table covers {self.max_pos} positions, batch needs {info.max_kv_len}")
         sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info, self.rope, self.max_pos,
-                           self.workspace, self.shape, self.sm_scale, self.stream)
+                           self.workspace, self.shape, self.sm_scale, self.stream, self.rope_style)
 
     def status(self) -> int:
         return sarathi_workspace_status(self.workspace, self.stream)

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define SARATHI_ABI_VERSION 2
+#define SARATHI_ABI_VERSION 3
 /* int32 words of one kernel work item in the packed plan.  Items are kernel
  * bookkeeping: their layout is private to the library and may change with
  * SARATHI_ABI_VERSION; callers copy the packed plan as a whole. */
@@ -185,6 +185,13 @@ int32_t sarathi_advance(sarathi_request* reqs, int32_t n_reqs, const sarathi_pla
 int32_t sarathi_rope_table(double* table, int32_t max_pos, int32_t head_dim, double rope_theta,
                            void* cuda_stream);
 
+/* RoPE pairing of the head dimensions; pair j turns by pos * theta^(-2j/d) in
+ * both.  Rotate-half pairs (x[j], x[j + d/2]) (the reading of the pages used
+ * by default); interleaved pairs (x[2j], x[2j+1]), the pairing of the
+ * original RoPE formulation (Su et al., RoFormer). */
+#define SARATHI_ROPE_ROTATE_HALF 0
+#define SARATHI_ROPE_INTERLEAVED 1
+
 /* Arguments of one step.  All pointers are device pointers unless noted. */
 typedef struct sarathi_attn_args {
     const void* q;              /* bf16 [T][H_q][d]  new tokens' queries, before RoPE   */
@@ -203,6 +210,7 @@ typedef struct sarathi_attn_args {
     int64_t workspace_bytes;    /*   once before first use; every launch leaves it so   */
     sarathi_shape shape;
     float sm_scale;             /* softmax scale, normally 1/sqrt(head_dim)             */
+    int32_t rope_style;         /* SARATHI_ROPE_ROTATE_HALF or SARATHI_ROPE_INTERLEAVED */
 } sarathi_attn_args;
 
 /* Enqueue the step on `cuda_stream` (a cudaStream_t): one kernel launch, no

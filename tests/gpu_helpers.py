@@ -25,13 +25,14 @@ class GpuStep:
     """One workload step on the GPU: history caches, new-token values, plan."""
 
     def __init__(self, wl: W.Workload, runner=None, seed_offset: int = 0, host_history: bool | None = None,
-                 max_pos: int | None = None, policy: tuple | None = None):
+                 max_pos: int | None = None, policy: tuple | None = None, rope_style: int = 0):
         """policy: (kind, token_budget, max_batch, chunk_align) to plan with
         sarathi_plan_ex (and the oracle's same policy) instead of the workload's
         stall-free budget."""
         import torch
         from chunked_prefill_mixed_gb300.runner import StepRunner
         self.wl = wl
+        self.rope_style = rope_style
         sh = wl.shape
         self.dev = torch.device("cuda")
         if policy is None:
@@ -51,7 +52,7 @@ class GpuStep:
             self.kc_dev, self.vc_dev = W.history_cache_torch(wl.num_pages, sh, wl.seed, self.dev)
             self.kc0, self.vc0 = to_u16(self.kc_dev), to_u16(self.vc_dev)
         self.runner = runner or StepRunner(sh.H_q, sh.H_kv, sh.d, max_pos or self._max_pos(), device=self.dev,
-                                           rope_theta=sh.rope_base)
+                                           rope_theta=sh.rope_base, rope_style=rope_style)
         if policy is None:
             self.status, self.info, self.packed = self.runner.plan(*wl.arrays(), wl.budget)
         else:
@@ -82,13 +83,14 @@ class GpuStep:
     def oracle_caches(self):
         sh = self.wl.shape
         kc, vc = self.kc0.copy(), self.vc0.copy()
-        oracle.append(self.meta, self.k, self.v, sh.H_kv, sh.d, sh.page_size, sh.rope_base, kc, vc)
+        oracle.append(self.meta, self.k, self.v, sh.H_kv, sh.d, sh.page_size, sh.rope_base, kc, vc,
+                      style=self.rope_style)
         return kc, vc
 
     def oracle_rows(self, kc, vc, rows_t=None, rows_hq=None):
         sh = self.wl.shape
         out, lse, rt, rh = oracle.attend(self.meta, self.q, sh.H_q, sh.H_kv, sh.d, sh.page_size, sh.rope_base,
-                                         kc, vc, rows_t, rows_hq)
+                                         kc, vc, rows_t, rows_hq, style=self.rope_style)
         return out, rt, rh
 
     def sample_rows(self, n_random: int, seed: int = 0):

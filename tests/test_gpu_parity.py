@@ -48,6 +48,15 @@ def test_mistral_request_set_under_other_plan_policies(policy):
     _check_step(gs)
 
 
+@pytest.mark.parametrize("make", [lambda: W.tiny(1), W.mistral, W.llama70b], ids=["tiny", "mistral", "llama70b"])
+def test_interleaved_rope_option(make):
+    """The interleaved RoPE pairing (x[2j], x[2j+1]): appended pages bit-exact
+    and outputs within tolerance of the oracle's interleaved step."""
+    wl = make()
+    gs = GpuStep(wl, rope_style=1)
+    _check_step(gs, rows="all" if wl.name in ("tiny", "mistral") else "sample")
+
+
 @pytest.mark.parametrize("k", [0, 3, 4])
 def test_llama7b_budget_2048_sampled(k):
     _check_step(GpuStep(W.llama7b(chunk_step=k)), rows="sample")
