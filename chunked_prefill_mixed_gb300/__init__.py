@@ -24,7 +24,8 @@ ABI_VERSION = 3   # SARATHI_ABI_VERSION of include/sarathi.h
 ROPE_ROTATE_HALF, ROPE_INTERLEAVED = 0, 1
 ITEM_INTS = 24    # SARATHI_ITEM_INTS
 
-EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_plan_ex", "sarathi_advance", "sarathi_rope_table",
+EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_plan_ex", "sarathi_advance", "sarathi_split_metadata",
+            "sarathi_rope_table",
             "sarathi_mixed_attn",
             "sarathi_mixed_attn_noalloc", "sarathi_workspace_status", "sarathi_last_error", "sarathi_abi_version")
 
@@ -46,6 +47,12 @@ POLICY_STALL_FREE, POLICY_DECODE_MAXIMAL = 0, 1
 class PlanPolicy(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("token_budget", ctypes.c_int32), ("max_batch", ctypes.c_int32),
                 ("chunk_align", ctypes.c_int32)]
+
+
+class MetaSet(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("rows", "tokens", "token_offset", "nnz_pages", "first_row",
+                                              "off_qo_indptr", "off_kv_page_indptr", "off_kv_page_indices",
+                                              "off_kv_last_page_len")]
 
 
 class Shape(ctypes.Structure):
@@ -93,6 +100,9 @@ def load(build_if_missing: bool = True):
     lib.sarathi_plan.restype = ctypes.c_int32
     lib.sarathi_plan.argtypes = [ctypes.POINTER(Request), ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Shape),
                                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(PlanInfo)]
+    lib.sarathi_split_metadata.restype = ctypes.c_int32
+    lib.sarathi_split_metadata.argtypes = [ctypes.POINTER(PlanInfo), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                           ctypes.POINTER(MetaSet), ctypes.POINTER(MetaSet)]
     lib.sarathi_advance.restype = ctypes.c_int32
     lib.sarathi_advance.argtypes = [ctypes.POINTER(Request), ctypes.c_int32, ctypes.POINTER(PlanInfo),
                                     ctypes.c_void_p]
@@ -166,6 +176,25 @@ def sarathi_plan(reqs, n_reqs: int, token_budget: int, shape: Shape, num_sms: in
                              host_buf.ctypes.data, host_buf.nbytes, ctypes.byref(info))
     _check(st, "sarathi_plan", allow=(OK, WARN_OVER_BUDGET_DECODES))
     return st, info, host_buf[:info.packed_ints]
+
+def sarathi_split_metadata(info: PlanInfo, packed: np.ndarray):
+    """The plan's decode and prefill metadata sets: returns (decode, prefill),
+    each a dict of qo_indptr / kv_page_indptr / kv_page_indices /
+    kv_last_page_len plus rows, tokens, token_offset, first_row."""
+    packed = np.ascontiguousarray(packed, dtype=np.int32)
+    out = np.zeros(3 * info.n_sched + 4 + info.nnz_pages, dtype=np.int32)
+    d, p = MetaSet(), MetaSet()
+    _check(load().sarathi_split_metadata(ctypes.byref(info), packed.ctypes.data, out.ctypes.data, out.nbytes,
+                                         ctypes.byref(d), ctypes.byref(p)), "sarathi_split_metadata")
+
+    def view(m):
+        return dict(rows=m.rows, tokens=m.tokens, token_offset=m.token_offset, first_row=m.first_row,
+                    qo_indptr=out[m.off_qo_indptr:m.off_qo_indptr + m.rows + 1].copy(),
+                    kv_page_indptr=out[m.off_kv_page_indptr:m.off_kv_page_indptr + m.rows + 1].copy(),
+                    kv_page_indices=out[m.off_kv_page_indices:m.off_kv_page_indices + m.nnz_pages].copy(),
+                    kv_last_page_len=out[m.off_kv_last_page_len:m.off_kv_last_page_len + m.rows].copy())
+    return view(d), view(p)
+
 
 def sarathi_advance(reqs, n_reqs: int, info: PlanInfo, packed: np.ndarray) -> None:
     """Apply the step's plan to the ctypes request array in place."""

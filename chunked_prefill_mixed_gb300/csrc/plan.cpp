@@ -413,3 +413,34 @@ extern "C" int32_t sarathi_advance(sarathi_request* reqs, int32_t n_reqs, const 
     set_error("");
     return SARATHI_OK;
 }
+
+extern "C" int32_t sarathi_split_metadata(const sarathi_plan_info* info, const int32_t* host_buf, int32_t* out,
+                                          size_t out_bytes, sarathi_meta_set* decode, sarathi_meta_set* prefill) {
+    if (!info || !host_buf || !out || !decode || !prefill) return fail(SARATHI_ERR_INVALID_ARG, "NULL pointer");
+    const int64_t need = 3 * (int64_t)info->n_sched + 4 + info->nnz_pages;
+    if ((int64_t)(out_bytes / 4) < need) return fail(SARATHI_ERR_CAPACITY, "split buffer too small");
+    const int32_t* qo = host_buf + info->off_qo_indptr;
+    const int32_t* kvp = host_buf + info->off_kv_page_indptr;
+    const int32_t* kvi = host_buf + info->off_kv_page_indices;
+    const int32_t* last = host_buf + info->off_kv_last_page_len;
+    int64_t off = 0;
+    auto emit = [&](sarathi_meta_set* m, int32_t r0, int32_t r1) {
+        m->rows = r1 - r0;
+        m->first_row = r0;
+        m->token_offset = qo[r0];
+        m->tokens = qo[r1] - qo[r0];
+        m->nnz_pages = kvp[r1] - kvp[r0];
+        m->off_qo_indptr = (int32_t)off;
+        for (int32_t s = r0; s <= r1; ++s) out[off++] = qo[s] - qo[r0];
+        m->off_kv_page_indptr = (int32_t)off;
+        for (int32_t s = r0; s <= r1; ++s) out[off++] = kvp[s] - kvp[r0];
+        m->off_kv_page_indices = (int32_t)off;
+        for (int32_t p = kvp[r0]; p < kvp[r1]; ++p) out[off++] = kvi[p];
+        m->off_kv_last_page_len = (int32_t)off;
+        for (int32_t s = r0; s < r1; ++s) out[off++] = last[s];
+    };
+    emit(decode, 0, info->num_decodes);
+    emit(prefill, info->num_decodes, info->n_sched);
+    set_error("");
+    return SARATHI_OK;
+}

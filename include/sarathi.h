@@ -164,6 +164,31 @@ int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, const sarat
                         const sarathi_shape* shape, int32_t num_sms,
                         int32_t* host_buf, size_t host_buf_bytes, sarathi_plan_info* info);
 
+/* One of the two metadata sets of a step, as an executor that runs prefill
+ * and decode attention separately builds them ([SS] §"混合批不是把两类注意力强行
+ * 做成同一个形状": separate qo_indptr / kv_page_indptr / kv_page_indices /
+ * kv_last_page_len for prefill and for decode requests).  Offsets count int32
+ * elements of the caller's output buffer. */
+typedef struct sarathi_meta_set {
+    int32_t rows;                /* requests in the set                                 */
+    int32_t tokens;              /* query rows: qo_indptr[rows]                          */
+    int32_t token_offset;        /* the set's first query row in the step's q / out     */
+    int32_t nnz_pages;           /* kv_page_indptr[rows]                                 */
+    int32_t first_row;           /* the set's first row in the combined plan            */
+    int32_t off_qo_indptr;       /* [rows + 1], from 0                                   */
+    int32_t off_kv_page_indptr;  /* [rows + 1], from 0                                   */
+    int32_t off_kv_page_indices; /* [nnz_pages]                                          */
+    int32_t off_kv_last_page_len;/* [rows]                                               */
+} sarathi_meta_set;
+
+/* Split a plan's metadata into its decode set (the first num_decodes rows) and
+ * its prefill set (the rest, chunks in plan order).  host_buf / info: as
+ * returned by sarathi_plan or sarathi_plan_ex.  out: >= 4 * (3 * n_sched + 4 +
+ * nnz_pages) bytes, 4-byte aligned.  Host only.  Errors: INVALID_ARG (NULL
+ * pointer), CAPACITY (out too small). */
+int32_t sarathi_split_metadata(const sarathi_plan_info* info, const int32_t* host_buf, int32_t* out,
+                               size_t out_bytes, sarathi_meta_set* decode, sarathi_meta_set* prefill);
+
 /* Apply a step's plan to the requests ([SS] §"一个 512-token 预算的例子";
  * [CP] §3.1): every scheduled request's num_computed grows by its num_new; a
  * prefill whose last chunk ran becomes SARATHI_DECODE, one with prompt left

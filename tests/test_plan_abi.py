@@ -261,3 +261,39 @@ def test_plan_ex_rejects_bad_policies():
         st = S.load().sarathi_plan_ex(reqs, len(wl.requests), ctypes.byref(pol), ctypes.byref(shp), 148,
                                       buf.ctypes.data, buf.nbytes, ctypes.byref(info))
         assert st == S.ERR_INVALID_ARG, (pol.kind, pol.token_budget, pol.max_batch, pol.chunk_align)
+
+
+# ------------------------------------------------------------ separate metadata sets
+
+def test_split_metadata_equals_oracle_plans_of_each_class():
+    """The decode set equals the oracle's plan of the decode requests alone, and
+    the prefill set the oracle's plan of the prefill requests alone with the
+    budget the decodes left (the stall-free rule fills prefills from what is
+    left): the separate sets an executor with two attention calls builds."""
+    rng = np.random.default_rng(77)
+    shp = S.Shape(8, 2, 64, 16)
+    for trial in range(150):
+        states, prompt, computed, tables = _random_policy_set(rng)
+        budget = int(rng.integers(1, 800))
+        reqs, keep = S.make_requests(states, prompt, computed, tables)
+        st, info, packed = S.sarathi_plan(reqs, len(states), budget, shp, 148)
+        dec, pre = S.sarathi_split_metadata(info, packed)
+        full = S.plan_arrays(info, packed)
+        assert dec["rows"] == info.num_decodes and dec["rows"] + pre["rows"] == info.n_sched
+        assert dec["token_offset"] == 0 and pre["token_offset"] == dec["tokens"]
+        di = [i for i in range(len(states)) if states[i] == W.DECODE]
+        pi = [i for i in range(len(states)) if states[i] != W.DECODE]
+        sub = lambda idx: ([states[i] for i in idx], [prompt[i] for i in idx], [computed[i] for i in idx],
+                           [tables[i] for i in idx])
+        if di:
+            _, od = oracle.plan(*sub(di), max(len(di), 1), 16)
+            for key in ("qo_indptr", "kv_page_indptr", "kv_page_indices", "kv_last_page_len"):
+                assert np.array_equal(np.asarray(od[key]), dec[key]), key
+        left = budget - len(di)
+        if pi and left > 0:
+            _, op = oracle.plan(*sub(pi), left, 16)
+            for key in ("qo_indptr", "kv_page_indptr", "kv_page_indices", "kv_last_page_len"):
+                assert np.array_equal(np.asarray(op[key]), pre[key]), key
+            assert [pi[i] for i in op["req_index"]] == list(full["req_index"][pre["first_row"]:])
+        else:
+            assert pre["rows"] == 0
