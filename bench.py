@@ -419,6 +419,73 @@ def policy_sweep(dev, flush):
     return res
 
 
+def run_qkv(args):
+    """The QKV projection as one tcgen05 GEMM over the step's concatenated
+    tokens (weights read once), against the same tokens projected in two
+    GEMMs, decodes alone and the prefill chunk alone (weights read twice):
+    the Mistral-7B-like layer (hidden 4096, 32 q / 8 kv heads, d 128) at its
+    512-token budget step (80 decodes + 432 prefill tokens) and the
+    Llama-2-7B-like layer (hidden 4096, 32 / 32 heads) at its 2048-token step
+    (64 decodes + 1984).  CUDA events, L2 flushed before each launch, median of
+    7 after 3 warm-ups; torch.matmul (cuBLAS) on the same operands for context."""
+    import torch
+    import chunked_prefill_mixed_gb300 as S
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    S.load()
+    hbm, tc, tc_sus, peak_kind = load_peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(17)
+
+    def timed(fn):
+        ms = []
+        for i in range(10):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            if i >= 3:
+                ms.append(a.elapsed_time(b))
+        return 1e3 * statistics.median(ms)
+
+    out = {"qkv": "QKV projection of a mixed batch, one tcgen05 GEMM (bf16 in, fp32 accumulate, bf16 out)",
+           "peak": {"tflops": tc, "hbm_gbs": hbm, "source": peak_kind}, "cases": {}}
+    for name, hidden, Hq, Hkv, d, n_dec, n_pf in (("mistral_budget512", 4096, 32, 8, 128, 80, 432),
+                                                  ("llama7b_budget2048", 4096, 32, 32, 128, 64, 1984)):
+        N = (Hq + 2 * Hkv) * d
+        T = n_dec + n_pf
+        x = torch.randn((T, hidden), generator=gen, device=dev).to(torch.bfloat16)
+        w = (torch.randn((N, hidden), generator=gen, device=dev) / hidden ** 0.5).to(torch.bfloat16)
+        q = torch.empty((T, Hq, d), dtype=torch.bfloat16, device=dev)
+        k = torch.empty((T, Hkv, d), dtype=torch.bfloat16, device=dev)
+        v = torch.empty((T, Hkv, d), dtype=torch.bfloat16, device=dev)
+        shp = S.Shape(Hq, Hkv, d, 16)
+
+        def proj(r0, r1):
+            S.sarathi_qkv_proj(x[r0:r1], w, q[r0:r1], k[r0:r1], v[r0:r1], shp, ws)
+        fused = timed(lambda: proj(0, T))
+        dec = timed(lambda: proj(0, n_dec))
+        pf = timed(lambda: proj(n_dec, T))
+        cub = timed(lambda: torch.matmul(x, w.t()))
+        if S.sarathi_workspace_status(ws) != 0:
+            raise RuntimeError("device error in the QKV projection")
+        flop = 2.0 * T * N * hidden
+        byt = 2.0 * (T * hidden + N * hidden + T * N)
+        out["cases"][name] = {
+            "tokens": T, "decodes": n_dec, "prefill_tokens": n_pf, "N": N, "hidden": hidden,
+            "fused_us": round(fused, 2), "fused_tflops": round(flop / fused / 1e6, 1),
+            "fused_frac_of_tensor_peak": round(flop / fused / 1e6 / tc, 3),
+            "roofline_us": round(max(flop / (tc * 1e12), byt / (hbm * 1e9)) * 1e6, 2),
+            "separate_us": round(dec + pf, 2), "decode_only_us": round(dec, 2), "prefill_only_us": round(pf, 2),
+            "weight_bytes": 2 * N * hidden, "cublas_us": round(cub, 2)}
+    print(json.dumps(out), flush=True)
+    return None
+
+
 def run_serve(args):
     """Many steps over an arrival trace (chunked_prefill_mixed_gb300.driver):
     the Mistral-7B-like layer under Sarathi-Serve's stall-free 512-token
@@ -559,6 +626,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true", help="chunk-size / tile-quantisation sweep (own JSON line)")
     ap.add_argument("--serve", action="store_true", help="multi-step loop over arrival traces (own JSON line)")
+    ap.add_argument("--qkv", action="store_true", help="QKV projection GEMM, fused vs separate (own JSON line)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -572,6 +640,9 @@ def main():
         return
     if args.serve:
         run_serve(args)
+        return
+    if args.qkv:
+        run_qkv(args)
         return
     res = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world, local_rank)
     if res is not None:

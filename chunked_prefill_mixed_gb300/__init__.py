@@ -25,7 +25,7 @@ ROPE_ROTATE_HALF, ROPE_INTERLEAVED = 0, 1
 ITEM_INTS = 24    # SARATHI_ITEM_INTS
 
 EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_plan_ex", "sarathi_advance", "sarathi_split_metadata",
-            "sarathi_rope_table",
+            "sarathi_rope_table", "sarathi_qkv_proj",
             "sarathi_mixed_attn",
             "sarathi_mixed_attn_noalloc", "sarathi_workspace_status", "sarathi_last_error", "sarathi_abi_version")
 
@@ -55,9 +55,18 @@ class MetaSet(ctypes.Structure):
                                               "off_kv_last_page_len")]
 
 
+class QkvArgs(ctypes.Structure):
+    pass
+
+
 class Shape(ctypes.Structure):
     _fields_ = [("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32)]
+
+
+QkvArgs._fields_ = [("x", ctypes.c_void_p), ("w", ctypes.c_void_p), ("q", ctypes.c_void_p),
+                    ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("tokens", ctypes.c_int32),
+                    ("hidden", ctypes.c_int32), ("shape", Shape), ("workspace", ctypes.c_void_p)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -100,6 +109,8 @@ def load(build_if_missing: bool = True):
     lib.sarathi_plan.restype = ctypes.c_int32
     lib.sarathi_plan.argtypes = [ctypes.POINTER(Request), ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Shape),
                                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(PlanInfo)]
+    lib.sarathi_qkv_proj.restype = ctypes.c_int32
+    lib.sarathi_qkv_proj.argtypes = [ctypes.POINTER(QkvArgs), ctypes.c_void_p]
     lib.sarathi_split_metadata.restype = ctypes.c_int32
     lib.sarathi_split_metadata.argtypes = [ctypes.POINTER(PlanInfo), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                                            ctypes.POINTER(MetaSet), ctypes.POINTER(MetaSet)]
@@ -282,6 +293,18 @@ def sarathi_mixed_attn_noalloc(q, k, v, k_cache, v_cache, out, plan_dev, info: P
     a.sm_scale = float(sm_scale)
     a.rope_style = int(rope_style)
     _check(load().sarathi_mixed_attn_noalloc(ctypes.byref(a), _stream_ptr(stream)), "sarathi_mixed_attn_noalloc")
+
+
+def sarathi_qkv_proj(x, w, q, k, v, shape: Shape, workspace, stream=None) -> None:
+    """Enqueue Y = X W^T split into q, k, v (bf16 device tensors: x [T][hidden],
+    w [(H_q + 2 H_kv) d][hidden], q [T][H_q][d], k / v [T][H_kv][d])."""
+    a = QkvArgs()
+    a.x, a.w, a.q, a.k, a.v = x.data_ptr(), w.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr()
+    a.tokens = int(x.shape[0])
+    a.hidden = int(x.shape[1])
+    a.shape = shape
+    a.workspace = workspace.data_ptr()
+    _check(load().sarathi_qkv_proj(ctypes.byref(a), _stream_ptr(stream)), "sarathi_qkv_proj")
 
 
 def sarathi_workspace_status(workspace, stream=None) -> int:

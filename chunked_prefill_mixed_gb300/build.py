@@ -8,7 +8,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libsarathi.so")
-SOURCES = [os.path.join(HERE, "csrc", f) for f in ("plan.cpp", "mixed_attn.cu", "noalloc.cu")]
+SOURCES = [os.path.join(HERE, "csrc", f) for f in ("plan.cpp", "mixed_attn.cu", "noalloc.cu", "qkv_gemm.cu")]
 HEADERS = [os.path.join(ROOT, "include", "sarathi.h"), os.path.join(HERE, "csrc", "sarathi_internal.h")]
 
 

@@ -270,6 +270,33 @@ int32_t sarathi_mixed_attn(const sarathi_attn_args* args, void* cuda_stream);
  * reported; use sarathi_mixed_attn with a workspace when it is needed. */
 int32_t sarathi_mixed_attn_noalloc(const sarathi_attn_args* args, void* cuda_stream);
 
+/* The Q/K/V projection of a step's tokens as ONE GEMM over the concatenated
+ * ragged batch ([SA] §"Decode-maximal batching：顺车的账本": the linear layers of
+ * the prefill chunk and of the decodes run as one matrix product, so the
+ * weights are read once for both; [SS] §"混合批不是把两类注意力强行做成同一个形状":
+ * the linear-layer inputs are concatenated along the token dimension).
+ *   Y = X W^T, X: bf16 [tokens][hidden], W: bf16 [N][hidden], N = (H_q + 2 H_kv) d;
+ *   q[t][h][:] = Y[t][h d ...], k = the next H_kv d columns, v the last H_kv d.
+ * fp32 accumulation, bf16 outputs (round to nearest even).  The outputs are the
+ * q / k / v of sarathi_attn_args for the same token order.  All pointers are
+ * device pointers, 16-byte aligned. */
+typedef struct sarathi_qkv_args {
+    const void* x;          /* bf16 [tokens][hidden] hidden states, plan token order    */
+    const void* w;          /* bf16 [(H_q + 2 H_kv) d][hidden] stacked Q, K, V weights   */
+    void* q;                /* bf16 [tokens][H_q][d]                                     */
+    void* k;                /* bf16 [tokens][H_kv][d]                                    */
+    void* v;                /* bf16 [tokens][H_kv][d]                                    */
+    int32_t tokens;         /* >= 1                                                      */
+    int32_t hidden;         /* multiple of 64                                            */
+    sarathi_shape shape;    /* num_heads_q, num_heads_kv, head_dim (multiple of 32)      */
+    void* workspace;        /* >= 256 bytes, ZEROED once; holds the device error word   */
+} sarathi_qkv_args;
+
+/* Enqueue the projection (one kernel) on `cuda_stream`.  A bounded wait that
+ * runs out sets the workspace's error word (read it with
+ * sarathi_workspace_status).  Errors: INVALID_ARG, CUDA. */
+int32_t sarathi_qkv_proj(const sarathi_qkv_args* args, void* cuda_stream);
+
 /* Synchronise `cuda_stream`, then read and clear the device error word of a
  * workspace.  *device_error receives 0 or the kernel's error code (1: a
  * bounded wait ran out; 2: a bounds check failed).  Returns SARATHI_OK, or

@@ -267,3 +267,18 @@ def reread_tokens(meta, page_size: int) -> int:
     lib = _load()
     ns, qo, kvp, _, last = _meta_arrays(meta)
     return int(lib.oracle_reread_tokens(ns, qo, kvp, last, page_size))
+
+
+def qkv_proj(x_bits, w_bits, H_q: int, H_kv: int, d: int):
+    """The Q/K/V projection of the step's tokens, in fp64: Y = X W^T with X
+    bf16 [T][hidden] and W bf16 [(H_q + 2 H_kv) d][hidden] (rows: q heads, then
+    k heads, then v heads); returns q [T][H_q][d], k, v [T][H_kv][d].
+    "Sarathi：让解码搭上 prefill 的顺风车" §"Decode-maximal batching：顺车的账本":
+    the linear layer of all the batch's tokens is one matrix product."""
+    x = bf16_to_double(np.asarray(x_bits))
+    w = bf16_to_double(np.asarray(w_bits))
+    y = x @ w.T
+    T = x.shape[0]
+    nq, nk = H_q * d, H_kv * d
+    return (y[:, :nq].reshape(T, H_q, d), y[:, nq:nq + nk].reshape(T, H_kv, d),
+            y[:, nq + nk:nq + 2 * nk].reshape(T, H_kv, d))

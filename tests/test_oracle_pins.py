@@ -541,3 +541,39 @@ def test_interleaved_step_equals_rotate_half_step_on_permuted_heads():
     out_h = oracle.step(m, reord(q), reord(k), reord(v), sh.H_q, sh.H_kv, sh.d, 16, sh.rope_base, kc_h, vc_h)
     assert np.array_equal(kc_h[..., perm], kc_i) and np.array_equal(vc_h[..., perm], vc_i)
     assert np.max(np.abs(out_h[..., perm] - out_i)) < 1e-12
+
+
+# ---------------------------------------------------------------- QKV projection
+
+def test_qkv_proj_matches_a_brute_force_loop():
+    rng = np.random.default_rng(41)
+    T, hidden, Hq, Hkv, d = 3, 8, 2, 1, 4
+    x = W.bf16_bits(rng.standard_normal((T, hidden)))
+    w = W.bf16_bits(rng.standard_normal(((Hq + 2 * Hkv) * d, hidden)))
+    q, k, v = oracle.qkv_proj(x, w, Hq, Hkv, d)
+    xd, wd = oracle.bf16_to_double(x), oracle.bf16_to_double(w)
+    y = [[sum(xd[t][i] * wd[n][i] for i in range(hidden)) for n in range(wd.shape[0])] for t in range(T)]
+    for t in range(T):
+        for n in range(wd.shape[0]):
+            if n < Hq * d:
+                got = q[t][n // d][n % d]
+            elif n < (Hq + Hkv) * d:
+                got = k[t][(n - Hq * d) // d][(n - Hq * d) % d]
+            else:
+                got = v[t][(n - (Hq + Hkv) * d) // d][(n - (Hq + Hkv) * d) % d]
+            assert abs(got - y[t][n]) < 1e-12
+
+
+def test_qkv_proj_permutation_weights_select_columns():
+    # W row n = e_{perm[n]}: Y[:, n] = X[:, perm[n]] exactly, and the split puts
+    # column n at the head and offset its position says
+    rng = np.random.default_rng(42)
+    T, hidden, Hq, Hkv, d = 5, 64, 4, 2, 8
+    N = (Hq + 2 * Hkv) * d
+    perm = rng.integers(0, hidden, size=N)
+    w = np.zeros((N, hidden)); w[np.arange(N), perm] = 1.0
+    x = W.bf16_bits(rng.standard_normal((T, hidden)))
+    q, k, v = oracle.qkv_proj(x, W.bf16_bits(w), Hq, Hkv, d)
+    xd = oracle.bf16_to_double(x)
+    y = np.concatenate([q.reshape(T, -1), k.reshape(T, -1), v.reshape(T, -1)], axis=1)
+    assert np.array_equal(y, xd[:, perm])
