@@ -1257,17 +1257,11 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (tid < 32) {
-        // one CTA per SM: take the whole tensor memory for the prefill tiles
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = s_tmem;
+    // tensor memory is taken when this CTA meets its first prefill item (one
+    // CTA per SM: all of it); CTAs that only append and decode never hold it
+    bool tmem_held = false;
+    uint32_t tmem = 0;
     // completed-phase parities / counters, carried across work items
     uint32_t dec_phase = 0;
     PfPhase pf_phase = {};
@@ -1290,8 +1284,23 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         if (it[0] < 0) break;
         if (it[0] == kAppend)
             run_append<D, IL>(P, it, smem, bars + 8 * kBarAppend, &s_app_phase, &s_abort);
-        else if (it[0] == kPrefill)
+        else if (it[0] == kPrefill) {
+            if (!tmem_held) {
+                if (tid < 32) {
+                    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                                     smem_u32(&s_tmem)),
+                                 "r"(kTmemCols)
+                                 : "memory");
+                    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+                }
+                tc_fence_before();
+                __syncthreads();
+                tc_fence_after();
+                tmem_held = true;
+                tmem = s_tmem;
+            }
             run_prefill<D, IL>(P, &tmK, &tmV, it, smem, &s_abort, pf_phase, tmem);
+        }
         else
             run_decode<D, IL>(P, &tmK3, &tmV3, it, smem, &s_abort, &s_flag, dec_phase);
         // shared memory written through the generic proxy this item (tiles,
@@ -1302,18 +1311,20 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         tc_fence_after();
         if (s_abort) break;  // the error word is set; the workspace must be re-zeroed
     }
-    // no tensor-core work may be in flight when the tensor memory is released
-    if (tid == 12 * 32) {
-        umma_commit(bars + 8 * kBarDrain);
-        const uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(bars + 8 * kBarDrain, 0))
-            if (globaltimer() - t0 > kWaitNs) break;
+    if (tmem_held) {
+        // no tensor-core work may be in flight when the tensor memory is released
+        if (tid == 12 * 32) {
+            umma_commit(bars + 8 * kBarDrain);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(bars + 8 * kBarDrain, 0))
+                if (globaltimer() - t0 > kWaitNs) break;
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid < 32)
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid < 32)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     if (s_abort) return;
     // the last CTA out leaves the counters at zero for the next launch
     if (tid == 0) {
