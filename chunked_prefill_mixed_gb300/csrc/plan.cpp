@@ -316,7 +316,33 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     });
     std::vector<Timed> attn;
     attn.reserve(keyed.size());
-    for (auto& k : keyed) attn.push_back(k.t);
+    {
+        // Longest first, except that a prefill item shorter than the median
+        // decode split waits no longer than the first wave (the SMs the appends
+        // leave free): short compute-bound tiles then run beside the
+        // memory-bound decode streams instead of alone at the end.
+        std::vector<double> dec_est;
+        for (auto& t : decs) dec_est.push_back(t.ns_est);
+        double median = 0;
+        if (!dec_est.empty()) {
+            std::nth_element(dec_est.begin(), dec_est.begin() + dec_est.size() / 2, dec_est.end());
+            median = dec_est[dec_est.size() / 2];
+        }
+        const size_t wave = (size_t)std::max<int64_t>(0, (int64_t)num_sms - (int64_t)appends.size());
+        std::vector<char> used(keyed.size(), 0);
+        for (size_t i = 0; i < keyed.size(); ++i) {
+            if (used[i]) continue;
+            if (attn.size() == wave)
+                for (size_t j = i; j < keyed.size(); ++j)
+                    if (keyed[j].group >= 0 && keyed[j].key < median && !used[j]) {
+                        attn.push_back(keyed[j].t);
+                        used[j] = 1;
+                    }
+            if (used[i]) continue;
+            attn.push_back(keyed[i].t);
+            used[i] = 1;
+        }
+    }
     const int64_t n_items = (int64_t)appends.size() + (int64_t)attn.size();
 
     // ---- 4. packed layout
