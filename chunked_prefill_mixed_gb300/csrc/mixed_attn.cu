@@ -172,6 +172,28 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// Three-input max and two-lane fp32 FMA / add (one instruction each on
+// sm_103a): the prefill softmax is bound by instruction issue.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+          "l"(*reinterpret_cast<uint64_t*>(&c)));
+    return *reinterpret_cast<float2*>(&r);
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+    return *reinterpret_cast<float2*>(&r);
+}
 
 // Round a double to bf16 in ONE rounding (ties to even): round to float with
 // round-to-odd (truncate, then force the last bit to 1 when inexact), then
@@ -856,10 +878,11 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                     const int kc = kb0 + h * 64;
                     if (kc + 63 > pos_r) {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, kc + e <= pos_r ? v[e] : -INFINITY);
+                        for (int e = 0; e < 64; e += 2)
+                            mx = fmax3(mx, kc + e <= pos_r ? v[e] : -INFINITY, kc + e + 1 <= pos_r ? v[e + 1] : -INFINITY);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, v[e]);
+                        for (int e = 0; e < 64; e += 2) mx = fmax3(mx, v[e], v[e + 1]);
                     }
                 }
                 // lazy rescale: move the exponent base only when the max grows by > 2^8
@@ -880,8 +903,8 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 // pass 2: P = 2^(s - m) in bf16, two keys per column, over the first
                 // 64 columns of S (columns of half h are written only after half h
                 // and every column below it have been read)
-                float sum = 0.f;
-                const float nm = -m_new;
+                float2 sum2 = make_float2(0.f, 0.f);
+                const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m_new, -m_new);
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     float v[64];
@@ -898,16 +921,16 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                         uint32_t pk[16];
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            const float p0 = ex2_approx(fmaf(v[q * 32 + e], sl2, nm));
-                            const float p1 = ex2_approx(fmaf(v[q * 32 + e + 1], sl2, nm));
-                            sum += p0 + p1;
-                            pk[e >> 1] = pack_bf16(p0, p1);
+                            const float2 x = ffma2(make_float2(v[q * 32 + e], v[q * 32 + e + 1]), sl2v, nmv);
+                            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            sum2 = fadd2(sum2, pp);
+                            pk[e >> 1] = pack_bf16(pp.x, pp.y);
                         }
                         tmem_st16_nw(lane_base + s_col + (uint32_t)(h * 32 + q * 16), pk);
                     }
                 }
                 tmem_wait_st();
-                l_run = l_run * alpha + sum;
+                l_run = l_run * alpha + (sum2.x + sum2.y);
                 m_run = m_new;
                 // last block: V rows past kv_hi hold stale bytes; zero them so 0 x V stays 0
                 if (T == zero_tile && j == nblk - 1 && kb0 + kTcKeys > kv_hi) {
