@@ -307,9 +307,30 @@ __device__ __forceinline__ int page_id(const KParams& P, const Row& R, int lp, i
 // 2^-52 (|a p| + |b q|).  When S + small lies farther than 2^-34 (|a p| +
 // |b q|) from both bf16 rounding boundaries around its nearest bf16 value w,
 // every value within those errors rounds to w, so w is the answer.  Otherwise
-// (about one element in 10^8) the fp64 evaluation runs as written.
+// (about one element in 10^8) the fp64 evaluation runs as written.  A cheaper
+// single-FMA test (below) settles most elements before the double-float step.
 __device__ __forceinline__ uint16_t rope_bf16(float a, float b, float p_hi, float p_lo, float q_hi, float q_lo,
                                              const double2* pq) {
+    // First, one fused multiply-add: u = fl(a p_hi + fl(b q_hi)).  With
+    // |p - p_hi| <= 2^-24 |p_hi| (and the same for q), |u - y| <= 3.1 2^-24
+    // (|a p_hi| + |b q_hi|) for the fp64 value y, i.e. at most 1.55 m / 2^E
+    // units of u's last place (2^E the power of two at or below |u|, m that
+    // magnitude sum).  The bf16 rounding boundaries lie where u's low 16 bits
+    // are 0x8000; when u is more than 8 m / 2^E units from them (and the
+    // cancellation m / |u| is below 2^10, so that the nearest boundary is in
+    // u's binade), y rounds to the same bf16 value as u.  About one element in
+    // 10^3 goes on to the double-float step below.
+    {
+        const float t = b * q_hi;
+        const float u = fmaf(a, p_hi, t);
+        const float m = fabsf(a * p_hi) + fabsf(t);
+        const uint32_t ub = __float_as_uint(u);
+        const float e2 = __uint_as_float(ub & 0x7F800000u);  // 0 for zero and subnormal u
+        const int low = (int)(ub & 0xFFFFu) - 0x8000;
+        const float dist = __uint_as_float(0x4B000000u | (uint32_t)abs(low)) - 8388608.f;  // |low|, exactly
+        if (dist * e2 > 8.f * m && 1024.f * e2 > m && e2 < 1e30f)
+            return (uint16_t)((ub + 0x7FFFu + ((ub >> 16) & 1u)) >> 16);
+    }
     const float P1 = a * p_hi, E1 = fmaf(a, p_hi, -P1);
     const float P2 = b * q_hi, E2 = fmaf(b, q_hi, -P2);
     const float S = P1 + P2;
