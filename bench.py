@@ -265,8 +265,13 @@ def run_ours(args, rank, world, local_rank):
 
     def bf(x):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
-    q_h, k_h, v_h = (bf(x).pin_memory() for x in (q, k, v))
-    q_d, k_d, v_d = (x.to(dev) for x in (q_h, k_h, v_h))
+    # the step's new-token q, k, v side by side in one pinned buffer and one
+    # device buffer (so that their host-to-device copy is one DMA)
+    nq, nk = q.size, k.size
+    qkv_h = torch.cat([bf(x).reshape(-1) for x in (q, k, v)]).pin_memory()
+    qkv_d = qkv_h.to(dev)
+    q_h, k_h, v_h = qkv_h[:nq].view(q.shape), qkv_h[nq:nq + nk].view(k.shape), qkv_h[nq + nk:].view(v.shape)
+    q_d, k_d, v_d = qkv_d[:nq].view(q.shape), qkv_d[nq:nq + nk].view(k.shape), qkv_d[nq + nk:].view(v.shape)
     out = torch.empty((T, sh.H_q, sh.d), dtype=torch.bfloat16, device=dev)
     out_h = torch.empty((T, sh.H_q, sh.d), dtype=torch.bfloat16).pin_memory()
     plan_pin = torch.empty(info.packed_ints + 64, dtype=torch.int32).pin_memory()
@@ -312,8 +317,10 @@ def run_ours(args, rank, world, local_rank):
     if runner.status() != 0:
         raise RuntimeError(f"device error in the timed region: workspace header {hdr[:12]}")
 
-    # e2e through the public API: plan on the host, pinned H2D, kernel, D2H
-    h2d = (q_h.numel() + k_h.numel() + v_h.numel()) * 2 + info.packed_ints * 4
+    # e2e through the public API: pinned H2D of q, k, v (one copy, enqueued
+    # first: it does not depend on the plan), the plan on the host meanwhile
+    # (straight into the runner's pinned buffer), its H2D, the kernel, D2H
+    h2d = qkv_h.numel() * 2 + info.packed_ints * 4
     d2h = out.numel() * 2
     e2e_times = []
     barrier()
@@ -322,14 +329,10 @@ def run_ours(args, rank, world, local_rank):
             flush.zero_()
         stream.synchronize()
         t0 = time.perf_counter()
-        st2, info2, packed2 = runner.plan(*wl.arrays(), wl.budget)
-        plan_pin[:info2.packed_ints].copy_(torch.from_numpy(packed2))
         with torch.cuda.stream(stream):
-            plan_dev[:info2.packed_ints].copy_(plan_pin[:info2.packed_ints], non_blocking=True)
-            q_d.copy_(q_h, non_blocking=True)
-            k_d.copy_(k_h, non_blocking=True)
-            v_d.copy_(v_h, non_blocking=True)
-            runner.run(q_d, k_d, v_d, kc, vc, out, plan_dev, info2)
+            qkv_d.copy_(qkv_h, non_blocking=True)
+            st2, info2, packed2 = runner.plan(*wl.arrays(), wl.budget)
+            runner.run_planned(q_d, k_d, v_d, kc, vc, out, info2)
             out_h.copy_(out, non_blocking=True)
         stream.synchronize()
         e2e_times.append(time.perf_counter() - t0)
@@ -359,7 +362,7 @@ def run_ours(args, rank, world, local_rank):
                      "algorithmic_flop": alg["flop"], "traffic": committed_traffic(args.workload)},
         "e2e": {"value": job_tokens_per_s(T, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "includes": "host plan + pinned H2D (q, k, v, plan) + kernel + D2H (out)"},
+                "includes": "pinned H2D of q, k, v (one copy) overlapping the host plan, pinned H2D of the plan and the kernel (one library call), D2H (out)"},
         "clocks": clk.summary(),
         "gpu_launches": args.steps,
         "timing": {"kernel_ms_min": min(ms), "kernel_ms_median": statistics.median(ms), "wall_s": t_wall},

@@ -20,7 +20,7 @@ _lib = None
 OK, ERR_INVALID_ARG, ERR_CAPACITY, WARN_OVER_BUDGET_DECODES = 0, 1, 2, 3
 ERR_CUDA, ERR_UNSUPPORTED, ERR_DEVICE_CHECK = 4, 5, 6
 DECODE, PREFILL_RUNNING, PREFILL_WAITING = 0, 1, 2
-ABI_VERSION = 3   # SARATHI_ABI_VERSION of include/sarathi.h
+ABI_VERSION = 4   # SARATHI_ABI_VERSION of include/sarathi.h
 ROPE_ROTATE_HALF, ROPE_INTERLEAVED = 0, 1
 ITEM_INTS = 24    # SARATHI_ITEM_INTS
 
@@ -85,7 +85,8 @@ class AttnArgs(ctypes.Structure):
                 ("plan", ctypes.c_void_p), ("info", ctypes.POINTER(PlanInfo)),
                 ("rope_table", ctypes.c_void_p), ("rope_max_pos", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64),
-                ("shape", Shape), ("sm_scale", ctypes.c_float), ("rope_style", ctypes.c_int32)]
+                ("shape", Shape), ("sm_scale", ctypes.c_float), ("rope_style", ctypes.c_int32),
+                ("plan_host", ctypes.c_void_p)]
 
 
 def lib_path() -> str:
@@ -152,20 +153,37 @@ def _check(st: int, where: str, allow=(OK,)):
     return st
 
 
+# sarathi_request as a numpy record (4 int32, then the page pointer at byte 16)
+_REQ_DTYPE = np.dtype({"names": ["state", "prompt_len", "num_computed", "num_pages", "pages"],
+                       "formats": ["<i4", "<i4", "<i4", "<i4", "<u8"], "offsets": [0, 4, 8, 12, 16],
+                       "itemsize": ctypes.sizeof(Request)})
+assert ctypes.sizeof(Request) == 24 and Request.pages.offset == 16
+
+
 def make_requests(states, prompt_len, num_computed, block_tables):
-    """ctypes request array plus the int32 block tables it points into (keep both alive)."""
+    """ctypes request array plus what it points into (keep both alive while
+    the array is in use).  The array is a view of a numpy record array filled
+    column by column, and the block tables are concatenated once, so the cost
+    does not grow with a Python loop per request."""
     n = len(states)
-    arr = (Request * max(n, 1))()
-    keep = []
-    for i in range(n):
-        t = np.ascontiguousarray(np.asarray(block_tables[i], dtype=np.int32))
-        keep.append(t)
-        arr[i].state = int(states[i])
-        arr[i].prompt_len = int(prompt_len[i])
-        arr[i].num_computed = int(num_computed[i])
-        arr[i].num_pages = int(t.size)
-        arr[i].pages = t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
-    return arr, keep
+    lens = np.fromiter(map(len, block_tables), dtype=np.int64, count=n)
+    if n and int(lens.sum()):
+        pages = np.ascontiguousarray(np.concatenate(block_tables), dtype=np.int32)
+        if pages.ndim != 1 or pages.size != int(lens.sum()):
+            raise ValueError("block tables must be 1-D sequences of page ids")
+    else:
+        pages = np.zeros(1, np.int32)
+    rec = np.zeros(max(n, 1), dtype=_REQ_DTYPE)
+    if n:
+        rec["state"][:n] = states
+        rec["prompt_len"][:n] = prompt_len
+        rec["num_computed"][:n] = num_computed
+        rec["num_pages"][:n] = lens
+        starts = np.zeros(n, np.int64)
+        np.cumsum(lens[:-1], out=starts[1:])
+        rec["pages"][:n] = pages.ctypes.data + 4 * starts
+    arr = (Request * max(n, 1)).from_buffer(rec)
+    return arr, (rec, pages)
 
 
 def sarathi_plan_bounds(reqs, n_reqs: int, token_budget: int, shape: Shape, num_sms: int):
@@ -256,9 +274,14 @@ def sarathi_rope_table(table, max_pos: int, head_dim: int, rope_theta: float, st
 
 
 def sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo, rope_table, rope_max_pos: int,
-                       workspace, shape: Shape, sm_scale: float, stream=None, rope_style: int = ROPE_ROTATE_HALF) -> None:
-    """Enqueue one step (one kernel) on ``stream`` (torch.cuda.Stream or raw handle)."""
+                       workspace, shape: Shape, sm_scale: float, stream=None, rope_style: int = ROPE_ROTATE_HALF,
+                       plan_host=None) -> None:
+    """Enqueue one step (one kernel) on ``stream`` (torch.cuda.Stream or raw handle).
+    plan_host: optional host tensor or array holding the packed plan; the call
+    then copies it into plan_dev first (same stream)."""
     a = AttnArgs()
+    if plan_host is not None:
+        a.plan_host = plan_host.data_ptr() if hasattr(plan_host, "data_ptr") else plan_host.ctypes.data
     a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
     a.k_cache, a.v_cache, a.out = k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr()
     a.plan = plan_dev.data_ptr()

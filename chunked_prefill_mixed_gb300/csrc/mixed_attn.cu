@@ -1607,6 +1607,12 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
 
     const int grid = std::min(sms, in->n_items);
     cudaStream_t stream = (cudaStream_t)cuda_stream;
+    if (a->plan_host) {
+        // the caller's host copy of the plan goes to the device first, on the same stream
+        e = cudaMemcpyAsync(const_cast<int32_t*>(a->plan), a->plan_host, (size_t)in->packed_ints * 4,
+                            cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "plan copy to the device");
+    }
     const bool il = a->rope_style == SARATHI_ROPE_INTERLEAVED;
     if (d == 128 && !il)
         mixed_step_kernel<128, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);

@@ -244,6 +244,9 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     std::vector<Timed> tiles, decs;
     const int tpt = tokens_per_tile(group);
     const int tpi = tokens_per_item(group);
+    tiles.reserve((size_t)(T / std::max(tpi, 1) + ns) * Hkv);
+    decs.reserve((size_t)ns * Hkv + (size_t)num_sms * kDecodeItemsPerSm);
+    appends.reserve((size_t)(T / kAppendTokens + ns));
     // decode split size from the total decode pages and the SM count
     int64_t dec_page_heads = 0;
     for (int32_t s = 0; s < ns; ++s)
@@ -294,34 +297,41 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
         }
     }
     // Longest first.  The tiles of one (request, kv head) read the same pages,
-    // so they stay contiguous: the group sorts by its costliest tile.
-    struct Keyed {
-        double key;
-        int64_t group;
-        Timed t;
-    };
-    std::vector<Keyed> keyed;
-    keyed.reserve(tiles.size() + decs.size());
-    for (size_t i = 0; i < tiles.size();) {
+    // so they stay contiguous: the group sorts by its costliest tile.  (The
+    // sort moves 4-byte indices, not the items.)
+    const size_t n_tiles = tiles.size(), nk = tiles.size() + decs.size();
+    auto item_at = [&](uint32_t i) -> const Timed& { return i < n_tiles ? tiles[i] : decs[i - n_tiles]; };
+    std::vector<double> key(nk);
+    std::vector<int64_t> grp(nk);
+    for (size_t i = 0; i < n_tiles;) {
         size_t e = i;
         const int32_t s0 = tiles[i].it[kS], g0 = tiles[i].it[kG];
         double mx = 0;
-        while (e < tiles.size() && tiles[e].it[kS] == s0 && tiles[e].it[kG] == g0) mx = std::max(mx, tiles[e++].ns_est);
-        for (; i < e; ++i) keyed.push_back({mx, (int64_t)s0 * Hkv + g0, tiles[i]});
+        while (e < n_tiles && tiles[e].it[kS] == s0 && tiles[e].it[kG] == g0) mx = std::max(mx, tiles[e++].ns_est);
+        for (; i < e; ++i) {
+            key[i] = mx;
+            grp[i] = (int64_t)s0 * Hkv + g0;
+        }
     }
-    for (auto& t : decs) keyed.push_back({t.ns_est, -1, t});
-    std::stable_sort(keyed.begin(), keyed.end(), [](const Keyed& a, const Keyed& b) {
-        if (a.key != b.key) return a.key > b.key;
-        return a.group < b.group;
+    for (size_t i = 0; i < decs.size(); ++i) {
+        key[n_tiles + i] = decs[i].ns_est;
+        grp[n_tiles + i] = -1;
+    }
+    std::vector<uint32_t> order(nk);
+    for (size_t i = 0; i < nk; ++i) order[i] = (uint32_t)i;
+    std::stable_sort(order.begin(), order.end(), [&](uint32_t a, uint32_t b) {
+        if (key[a] != key[b]) return key[a] > key[b];
+        return grp[a] < grp[b];
     });
-    std::vector<Timed> attn;
-    attn.reserve(keyed.size());
+    std::vector<uint32_t> attn;
+    attn.reserve(nk);
     {
         // Longest first, except that a prefill item shorter than the median
         // decode split waits no longer than the first wave (the SMs the appends
         // leave free): short compute-bound tiles then run beside the
         // memory-bound decode streams instead of alone at the end.
         std::vector<double> dec_est;
+        dec_est.reserve(decs.size());
         for (auto& t : decs) dec_est.push_back(t.ns_est);
         double median = 0;
         if (!dec_est.empty()) {
@@ -329,17 +339,17 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
             median = dec_est[dec_est.size() / 2];
         }
         const size_t wave = (size_t)std::max<int64_t>(0, (int64_t)num_sms - (int64_t)appends.size());
-        std::vector<char> used(keyed.size(), 0);
-        for (size_t i = 0; i < keyed.size(); ++i) {
+        std::vector<char> used(nk, 0);
+        for (size_t i = 0; i < nk; ++i) {
             if (used[i]) continue;
             if (attn.size() == wave)
-                for (size_t j = i; j < keyed.size(); ++j)
-                    if (keyed[j].group >= 0 && keyed[j].key < median && !used[j]) {
-                        attn.push_back(keyed[j].t);
+                for (size_t j = i; j < nk; ++j)
+                    if (grp[order[j]] >= 0 && key[order[j]] < median && !used[j]) {
+                        attn.push_back(order[j]);
                         used[j] = 1;
                     }
             if (used[i]) continue;
-            attn.push_back(keyed[i].t);
+            attn.push_back(order[i]);
             used[i] = 1;
         }
     }
@@ -416,7 +426,7 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
         }
     };
     for (auto& it : appends) put(it);
-    for (auto& t : attn) put(t.it);
+    for (uint32_t i : attn) put(item_at(i).it);
     set_error("");
     return (policy->kind == SARATHI_POLICY_STALL_FREE && decodes > token_budget) ? SARATHI_WARN_OVER_BUDGET_DECODES
                                                                                  : SARATHI_OK;

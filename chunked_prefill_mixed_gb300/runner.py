@@ -9,8 +9,8 @@ import math
 import numpy as np
 import torch
 
-from . import (PlanInfo, PlanPolicy, Shape, make_requests, sarathi_mixed_attn, sarathi_plan, sarathi_plan_bounds,
-               sarathi_plan_ex, sarathi_rope_table, sarathi_workspace_status)
+from . import (ERR_CAPACITY, PlanInfo, PlanPolicy, SarathiError, Shape, make_requests, sarathi_mixed_attn,
+               sarathi_plan, sarathi_plan_bounds, sarathi_plan_ex, sarathi_rope_table, sarathi_workspace_status)
 
 
 class StepRunner:
@@ -26,7 +26,13 @@ class StepRunner:
         self.rope = torch.empty(2 * self.max_pos * d, dtype=torch.float64, device=self.device)
         sarathi_rope_table(self.rope, self.max_pos, d, rope_theta, self.stream)
         self.workspace = torch.zeros(1 << 16, dtype=torch.uint8, device=self.device)
-        self._host_buf = np.zeros(0, dtype=np.int32)
+        # the packed plan is written straight into pinned memory, so that its
+        # copy to the device is one asynchronous DMA from there
+        self._host_t = torch.empty(0, dtype=torch.int32)
+        self._host_buf = self._host_t.numpy()
+        self._plan_dev = torch.empty(0, dtype=torch.int32, device=self.device)
+        self._upload_evt = torch.cuda.Event()
+        self._uploaded = False  # a copy out of the host buffer may be in flight (_upload_evt)
 
     def plan(self, states, prompt_len, num_computed, block_tables, budget: int, policy: PlanPolicy | None = None):
         """Plans into a host buffer the runner keeps (grown when a batch needs
@@ -35,12 +41,45 @@ class StepRunner:
         is used); None plans with sarathi_plan and `budget`."""
         reqs, keep = make_requests(states, prompt_len, num_computed, block_tables)
         tb = policy.token_budget if policy is not None else budget
-        hb, _ = sarathi_plan_bounds(reqs, len(states), tb, self.shape, self.num_sms)
-        if self._host_buf.nbytes < hb:
-            self._host_buf = np.zeros(max(hb // 4 + 4, 2 * self._host_buf.size), dtype=np.int32)
-        if policy is not None:
-            return sarathi_plan_ex(reqs, len(states), policy, self.shape, self.num_sms, self._host_buf)
-        return sarathi_plan(reqs, len(states), budget, self.shape, self.num_sms, self._host_buf)
+        if self._uploaded:
+            self._upload_evt.synchronize()  # the previous plan's copy has left the buffer
+            self._uploaded = False
+        for attempt in range(2):
+            try:
+                if policy is not None:
+                    return sarathi_plan_ex(reqs, len(states), policy, self.shape, self.num_sms, self._host_buf)
+                return sarathi_plan(reqs, len(states), budget, self.shape, self.num_sms, self._host_buf)
+            except SarathiError as e:
+                if e.status != ERR_CAPACITY or attempt:
+                    raise
+                # host_buf too small, or a block table too short: size the
+                # buffer by the bounds and plan again (the bounds call fails
+                # the same way in the second case)
+                hb, _ = sarathi_plan_bounds(reqs, len(states), tb, self.shape, self.num_sms)
+                if self._host_buf.nbytes >= hb:
+                    raise
+                self._host_t = torch.empty(max(hb // 4 + 4, 2 * self._host_buf.size), dtype=torch.int32,
+                                           pin_memory=True)
+                self._host_buf = self._host_t.numpy()
+
+    def upload_plan(self, info: PlanInfo) -> torch.Tensor:
+        """Enqueues on the runner's stream the copy of the packed plan of the
+        last plan() call (pinned memory) into a device buffer the runner
+        keeps; returns that buffer, valid until the next upload_plan."""
+        n = int(info.packed_ints)
+        if self._plan_dev.numel() < n + 4:
+            self.stream.synchronize()  # the old buffer may be in use by an enqueued step
+            self._plan_dev = torch.empty(max(n + 4, 2 * self._plan_dev.numel()), dtype=torch.int32,
+                                         device=self.device)
+        # (the buffer is pinned once plan() has sized it)
+        if torch.cuda.current_stream(self.device) == self.stream:
+            self._plan_dev[:n].copy_(self._host_t[:n], non_blocking=True)
+        else:
+            with torch.cuda.stream(self.stream):
+                self._plan_dev[:n].copy_(self._host_t[:n], non_blocking=True)
+        self._upload_evt.record(self.stream)
+        self._uploaded = True
+        return self._plan_dev
 
     def ensure_workspace(self, nbytes: int):
         if self.workspace.numel() < nbytes:
@@ -56,12 +95,25 @@ class StepRunner:
         self.stream.wait_stream(torch.cuda.current_stream(self.device))
         return dev
 
-    def run(self, q, k, v, k_cache, v_cache, out, plan_dev: torch.Tensor, info: PlanInfo) -> None:
+    def run(self, q, k, v, k_cache, v_cache, out, plan_dev: torch.Tensor, info: PlanInfo, plan_host=None) -> None:
         self.ensure_workspace(int(info.workspace_bytes))
         if info.max_kv_len > self.max_pos:
             raise ValueError(f"RoPE table covers {self.max_pos} positions, batch needs {info.max_kv_len}")
         sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info, self.rope, self.max_pos,
-                           self.workspace, self.shape, self.sm_scale, self.stream, self.rope_style)
+                           self.workspace, self.shape, self.sm_scale, self.stream, self.rope_style, plan_host)
+
+    def run_planned(self, q, k, v, k_cache, v_cache, out, info: PlanInfo) -> None:
+        """Enqueues the step planned by the last plan() call: one library call
+        copies the packed plan from the runner's pinned buffer into its device
+        buffer and launches the kernel."""
+        n = int(info.packed_ints)
+        if self._plan_dev.numel() < n + 4:
+            self.stream.synchronize()  # the old buffer may be in use by an enqueued step
+            self._plan_dev = torch.empty(max(n + 4, 2 * self._plan_dev.numel()), dtype=torch.int32,
+                                         device=self.device)
+        self.run(q, k, v, k_cache, v_cache, out, self._plan_dev, info, plan_host=self._host_t)
+        self._upload_evt.record(self.stream)
+        self._uploaded = True
 
     def status(self) -> int:
         return sarathi_workspace_status(self.workspace, self.stream)

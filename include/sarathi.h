@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define SARATHI_ABI_VERSION 3
+#define SARATHI_ABI_VERSION 4
 /* int32 words of one kernel work item in the packed plan.  Items are kernel
  * bookkeeping: their layout is private to the library and may change with
  * SARATHI_ABI_VERSION; callers copy the packed plan as a whole. */
@@ -236,6 +236,11 @@ typedef struct sarathi_attn_args {
     sarathi_shape shape;
     float sm_scale;             /* softmax scale, normally 1/sqrt(head_dim)             */
     int32_t rope_style;         /* SARATHI_ROPE_ROTATE_HALF or SARATHI_ROPE_INTERLEAVED */
+    const int32_t* plan_host;   /* optional HOST copy of the packed plan (pinned memory */
+                                /*   for an asynchronous copy): when not NULL the call  */
+                                /*   first enqueues its copy into `plan` (packed_ints    */
+                                /*   int32), so that it must not change until the copy   */
+                                /*   has run on the stream; NULL: `plan` already holds it */
 } sarathi_attn_args;
 
 /* Enqueue the step on `cuda_stream` (a cudaStream_t): one kernel launch, no

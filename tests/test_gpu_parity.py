@@ -107,6 +107,27 @@ def test_repeat_launch_is_deterministic_and_leaves_workspace_clean():
     assert np.all(hdr[:3] == 0)
 
 
+def test_plan_copied_inside_the_step_call_gives_the_same_bits():
+    """StepRunner.run_planned: the packed plan goes from the runner's pinned
+    buffer to the device inside sarathi_mixed_attn (args.plan_host); the step
+    equals the one launched with a plan already on the device."""
+    import torch
+    gs = GpuStep(W.mistral())
+    k0, v0 = gs.kc_dev.clone(), gs.vc_dev.clone()
+    assert gs.run() == 0
+    out1, k1 = gs.out.clone(), gs.kc_dev.clone()
+    gs.kc_dev.copy_(k0)
+    gs.vc_dev.copy_(v0)
+    gs.out.fill_(float("nan"))
+    r = gs.runner
+    st, info, packed = r.plan(*gs.wl.arrays(), gs.wl.budget)
+    r.run_planned(gs.q_dev, gs.k_dev, gs.v_dev, gs.kc_dev, gs.vc_dev, gs.out, info)
+    torch.cuda.synchronize()
+    assert r.status() == 0
+    assert np.array_equal(to_u16(gs.out), to_u16(out1))
+    assert np.array_equal(to_u16(gs.kc_dev), to_u16(k1))
+
+
 def test_tiny_chunked_schedule_equals_one_shot_and_oracle():
     """The 200-token prompt in chunks of 64 over 4 steps next to 2 decodes, then
     the same prompt in one shot: same KV pages, outputs within tolerance, and
