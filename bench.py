@@ -313,6 +313,17 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     torch.cuda.synchronize(dev)
+    # context only: the same launch with L2 left warm (no flush between launches)
+    warm = []
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            runner.run(q_d, k_d, v_d, kc, vc, out, plan_dev, info)
+            b.record(stream)
+            warm.append((a, b))
+    stream.synchronize()
+    warm_ms = statistics.median([a.elapsed_time(b) for a, b in warm[3:]])
     hdr = runner.workspace[:64].view(torch.int32).cpu().tolist()
     if runner.status() != 0:
         raise RuntimeError(f"device error in the timed region: workspace header {hdr[:12]}")
@@ -365,7 +376,8 @@ def run_ours(args, rank, world, local_rank):
                 "includes": "pinned H2D of q, k, v (one copy) overlapping the host plan, pinned H2D of the plan and the kernel (one library call), D2H (out)"},
         "clocks": clk.summary(),
         "gpu_launches": args.steps,
-        "timing": {"kernel_ms_min": min(ms), "kernel_ms_median": statistics.median(ms), "wall_s": t_wall},
+        "timing": {"kernel_ms_min": min(ms), "kernel_ms_median": statistics.median(ms), "wall_s": t_wall,
+                   "kernel_ms_median_warm_l2": warm_ms},
     }
     if not args.no_cpu_baseline:
         kc_h = kc.view(torch.int16).cpu().numpy().view(np.uint16)
@@ -374,6 +386,12 @@ def run_ours(args, rank, world, local_rank):
         # re-appends the same values, so the sample sees the same state
         est, cores, desc = oracle_sample_time(wl, meta, q, k, v, kc_h, vc_h, args.cpu_seconds)
         res["cpu_baseline"] = {"value": T / est, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        # the same oracle on one core, on a smaller sample
+        import oracle
+        oracle.set_num_threads(1)
+        est1, _, desc1 = oracle_sample_time(wl, meta, q, k, v, kc_h, vc_h, args.cpu_seconds / 4, seed=1)
+        oracle.set_num_threads(cores)
+        res["cpu_baseline"]["one_core"] = {"value": T / est1, "unit": UNIT, "sample": desc1}
     return res
 
 
@@ -569,20 +587,22 @@ def run_sweep(args):
     runner = StepRunner(sh.H_q, sh.H_kv, sh.d, L + 64, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
+    reps = 1 if args.sweep_once else 7
+
     def time_step(wl, t0):
         st, info, packed = runner.plan(*wl.arrays(), wl.budget)
         pd = runner.upload(packed)
         n = info.num_tokens
         out = torch.empty((n, sh.H_q, sh.d), dtype=torch.bfloat16, device=dev)
         ms = []
-        for i in range(7):
+        for i in range(reps):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             runner.run(qd[t0:t0 + n], kd[t0:t0 + n], vd[t0:t0 + n], kc, vc, out, pd, info)
             b.record()
             b.synchronize()
-            if i >= 2:
+            if i >= 2 or reps == 1:
                 ms.append(a.elapsed_time(b))
         if runner.status() != 0:
             raise RuntimeError("device error in the sweep")
@@ -602,6 +622,10 @@ def run_sweep(args):
     one = chunks[L]["prompt_us"]
     for c in chunks:
         chunks[c]["overhead_vs_one_shot"] = chunks[c]["prompt_us"] / one - 1.0
+    if args.sweep_once:
+        # one launch per chunk step, for a DRAM-traffic capture of each (ncu)
+        print(json.dumps({"sweep_once": {str(c): v["steps"] for c, v in chunks.items()}}), flush=True)
+        return None
     tq = {}
     for n in (128, 129, 256, 257, 512, 513):
         wl = W._build("tq", sh, n, [(W.PREFILL_RUNNING, 4096 + n, 4096, 4096 + n)], base.seed)
@@ -630,6 +654,8 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="chunk-size / tile-quantisation sweep (own JSON line)")
     ap.add_argument("--serve", action="store_true", help="multi-step loop over arrival traces (own JSON line)")
     ap.add_argument("--qkv", action="store_true", help="QKV projection GEMM, fused vs separate (own JSON line)")
+    ap.add_argument("--sweep-once", action="store_true",
+                    help="with --sweep: one launch per chunk step and nothing else (for ncu traffic captures)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

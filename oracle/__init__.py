@@ -97,6 +97,8 @@ def _load():
     lib.oracle_reread_tokens.argtypes = [ctypes.c_int, _i32p, _i32p, _i32p, ctypes.c_int]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
+    lib.oracle_set_num_threads.restype = None
+    lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
     _lib = lib
     return lib
 
@@ -107,6 +109,11 @@ def _i32(a):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the OpenMP loops from now on."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def bf16_rne(x) -> np.ndarray:

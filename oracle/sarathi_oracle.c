@@ -451,6 +451,15 @@ int64_t oracle_reread_tokens(int n_sched, const int32_t* qo_indptr, const int32_
     return total;
 }
 
+/* Threads the OpenMP loops use from now on (timing on one core). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
