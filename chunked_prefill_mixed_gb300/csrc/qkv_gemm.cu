@@ -34,17 +34,26 @@
 namespace sarathi {
 namespace qkv {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;  // tile and K slice
-constexpr int kStages = 4;
+constexpr int kBM = 128, kBK = 64;             // tile rows and K slice
 constexpr int kABytes = kBM * kBK * 2;         // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;         // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;                  // 6 warps
-constexpr int kSmemBars = kStages * kStageBytes;
-constexpr int kSmemBytes = kSmemBars + 256;
-constexpr int kSmemAlloc = kSmemBytes + 1024;  // + alignment slack
 constexpr unsigned long long kWaitNs = 2000000000ull;
-static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
+// Tile width BN (256 or 192): as many stages of A 16 KB + B BN x 128 B as fit
+// 200 KB (4 at 256, 5 at 192).
+template <int BN>
+struct Tile {
+    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = (200 * 1024) / kStageBytes;
+    static constexpr int kSmemBars = kStages * kStageBytes;
+    static constexpr int kSmemAlloc = kSmemBars + 256 + 1024;  // barriers + alignment slack
+    // barriers: full / empty per stage, accumulator full / empty per TMEM buffer, drain
+    static constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAccFull = 2 * kStages;
+    static constexpr int kBarAccEmpty = 2 * kStages + 2, kBarDrain = 2 * kStages + 4, kNumBars = kBarDrain + 1;
+    static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
+    static_assert(kNumBars * 8 <= 256, "barrier area");
+    static_assert(BN % 32 == 0 && BN <= 256 && 2 * BN <= 512, "MMA N and TMEM columns");
+};
 
 struct Params {
     __nv_bfloat16* q;
@@ -149,14 +158,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) asm volatile("" : "+f"(v[i]));
 }
 
-// Barriers: full / empty per stage, accumulator full / empty per TMEM buffer, drain.
-constexpr int kBarFull = 0, kBarEmpty = kStages, kBarAccFull = 2 * kStages, kBarAccEmpty = 2 * kStages + 2;
-constexpr int kBarDrain = 2 * kStages + 4, kNumBars = kBarDrain + 1;
-static_assert(kNumBars * 8 <= 256, "barrier area");
-
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) qkv_kernel(const __grid_constant__ Params P,
                                                           const __grid_constant__ CUtensorMap tmX,
                                                           const __grid_constant__ CUtensorMap tmW) {
+    using TL = Tile<BN>;
+    constexpr int kBN = BN, kStages = TL::kStages, kStageBytes = TL::kStageBytes, kSmemBars = TL::kSmemBars;
+    constexpr int kBarFull = TL::kBarFull, kBarEmpty = TL::kBarEmpty, kBarAccFull = TL::kBarAccFull;
+    constexpr int kBarAccEmpty = TL::kBarAccEmpty, kBarDrain = TL::kBarDrain, kNumBars = TL::kNumBars;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint32_t s_tmem;
@@ -355,13 +364,7 @@ extern "C" int32_t sarathi_qkv_proj(const sarathi_qkv_args* a, void* cuda_stream
     P.Nk = Hkv * d;
     P.N = P.Nq + 2 * P.Nk;
     P.mt = (P.T + kBM - 1) / kBM;
-    P.nt = (P.N + kBN - 1) / kBN;
     P.status = static_cast<int32_t*>(a->workspace);
-    CUtensorMap tmX, tmW;
-    int32_t st = make_map(&tmX, a->x, P.T, P.hidden, kBM);
-    if (st) return st;
-    st = make_map(&tmW, a->w, P.N, P.hidden, kBN);
-    if (st) return st;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_err(e, "cudaGetDevice");
@@ -373,19 +376,41 @@ extern "C" int32_t sarathi_qkv_proj(const sarathi_qkv_args* a, void* cuda_stream
         if (!ds.ready) {
             e = cudaDeviceGetAttribute(&ds.sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return cuda_err(e, "cudaDeviceGetAttribute");
-            e = cudaFuncSetAttribute(qkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-            if (e != cudaSuccess) return cuda_err(e, "cudaFuncSetAttribute");
-            int resident = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, qkv_kernel, kThreads, kSmemAlloc);
-            if (e != cudaSuccess) return cuda_err(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-            if (resident < 1) return fail(SARATHI_ERR_CUDA, "QKV kernel does not fit one SM");
+            for (int w = 0; w < 2; ++w) {
+                const void* fn = w ? (const void*)qkv_kernel<192> : (const void*)qkv_kernel<256>;
+                const int bytes = w ? Tile<192>::kSmemAlloc : Tile<256>::kSmemAlloc;
+                e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+                if (e != cudaSuccess) return cuda_err(e, "cudaFuncSetAttribute");
+                int resident = 0;
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, fn, kThreads, bytes);
+                if (e != cudaSuccess) return cuda_err(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+                if (resident < 1) return fail(SARATHI_ERR_CUDA, "QKV kernel does not fit one SM");
+            }
             ds.ready = true;
         }
         sms = ds.sms;
     }
+    // Tile width: the one whose waves of tiles over the SMs move the fewest
+    // operand bytes per SM (a tile's K slice is 16 KB of X plus BN x 128 B of W),
+    // the wider one on ties.  At 512 tokens x 6144 columns 192 fills one wave
+    // with 128 tiles where 256 leaves 56 SMs idle.
+    auto cost = [&](int bn) {
+        const long long tiles = (long long)P.mt * ((P.N + bn - 1) / bn);
+        return ((tiles + sms - 1) / sms) * (long long)(kABytes + bn * kBK * 2);
+    };
+    const int BN = cost(192) < cost(256) ? 192 : 256;
+    P.nt = (P.N + BN - 1) / BN;
+    CUtensorMap tmX, tmW;
+    int32_t st = make_map(&tmX, a->x, P.T, P.hidden, kBM);
+    if (st) return st;
+    st = make_map(&tmW, a->w, P.N, P.hidden, BN);
+    if (st) return st;
     const int tiles = P.mt * P.nt;
     const int grid = tiles < sms ? tiles : sms;
-    qkv_kernel<<<grid, kThreads, kSmemAlloc, (cudaStream_t)cuda_stream>>>(P, tmX, tmW);
+    if (BN == 192)
+        qkv_kernel<192><<<grid, kThreads, Tile<192>::kSmemAlloc, (cudaStream_t)cuda_stream>>>(P, tmX, tmW);
+    else
+        qkv_kernel<256><<<grid, kThreads, Tile<256>::kSmemAlloc, (cudaStream_t)cuda_stream>>>(P, tmX, tmW);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_err(e, "qkv_kernel launch");
     sarathi::set_error("");
