@@ -38,8 +38,8 @@ constexpr int kBM = 128, kBK = 64;             // tile rows and K slice
 constexpr int kABytes = kBM * kBK * 2;         // 16 KB
 constexpr int kThreads = 192;                  // 6 warps
 constexpr unsigned long long kWaitNs = 2000000000ull;
-// Tile width BN (256 or 192): as many stages of A 16 KB + B BN x 128 B as fit
-// 200 KB (4 at 256, 5 at 192).
+// Tile width BN (128, 192 or 256): as many stages of A 16 KB + B BN x 128 B as
+// fit 200 KB (6 at 128, 5 at 192, 4 at 256).
 template <int BN>
 struct Tile {
     static constexpr int kBBytes = BN * kBK * 2;
@@ -376,9 +376,10 @@ extern "C" int32_t sarathi_qkv_proj(const sarathi_qkv_args* a, void* cuda_stream
         if (!ds.ready) {
             e = cudaDeviceGetAttribute(&ds.sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return cuda_err(e, "cudaDeviceGetAttribute");
-            for (int w = 0; w < 2; ++w) {
-                const void* fn = w ? (const void*)qkv_kernel<192> : (const void*)qkv_kernel<256>;
-                const int bytes = w ? Tile<192>::kSmemAlloc : Tile<256>::kSmemAlloc;
+            for (int w = 0; w < 3; ++w) {
+                const void* fn = w == 0 ? (const void*)qkv_kernel<128>
+                               : w == 1 ? (const void*)qkv_kernel<192> : (const void*)qkv_kernel<256>;
+                const int bytes = w == 0 ? Tile<128>::kSmemAlloc : w == 1 ? Tile<192>::kSmemAlloc : Tile<256>::kSmemAlloc;
                 e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
                 if (e != cudaSuccess) return cuda_err(e, "cudaFuncSetAttribute");
                 int resident = 0;
@@ -393,12 +394,15 @@ extern "C" int32_t sarathi_qkv_proj(const sarathi_qkv_args* a, void* cuda_stream
     // Tile width: the one whose waves of tiles over the SMs move the fewest
     // operand bytes per SM (a tile's K slice is 16 KB of X plus BN x 128 B of W),
     // the wider one on ties.  At 512 tokens x 6144 columns 192 fills one wave
-    // with 128 tiles where 256 leaves 56 SMs idle.
+    // with 128 tiles where 256 leaves 56 SMs idle.  (A 224-wide tile, four
+    // stages deep, measured slower than both at 2048 tokens and is not used.)
     auto cost = [&](int bn) {
         const long long tiles = (long long)P.mt * ((P.N + bn - 1) / bn);
         return ((tiles + sms - 1) / sms) * (long long)(kABytes + bn * kBK * 2);
     };
-    const int BN = cost(192) < cost(256) ? 192 : 256;
+    int BN = 256;
+    for (int bn : {192, 128})
+        if (cost(bn) < cost(BN)) BN = bn;
     P.nt = (P.N + BN - 1) / BN;
     CUtensorMap tmX, tmW;
     int32_t st = make_map(&tmX, a->x, P.T, P.hidden, kBM);
@@ -407,10 +411,13 @@ extern "C" int32_t sarathi_qkv_proj(const sarathi_qkv_args* a, void* cuda_stream
     if (st) return st;
     const int tiles = P.mt * P.nt;
     const int grid = tiles < sms ? tiles : sms;
-    if (BN == 192)
-        qkv_kernel<192><<<grid, kThreads, Tile<192>::kSmemAlloc, (cudaStream_t)cuda_stream>>>(P, tmX, tmW);
+    cudaStream_t strm = (cudaStream_t)cuda_stream;
+    if (BN == 128)
+        qkv_kernel<128><<<grid, kThreads, Tile<128>::kSmemAlloc, strm>>>(P, tmX, tmW);
+    else if (BN == 192)
+        qkv_kernel<192><<<grid, kThreads, Tile<192>::kSmemAlloc, strm>>>(P, tmX, tmW);
     else
-        qkv_kernel<256><<<grid, kThreads, Tile<256>::kSmemAlloc, (cudaStream_t)cuda_stream>>>(P, tmX, tmW);
+        qkv_kernel<256><<<grid, kThreads, Tile<256>::kSmemAlloc, strm>>>(P, tmX, tmW);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_err(e, "qkv_kernel launch");
     sarathi::set_error("");

@@ -36,14 +36,34 @@ def _run(x, w, Hq, Hkv, d):
     return q, k, v
 
 
+# The launcher picks the tile width from the product's shape: 128 for the small
+# products, 192 for the Mistral-like 512 tokens x 6144 columns (and the
+# Llama-like 2048-token product below), 256 for 19 M tiles x 2048 columns (152
+# tiles: one whole wave).
 @pytest.mark.parametrize("T,hidden,Hq,Hkv,d", [(1, 256, 4, 4, 64), (66, 256, 4, 4, 64), (200, 512, 8, 2, 64),
-                                               (129, 1024, 16, 4, 128), (512, 4096, 32, 8, 128)])
+                                               (129, 1024, 16, 4, 128), (512, 4096, 32, 8, 128),
+                                               (19 * 128, 512, 8, 4, 128)])
 def test_qkv_proj_matches_oracle(T, hidden, Hq, Hkv, d):
     x, w = _inputs(T, hidden, Hq, Hkv, d, seed=T + hidden)
     gq, gk, gv = _run(x, w, Hq, Hkv, d)
     oq, ok, ov = oracle.qkv_proj(x, w, Hq, Hkv, d)
     for g, o, name in ((gq, oq, "q"), (gk, ok, "k"), (gv, ov, "v")):
         gd = oracle.bf16_to_double(to_u16(g))
+        assert np.all(np.isfinite(gd)), name
+        err = np.abs(gd - o)
+        assert np.all(err <= 2.0 ** -7 * np.abs(o) + 1e-4), (name, float(err.max()))
+
+
+def test_qkv_proj_llama7b_step_sampled_rows():
+    """The Llama-2-7B-like 2048-token product (16 M tiles x 12288 columns),
+    checked on 3 rows of every 128-row tile over all columns."""
+    T, hidden, Hq, Hkv, d = 2048, 4096, 32, 32, 128
+    x, w = _inputs(T, hidden, Hq, Hkv, d, seed=2048)
+    gq, gk, gv = _run(x, w, Hq, Hkv, d)
+    rows = np.array(sorted({r for m in range(T // 128) for r in (128 * m, 128 * m + 77, 128 * m + 127)}))
+    oq, ok, ov = oracle.qkv_proj(x[rows], w, Hq, Hkv, d)
+    for g, o, name in ((gq, oq, "q"), (gk, ok, "k"), (gv, ov, "v")):
+        gd = oracle.bf16_to_double(to_u16(g[rows.tolist()]))
         assert np.all(np.isfinite(gd)), name
         err = np.abs(gd - o)
         assert np.all(err <= 2.0 ** -7 * np.abs(o) + 1e-4), (name, float(err.max()))
