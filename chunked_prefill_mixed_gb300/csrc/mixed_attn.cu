@@ -65,7 +65,7 @@ struct KParams {
     int slot_floats;
 };
 
-constexpr int kThreads = 416;                                  // 13 warps
+constexpr int kThreads = 352;                                  // 11 warps
 constexpr int kDecWarps = 8;                                   // warps that stream decode pages
 constexpr int kDecStages = 3;                                  // per-warp page ring
 constexpr int kPageHalfBytes = kPage * 128;                    // 16 rows x 64 bf16
@@ -661,9 +661,11 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // MMAs issued by one thread run in order, so when S_T(j+1) is complete the
 // P.V of block j has read P_T and finished with O_T: the softmax needs no
 // other wait before it overwrites S_T or rescales O_T.
-// Roles: warps 8-11 are four TMA streams (K and V rings, one 64-column half
-// per stream: one issuing thread sustains only ~14 boxes/us), warp 12 lane 0
-// issues the MMAs, warps 0-7 run the two softmaxes and epilogues.
+// Roles: warps 8 and 9 are the TMA producers of the K and V rings (sixteen
+// lanes each, one box per lane: the whole 128-key block of a ring in one
+// instruction), warp 10 lane 0 issues the MMAs, warps 0-7 run the two
+// softmaxes and epilogues.  Eleven warps leave room for 168 registers a
+// thread (thirteen capped it at 128 and made the kernel spill).
 // ----------------------------------------------------------------------------
 constexpr int kTcKeys = 128;                     // keys per block
 constexpr int kTcTiles = kTilesPerItem;          // Q tiles per prefill item
@@ -715,11 +717,11 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
     const uint32_t bars = smem_u32(smem + kSmemBars);
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
-    // The TMA producers (warps 8-11) start on the history pages at once; only
+    // The TMA producers (warps 8 and 9) start on the history pages at once; only
     // the blocks holding the chunk's own keys wait for this request's APPENDs.
-    // Meanwhile warps 0-7 and 12 write the Q tiles and meet on named barrier 5.
-    const bool q_writer = warp < 8 || warp == 12;
-    const int qtid = warp == 12 ? 256 + lane : tid;
+    // Meanwhile warps 0-7 and 10 write the Q tiles and meet on named barrier 5.
+    const bool q_writer = warp < 8 || warp == 10;
+    const int qtid = warp == 10 ? 256 + lane : tid;
     constexpr int kQThreads = 288;
     constexpr int kQUnits = kTileRows * (HALF / 8);  // per tile
     // Q rows, RoPE'd in fp32 at their absolute positions, into the swizzled
@@ -749,20 +751,21 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         tc_fence_after();
     }
 
-    if (warp >= 8 && warp < 12) {
-        // ---------------- TMA producers: warp 8+2v+hf loads column half hf of ring v ----------------
-        const int stream = warp - 8;
-        const bool is_v = stream >= 2;
-        const int hf = stream & 1;
-        if (hf < HALVES) {
-            // lanes 0-7 each issue one page's box in the same instruction
+    if (warp == 8 || warp == 9) {
+        // ---------------- TMA producers: warp 8 fills the K ring, warp 9 the V ring ----------------
+        const bool is_v = warp == 9;
+        // lane 8 hf + q issues the box of page q of the block, column half hf:
+        // the whole block in one instruction
+        const int hf = lane >> 3, pq = lane & 7;
+        const bool issuer = hf < HALVES;
+        {
             const CUtensorMap* map = is_v ? tmV : tmK;
             const int full0 = is_v ? kBarVFull : kBarKFull;
             const int empty0 = is_v ? kBarVEmpty : kBarKEmpty;
             const int fill = is_v ? kPhVFill : kPhKFill;
             uint8_t* ring = smem + (is_v ? L::kV : L::kK) + hf * BLK_HALF;
             const int32_t* kvi = P.plan + P.off_kvi + R.kvp0;
-            int id = (lane < 8 && lane < pages_hi) ? it[kIds + lane] : 0;  // block 0's ids come with the item
+            int id = (issuer && pq < pages_hi) ? it[kIds + pq] : 0;  // block 0's ids come with the item
             const int j_chunk = R.h / kTcKeys;  // first block with a key of the chunk
             for (int j = 0; j < nblk; ++j) {
                 if (j == j_chunk) {
@@ -785,19 +788,19 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 }
                 if (*(volatile int*)s_abort) break;
                 const int st = j % NST;
-                const int nxt = (lane < 8 && (j + 1) * 8 + lane < pages_hi) ? kvi[(j + 1) * 8 + lane] : 0;
+                const int nxt = (issuer && (j + 1) * 8 + pq < pages_hi) ? kvi[(j + 1) * 8 + pq] : 0;
                 const int npg = min(kTcKeys / kPage, pages_hi - j * 8);
                 mbar_wait_bounded(P, bar(empty0 + st), ph_get(ph, fill + st) ^ 1u, s_abort, (is_v ? 2000 : 1000) + j,
                                   it);
-                if (lane == 0) mbar_expect_tx(bar(full0 + st), (uint32_t)npg * kPageHalfBytes);
+                if (lane == 0) mbar_expect_tx(bar(full0 + st), (uint32_t)(npg * HALVES) * kPageHalfBytes);
                 __syncwarp();
-                if (lane < npg) {
+                if (issuer && pq < npg) {
                     int page = id;
                     if (page < 0 || page >= P.num_pages) {
                         raise_error(P, kErrBounds, page, s_abort);
                         page = 0;
                     }
-                    tma_load_2d(smem_u32(ring + st * L::kTile + lane * kPageHalfBytes), map, hf * 64,
+                    tma_load_2d(smem_u32(ring + st * L::kTile + pq * kPageHalfBytes), map, hf * 64,
                                 (page * P.Hkv + g) * kPage, bar(full0 + st));
                 }
                 __syncwarp();
@@ -805,7 +808,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 id = nxt;
             }
         }
-    } else if (warp == 12) {
+    } else if (warp == 10) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc_s = umma_idesc(kTcKeys, false);
@@ -1295,8 +1298,6 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
             if (i == kBarPFull || i == kBarPFull + 1) count = 128;  // the tile's softmax threads
-            if (i >= kBarKFull && i < kBarKFull + kPfStagesMax) count = D / 64;
-            if (i >= kBarVFull && i < kBarVFull + kPfStagesMax) count = D / 64;
             mbar_init(bars + 8 * i, count);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1357,7 +1358,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
     }
     if (tmem_held) {
         // no tensor-core work may be in flight when the tensor memory is released
-        if (tid == 12 * 32) {
+        if (tid == 10 * 32) {
             umma_commit(bars + 8 * kBarDrain);
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(bars + 8 * kBarDrain, 0))
