@@ -640,6 +640,17 @@ __device__ __forceinline__ void tmem_st16_nw(uint32_t taddr, const uint32_t (&v)
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 16 consecutive 32-bit columns of this thread's TMEM lane, waited for.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(v[i]));
+}
 
 // ----------------------------------------------------------------------------
 // PREFILL item on the 5th-generation tensor cores: two Q tiles (A, B) of up to
@@ -651,9 +662,10 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // the tensor cores read) serve 256 query rows.
 //   S_T = Q_T K^T per block: tcgen05.mma (M 128, N 128, K 16 steps), fp32 in
 //       TMEM columns [128 T, 128 T + 128);
-//   softmax (warps 4T..4T+3, thread = query row = TMEM lane): a max pass and
-//       an exponent pass over the row's 128 scores, lazy rescale of O (only
-//       when the max grows by more than 2^8), bf16 P written over the first
+//   softmax (warps 4T..4T+3, thread = query row = TMEM lane): one pass over
+//       the row's 128 scores in two halves of 64 (each half's max from the
+//       registers that then give its P), lazy rescale of O (only when the max
+//       grows by more than 2^8), bf16 P written over the first
 //       64 columns of S_T;
 //   O_T += P_T V: tcgen05.mma with A = P from TMEM and V read as an MN-major
 //       operand straight from the TMA-loaded pages; O_T in TMEM columns
@@ -891,44 +903,15 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 mbar_wait_bounded(P, bar(kBarSFull + T), ph_get(ph, kPhSUse + T), s_abort, 6000 + j, it);
                 ph_flip(ph, kPhSUse + T);
                 tc_fence_after();
-                // pass 1: the row max of the raw scores (the scale > 0 is applied after)
-                float mx = -INFINITY;
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    float v[64];
-                    tmem_ld32_nw(lane_base + s_col + (uint32_t)(h * 64), v);
-                    tmem_ld32_nw(lane_base + s_col + (uint32_t)(h * 64 + 32), v + 32);
-                    tmem_wait_ld(v);
-                    const int kc = kb0 + h * 64;
-                    if (kc + 63 > pos_r) {
-#pragma unroll
-                        for (int e = 0; e < 64; e += 2)
-                            mx = fmax3(mx, kc + e <= pos_r ? v[e] : -INFINITY, kc + e + 1 <= pos_r ? v[e + 1] : -INFINITY);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 64; e += 2) mx = fmax3(mx, v[e], v[e + 1]);
-                    }
-                }
-                // lazy rescale: move the exponent base only when the max grows by > 2^8
-                const float mxs = mx * sl2;
-                const bool grow = mxs > m_run + 8.f;
-                const float m_new = grow ? mxs : m_run;
-                const float alpha = grow ? exp2f(m_run - m_new) : 1.f;
-                if (j > 0 && __any_sync(0xffffffffu, grow)) {
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(lane_base + o_col + (uint32_t)(c * 32), o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tmem_st32(lane_base + o_col + (uint32_t)(c * 32), o);
-                    }
-                }
-                // pass 2: P = 2^(s - m) in bf16, two keys per column, over the first
-                // 64 columns of S (columns of half h are written only after half h
-                // and every column below it have been read)
+                // One pass over the row's 128 scores, 64 at a time: each half's max
+                // comes from the registers it is loaded into, and the exponent base
+                // moves only when a half's max exceeds it by more than 2^8 (lazy
+                // rescaling).  When the second half moves it, the first half's P,
+                // already written in bf16, is rescaled in place (warp-wide; rare
+                // after a tile's first block).
                 float2 sum2 = make_float2(0.f, 0.f);
-                const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(-m_new, -m_new);
+                const float2 sl2v = make_float2(sl2, sl2);
+                float m_use = m_run;  // exponent base of this block's P
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     float v[64];
@@ -940,6 +923,32 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
 #pragma unroll
                         for (int e = 0; e < 64; ++e) v[e] = kc + e <= pos_r ? v[e] : -INFINITY;
                     }
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 64; e += 2) mx = fmax3(mx, v[e], v[e + 1]);
+                    const float mxs = mx * sl2;  // raw scores; the scale (> 0) applied to the max
+                    const bool grow = mxs > m_use + 8.f;
+                    if (h == 1 && __any_sync(0xffffffffu, grow)) {
+                        const float a = grow ? exp2f(m_use - mxs) : 1.f;
+                        sum2.x *= a;
+                        sum2.y *= a;
+                        tmem_wait_st();
+#pragma unroll 1
+                        for (int q = 0; q < 2; ++q) {
+                            uint32_t pw[16];
+                            tmem_ld16(lane_base + s_col + (uint32_t)(q * 16), pw);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pw[i] = pack_bf16(__uint_as_float(pw[i] << 16) * a,
+                                                  __uint_as_float(pw[i] & 0xFFFF0000u) * a);
+                            tmem_st16_nw(lane_base + s_col + (uint32_t)(q * 16), pw);
+                        }
+                    }
+                    if (grow) m_use = mxs;
+                    // P = 2^(s - m) in bf16, two keys per column, over the first 64
+                    // columns of S (half h's columns are written after half h and
+                    // every column below it have been read)
+                    const float2 nmv = make_float2(-m_use, -m_use);
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
                         uint32_t pk[16];
@@ -954,8 +963,21 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                     }
                 }
                 tmem_wait_st();
+                // O and l hold sums with base m_run: bring them to m_use
+                const bool moved = m_use != m_run;
+                const float alpha = moved ? exp2f(m_run - m_use) : 1.f;
+                if (j > 0 && __any_sync(0xffffffffu, moved)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(lane_base + o_col + (uint32_t)(c * 32), o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st32(lane_base + o_col + (uint32_t)(c * 32), o);
+                    }
+                }
                 l_run = l_run * alpha + (sum2.x + sum2.y);
-                m_run = m_new;
+                m_run = m_use;
                 // last block: V rows past kv_hi hold stale bytes; zero them so 0 x V stays 0
                 if (T == zero_tile && j == nblk - 1 && kb0 + kTcKeys > kv_hi) {
                     const int vst = j % NST;
