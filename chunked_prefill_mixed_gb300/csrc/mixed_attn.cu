@@ -1120,10 +1120,13 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     __syncthreads();
 
     const int mi = lane >> 3;
-    // Q fragments are re-read from shared memory for every page (4 KB per
-    // 8 KB page) rather than held: the accumulator alone takes D / 2
-    // registers a thread
+    // the Q fragments of every 16-wide k step, held for the whole item
     const int qrow = (mi & 1) * 8 + (lane & 7);
+    uint32_t qf[D / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+        ldsm_x4(smem_u32(qtile + sw128_chunk(16, qrow, 2 * kk + (mi >> 1))), qf[kk][0], qf[kk][1], qf[kk][2],
+                qf[kk][3]);
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
     float o[D / 8][4];
 #pragma unroll
@@ -1156,11 +1159,10 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int key = (mi >> 1) * 8 + (lane & 7);
-            uint32_t qa[4], b0, b1, b2, b3;
-            ldsm_x4(smem_u32(qtile + sw128_chunk(16, qrow, 2 * kk + (mi >> 1))), qa[0], qa[1], qa[2], qa[3]);
+            uint32_t b0, b1, b2, b3;
             ldsm_x4(smem_u32(kb + sw128_chunk(kPage, key, 2 * kk + (mi & 1))), b0, b1, b2, b3);
-            mma_bf16(sc[0], qa, b0, b1);
-            mma_bf16(sc[1], qa, b2, b3);
+            mma_bf16(sc[0], qf[kk], b0, b1);
+            mma_bf16(sc[1], qf[kk], b2, b3);
         }
         float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll
