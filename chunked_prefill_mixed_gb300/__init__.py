@@ -20,7 +20,7 @@ _lib = None
 OK, ERR_INVALID_ARG, ERR_CAPACITY, WARN_OVER_BUDGET_DECODES = 0, 1, 2, 3
 ERR_CUDA, ERR_UNSUPPORTED, ERR_DEVICE_CHECK = 4, 5, 6
 DECODE, PREFILL_RUNNING, PREFILL_WAITING = 0, 1, 2
-ABI_VERSION = 4   # SARATHI_ABI_VERSION of include/sarathi.h
+ABI_VERSION = 5   # SARATHI_ABI_VERSION of include/sarathi.h
 ROPE_ROTATE_HALF, ROPE_INTERLEAVED = 0, 1
 ITEM_INTS = 24    # SARATHI_ITEM_INTS
 
@@ -76,7 +76,7 @@ class PlanInfo(ctypes.Structure):
                [(n, ctypes.c_int32) for n in ("off_req_index", "off_num_new", "off_last_chunk", "off_qo_indptr",
                                              "off_kv_page_indptr", "off_kv_page_indices", "off_kv_last_page_len",
                                              "off_req_aux", "off_items", "packed_ints")] + \
-               [("workspace_bytes", ctypes.c_int64)]
+               [("workspace_bytes", ctypes.c_int64), ("n_first", ctypes.c_int32), ("first_sms", ctypes.c_int32)]
 
 
 class AttnArgs(ctypes.Structure):

@@ -55,6 +55,7 @@ struct KParams {
     const int32_t* plan;
     int off_qo, off_kvp, off_kvi, off_last, off_aux, off_items;
     int n_items, n_sched;
+    int n_first, first_sms;   // the work list's two queues (see the kernel's claim loop)
     const double2* rope;  // [max_pos][d/2] {cos, sin} in fp64
     const float4* ropef;  // [max_pos][d/2] {cos_hi, cos_lo, sin_hi, sin_lo}: cos = cos_hi + cos_lo to ~2^-48
     int rope_max_pos;
@@ -1334,10 +1335,24 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
     // completed-phase parities / counters, carried across work items
     uint32_t dec_phase = 0;
     PfPhase pf_phase = {};
+    // CTAs below first_sms take items from the first queue (list positions
+    // [0, n_first), head in header word 12) before the second (the rest, head
+    // in word 0); the others the other way round.  A queue's head runs past its
+    // end once it is empty; the last CTA out resets both.
+    const bool first_pref = (int)blockIdx.x < P.first_sms;
     for (;;) {
         if (tid == 0) {
-            const int idx = atomicAdd(&P.ws_int[0], 1);
-            if (idx < P.n_items) {
+            int idx = -1;
+            for (int q = 0; q < 2 && idx < 0; ++q) {
+                if ((q == 0) == first_pref) {
+                    const int k = atomicAdd(&P.ws_int[12], 1);
+                    if (k < P.n_first) idx = k;
+                } else {
+                    const int k = atomicAdd(&P.ws_int[0], 1);
+                    if (k < P.n_items - P.n_first) idx = P.n_first + k;
+                }
+            }
+            if (idx >= 0) {
                 const int4* src = reinterpret_cast<const int4*>(P.plan + P.off_items + (size_t)idx * kItemInts);
                 int4 v[kItemInts / 4];
 #pragma unroll
@@ -1408,6 +1423,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         if (tid == 0) {
             P.ws_int[0] = 0;
             P.ws_int[1] = 0;
+            P.ws_int[12] = 0;
         }
     }
 }
@@ -1556,7 +1572,8 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
     if (a->num_pages <= 0) return fail(SARATHI_ERR_INVALID_ARG, "num_pages must be positive");
     if (a->rope_max_pos < in->max_kv_len) return fail(SARATHI_ERR_CAPACITY, "RoPE table shorter than max_kv_len");
     if (a->workspace_bytes < in->workspace_bytes) return fail(SARATHI_ERR_CAPACITY, "workspace too small");
-    if (in->n_sched <= 0 || in->packed_ints <= 0 || in->off_items < 0 || (in->off_items & 3))
+    if (in->n_sched <= 0 || in->packed_ints <= 0 || in->off_items < 0 || (in->off_items & 3) || in->n_first < 0 ||
+        in->n_first > in->n_items || in->first_sms < 0)
         return fail(SARATHI_ERR_INVALID_ARG, "inconsistent plan info");
     const int d = a->shape.head_dim;
     const int Hkv = a->shape.num_heads_kv;
@@ -1616,6 +1633,7 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
     P.off_aux = in->off_req_aux;
     P.off_items = in->off_items;
     P.n_items = in->n_items;
+    P.n_first = in->n_first;
     P.n_sched = in->n_sched;
     P.rope = reinterpret_cast<const double2*>(a->rope_table);
     P.ropef = reinterpret_cast<const float4*>(a->rope_table + (size_t)a->rope_max_pos * d);
@@ -1631,6 +1649,9 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
     P.slot_floats = (int)partial_slot_floats(P.group, d);
 
     const int grid = std::min(sms, in->n_items);
+    // at least one CTA prefers the second queue whenever it holds items (its
+    // APPEND items must be taken while first-queue tiles may wait for them)
+    P.first_sms = in->n_first < in->n_items ? std::min(in->first_sms, grid - 1) : grid;
     cudaStream_t stream = (cudaStream_t)cuda_stream;
     if (a->plan_host) {
         // the caller's host copy of the plan goes to the device first, on the same stream

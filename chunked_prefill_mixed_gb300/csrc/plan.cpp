@@ -67,15 +67,19 @@ int32_t validate_requests(const sarathi_request* reqs, int32_t n_reqs) {
     return SARATHI_OK;
 }
 
-// Per-SM cost model used only to order the work list (longest first), fitted
-// to per-item times of the step kernel on GB300 with every SM busy: a prefill
-// tile costs a fixed start (Q fill, first loads, epilogue) plus its 128-key
-// blocks at tensor-core speed; a decode split a fixed start plus its pages at
-// an equal share of HBM bandwidth.
+// Cost model that orders the work list (longest first) and sizes the SM
+// partition between its two queues, fitted to per-item times of the step
+// kernel on GB300 and to step times over the partition size: a prefill tile
+// costs a fixed start (Q fill, first loads, epilogue) plus its 128-key blocks
+// at tensor-core speed; a decode split a fixed start plus its pages at an
+// equal share of HBM bandwidth (every SM streaming), or at one SM's own rate
+// while fewer SMs stream than saturate HBM.
 constexpr double kPrefillFixedNs = 8000.0;
 constexpr double kPrefillFlopPerNs = 6000.0;
 constexpr double kDecodeFixedNs = 2000.0;
-constexpr double kDecodeBytesPerNs = 40.0;
+constexpr double kDecodeBytesPerNs = 40.0;       // a decode split's share of HBM with every SM streaming
+constexpr double kDecodeAloneBytesPerNs = 80.0;  // one SM's own streaming rate when HBM has room
+constexpr double kHbmBytesPerNs = 6500.0;        // the whole GPU
 
 }  // namespace
 }  // namespace sarathi
@@ -296,13 +300,22 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
             }
         }
     }
-    // Longest first.  The tiles of one (request, kv head) read the same pages,
-    // so they stay contiguous: the group sorts by its costliest tile.  (The
-    // sort moves 4-byte indices, not the items.)
-    const size_t n_tiles = tiles.size(), nk = tiles.size() + decs.size();
-    auto item_at = [&](uint32_t i) -> const Timed& { return i < n_tiles ? tiles[i] : decs[i - n_tiles]; };
-    std::vector<double> key(nk);
-    std::vector<int64_t> grp(nk);
+    // Two queues.  The first holds the prefill tiles, longest first (the tiles
+    // of one (request, kv head) read the same pages, so they stay contiguous:
+    // the group sorts by its costliest tile); the second the decode splits,
+    // longest first.  CTAs [0, first_sms) take items from the first queue and
+    // the others from the second, each falling back to the other queue once its
+    // own is empty: the compute-bound prefill tiles run on a partition of the
+    // SMs for the whole step while the other SMs stream the decodes' KV at the
+    // full HBM rate (with every SM on prefill at the start of a step, the
+    // decodes would stream from a few SMs meanwhile); first_sms comes from a
+    // fluid model of the two sides (below).  APPEND items lead
+    // the second queue (they never wait, so the streaming CTAs take them first
+    // and the tiles that wait for them are not held up), or the first when
+    // there are no decodes.  (The sorts move 4-byte indices, not the items.)
+    const size_t n_tiles = tiles.size();
+    std::vector<double> key(n_tiles);
+    std::vector<int64_t> grp(n_tiles);
     for (size_t i = 0; i < n_tiles;) {
         size_t e = i;
         const int32_t s0 = tiles[i].it[kS], g0 = tiles[i].it[kG];
@@ -313,47 +326,62 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
             grp[i] = (int64_t)s0 * Hkv + g0;
         }
     }
-    for (size_t i = 0; i < decs.size(); ++i) {
-        key[n_tiles + i] = decs[i].ns_est;
-        grp[n_tiles + i] = -1;
-    }
-    std::vector<uint32_t> order(nk);
-    for (size_t i = 0; i < nk; ++i) order[i] = (uint32_t)i;
-    std::stable_sort(order.begin(), order.end(), [&](uint32_t a, uint32_t b) {
+    std::vector<uint32_t> pf_order(n_tiles), dec_order(decs.size());
+    for (size_t i = 0; i < n_tiles; ++i) pf_order[i] = (uint32_t)i;
+    for (size_t i = 0; i < decs.size(); ++i) dec_order[i] = (uint32_t)i;
+    std::stable_sort(pf_order.begin(), pf_order.end(), [&](uint32_t a, uint32_t b) {
         if (key[a] != key[b]) return key[a] > key[b];
         return grp[a] < grp[b];
     });
-    std::vector<uint32_t> attn;
-    attn.reserve(nk);
-    {
-        // Longest first, except that a prefill item shorter than the median
-        // decode split waits no longer than the first wave (the SMs the appends
-        // leave free): short compute-bound tiles then run beside the
-        // memory-bound decode streams instead of alone at the end.
-        std::vector<double> dec_est;
-        dec_est.reserve(decs.size());
-        for (auto& t : decs) dec_est.push_back(t.ns_est);
-        double median = 0;
-        if (!dec_est.empty()) {
-            std::nth_element(dec_est.begin(), dec_est.begin() + dec_est.size() / 2, dec_est.end());
-            median = dec_est[dec_est.size() / 2];
+    std::stable_sort(dec_order.begin(), dec_order.end(),
+                     [&](uint32_t a, uint32_t b) { return decs[a].ns_est > decs[b].ns_est; });
+    int32_t first_sms = 0;
+    if (!tiles.empty() && decs.empty()) {
+        first_sms = num_sms;
+    } else if (!tiles.empty() && num_sms > 1) {
+        double wp = 0, maxp = 0, dec_bytes = 0;
+        for (auto& t : tiles) {
+            wp += t.ns_est;
+            maxp = std::max(maxp, t.ns_est);
         }
-        const size_t wave = (size_t)std::max<int64_t>(0, (int64_t)num_sms - (int64_t)appends.size());
-        std::vector<char> used(nk, 0);
-        for (size_t i = 0; i < nk; ++i) {
-            if (used[i]) continue;
-            if (attn.size() == wave)
-                for (size_t j = i; j < nk; ++j)
-                    if (grp[order[j]] >= 0 && key[order[j]] < median && !used[j]) {
-                        attn.push_back(order[j]);
-                        used[j] = 1;
-                    }
-            if (used[i]) continue;
-            attn.push_back(order[i]);
-            used[i] = 1;
+        for (auto& t : decs) dec_bytes += t.it[kCount] * kv_page_bytes;
+        // Fluid model of the step with k CTAs on the first queue (more than
+        // n_tiles act as n_tiles: the rest find it empty and move on): the
+        // tiles take wp / k; the decodes stream from the other SMs at
+        // min(SMs x one SM's rate, HBM rate); whichever side ends first hands
+        // its SMs to the other.  The predicted step is flat over a range of k
+        // (the decode streams saturate HBM and the tiles end in time); take
+        // the middle of the range within 0.5% of the minimum, away from both
+        // edges where the model's error costs most.
+        const double r_all = std::min(num_sms * kDecodeAloneBytesPerNs, kHbmBytesPerNs);
+        std::vector<double> pred(num_sms, 0.0);
+        double best = 0;
+        for (int32_t k = 1; k < num_sms; ++k) {
+            const double ke = (double)std::min<size_t>((size_t)k, n_tiles);
+            const double r1 = std::min((num_sms - ke) * kDecodeAloneBytesPerNs, kHbmBytesPerNs);
+            const double tp = wp / ke, td = dec_bytes / r1;
+            double t = tp <= td ? tp + (dec_bytes - tp * r1) / r_all : td + (wp - ke * td) / num_sms;
+            pred[k] = t = std::max(t, maxp);
+            if (k == 1 || t < best) best = t;
         }
+        int32_t lo = 0, hi = 0;
+        for (int32_t k = 1; k < num_sms; ++k)
+            if (pred[k] <= best * 1.005) {
+                if (!lo) lo = k;
+                hi = k;
+            }
+        first_sms = std::min<int32_t>((lo + hi) / 2, (int32_t)n_tiles);
     }
-    const int64_t n_items = (int64_t)appends.size() + (int64_t)attn.size();
+    std::vector<const Timed*> first, second;
+    first.reserve(n_tiles + appends.size());
+    second.reserve(decs.size() + appends.size());
+    std::vector<Timed> app_items;
+    app_items.reserve(appends.size());
+    for (auto& a : appends) app_items.push_back({0.0, a});
+    for (auto& a : app_items) (decs.empty() ? first : second).push_back(&a);
+    for (uint32_t i : pf_order) first.push_back(&tiles[i]);
+    for (uint32_t i : dec_order) second.push_back(&decs[i]);
+    const int64_t n_items = (int64_t)first.size() + (int64_t)second.size();
 
     // ---- 4. packed layout
     int64_t off = 0;
@@ -380,6 +408,8 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     info->n_items = (int32_t)n_items;
     info->n_partials = n_partials;
     info->n_merge = n_merge;
+    info->n_first = (int32_t)first.size();
+    info->first_sms = first.empty() ? 0 : (second.empty() ? num_sms : first_sms);
     info->max_kv_len = max_kv;
     info->pairs = pairs;
     info->history_tokens = history;
@@ -425,8 +455,8 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
             for (int k = 0; k < kItemIds; ++k) it[kIds + k] = k < np[s] ? kvi[kvp[s] + k] : 0;
         }
     };
-    for (auto& it : appends) put(it);
-    for (uint32_t i : attn) put(item_at(i).it);
+    for (const Timed* t : first) put(t->it);
+    for (const Timed* t : second) put(t->it);
     set_error("");
     return (policy->kind == SARATHI_POLICY_STALL_FREE && decodes > token_budget) ? SARATHI_WARN_OVER_BUDGET_DECODES
                                                                                  : SARATHI_OK;

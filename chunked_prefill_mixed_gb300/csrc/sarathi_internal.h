@@ -46,7 +46,8 @@ enum ItemField { kKind = 0, kS, kG, kStart, kCount, kSlot, kMerge, kNSplit, kQo0
                  kIds = 16 };
 
 // Workspace: an int32 header, then fp32 partial slots from byte kPartialOffset.
-//   [0] work-queue head   [1] CTAs exited   [2] error word   [3] error detail
+//   [0] second queue's head   [1] CTAs exited   [2] error word   [3] error detail
+//   [4..11] where a bounded wait ran out   [12] first queue's head
 //   [kHdrInts + s]             append items finished for row s
 //   [kHdrInts + n_sched + m]   arrivals in merge group m
 constexpr int kHdrInts = 16;

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define SARATHI_ABI_VERSION 4
+#define SARATHI_ABI_VERSION 5
 /* int32 words of one kernel work item in the packed plan.  Items are kernel
  * bookkeeping: their layout is private to the library and may change with
  * SARATHI_ABI_VERSION; callers copy the packed plan as a whole. */
@@ -103,6 +103,9 @@ typedef struct sarathi_plan_info {
     int32_t off_items;          /* [n_items][SARATHI_ITEM_INTS] kernel work list         */
     int32_t packed_ints;        /* int32 elements to copy to the device                  */
     int64_t workspace_bytes;    /* device workspace sarathi_mixed_attn needs             */
+    int32_t n_first;            /* the work list's first n_first items form the first    */
+                                /*   queue (prefill tiles), the rest the second (decodes) */
+    int32_t first_sms;          /* CTAs that take from the first queue before the second */
 } sarathi_plan_info;
 
 /* Upper bounds for the buffers of sarathi_plan on this request set at ANY

@@ -84,16 +84,18 @@ def test_plan_matches_oracle_random_request_sets():
             tables.append(rng.permutation(5000)[:npages].astype(np.int32))
         budget = int(rng.integers(1, 600))
         st_o, mo = oracle.plan(states, prompt, computed, tables, budget, 16)
-        st_p, info, mp = _product_plan(states, prompt, computed, tables, budget, shape,
-                                       num_sms=int(rng.integers(1, 200)))
+        nsm = int(rng.integers(1, 200))
+        st_p, info, mp = _product_plan(states, prompt, computed, tables, budget, shape, num_sms=nsm)
         _compare(st_o, mo, st_p, mp)
-        _check_work_list(info, mp, shape)
+        _check_work_list(info, mp, shape, nsm)
 
 
-def _check_work_list(info, m, shape):
+def _check_work_list(info, m, shape, num_sms=148):
     """Every (row, q head) is produced once; every new token's K/V is appended
-    once per kv head; decode splits tile each decode's pages; appends come
-    before the tiles that wait on them."""
+    once per kv head; decode splits tile each decode's pages; the first queue
+    holds the prefill tiles and the second the decode splits; the appends lead
+    the second queue (the first when there are no decodes), so a CTA that waits
+    on one never holds up the CTAs that take them."""
     G = shape.H_q // shape.H_kv
     n = m["n_sched"]
     qo, kvp = m["qo_indptr"], m["kv_page_indptr"]
@@ -101,10 +103,23 @@ def _check_work_list(info, m, shape):
     T = int(qo[-1]) if n else 0
     covered = np.zeros((T, shape.H_q), np.int32)
     appended = np.zeros((T, shape.H_kv), np.int32)
-    first_prefill = None
     seen_slots = set()
     pages_cov = {}
     kvi, last = m["kv_page_indices"], m["kv_last_page_len"]
+    kinds = items[:, 0] if len(items) else np.zeros(0, np.int32)
+    nf = info.n_first
+    assert 0 <= nf <= info.n_items == len(items)
+    has_dec = bool((kinds == 2).any())
+    assert not (kinds[:nf] == 2).any() and not (kinds[nf:] == 1).any()
+    app_q = kinds[nf:] if has_dec else kinds[:nf]
+    n_app = int((kinds == 0).sum())
+    assert (app_q[:n_app] == 0).all() and not (app_q[n_app:] == 0).any()
+    if nf == 0:
+        assert info.first_sms == 0
+    elif nf == info.n_items:
+        assert info.first_sms == num_sms
+    else:
+        assert 0 <= info.first_sms < num_sms
     for idx, it in enumerate(items):
         kind, s, g, start, count, slot, merge, nsplit = (int(x) for x in it[:8])
         nn = qo[s + 1] - qo[s]
@@ -122,11 +137,9 @@ def _check_work_list(info, m, shape):
             k = min(8, count)
             assert list(ids[:k]) == list(kvi[kvp[s] + start:kvp[s] + start + k]) and not ids[k:].any()
         if kind == 0:
-            assert first_prefill is None, "append after a prefill tile"
             assert nn >= 2
             appended[qo[s] + start: qo[s] + start + count, :] += 1
         elif kind == 1:
-            first_prefill = idx if first_prefill is None else first_prefill
             # up to two Q tiles of 128 // G tokens, starting on an item boundary
             tpi = 2 * (128 // G)
             assert 0 < count <= tpi and start % tpi == 0 and start + count <= nn
@@ -229,10 +242,11 @@ def test_plan_policies_match_oracle_random_request_sets():
         reqs, keep = S.make_requests(states, prompt, computed, tables)
         pol = S.PlanPolicy(kind, budget, max_batch, align)
         hb, wb = S.sarathi_plan_bounds(reqs, len(states), budget, shp, 148)
-        st_p, info, packed = S.sarathi_plan_ex(reqs, len(states), pol, shp, int(rng.integers(1, 200)))
+        nsm = int(rng.integers(1, 200))
+        st_p, info, packed = S.sarathi_plan_ex(reqs, len(states), pol, shp, nsm)
         mp = S.plan_arrays(info, packed)
         _compare(st_o, mo, st_p, mp)
-        _check_work_list(info, mp, shape)
+        _check_work_list(info, mp, shape, nsm)
         assert info.packed_ints * 4 <= hb
 
 
