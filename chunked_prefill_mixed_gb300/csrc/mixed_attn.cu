@@ -4,8 +4,10 @@
 // prefill with stall-free batching produces ("Sarathi-Serve 完全拆解", §"混合批不是
 // 把两类注意力强行做成同一个形状": one ragged batch, attention split back per
 // request through qo_indptr / kv_page_indptr / kv_page_indices /
-// kv_last_page_len).  CTAs pull work items from the planner's list through an
-// atomic head counter, longest items first:
+// kv_last_page_len).  CTAs pull work items from the planner's two queues
+// (prefill tiles; decode splits) through an atomic head counter each, longest
+// items first; CTAs below first_sms start on the first queue, the others on
+// the second, and each moves to the other queue once its own is empty:
 //
 //   APPEND   new prefill tokens: K rotated at its ABSOLUTE position in fp64 and
 //            rounded once to bf16, V copied, both into the page that holds the
@@ -23,8 +25,9 @@
 //            owns the last page also appends the decode token's K/V.
 //
 // No CTA waits on a CTA that took a later item, and the only cross-CTA wait
-// (PREFILL on its request's APPENDs, which precede it in the list) is bounded
-// by a timer; a wait that runs out sets an error word in the workspace.
+// (PREFILL on its request's APPENDs, which lead the second queue, or the first
+// when there are no decodes, and which some CTA starts on at launch) is
+// bounded by a timer; a wait that runs out sets an error word in the workspace.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
