@@ -141,6 +141,28 @@ extern "C" int32_t sarathi_plan(const sarathi_request* reqs, int32_t n_reqs, int
     return sarathi_plan_ex(reqs, n_reqs, &policy, shape, num_sms, host_buf, host_buf_bytes, info);
 }
 
+namespace {
+// The head of a work item (fields kKind..kNSplit); the rest is filled when the
+// item is written into the packed plan.
+using ItemHead = std::array<int32_t, 8>;
+struct Timed {
+    double ns_est;
+    ItemHead it;
+};
+// Per-thread buffers reused across calls: a step's plan allocates nothing once
+// the buffers have grown to its size.
+struct PlanScratch {
+    std::vector<Sched> sched;
+    std::vector<int32_t> np, hist, aux;
+    std::vector<ItemHead> appends;
+    std::vector<Timed> tiles, decs;
+    std::vector<double> key, pred;
+    std::vector<int64_t> grp;
+    std::vector<uint32_t> pf_order, dec_order, bucket;
+};
+thread_local PlanScratch t_scratch;
+}  // namespace
+
 extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, const sarathi_plan_policy* policy,
                                    const sarathi_shape* shape, int32_t num_sms,
                                    int32_t* host_buf, size_t host_buf_bytes, sarathi_plan_info* info) {
@@ -164,9 +186,10 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     const int group = shape->num_heads_q / Hkv;
     const int d = shape->head_dim;
 
+    PlanScratch& sc = t_scratch;
     // ---- 1. the batch
-    std::vector<Sched> sched;
-    sched.reserve(n_reqs);
+    std::vector<Sched>& sched = sc.sched;
+    sched.clear();
     int32_t decodes = 0;
     const int32_t align = policy->chunk_align;
     if (policy->kind == SARATHI_POLICY_STALL_FREE) {
@@ -215,7 +238,10 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     const int32_t ns = (int32_t)sched.size();
 
     // ---- 2. per-row KV extent, checked against the block tables
-    std::vector<int32_t> np(ns), hist(ns);
+    std::vector<int32_t>& np = sc.np;
+    std::vector<int32_t>& hist = sc.hist;
+    np.assign(ns, 0);
+    hist.assign(ns, 0);
     int64_t nnz = 0, T = 0, pairs = 0, history = 0;
     int32_t max_kv = 0;
     for (int32_t s = 0; s < ns; ++s) {
@@ -239,18 +265,16 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     }
 
     // ---- 3. work list
-    std::vector<int32_t> aux(ns, 0);
-    std::vector<std::array<int32_t, kItemInts>> appends;
-    struct Timed {
-        double ns_est;
-        std::array<int32_t, kItemInts> it;
-    };
-    std::vector<Timed> tiles, decs;
+    std::vector<int32_t>& aux = sc.aux;
+    aux.assign(ns, 0);
+    std::vector<ItemHead>& appends = sc.appends;
+    std::vector<Timed>& tiles = sc.tiles;
+    std::vector<Timed>& decs = sc.decs;
+    appends.clear();
+    tiles.clear();
+    decs.clear();
     const int tpt = tokens_per_tile(group);
     const int tpi = tokens_per_item(group);
-    tiles.reserve((size_t)(T / std::max(tpi, 1) + ns) * Hkv);
-    decs.reserve((size_t)ns * Hkv + (size_t)num_sms * kDecodeItemsPerSm);
-    appends.reserve((size_t)(T / kAppendTokens + ns));
     // decode split size from the total decode pages and the SM count
     int64_t dec_page_heads = 0;
     for (int32_t s = 0; s < ns; ++s)
@@ -314,8 +338,10 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     // and the tiles that wait for them are not held up), or the first when
     // there are no decodes.  (The sorts move 4-byte indices, not the items.)
     const size_t n_tiles = tiles.size();
-    std::vector<double> key(n_tiles);
-    std::vector<int64_t> grp(n_tiles);
+    std::vector<double>& key = sc.key;
+    std::vector<int64_t>& grp = sc.grp;
+    key.resize(n_tiles);
+    grp.resize(n_tiles);
     for (size_t i = 0; i < n_tiles;) {
         size_t e = i;
         const int32_t s0 = tiles[i].it[kS], g0 = tiles[i].it[kG];
@@ -326,15 +352,26 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
             grp[i] = (int64_t)s0 * Hkv + g0;
         }
     }
-    std::vector<uint32_t> pf_order(n_tiles), dec_order(decs.size());
+    std::vector<uint32_t>& pf_order = sc.pf_order;
+    std::vector<uint32_t>& dec_order = sc.dec_order;
+    pf_order.resize(n_tiles);
+    dec_order.resize(decs.size());
     for (size_t i = 0; i < n_tiles; ++i) pf_order[i] = (uint32_t)i;
-    for (size_t i = 0; i < decs.size(); ++i) dec_order[i] = (uint32_t)i;
     std::stable_sort(pf_order.begin(), pf_order.end(), [&](uint32_t a, uint32_t b) {
         if (key[a] != key[b]) return key[a] > key[b];
         return grp[a] < grp[b];
     });
-    std::stable_sort(dec_order.begin(), dec_order.end(),
-                     [&](uint32_t a, uint32_t b) { return decs[a].ns_est > decs[b].ns_est; });
+    {
+        // a decode split's estimate grows with its page count: a stable
+        // counting sort on the count, largest first
+        int32_t max_pc = 0;
+        for (auto& t : decs) max_pc = std::max(max_pc, t.it[kCount]);
+        std::vector<uint32_t>& bucket = sc.bucket;
+        bucket.assign((size_t)max_pc + 2, 0);
+        for (auto& t : decs) ++bucket[(size_t)(max_pc - t.it[kCount]) + 1];
+        for (size_t c = 1; c < bucket.size(); ++c) bucket[c] += bucket[c - 1];
+        for (size_t i = 0; i < decs.size(); ++i) dec_order[bucket[(size_t)(max_pc - decs[i].it[kCount])]++] = (uint32_t)i;
+    }
     int32_t first_sms = 0;
     if (!tiles.empty() && decs.empty()) {
         first_sms = num_sms;
@@ -354,7 +391,8 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
         // the middle of the range within 0.5% of the minimum, away from both
         // edges where the model's error costs most.
         const double r_all = std::min(num_sms * kDecodeAloneBytesPerNs, kHbmBytesPerNs);
-        std::vector<double> pred(num_sms, 0.0);
+        std::vector<double>& pred = sc.pred;
+        pred.assign(num_sms, 0.0);
         double best = 0;
         for (int32_t k = 1; k < num_sms; ++k) {
             const double ke = (double)std::min<size_t>((size_t)k, n_tiles);
@@ -372,16 +410,9 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
             }
         first_sms = std::min<int32_t>((lo + hi) / 2, (int32_t)n_tiles);
     }
-    std::vector<const Timed*> first, second;
-    first.reserve(n_tiles + appends.size());
-    second.reserve(decs.size() + appends.size());
-    std::vector<Timed> app_items;
-    app_items.reserve(appends.size());
-    for (auto& a : appends) app_items.push_back({0.0, a});
-    for (auto& a : app_items) (decs.empty() ? first : second).push_back(&a);
-    for (uint32_t i : pf_order) first.push_back(&tiles[i]);
-    for (uint32_t i : dec_order) second.push_back(&decs[i]);
-    const int64_t n_items = (int64_t)first.size() + (int64_t)second.size();
+    const bool apps_first = decs.empty();
+    const int64_t n_first = (int64_t)n_tiles + (apps_first ? (int64_t)appends.size() : 0);
+    const int64_t n_items = (int64_t)n_tiles + (int64_t)appends.size() + (int64_t)decs.size();
 
     // ---- 4. packed layout
     int64_t off = 0;
@@ -408,8 +439,8 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     info->n_items = (int32_t)n_items;
     info->n_partials = n_partials;
     info->n_merge = n_merge;
-    info->n_first = (int32_t)first.size();
-    info->first_sms = first.empty() ? 0 : (second.empty() ? num_sms : first_sms);
+    info->n_first = (int32_t)n_first;
+    info->first_sms = n_first == 0 ? 0 : (n_first == n_items ? num_sms : first_sms);
     info->max_kv_len = max_kv;
     info->pairs = pairs;
     info->history_tokens = history;
@@ -419,7 +450,8 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
         return fail(SARATHI_ERR_CAPACITY, "host_buf too small (info->packed_ints holds the size needed)");
 
     int32_t* b = host_buf;
-    std::memset(b, 0, (size_t)off * 4);
+    // every int is written below but the padding before the items
+    std::memset(b + info->off_req_aux + ns, 0, (size_t)(info->off_items - info->off_req_aux - ns) * 4);
     int32_t* qo = b + info->off_qo_indptr;
     int32_t* kvp = b + info->off_kv_page_indptr;
     int32_t* kvi = b + info->off_kv_page_indices;
@@ -439,24 +471,32 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     }
     int32_t* items = b + info->off_items;
     int64_t w = 0;
-    auto put = [&](const std::array<int32_t, kItemInts>& src) {
+    auto put = [&](const ItemHead& src) {
         int32_t* it = items + kItemInts * w++;
-        std::memcpy(it, src.data(), sizeof(int32_t) * kItemInts);
+        std::memcpy(it, src.data(), sizeof src);
         const int32_t s = it[kS];
         it[kQo0] = qo[s];
         it[kNNew] = qo[s + 1] - qo[s];
         it[kKvp0] = kvp[s];
         it[kNp] = np[s];
         it[kKvLen] = kPage * (np[s] - 1) + b[info->off_kv_last_page_len + s];
+        for (int k = kKvLen + 1; k < kIds; ++k) it[k] = 0;
+        int32_t* ids = it + kIds;
         if (it[kKind] == kDecode) {
-            for (int k = 0; k < kItemIds; ++k)
-                it[kIds + k] = k < it[kCount] ? kvi[kvp[s] + it[kStart] + k] : 0;
+            for (int k = 0; k < kItemIds; ++k) ids[k] = k < it[kCount] ? kvi[kvp[s] + it[kStart] + k] : 0;
         } else if (it[kKind] == kPrefill) {
-            for (int k = 0; k < kItemIds; ++k) it[kIds + k] = k < np[s] ? kvi[kvp[s] + k] : 0;
+            for (int k = 0; k < kItemIds; ++k) ids[k] = k < np[s] ? kvi[kvp[s] + k] : 0;
+        } else {
+            for (int k = 0; k < kItemIds; ++k) ids[k] = 0;
         }
     };
-    for (const Timed* t : first) put(t->it);
-    for (const Timed* t : second) put(t->it);
+    // the first queue, then the second
+    if (apps_first)
+        for (auto& a : appends) put(a);
+    for (uint32_t i : pf_order) put(tiles[i].it);
+    if (!apps_first)
+        for (auto& a : appends) put(a);
+    for (uint32_t i : dec_order) put(decs[i].it);
     set_error("");
     return (policy->kind == SARATHI_POLICY_STALL_FREE && decodes > token_budget) ? SARATHI_WARN_OVER_BUDGET_DECODES
                                                                                  : SARATHI_OK;

@@ -27,28 +27,36 @@ class StepRunner:
         sarathi_rope_table(self.rope, self.max_pos, d, rope_theta, self.stream)
         self.workspace = torch.zeros(1 << 16, dtype=torch.uint8, device=self.device)
         # the packed plan is written straight into pinned memory, so that its
-        # copy to the device is one asynchronous DMA from there
-        self._host_t = torch.empty(0, dtype=torch.int32)
-        self._host_buf = self._host_t.numpy()
+        # copy to the device is one asynchronous DMA from there; two buffers
+        # in turn, so that the next step can be planned while the copy out of
+        # the last one (and the step after it) is still queued
+        self._host_ts = [torch.empty(0, dtype=torch.int32), torch.empty(0, dtype=torch.int32)]
+        self._cur = 0
         self._plan_dev = torch.empty(0, dtype=torch.int32, device=self.device)
-        self._upload_evt = torch.cuda.Event()
-        self._uploaded = False  # a copy out of the host buffer may be in flight (_upload_evt)
+        self._upload_evts = [torch.cuda.Event(), torch.cuda.Event()]
+        self._uploaded = [False, False]  # a copy out of buffer i may be in flight (_upload_evts[i])
 
     def plan(self, states, prompt_len, num_computed, block_tables, budget: int, policy: PlanPolicy | None = None):
-        """Plans into a host buffer the runner keeps (grown when a batch needs
-        more); the returned packed array is a view of it, valid until the
-        next call.  policy: a PlanPolicy for sarathi_plan_ex (its token_budget
-        is used); None plans with sarathi_plan and `budget`."""
+        """Plans into one of two pinned host buffers the runner keeps (taken in
+        turn, grown when a batch needs more); the returned packed array is a
+        view of it, valid until the next call.  The buffer's previous copy to
+        the device (two plans ago) is waited for, not the last one, so a step
+        can be planned while the one before it runs.  policy: a PlanPolicy
+        for sarathi_plan_ex (its token_budget is used); None plans with
+        sarathi_plan and `budget`."""
         reqs, keep = make_requests(states, prompt_len, num_computed, block_tables)
         tb = policy.token_budget if policy is not None else budget
-        if self._uploaded:
-            self._upload_evt.synchronize()  # the previous plan's copy has left the buffer
-            self._uploaded = False
+        self._cur ^= 1
+        c = self._cur
+        if self._uploaded[c]:
+            self._upload_evts[c].synchronize()  # that plan's copy has left the buffer
+            self._uploaded[c] = False
+        host_buf = self._host_ts[c].numpy()
         for attempt in range(2):
             try:
                 if policy is not None:
-                    return sarathi_plan_ex(reqs, len(states), policy, self.shape, self.num_sms, self._host_buf)
-                return sarathi_plan(reqs, len(states), budget, self.shape, self.num_sms, self._host_buf)
+                    return sarathi_plan_ex(reqs, len(states), policy, self.shape, self.num_sms, host_buf)
+                return sarathi_plan(reqs, len(states), budget, self.shape, self.num_sms, host_buf)
             except SarathiError as e:
                 if e.status != ERR_CAPACITY or attempt:
                     raise
@@ -56,11 +64,11 @@ class StepRunner:
                 # buffer by the bounds and plan again (the bounds call fails
                 # the same way in the second case)
                 hb, _ = sarathi_plan_bounds(reqs, len(states), tb, self.shape, self.num_sms)
-                if self._host_buf.nbytes >= hb:
+                if host_buf.nbytes >= hb:
                     raise
-                self._host_t = torch.empty(max(hb // 4 + 4, 2 * self._host_buf.size), dtype=torch.int32,
-                                           pin_memory=True)
-                self._host_buf = self._host_t.numpy()
+                self._host_ts[c] = torch.empty(max(hb // 4 + 4, 2 * host_buf.size), dtype=torch.int32,
+                                               pin_memory=True)
+                host_buf = self._host_ts[c].numpy()
 
     def upload_plan(self, info: PlanInfo) -> torch.Tensor:
         """Enqueues on the runner's stream the copy of the packed plan of the
@@ -72,13 +80,14 @@ class StepRunner:
             self._plan_dev = torch.empty(max(n + 4, 2 * self._plan_dev.numel()), dtype=torch.int32,
                                          device=self.device)
         # (the buffer is pinned once plan() has sized it)
+        c = self._cur
         if torch.cuda.current_stream(self.device) == self.stream:
-            self._plan_dev[:n].copy_(self._host_t[:n], non_blocking=True)
+            self._plan_dev[:n].copy_(self._host_ts[c][:n], non_blocking=True)
         else:
             with torch.cuda.stream(self.stream):
-                self._plan_dev[:n].copy_(self._host_t[:n], non_blocking=True)
-        self._upload_evt.record(self.stream)
-        self._uploaded = True
+                self._plan_dev[:n].copy_(self._host_ts[c][:n], non_blocking=True)
+        self._upload_evts[c].record(self.stream)
+        self._uploaded[c] = True
         return self._plan_dev
 
     def ensure_workspace(self, nbytes: int):
@@ -111,9 +120,10 @@ class StepRunner:
             self.stream.synchronize()  # the old buffer may be in use by an enqueued step
             self._plan_dev = torch.empty(max(n + 4, 2 * self._plan_dev.numel()), dtype=torch.int32,
                                          device=self.device)
-        self.run(q, k, v, k_cache, v_cache, out, self._plan_dev, info, plan_host=self._host_t)
-        self._upload_evt.record(self.stream)
-        self._uploaded = True
+        c = self._cur
+        self.run(q, k, v, k_cache, v_cache, out, self._plan_dev, info, plan_host=self._host_ts[c])
+        self._upload_evts[c].record(self.stream)
+        self._uploaded[c] = True
 
     def status(self) -> int:
         return sarathi_workspace_status(self.workspace, self.stream)
