@@ -349,18 +349,21 @@ def run_ours(args, rank, world, local_rank):
         e2e_times.append(time.perf_counter() - t0)
     barrier()
 
-    # e2e pipelined as a serving loop drives it: step i + 1's input copy (copy
-    # stream) and plan (host) overlap step i's kernel, and step i's output
-    # copy (second copy stream) overlaps step i + 1; two device input and
-    # output buffers and two pinned output buffers in turn.  The host reads
-    # each step's result from its pinned buffer before that buffer is reused.
-    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    qkv_ds = [qkv_d, torch.empty_like(qkv_d)]
-    outs = [out, torch.empty_like(out)]
+    # e2e pipelined as a serving loop drives it, through the host-buffer entry
+    # (sarathi_mixed_attn_host: q, k, v in, the plan in, the kernel, out back,
+    # all enqueued by one library call): two streams in turn, each with its
+    # own device buffers and pinned output, each step waiting for the one
+    # before it; step i + 1's copies and host planning overlap step i's
+    # kernel.  The host reads each step's result from its pinned buffer
+    # before that buffer is reused.
+    streams = [stream, torch.cuda.Stream(dev)]
+    dbufs = [(q_d, k_d, v_d, out)] + [tuple(torch.empty_like(x) for x in (q_d, k_d, v_d, out))]
     out_hs = [out_h, torch.empty(out_h.shape, dtype=out_h.dtype, pin_memory=True)]
-    ev = lambda: torch.cuda.Event()
-    in_ready, k_done, o_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-    views = [(qd[:nq].view(q.shape), qd[nq:nq + nk].view(k.shape), qd[nq + nk:].view(v.shape)) for qd in qkv_ds]
+    k_done = [torch.cuda.Event(), torch.cuda.Event()]
+    # the request table, kept across steps as a serving loop keeps it (there
+    # it is advanced in place by sarathi_advance; this loop repeats one step)
+    reqs_t, keep_t = S.make_requests(*wl.arrays())
+    n_reqs = len(wl.requests)
     checks = []
     n_pipe = max(args.steps, 8)
     with torch.cuda.stream(stream):
@@ -370,24 +373,13 @@ def run_ours(args, rank, world, local_rank):
     for i in range(n_pipe):
         b = i & 1
         if i >= 2:
-            o_done[b].synchronize()  # step i - 2's result is on the host
+            streams[b].synchronize()  # step i - 2's result is on the host
             checks.append(float(out_hs[b].view(-1)[0]))
-        with torch.cuda.stream(h2d_s):
-            if i >= 2:
-                h2d_s.wait_event(k_done[b])  # step i - 2's kernel has read this input buffer
-            qkv_ds[b].copy_(qkv_h, non_blocking=True)
-            in_ready[b].record(h2d_s)
-        st2, info2, packed2 = runner.plan(*wl.arrays(), wl.budget)
-        with torch.cuda.stream(stream):
-            stream.wait_event(in_ready[b])
-            runner.run_planned(*views[b], kc, vc, outs[b], info2)
-            k_done[b].record(stream)
-        with torch.cuda.stream(d2h_s):
-            d2h_s.wait_event(k_done[b])
-            out_hs[b].copy_(outs[b], non_blocking=True)
-            o_done[b].record(d2h_s)
+        st2, info2, packed2 = runner.plan_requests(reqs_t, n_reqs, wl.budget)
+        runner.run_host(q_h, k_h, v_h, out_hs[b], *dbufs[b][:3], kc, vc, dbufs[b][3], info2, stream=streams[b],
+                        wait_event=k_done[b ^ 1] if i else None, done_event=k_done[b])
     for b in range(2):
-        o_done[b].synchronize()
+        streams[b].synchronize()
         checks.append(float(out_hs[b].view(-1)[0]))
     t_pipe = (time.perf_counter() - t0) / n_pipe
     torch.cuda.synchronize(dev)
@@ -422,10 +414,11 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": int(d2h), "us_per_step": e2e_s * 1e6, "steps": n_pipe,
                 "l2": f"not flushed between pipelined steps: a step reads {alg['bytes'] / 1e6:.0f} MB "
                       "(the L2 holds 129 MB)",
-                "includes": "per step: host request records and plan (StepRunner.plan), pinned H2D of q, k, v "
-                            "(one copy), pinned H2D of the plan and the kernel (one library call), D2H of out "
-                            "into pinned memory and a host read of it; pipelined: step i+1's input copy and "
-                            "plan overlap step i's kernel",
+                "includes": "per step: the host plan (StepRunner.plan_requests on the kept request table), "
+                            "then one library call "
+                            "(sarathi_mixed_attn_host) enqueuing pinned H2D of q, k, v and the plan, the kernel "
+                            "and D2H of out into pinned memory, and a host read of the result; two streams in "
+                            "turn, so step i+1's copies and plan overlap step i's kernel",
                 "serial": {"value": job_tokens_per_s(T, world, e2e_serial_s), "us_per_step": e2e_serial_s * 1e6,
                            "includes": "the same, one step at a time (synchronised after each step)"}},
         "clocks": clk.summary(),

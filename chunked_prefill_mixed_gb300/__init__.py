@@ -20,13 +20,13 @@ _lib = None
 OK, ERR_INVALID_ARG, ERR_CAPACITY, WARN_OVER_BUDGET_DECODES = 0, 1, 2, 3
 ERR_CUDA, ERR_UNSUPPORTED, ERR_DEVICE_CHECK = 4, 5, 6
 DECODE, PREFILL_RUNNING, PREFILL_WAITING = 0, 1, 2
-ABI_VERSION = 5   # SARATHI_ABI_VERSION of include/sarathi.h
+ABI_VERSION = 6   # SARATHI_ABI_VERSION of include/sarathi.h
 ROPE_ROTATE_HALF, ROPE_INTERLEAVED = 0, 1
 ITEM_INTS = 24    # SARATHI_ITEM_INTS
 
 EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_plan_ex", "sarathi_advance", "sarathi_split_metadata",
             "sarathi_rope_table", "sarathi_qkv_proj",
-            "sarathi_mixed_attn",
+            "sarathi_mixed_attn", "sarathi_mixed_attn_host",
             "sarathi_mixed_attn_noalloc", "sarathi_workspace_status", "sarathi_last_error", "sarathi_abi_version")
 
 
@@ -89,6 +89,11 @@ class AttnArgs(ctypes.Structure):
                 ("plan_host", ctypes.c_void_p)]
 
 
+class HostIO(ctypes.Structure):
+    _fields_ = [("q_host", ctypes.c_void_p), ("k_host", ctypes.c_void_p), ("v_host", ctypes.c_void_p),
+                ("out_host", ctypes.c_void_p), ("wait_event", ctypes.c_void_p), ("done_event", ctypes.c_void_p)]
+
+
 def lib_path() -> str:
     return _build.LIB
 
@@ -127,6 +132,8 @@ def load(build_if_missing: bool = True):
                                        ctypes.c_void_p]
     lib.sarathi_mixed_attn.restype = ctypes.c_int32
     lib.sarathi_mixed_attn.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p]
+    lib.sarathi_mixed_attn_host.restype = ctypes.c_int32
+    lib.sarathi_mixed_attn_host.argtypes = [ctypes.POINTER(AttnArgs), ctypes.POINTER(HostIO), ctypes.c_void_p]
     lib.sarathi_mixed_attn_noalloc.restype = ctypes.c_int32
     lib.sarathi_mixed_attn_noalloc.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p]
     lib.sarathi_workspace_status.restype = ctypes.c_int32
@@ -273,12 +280,8 @@ def sarathi_rope_table(table, max_pos: int, head_dim: int, rope_theta: float, st
            "sarathi_rope_table")
 
 
-def sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo, rope_table, rope_max_pos: int,
-                       workspace, shape: Shape, sm_scale: float, stream=None, rope_style: int = ROPE_ROTATE_HALF,
-                       plan_host=None) -> None:
-    """Enqueue one step (one kernel) on ``stream`` (torch.cuda.Stream or raw handle).
-    plan_host: optional host tensor or array holding the packed plan; the call
-    then copies it into plan_dev first (same stream)."""
+def _attn_args(q, k, v, k_cache, v_cache, out, plan_dev, info, rope_table, rope_max_pos, workspace, shape,
+               sm_scale, rope_style, plan_host) -> AttnArgs:
     a = AttnArgs()
     if plan_host is not None:
         a.plan_host = plan_host.data_ptr() if hasattr(plan_host, "data_ptr") else plan_host.ctypes.data
@@ -294,7 +297,46 @@ def sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo,
     a.shape = shape
     a.sm_scale = float(sm_scale)
     a.rope_style = int(rope_style)
+    return a
+
+
+def sarathi_mixed_attn(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo, rope_table, rope_max_pos: int,
+                       workspace, shape: Shape, sm_scale: float, stream=None, rope_style: int = ROPE_ROTATE_HALF,
+                       plan_host=None) -> None:
+    """Enqueue one step (one kernel) on ``stream`` (torch.cuda.Stream or raw handle).
+    plan_host: optional host tensor or array holding the packed plan; the call
+    then copies it into plan_dev first (same stream)."""
+    a = _attn_args(q, k, v, k_cache, v_cache, out, plan_dev, info, rope_table, rope_max_pos, workspace, shape,
+                   sm_scale, rope_style, plan_host)
     _check(load().sarathi_mixed_attn(ctypes.byref(a), _stream_ptr(stream)), "sarathi_mixed_attn")
+
+
+def _event_ptr(ev, stream) -> int:
+    """Raw cudaEvent_t of a torch.cuda.Event (created by recording it once on
+    ``stream`` if torch has not created it yet), of a raw handle, or 0."""
+    if ev is None:
+        return 0
+    if hasattr(ev, "cuda_event"):
+        if not ev.cuda_event:
+            ev.record(stream)
+        return int(ev.cuda_event)
+    return int(ev)
+
+
+def sarathi_mixed_attn_host(q_host, k_host, v_host, out_host, q, k, v, k_cache, v_cache, out, plan_dev,
+                            info: PlanInfo, rope_table, rope_max_pos: int, workspace, shape: Shape,
+                            sm_scale: float, stream=None, rope_style: int = ROPE_ROTATE_HALF, plan_host=None,
+                            wait_event=None, done_event=None) -> None:
+    """The step end to end from host buffers on ``stream``: q_host, k_host,
+    v_host (pinned host tensors) copied into the device q, k, v; the plan from
+    plan_host into plan_dev; a wait for ``wait_event``; the kernel;
+    ``done_event`` recorded; out copied into out_host (pinned)."""
+    a = _attn_args(q, k, v, k_cache, v_cache, out, plan_dev, info, rope_table, rope_max_pos, workspace, shape,
+                   sm_scale, rope_style, plan_host)
+    io = HostIO(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), out_host.data_ptr(),
+                _event_ptr(wait_event, stream), _event_ptr(done_event, stream))
+    _check(load().sarathi_mixed_attn_host(ctypes.byref(a), ctypes.byref(io), _stream_ptr(stream)),
+           "sarathi_mixed_attn_host")
 
 
 def sarathi_mixed_attn_noalloc(q, k, v, k_cache, v_cache, out, plan_dev, info: PlanInfo, rope_table,

@@ -1556,13 +1556,41 @@ extern "C" int32_t sarathi_rope_table(double* table, int32_t max_pos, int32_t he
     return SARATHI_OK;
 }
 
+namespace {
+int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void* cuda_stream);
+}
+
 extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_stream) {
+    return launch_step(a, nullptr, cuda_stream);
+}
+
+extern "C" int32_t sarathi_mixed_attn_host(const sarathi_attn_args* a, const sarathi_host_io* io,
+                                           void* cuda_stream) {
+    if (!io) return fail(SARATHI_ERR_INVALID_ARG, "io is NULL");
+    if (!io->q_host || !io->k_host || !io->v_host || !io->out_host)
+        return fail(SARATHI_ERR_INVALID_ARG, "NULL host pointer");
+    return launch_step(a, io, cuda_stream);
+}
+
+namespace {
+int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void* cuda_stream) {
     if (!a) return fail(SARATHI_ERR_INVALID_ARG, "args is NULL");
     int32_t st = check_shape(&a->shape);
     if (st) return st;
     const sarathi_plan_info* in = a->info;
     if (!in) return fail(SARATHI_ERR_INVALID_ARG, "info is NULL");
-    if (in->n_items == 0) return SARATHI_OK;
+    if (in->n_items == 0) {
+        // an empty step: nothing to copy or run; its done event still follows the step before
+        if (io && io->wait_event) {
+            cudaError_t e = cudaStreamWaitEvent((cudaStream_t)cuda_stream, (cudaEvent_t)io->wait_event, 0);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+        }
+        if (io && io->done_event) {
+            cudaError_t e = cudaEventRecord((cudaEvent_t)io->done_event, (cudaStream_t)cuda_stream);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        }
+        return SARATHI_OK;
+    }
     if (!a->q || !a->k || !a->v || !a->k_cache || !a->v_cache || !a->out || !a->plan || !a->rope_table ||
         !a->workspace)
         return fail(SARATHI_ERR_INVALID_ARG, "NULL device pointer");
@@ -1656,11 +1684,26 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
     // APPEND items must be taken while first-queue tiles may wait for them)
     P.first_sms = in->n_first < in->n_items ? std::min(in->first_sms, grid - 1) : grid;
     cudaStream_t stream = (cudaStream_t)cuda_stream;
+    const size_t q_bytes = (size_t)in->num_tokens * a->shape.num_heads_q * d * 2;
+    const size_t kv_bytes = (size_t)in->num_tokens * Hkv * d * 2;
+    if (io) {
+        // this step's new tokens, from the host
+        e = cudaMemcpyAsync(const_cast<void*>(a->q), io->q_host, q_bytes, cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(const_cast<void*>(a->k), io->k_host, kv_bytes, cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(const_cast<void*>(a->v), io->v_host, kv_bytes, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "q, k, v copy to the device");
+    }
     if (a->plan_host) {
         // the caller's host copy of the plan goes to the device first, on the same stream
         e = cudaMemcpyAsync(const_cast<int32_t*>(a->plan), a->plan_host, (size_t)in->packed_ints * 4,
                             cudaMemcpyHostToDevice, stream);
         if (e != cudaSuccess) return cuda_fail(e, "plan copy to the device");
+    }
+    if (io && io->wait_event) {
+        e = cudaStreamWaitEvent(stream, (cudaEvent_t)io->wait_event, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
     }
     const bool il = a->rope_style == SARATHI_ROPE_INTERLEAVED;
     if (d == 128 && !il)
@@ -1673,8 +1716,17 @@ extern "C" int32_t sarathi_mixed_attn(const sarathi_attn_args* a, void* cuda_str
         mixed_step_kernel<64, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "mixed_step_kernel launch");
+    if (io) {
+        if (io->done_event) {
+            e = cudaEventRecord((cudaEvent_t)io->done_event, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+        }
+        e = cudaMemcpyAsync(io->out_host, a->out, q_bytes, cudaMemcpyDeviceToHost, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "out copy to the host");
+    }
     return SARATHI_OK;
 }
+}  // namespace
 
 extern "C" int32_t sarathi_workspace_status(void* workspace, void* cuda_stream, int32_t* device_error) {
     if (!workspace || !device_error) return fail(SARATHI_ERR_INVALID_ARG, "NULL pointer");

@@ -10,6 +10,7 @@ import numpy as np
 import torch
 
 from . import (ERR_CAPACITY, PlanInfo, PlanPolicy, SarathiError, Shape, make_requests, sarathi_mixed_attn,
+               sarathi_mixed_attn_host,
                sarathi_plan, sarathi_plan_bounds, sarathi_plan_ex, sarathi_rope_table, sarathi_workspace_status)
 
 
@@ -32,7 +33,9 @@ class StepRunner:
         # the last one (and the step after it) is still queued
         self._host_ts = [torch.empty(0, dtype=torch.int32), torch.empty(0, dtype=torch.int32)]
         self._cur = 0
-        self._plan_dev = torch.empty(0, dtype=torch.int32, device=self.device)
+        # a device copy of each: a step's plan buffers are free again once the
+        # event recorded after its kernel has passed
+        self._plan_devs = [torch.empty(0, dtype=torch.int32, device=self.device) for _ in range(2)]
         self._upload_evts = [torch.cuda.Event(), torch.cuda.Event()]
         self._uploaded = [False, False]  # a copy out of buffer i may be in flight (_upload_evts[i])
 
@@ -45,6 +48,12 @@ class StepRunner:
         for sarathi_plan_ex (its token_budget is used); None plans with
         sarathi_plan and `budget`."""
         reqs, keep = make_requests(states, prompt_len, num_computed, block_tables)
+        return self.plan_requests(reqs, len(states), budget, policy)
+
+    def plan_requests(self, reqs, n_reqs: int, budget: int, policy: PlanPolicy | None = None):
+        """plan() from a request table the caller keeps (the ctypes array of
+        make_requests, with its block tables alive; a serving loop advances it
+        in place with sarathi_advance between steps)."""
         tb = policy.token_budget if policy is not None else budget
         self._cur ^= 1
         c = self._cur
@@ -55,15 +64,15 @@ class StepRunner:
         for attempt in range(2):
             try:
                 if policy is not None:
-                    return sarathi_plan_ex(reqs, len(states), policy, self.shape, self.num_sms, host_buf)
-                return sarathi_plan(reqs, len(states), budget, self.shape, self.num_sms, host_buf)
+                    return sarathi_plan_ex(reqs, n_reqs, policy, self.shape, self.num_sms, host_buf)
+                return sarathi_plan(reqs, n_reqs, budget, self.shape, self.num_sms, host_buf)
             except SarathiError as e:
                 if e.status != ERR_CAPACITY or attempt:
                     raise
                 # host_buf too small, or a block table too short: size the
                 # buffer by the bounds and plan again (the bounds call fails
                 # the same way in the second case)
-                hb, _ = sarathi_plan_bounds(reqs, len(states), tb, self.shape, self.num_sms)
+                hb, _ = sarathi_plan_bounds(reqs, n_reqs, tb, self.shape, self.num_sms)
                 if host_buf.nbytes >= hb:
                     raise
                 self._host_ts[c] = torch.empty(max(hb // 4 + 4, 2 * host_buf.size), dtype=torch.int32,
@@ -75,27 +84,33 @@ class StepRunner:
         last plan() call (pinned memory) into a device buffer the runner
         keeps; returns that buffer, valid until the next upload_plan."""
         n = int(info.packed_ints)
-        if self._plan_dev.numel() < n + 4:
-            self.stream.synchronize()  # the old buffer may be in use by an enqueued step
-            self._plan_dev = torch.empty(max(n + 4, 2 * self._plan_dev.numel()), dtype=torch.int32,
-                                         device=self.device)
-        # (the buffer is pinned once plan() has sized it)
         c = self._cur
+        dev = self._plan_device_buffer(n)
+        # (the buffer is pinned once plan() has sized it)
         if torch.cuda.current_stream(self.device) == self.stream:
-            self._plan_dev[:n].copy_(self._host_ts[c][:n], non_blocking=True)
+            dev[:n].copy_(self._host_ts[c][:n], non_blocking=True)
         else:
             with torch.cuda.stream(self.stream):
-                self._plan_dev[:n].copy_(self._host_ts[c][:n], non_blocking=True)
+                dev[:n].copy_(self._host_ts[c][:n], non_blocking=True)
         self._upload_evts[c].record(self.stream)
         self._uploaded[c] = True
-        return self._plan_dev
+        return dev
+
+    def _plan_device_buffer(self, n: int) -> torch.Tensor:
+        c = self._cur
+        if self._plan_devs[c].numel() < n + 4:
+            torch.cuda.synchronize(self.device)  # the old buffer may be in use by an enqueued step
+            self._plan_devs[c] = torch.empty(max(n + 4, 2 * self._plan_devs[c].numel()), dtype=torch.int32,
+                                             device=self.device)
+        return self._plan_devs[c]
 
     def ensure_workspace(self, nbytes: int):
         if self.workspace.numel() < nbytes:
-            torch.cuda.current_stream(self.device).wait_stream(self.stream)
+            # rare: wait for every stream that may run a step on the old one
+            torch.cuda.synchronize(self.device)
             self.workspace = torch.zeros(max(nbytes, 2 * self.workspace.numel()), dtype=torch.uint8,
                                          device=self.device)
-            self.stream.wait_stream(torch.cuda.current_stream(self.device))
+            torch.cuda.synchronize(self.device)
 
     def upload(self, packed: np.ndarray) -> torch.Tensor:
         src = torch.from_numpy(np.ascontiguousarray(packed))
@@ -115,14 +130,33 @@ class StepRunner:
         """Enqueues the step planned by the last plan() call: one library call
         copies the packed plan from the runner's pinned buffer into its device
         buffer and launches the kernel."""
-        n = int(info.packed_ints)
-        if self._plan_dev.numel() < n + 4:
-            self.stream.synchronize()  # the old buffer may be in use by an enqueued step
-            self._plan_dev = torch.empty(max(n + 4, 2 * self._plan_dev.numel()), dtype=torch.int32,
-                                         device=self.device)
         c = self._cur
-        self.run(q, k, v, k_cache, v_cache, out, self._plan_dev, info, plan_host=self._host_ts[c])
+        dev = self._plan_device_buffer(int(info.packed_ints))
+        self.run(q, k, v, k_cache, v_cache, out, dev, info, plan_host=self._host_ts[c])
         self._upload_evts[c].record(self.stream)
+        self._uploaded[c] = True
+
+    def run_host(self, q_host, k_host, v_host, out_host, q, k, v, k_cache, v_cache, out, info: PlanInfo,
+                 stream=None, wait_event=None, done_event=None) -> None:
+        """Enqueues the step planned by the last plan() call end to end from
+        host buffers (one library call, sarathi_mixed_attn_host) on ``stream``
+        (default: the runner's): q_host, k_host, v_host (pinned) into the
+        device q, k, v, the plan into the runner's device buffer, a wait for
+        ``wait_event``, the kernel, ``done_event``, out into out_host
+        (pinned).  Alternating two streams, each with its own q, k, v, out
+        and host buffers and the other's last done_event as wait_event,
+        overlaps one step's copies and the host's planning of the next with
+        the kernel before it."""
+        stream = self.stream if stream is None else stream
+        self.ensure_workspace(int(info.workspace_bytes))
+        if info.max_kv_len > self.max_pos:
+            raise ValueError(f"RoPE table covers {self.max_pos} positions, batch needs {info.max_kv_len}")
+        c = self._cur
+        dev = self._plan_device_buffer(int(info.packed_ints))
+        sarathi_mixed_attn_host(q_host, k_host, v_host, out_host, q, k, v, k_cache, v_cache, out, dev, info,
+                                self.rope, self.max_pos, self.workspace, self.shape, self.sm_scale, stream,
+                                self.rope_style, self._host_ts[c], wait_event, done_event)
+        self._upload_evts[c].record(stream)
         self._uploaded[c] = True
 
     def status(self) -> int:

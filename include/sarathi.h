@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define SARATHI_ABI_VERSION 5
+#define SARATHI_ABI_VERSION 6
 /* int32 words of one kernel work item in the packed plan.  Items are kernel
  * bookkeeping: their layout is private to the library and may change with
  * SARATHI_ABI_VERSION; callers copy the packed plan as a whole. */
@@ -260,6 +260,34 @@ typedef struct sarathi_attn_args {
  * Errors (before anything is enqueued): INVALID_ARG, CAPACITY (workspace or
  * RoPE table too small), UNSUPPORTED, CUDA. */
 int32_t sarathi_mixed_attn(const sarathi_attn_args* args, void* cuda_stream);
+
+/* Host side of one step for sarathi_mixed_attn_host.  q_host, k_host, v_host
+ * and out_host are HOST pointers, in the layouts of sarathi_attn_args' q, k, v
+ * and out (num_tokens = info->num_tokens rows); page-locked memory makes the
+ * copies asynchronous, pageable memory makes the call wait for them.  The
+ * events are cudaEvent_t handles owned by the caller, or NULL. */
+typedef struct sarathi_host_io {
+    const void* q_host;         /* bf16 [T][H_q][d]                                       */
+    const void* k_host;         /* bf16 [T][H_kv][d]                                      */
+    const void* v_host;         /* bf16 [T][H_kv][d]                                      */
+    void* out_host;             /* bf16 [T][H_q][d], written when the stream reaches it   */
+    void* wait_event;           /* the kernel starts after this event (the step before:   */
+                                /*   it wrote the pages this step reads), or NULL         */
+    void* done_event;           /* recorded right after the kernel, or NULL               */
+} sarathi_host_io;
+
+/* sarathi_mixed_attn from host buffers, end to end on `cuda_stream`: copies
+ * q, k, v from the host into args->q, k, v (device), the plan from
+ * args->plan_host into args->plan when plan_host is set, waits for
+ * io->wait_event, runs the step kernel, records io->done_event, and copies
+ * args->out into io->out_host.  The copies in ahead of the wait let a caller
+ * that alternates two streams (each with its own q, k, v, out, plan buffers,
+ * one workspace shared) overlap one step's copies with the other's kernel,
+ * passing each step the event of the step before it.  The host must not
+ * change q_host, k_host, v_host or plan_host, nor read out_host, before the
+ * stream has passed them.  Errors as sarathi_mixed_attn, all before anything
+ * is enqueued; INVALID_ARG also for NULL io or host pointers. */
+int32_t sarathi_mixed_attn_host(const sarathi_attn_args* args, const sarathi_host_io* io, void* cuda_stream);
 
 /* The same step as sarathi_mixed_attn, for callers that cannot allocate device
  * memory when they run it -- for example a plugin inside a process whose

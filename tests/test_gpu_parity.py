@@ -228,3 +228,66 @@ def test_repeated_launches_with_long_prefill_tiles():
         outs.append(to_u16(gs.out))
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
+
+
+def test_host_buffer_steps_on_two_streams_give_the_same_bits():
+    """StepRunner.run_host (sarathi_mixed_attn_host): four steps from pinned
+    host buffers, alternating two streams with their own device buffers,
+    each waiting for the step before it; every step's host output and the
+    pages equal the step launched from device buffers."""
+    import torch
+    gs = GpuStep(W.mistral())
+    k0, v0 = gs.kc_dev.clone(), gs.vc_dev.clone()
+    assert gs.run() == 0
+    out1, k1, v1 = to_u16(gs.out), to_u16(gs.kc_dev), to_u16(gs.vc_dev)
+    gs.kc_dev.copy_(k0)
+    gs.vc_dev.copy_(v0)
+    torch.cuda.synchronize()
+    r = gs.runner
+    pin = lambda t: t.cpu().pin_memory()
+    q_h, k_h, v_h = pin(gs.q_dev), pin(gs.k_dev), pin(gs.v_dev)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    dq = [[torch.empty_like(x) for x in (gs.q_dev, gs.k_dev, gs.v_dev, gs.out)] for _ in range(2)]
+    out_hs = [torch.full(gs.out.shape, float("nan"), dtype=gs.out.dtype).pin_memory() for _ in range(2)]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    results = []
+    for i in range(4):
+        b = i & 1
+        if i >= 2:
+            streams[b].synchronize()
+            results.append(to_u16(out_hs[b]).copy())
+            out_hs[b].fill_(float("nan"))
+        st, info, packed = r.plan(*gs.wl.arrays(), gs.wl.budget)
+        q, k, v, out = dq[b]
+        r.run_host(q_h, k_h, v_h, out_hs[b], q, k, v, gs.kc_dev, gs.vc_dev, out, info, stream=streams[b],
+                   wait_event=done[b ^ 1] if i else None, done_event=done[b])
+    torch.cuda.synchronize()
+    results += [to_u16(out_hs[0]), to_u16(out_hs[1])]
+    assert r.status() == 0
+    for res in results:
+        assert np.array_equal(res, out1)
+    assert np.array_equal(to_u16(gs.kc_dev), k1) and np.array_equal(to_u16(gs.vc_dev), v1)
+
+
+def test_host_buffer_step_with_an_empty_batch_records_its_event():
+    """An empty step (no items) copies and runs nothing but still records its
+    done event after the event it waits for."""
+    import ctypes
+    import torch
+    import chunked_prefill_mixed_gb300 as S
+    s = torch.cuda.Stream()
+    before, done = torch.cuda.Event(), torch.cuda.Event()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(1000)
+    before.record(s)
+    info = S.PlanInfo()
+    a = S.AttnArgs()
+    a.info = ctypes.pointer(info)
+    a.shape = S.Shape(32, 8, 128, 16)
+    buf = torch.empty(16, dtype=torch.int16).pin_memory()
+    io = S.HostIO(buf.data_ptr(), buf.data_ptr(), buf.data_ptr(), buf.data_ptr(), S._event_ptr(before, s),
+                  S._event_ptr(done, s))
+    other = torch.cuda.Stream()
+    assert S.load().sarathi_mixed_attn_host(ctypes.byref(a), ctypes.byref(io), other.cuda_stream) == S.OK
+    other.synchronize()
+    assert done.query() and before.query()

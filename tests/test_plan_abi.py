@@ -311,3 +311,18 @@ def test_split_metadata_equals_oracle_plans_of_each_class():
             assert [pi[i] for i in op["req_index"]] == list(full["req_index"][pre["first_row"]:])
         else:
             assert pre["rows"] == 0
+
+
+def test_host_buffer_step_rejects_missing_host_side_before_any_cuda_call():
+    """sarathi_mixed_attn_host checks its host side first: a NULL io or NULL
+    host pointer is INVALID_ARG, returned before the library touches CUDA
+    (so this runs without a GPU)."""
+    import ctypes
+    lib = S.load()
+    a = S.AttnArgs()
+    st = lib.sarathi_mixed_attn_host(ctypes.byref(a), None, None)
+    assert st == S.ERR_INVALID_ARG and b"io" in lib.sarathi_last_error()
+    buf = np.zeros(16, np.uint16)
+    io = S.HostIO(buf.ctypes.data, buf.ctypes.data, 0, buf.ctypes.data, 0, 0)
+    st = lib.sarathi_mixed_attn_host(ctypes.byref(a), ctypes.byref(io), None)
+    assert st == S.ERR_INVALID_ARG and b"host pointer" in lib.sarathi_last_error()
