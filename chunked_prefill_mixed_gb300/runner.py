@@ -28,23 +28,26 @@ class StepRunner:
         sarathi_rope_table(self.rope, self.max_pos, d, rope_theta, self.stream)
         self.workspace = torch.zeros(1 << 16, dtype=torch.uint8, device=self.device)
         # the packed plan is written straight into pinned memory, so that its
-        # copy to the device is one asynchronous DMA from there; two buffers
-        # in turn, so that the next step can be planned while the copy out of
-        # the last one (and the step after it) is still queued
-        self._host_ts = [torch.empty(0, dtype=torch.int32), torch.empty(0, dtype=torch.int32)]
+        # copy to the device is one asynchronous DMA from there; PLAN_BUFFERS
+        # buffers in turn, so that the host can plan up to two steps ahead of
+        # the GPU without waiting
+        n = self.PLAN_BUFFERS
+        self._host_ts = [torch.empty(0, dtype=torch.int32) for _ in range(n)]
         self._cur = 0
         # a device copy of each: a step's plan buffers are free again once the
-        # event recorded after its kernel has passed
-        self._plan_devs = [torch.empty(0, dtype=torch.int32, device=self.device) for _ in range(2)]
-        self._upload_evts = [torch.cuda.Event(), torch.cuda.Event()]
-        self._uploaded = [False, False]  # a copy out of buffer i may be in flight (_upload_evts[i])
+        # event recorded after its step call has passed
+        self._plan_devs = [torch.empty(0, dtype=torch.int32, device=self.device) for _ in range(n)]
+        self._upload_evts = [torch.cuda.Event() for _ in range(n)]
+        self._uploaded = [False] * n  # a copy out of buffer i may be in flight (_upload_evts[i])
+
+    PLAN_BUFFERS = 3
 
     def plan(self, states, prompt_len, num_computed, block_tables, budget: int, policy: PlanPolicy | None = None):
-        """Plans into one of two pinned host buffers the runner keeps (taken in
-        turn, grown when a batch needs more); the returned packed array is a
-        view of it, valid until the next call.  The buffer's previous copy to
-        the device (two plans ago) is waited for, not the last one, so a step
-        can be planned while the one before it runs.  policy: a PlanPolicy
+        """Plans into one of three pinned host buffers the runner keeps (taken
+        in turn, grown when a batch needs more); the returned packed array is a
+        view of it, valid until the next call.  The buffer's previous use
+        (three plans ago) is waited for, not the last one, so a step can be
+        planned while the steps before it run.  policy: a PlanPolicy
         for sarathi_plan_ex (its token_budget is used); None plans with
         sarathi_plan and `budget`."""
         reqs, keep = make_requests(states, prompt_len, num_computed, block_tables)
@@ -55,7 +58,7 @@ class StepRunner:
         make_requests, with its block tables alive; a serving loop advances it
         in place with sarathi_advance between steps)."""
         tb = policy.token_budget if policy is not None else budget
-        self._cur ^= 1
+        self._cur = (self._cur + 1) % self.PLAN_BUFFERS
         c = self._cur
         if self._uploaded[c]:
             self._upload_evts[c].synchronize()  # that plan's copy has left the buffer
