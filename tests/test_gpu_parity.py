@@ -62,6 +62,13 @@ def test_llama7b_budget_2048_sampled(k):
     _check_step(GpuStep(W.llama7b(chunk_step=k)), rows="sample")
 
 
+@pytest.mark.parametrize("chunk", [128, 512])
+def test_llama7b_last_prefill_chunk_sampled(chunk):
+    """The last chunk of an 8192-token prompt alone in the step (its items
+    fill fewer than half the SMs); sampled rows against the oracle."""
+    _check_step(GpuStep(W.llama7b_prefill_only(chunk, 8192 // chunk - 1)), rows="sample")
+
+
 def test_llama70b_budget_1536_sampled():
     _check_step(GpuStep(W.llama70b()), rows="sample")
 
