@@ -69,6 +69,29 @@ def test_llama7b_last_prefill_chunk_sampled(chunk):
     _check_step(GpuStep(W.llama7b_prefill_only(chunk, 8192 // chunk - 1)), rows="sample")
 
 
+@pytest.mark.parametrize("make,num_sms", [(W.mistral, 1), (W.mistral, 7), (W.llama70b, 400)],
+                         ids=["mistral-1", "mistral-7", "llama70b-400"])
+def test_work_queues_planned_for_another_sm_count(make, num_sms):
+    """A plan sized for another SM count than the device's: with 1 SM every
+    CTA starts on the second queue (APPEND items and decodes) and moves to the
+    tiles; with 400 the planner's partition (221 CTAs) exceeds the grid and the
+    launcher keeps one CTA on the second queue.  The step ends without a
+    device error and matches the oracle."""
+    import torch
+    from chunked_prefill_mixed_gb300.runner import StepRunner
+    wl = make()
+    sh = wl.shape
+    st, meta = oracle.plan(*wl.arrays(), wl.budget, sh.page_size)
+    max_pos = int(((np.diff(meta["kv_page_indptr"]) - 1) * 16 + meta["kv_last_page_len"]).max()) + 16
+    runner = StepRunner(sh.H_q, sh.H_kv, sh.d, max_pos, device="cuda", rope_theta=sh.rope_base)
+    runner.num_sms = num_sms
+    gs = GpuStep(wl, runner=runner)
+    assert 0 < gs.info.n_first < gs.info.n_items
+    if num_sms == 400:
+        assert gs.info.first_sms >= torch.cuda.get_device_properties(0).multi_processor_count
+    _check_step(gs, rows="sample")
+
+
 def test_llama70b_budget_1536_sampled():
     _check_step(GpuStep(W.llama70b()), rows="sample")
 
