@@ -69,6 +69,33 @@ def test_llama7b_last_prefill_chunk_sampled(chunk):
     _check_step(GpuStep(W.llama7b_prefill_only(chunk, 8192 // chunk - 1)), rows="sample")
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_random_request_sets_sampled(seed):
+    """Random mixed batches: a GQA shape, 0-48 decodes with contexts 0-3000,
+    0-4 prefill chunks (running with a random history, or waiting), a random
+    budget and scattered pages; sampled rows and the pages against the
+    oracle."""
+    rng = np.random.default_rng(1234 + seed)
+    H_q, H_kv, d = [(32, 8, 128), (8, 1, 64), (28, 4, 128), (16, 16, 64), (64, 8, 128), (12, 2, 128)][seed]
+    specs = []
+    for _ in range(int(rng.integers(0, 49))):
+        c = int(rng.integers(0, 3001))
+        specs.append((W.DECODE, 0, c, c + 1))
+    for _ in range(int(rng.integers(0 if specs else 1, 5))):
+        if rng.random() < 0.5:
+            h = int(rng.integers(1, 4000))
+            pl = h + int(rng.integers(1, 900))
+            specs.append((W.PREFILL_RUNNING, pl, h, pl))
+        else:
+            pl = int(rng.integers(1, 1200))
+            specs.append((W.PREFILL_WAITING, pl, 0, pl))
+    order = rng.permutation(len(specs))
+    specs = [specs[i] for i in order]
+    budget = int(rng.integers(len([x for x in specs if x[0] == W.DECODE]) + 1, 2600))
+    _check_step(GpuStep(_custom(W.Shape(H_q, H_kv, d), specs, budget, seed=seed, name=f"random{seed}")),
+                rows="sample")
+
+
 @pytest.mark.parametrize("make,num_sms", [(W.mistral, 1), (W.mistral, 7), (W.llama70b, 400)],
                          ids=["mistral-1", "mistral-7", "llama70b-400"])
 def test_work_queues_planned_for_another_sm_count(make, num_sms):
