@@ -285,8 +285,12 @@ typedef struct sarathi_host_io {
  * one workspace shared) overlap one step's copies with the other's kernel,
  * passing each step the event of the step before it.  The host must not
  * change q_host, k_host, v_host or plan_host, nor read out_host, before the
- * stream has passed them.  Errors as sarathi_mixed_attn, all before anything
- * is enqueued; INVALID_ARG also for NULL io or host pointers. */
+ * stream has passed them.  The pages define the step itself (see
+ * sarathi_mixed_attn); this host-side packaging is the library's own.
+ * Errors: as sarathi_mixed_attn, and INVALID_ARG for a NULL io or host
+ * pointer, all before anything is enqueued; a CUDA error from one of the
+ * enqueued calls returns SARATHI_ERR_CUDA with the calls before it already
+ * enqueued. */
 int32_t sarathi_mixed_attn_host(const sarathi_attn_args* args, const sarathi_host_io* io, void* cuda_stream);
 
 /* The same step as sarathi_mixed_attn, for callers that cannot allocate device
