@@ -162,6 +162,85 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def clocks_summary(nvml: dict, smi: dict) -> dict:
+    """The NVML samples taken inside the timed region when there are any (the
+    nvidia-smi samples, every 100 ms around it, beside them), else nvidia-smi's."""
+    if nvml.get("samples"):
+        out = dict(nvml)
+        out["reasons"] = sorted(set(nvml["reasons"]) | set(smi.get("reasons") or []))
+        out["nvidia_smi"] = smi
+        return out
+    return smi
+
+
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, by ctypes) every half millisecond while the timed region
+    runs, so that a region of a few milliseconds still holds samples; read-only.
+    Any failure leaves it empty (the nvidia-smi sampler still reports)."""
+
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, index: int, uuid: str | None = None):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.ok = False
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            got = False
+            if uuid:
+                u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+                got = nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0
+            if not got and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+                return
+            try:
+                self.get_reasons = nv.nvmlDeviceGetCurrentClocksEventReasons
+            except AttributeError:
+                self.get_reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nv, self.h, self.ct = nv, h, ctypes
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = False
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        return self
+
+    def _run(self):
+        nv, h, ct = self.nv, self.h, self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop:
+            try:
+                if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0:
+                    self.samples.append(float(clk.value))
+                if self.get_reasons(h, ct.byref(rs)) == 0:
+                    for bit, name in self.REASONS.items():
+                        if rs.value & bit:
+                            self.reasons.add(name)
+            except Exception:
+                return
+            time.sleep(0.0005)
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop = True
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples), "source": "nvml, every 0.5 ms"}
+
+
 def reduce_max(values, world: int, device=None):
     """Max over ranks of per-rank timings (all_reduce MAX); the job is as slow
     as its slowest replica."""
@@ -300,7 +379,12 @@ def run_ours(args, rank, world, local_rank):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    nvml = NvmlSampler(dev.index if dev.index is not None else 0, uuid)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk, nvml:
         t_wall0 = time.perf_counter()
         with torch.cuda.stream(stream):
             for i in range(args.steps):
@@ -424,7 +508,7 @@ def run_ours(args, rank, world, local_rank):
                             "before it",
                 "serial": {"value": job_tokens_per_s(T, world, e2e_serial_s), "us_per_step": e2e_serial_s * 1e6,
                            "includes": "the same, one step at a time (synchronised after each step)"}},
-        "clocks": clk.summary(),
+        "clocks": clocks_summary(nvml.summary(), clk.summary()),
         "gpu_launches": args.steps,
         "timing": {"kernel_ms_min": min(ms), "kernel_ms_median": statistics.median(ms), "wall_s": t_wall,
                    "kernel_ms_median_warm_l2": warm_ms},
