@@ -45,6 +45,20 @@ extern "C" int32_t sarathi_mixed_attn_noalloc(const sarathi_attn_args* args, voi
         return fail(SARATHI_ERR_CAPACITY, msg);
     }
     if (in->n_items == 0) return SARATHI_OK;
+    // The counters cleared below sit in front of the partial slots; their size
+    // comes from n_sched and n_merge, so both are checked against the array
+    // before anything is enqueued (an inconsistent plan info must not make the
+    // memset run past the array).
+    if (in->n_sched <= 0 || in->n_merge < 0 || in->n_partials < 0 || in->n_items < 0)
+        return fail(SARATHI_ERR_INVALID_ARG, "inconsistent plan info (n_sched, n_merge, n_partials or n_items)");
+    const int32_t st = check_shape(&args->shape);
+    if (st) return st;
+    const int64_t clear_bytes = partial_offset_bytes(in->n_sched, in->n_merge);
+    const int64_t need = clear_bytes + (int64_t)in->n_partials *
+                                           partial_slot_floats(args->shape.num_heads_q / args->shape.num_heads_kv,
+                                                               args->shape.head_dim) * 4;
+    if (need > in->workspace_bytes)
+        return fail(SARATHI_ERR_INVALID_ARG, "inconsistent plan info (counters and partials exceed its workspace_bytes)");
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(SARATHI_ERR_CUDA, cudaGetErrorString(e));
@@ -69,8 +83,7 @@ extern "C" int32_t sarathi_mixed_attn_noalloc(const sarathi_attn_args* args, voi
     // The array keeps whatever the previous call left.  The counters, tickets
     // and error word must start at zero; the partial slots are always written
     // before they are read.
-    const size_t clear = (size_t)partial_offset_bytes(in->n_sched, in->n_merge);
-    e = cudaMemsetAsync(scratch, 0, clear, (cudaStream_t)cuda_stream);
+    e = cudaMemsetAsync(scratch, 0, (size_t)clear_bytes, (cudaStream_t)cuda_stream);
     if (e != cudaSuccess) return fail(SARATHI_ERR_CUDA, cudaGetErrorString(e));
     sarathi_attn_args a = *args;
     a.workspace = scratch;

@@ -303,11 +303,22 @@ int32_t sarathi_mixed_attn_host(const sarathi_attn_args* args, const sarathi_hos
  * 8 MiB is rejected with SARATHI_ERR_CAPACITY before anything is enqueued.
  * The call allocates nothing: it clears the array's counters with
  * cudaMemsetAsync on `cuda_stream` and enqueues the step kernel.  The first
- * call on each device looks up the array's device address; make that first
- * call before any stream capture.  All calls share the one array, so calls
- * whose work overlaps on the GPU (other streams, other threads) race and give
- * wrong results.  The device error word lives in the shared array and is not
- * reported; use sarathi_mixed_attn with a workspace when it is needed. */
+ * call on each device looks up the array's device address; with lazy module
+ * loading (the CUDA default) that first lookup is also when the device
+ * reserves the array, so make the first call on each device before a host
+ * allocator claims the GPU's memory, and before any stream capture.  The
+ * address is kept per device index for the life of the process: do not use
+ * this call after cudaDeviceReset on that device.  All calls share the one
+ * array, so calls whose work overlaps on the GPU (other streams, other
+ * threads) race and give wrong results.  The device error word lives in the
+ * shared array and is not reported: a bounded wait that runs out or a page id
+ * outside the pool leaves the outputs and pages partly written while the call
+ * still returned SARATHI_OK; use sarathi_mixed_attn with a workspace (and
+ * sarathi_workspace_status) when such failures must be detected.
+ * Errors, all before anything is enqueued: CAPACITY when
+ * info->workspace_bytes exceeds the array; INVALID_ARG when the plan info is
+ * inconsistent (n_sched <= 0, negative counts, or counters and partial slots
+ * larger than info->workspace_bytes); then as sarathi_mixed_attn. */
 int32_t sarathi_mixed_attn_noalloc(const sarathi_attn_args* args, void* cuda_stream);
 
 /* The Q/K/V projection of a step's tokens as ONE GEMM over the concatenated

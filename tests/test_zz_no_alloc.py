@@ -29,6 +29,25 @@ def test_noalloc_refuses_batches_beyond_the_scratch_limit():
     assert "scratch" in S.sarathi_last_error()
 
 
+def test_noalloc_refuses_inconsistent_plan_info_before_any_cuda_call():
+    """A plan info whose counters (n_sched, n_merge) would not fit the
+    workspace it states is refused before anything is enqueued, so the
+    clearing of the array can never run past its end."""
+    for n_sched, n_merge, n_partials in ((1 << 28, 0, 0), (4, 1 << 27, 0), (4, 0, 1 << 20), (0, 0, 0)):
+        info = S.PlanInfo()
+        info.n_items = 1
+        info.n_sched = n_sched
+        info.n_merge = n_merge
+        info.n_partials = n_partials
+        info.workspace_bytes = 1024
+        a = S.AttnArgs()
+        a.info = ctypes.pointer(info)
+        a.shape = S.Shape(32, 8, 128, 16)
+        st = S.load().sarathi_mixed_attn_noalloc(ctypes.byref(a), None)
+        assert st == S.ERR_INVALID_ARG, (n_sched, n_merge, n_partials, st)
+        assert "inconsistent plan info" in S.sarathi_last_error()
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
     import torch
