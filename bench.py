@@ -1,6 +1,6 @@
 """Benchmark of the mixed-batch paged-attention step (one kernel launch per step).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mistral]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama7b]
                     [--impl ours|reference]
 
 Prints ONE JSON line on rank 0.  ``value`` is tokens/s over the whole job: the
@@ -293,10 +293,20 @@ def oracle_sample_time(wl: W.Workload, meta, q, k, v, kc, vc, budget_s: float, s
 
 
 def setup_inputs(wl: W.Workload):
+    """The oracle's own plan of the workload and the step's new-token values
+    (the oracle legs: the reference arm and the CPU baseline)."""
     import oracle
     st, meta = oracle.plan(*wl.arrays(), wl.budget, 16)
     q, k, v = W.new_token_values(meta["num_tokens"], wl.shape, wl.seed)
     return meta, q, k, v
+
+
+def max_positions(wl: W.Workload) -> int:
+    """An upper bound on the KV length of any row the workload can schedule."""
+    m = 1
+    for r in wl.requests:
+        m = max(m, r.num_computed + 1 if r.state == W.DECODE else r.prompt_len)
+    return m
 
 
 def run_reference(args, rank, world):
@@ -332,15 +342,19 @@ def run_ours(args, rank, world, local_rank):
     S.load()
     wl = make_workload(args.workload)
     sh = wl.shape
-    meta, q, k, v = setup_inputs(wl)
+    kc, vc = W.history_cache_torch(wl.num_pages, sh, wl.seed, dev)
+    stream = torch.cuda.Stream(dev)
+    runner = StepRunner(sh.H_q, sh.H_kv, sh.d, max_positions(wl) + 16, device=dev, rope_theta=sh.rope_base,
+                        stream=stream)
+    st, info, packed = runner.plan(*wl.arrays(), wl.budget)
+    packed = packed.copy()  # the runner's buffer is reused by its next plan
+    runner.ensure_workspace(int(info.workspace_bytes))
+    # the roofline's algorithmic bytes and FLOP come from the library's own
+    # plan of the step, the metadata the timed kernel runs
+    meta = S.plan_arrays(info, packed)
     alg = algorithmic(wl, meta)
     T = alg["T"]
-    kc, vc = W.history_cache_torch(wl.num_pages, sh, wl.seed, dev)
-    max_kv = int(((np.diff(meta["kv_page_indptr"]) - 1) * 16 + meta["kv_last_page_len"]).max())
-    stream = torch.cuda.Stream(dev)
-    runner = StepRunner(sh.H_q, sh.H_kv, sh.d, max_kv + 16, device=dev, rope_theta=sh.rope_base, stream=stream)
-    st, info, packed = runner.plan(*wl.arrays(), wl.budget)
-    runner.ensure_workspace(int(info.workspace_bytes))
+    q, k, v = W.new_token_values(info.num_tokens, sh, wl.seed)
 
     def bf(x):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
@@ -517,13 +531,15 @@ def run_ours(args, rank, world, local_rank):
         kc_h = kc.view(torch.int16).cpu().numpy().view(np.uint16)
         vc_h = vc.view(torch.int16).cpu().numpy().view(np.uint16)
         # the device caches already hold this step's appends; the oracle
-        # re-appends the same values, so the sample sees the same state
-        est, cores, desc = oracle_sample_time(wl, meta, q, k, v, kc_h, vc_h, args.cpu_seconds)
+        # re-appends the same values, so the sample sees the same state; the
+        # oracle runs its own plan of the step
+        meta_o, q, k, v = setup_inputs(wl)
+        est, cores, desc = oracle_sample_time(wl, meta_o, q, k, v, kc_h, vc_h, args.cpu_seconds)
         res["cpu_baseline"] = {"value": T / est, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
         # the same oracle on one core, on a smaller sample
         import oracle
         oracle.set_num_threads(1)
-        est1, _, desc1 = oracle_sample_time(wl, meta, q, k, v, kc_h, vc_h, args.cpu_seconds / 4, seed=1)
+        est1, _, desc1 = oracle_sample_time(wl, meta_o, q, k, v, kc_h, vc_h, args.cpu_seconds / 4, seed=1)
         oracle.set_num_threads(cores)
         res["cpu_baseline"]["one_core"] = {"value": T / est1, "unit": UNIT, "sample": desc1}
     return res
@@ -780,7 +796,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mistral", choices=sorted(DESCR))
+    ap.add_argument("--workload", default="llama7b", choices=sorted(DESCR))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0)

@@ -236,38 +236,65 @@ def test_tiny_chunked_schedule_equals_one_shot_and_oracle():
     assert diff.max() <= 2e-2
 
 
-@pytest.mark.parametrize("chunk", [512, 2048])
-def test_llama7b_prefill_chunk_sweep_pages_equal_one_shot(chunk):
-    """Prefill-only 8192-token prompt: every chunking writes the same pages as
-    one shot, chunk outputs agree with one shot, and sampled rows of the one
-    shot match the oracle."""
+@pytest.mark.parametrize("chunk", [512, 1024, 2048])
+def test_llama7b_prefill_chunk_sweep_against_oracle_and_one_shot(chunk):
+    """The 8192-token prompt prefilled alone in chunks of 512, 1024 and 2048
+    tokens ("Sarathi-Serve 完全拆解", §"先验证数值与状态正确性": chunked prefill
+    must equal one-shot prefill, checked at the long-context boundaries).
+    After every chunk step the whole page pool equals the oracle's, bit for
+    bit; every step's sampled rows (the chunk's first, second, middle and last
+    two rows over all heads, plus random pairs) match the oracle; the final
+    pages equal the one-shot step's, and each chunk's outputs agree with the
+    one-shot outputs of the same rows."""
     import torch
     L = 8192
     one = GpuStep(W.llama7b_prefill_only(L, 0))
     assert one.run() == 0
+    sh = one.wl.shape
     pages = one.wl.requests[0].pages
-    ref_k = to_u16(one.kc_dev)[pages]
-    ref_v = to_u16(one.vc_dev)[pages]
+    kc_one, vc_one = one.oracle_caches()
+    assert np.array_equal(to_u16(one.kc_dev), kc_one) and np.array_equal(to_u16(one.vc_dev), vc_one)
     rt = np.array([0, 1, 511, 512, 513, 4095, 4096, 8190, 8191], np.int32)
     rh = np.array([0, 31, 5, 17, 3, 9, 30, 2, 31], np.int32)
-    kc_o, vc_o = one.oracle_caches()
-    ref, _, _ = one.oracle_rows(kc_o, vc_o, rt, rh)
+    ref, _, _ = one.oracle_rows(kc_one, vc_one, rt, rh)
     assert_close(oracle.bf16_to_double(to_u16(one.out))[rt, rh], ref, "one-shot 8192")
-    gs = GpuStep(W.llama7b_prefill_only(chunk, 0), runner=one.runner)
-    done = 0
+
+    dev = one.dev
+    runner = one.runner
+    kc, vc = from_u16(one.kc0, dev), from_u16(one.vc0, dev)
+    okc, ovc = one.kc0.copy(), one.vc0.copy()
+    rng = np.random.default_rng(chunk)
+    done, step = 0, 0
     while done < L:
-        wl = W.llama7b_prefill_only(chunk, done // chunk)
-        st, info, packed = gs.runner.plan(*wl.arrays(), wl.budget)
+        wl = W.llama7b_prefill_only(chunk, step)
+        st_o, meta = oracle.plan(*wl.arrays(), wl.budget, 16)
+        st, info, packed = runner.plan(*wl.arrays(), wl.budget)
         n = info.num_tokens
-        out = torch.empty((n, 32, 128), dtype=torch.bfloat16, device="cuda")
-        gs.runner.run(one.q_dev[done:done + n], one.k_dev[done:done + n], one.v_dev[done:done + n],
-                      gs.kc_dev, gs.vc_dev, out, gs.runner.upload(packed), info)
-        assert gs.runner.status() == 0
+        assert n == meta["num_tokens"] == min(chunk, L - done)
+        out = torch.full((n, sh.H_q, sh.d), float("nan"), dtype=torch.bfloat16, device=dev)
+        runner.run(one.q_dev[done:done + n], one.k_dev[done:done + n], one.v_dev[done:done + n],
+                   kc, vc, out, runner.upload(packed.copy()), info)
+        torch.cuda.synchronize()
+        assert runner.status() == 0, f"chunk {chunk} step {step}: device error"
+        q, k, v = one.q[done:done + n], one.k[done:done + n], one.v[done:done + n]
+        oracle.append(meta, k, v, sh.H_kv, sh.d, 16, sh.rope_base, okc, ovc)
+        assert np.array_equal(to_u16(kc), okc), f"chunk {chunk} step {step}: K pages differ from the oracle"
+        assert np.array_equal(to_u16(vc), ovc), f"chunk {chunk} step {step}: V pages differ from the oracle"
+        local = sorted({0, 1, n // 2, n - 2, n - 1})
+        st_rows = [(t, hq) for t in local for hq in range(sh.H_q)]
+        st_rows += [(int(rng.integers(0, n)), int(rng.integers(0, sh.H_q))) for _ in range(64)]
+        st_rows = sorted(set(st_rows))
+        srt = np.array([r[0] for r in st_rows], np.int32)
+        srh = np.array([r[1] for r in st_rows], np.int32)
+        sref, _, _, _ = oracle.attend(meta, q, sh.H_q, sh.H_kv, sh.d, 16, sh.rope_base, okc, ovc, srt, srh)
+        got = oracle.bf16_to_double(to_u16(out))
+        assert_close(got[srt, srh], sref, f"chunk {chunk} step {step}")
         diff = (out.float() - one.out[done:done + n].float()).abs()
-        assert float(diff.max()) <= 2e-2
+        assert float(diff.max()) <= 2e-2, f"chunk {chunk} step {step}: differs from the one-shot outputs"
         done += n
-    assert np.array_equal(to_u16(gs.kc_dev)[pages], ref_k)
-    assert np.array_equal(to_u16(gs.vc_dev)[pages], ref_v)
+        step += 1
+    assert np.array_equal(to_u16(kc)[pages], to_u16(one.kc_dev)[pages])
+    assert np.array_equal(to_u16(vc)[pages], to_u16(one.vc_dev)[pages])
 
 
 def test_repeated_launches_with_long_prefill_tiles():
