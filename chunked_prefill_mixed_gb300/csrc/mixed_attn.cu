@@ -60,7 +60,7 @@ struct KParams {
     int n_items, n_sched;
     int n_first, first_sms;   // the work list's two queues (see the kernel's claim loop)
     const double2* rope;  // [max_pos][d/2] {cos, sin} in fp64
-    const float4* ropef;  // [max_pos][d/2] {cos_hi, cos_lo, sin_hi, sin_lo}: cos = cos_hi + cos_lo to ~2^-48
+    const float* ropef;   // [max_pos][d/16][32]: per 8 pairs cos_hi[8], sin_hi[8], cos_lo[8], sin_lo[8] (cos = hi + lo to ~2^-48)
     int rope_max_pos;
     int32_t* ws_int;      // header, append counters, merge tickets
     float* ws_part;       // split partials
@@ -69,7 +69,7 @@ struct KParams {
     int slot_floats;
 };
 
-constexpr int kThreads = 352;                                  // 11 warps
+constexpr int kThreads = 384;                                  // 12 warps
 constexpr int kDecWarps = 8;                                   // warps that stream decode pages
 constexpr int kDecStages = 3;                                  // per-warp page ring
 constexpr int kPageHalfBytes = kPage * 128;                    // 16 rows x 64 bf16
@@ -85,6 +85,7 @@ static_assert(kDecWarps * 16 * 128 * 4 + 2 * kDecWarps * 16 * 4 <= kSmemStages, 
 static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s bound on any wait
+constexpr uint32_t kWaitSleepNs = 200000u;             // longest sleep of one suspended try-wait
 
 // ----------------------------------------------------------------------------
 // PTX helpers
@@ -114,6 +115,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// The same with a suspend-time hint: a thread whose phase is not complete
+// sleeps (up to the hint, in ns) until it completes instead of spinning, so a
+// waiting thread takes no issue slots from the warps that share its SM
+// sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kWaitSleepNs)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -126,6 +142,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
             dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+// 5-D box: coordinates {x0..x4} innermost first.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int x0, int x1, int x2, int x3,
+                                            int x4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
+        "%6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x0), "r"(x1), "r"(x2), "r"(x3), "r"(x4), "r"(bar)
         : "memory");
 }
 // Plain (untiled) bulk copy global -> shared; both addresses 16-byte aligned,
@@ -237,13 +262,17 @@ __device__ __forceinline__ void raise_error(const KParams& P, int code, int deta
 
 // Bounded wait on an mbarrier phase; returns false (and flags the CTA) on
 // timeout, recording the work item, the thread and the barrier's raw state in
-// header words 3..11 for the host to read.
+// header words 3..11 for the host to read.  SLEEP: the thread suspends while it
+// waits (for threads that wait long and share an SM sub-partition with warps
+// that compute); otherwise it polls, which wakes sooner.
+template <bool SLEEP>
 __device__ __noinline__ bool mbar_wait_slow(const KParams& P, uint32_t bar, uint32_t parity, int* s_abort,
                                             int detail, const int* it) {
-    for (int i = 0; i < 256; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (!SLEEP)
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!(SLEEP ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity))) {
         if (*(volatile int*)s_abort) return false;
         if (globaltimer() - t0 > kWaitNs) {
             if (atomicCAS(&P.ws_int[2], 0, kErrWait) == 0) {
@@ -261,10 +290,11 @@ __device__ __noinline__ bool mbar_wait_slow(const KParams& P, uint32_t bar, uint
     }
     return true;
 }
+template <bool SLEEP = false>
 __device__ __forceinline__ bool mbar_wait_bounded(const KParams& P, uint32_t bar, uint32_t parity, int* s_abort,
                                                   int detail, const int* it) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(P, bar, parity, s_abort, detail, it);
+    return mbar_wait_slow<SLEEP>(P, bar, parity, s_abort, detail, it);
 }
 
 struct Row {
@@ -362,6 +392,13 @@ __device__ __forceinline__ uint16_t rope_bf16(float a, float b, float p_hi, floa
     const double2 c = *pq;  // fp64 {cos, sin}: read only on this rare path
     return bf16_from_double(__dadd_rn(__dmul_rn((double)a, c.x), __dmul_rn((double)b, c.y)));
 }
+// fp32 RoPE table: the 8 pairs 8c..8c+7 of one position form a chunk of 32
+// floats, cos_hi[8], sin_hi[8], cos_lo[8], sin_lo[8], so that a query unit
+// (which needs only the hi parts) loads 64 contiguous bytes.
+constexpr int kRopeChunk = 32;
+__device__ __forceinline__ float4 rope_chunk_pair(const float* ch, int e) {
+    return make_float4(ch[e], ch[16 + e], ch[8 + e], ch[24 + e]);  // {cos_hi, cos_lo, sin_hi, sin_lo}
+}
 __device__ __forceinline__ void rope_pair(float x0, float x1, float4 cf, const double2* cs, uint16_t& y0,
                                           uint16_t& y1) {
     y0 = rope_bf16(x0, -x1, cf.x, cf.y, cf.z, cf.w, cs);
@@ -369,14 +406,15 @@ __device__ __forceinline__ void rope_pair(float x0, float x1, float4 cf, const d
 }
 // Interleaved pairing: a holds dims 2j0..2j0+7 (pairs j0..j0+3), b the next
 // eight (pairs j0+4..j0+7); the outputs replace them in place.
-__device__ __forceinline__ void rope8_interleaved(uint4 a, uint4 b, const float4* cf, const double2* fb, uint4& oa,
+__device__ __forceinline__ void rope8_interleaved(uint4 a, uint4 b, const float* ch, const double2* fb, uint4& oa,
                                                   uint4& ob) {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     uint32_t o[8];
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
         uint16_t y0, y1;
-        rope_pair(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xFFFF0000u), cf[p], fb + p, y0, y1);
+        rope_pair(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xFFFF0000u), rope_chunk_pair(ch, p), fb + p, y0,
+                  y1);
         o[p] = (uint32_t)y0 | ((uint32_t)y1 << 16);
     }
     oa = make_uint4(o[0], o[1], o[2], o[3]);
@@ -384,14 +422,15 @@ __device__ __forceinline__ void rope8_interleaved(uint4 a, uint4 b, const float4
 }
 // Eight consecutive pairs (x0 = a, x1 = b, 8 bf16 each) of one key row:
 // lo = first-half outputs, hi = second-half outputs.
-__device__ __forceinline__ void rope8(uint4 a, uint4 b, const float4* cf, const double2* fb, uint4& lo, uint4& hi) {
+__device__ __forceinline__ void rope8(uint4 a, uint4 b, const float* ch, const double2* fb, uint4& lo, uint4& hi) {
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
     uint32_t w0[4], w1[4];
 #pragma unroll
     for (int e2 = 0; e2 < 4; ++e2) {
         uint16_t lo0, lo1, hi0, hi1;
-        rope_pair(__uint_as_float(aw[e2] << 16), __uint_as_float(bw[e2] << 16), cf[2 * e2], fb + 2 * e2, lo0, lo1);
-        rope_pair(__uint_as_float(aw[e2] & 0xFFFF0000u), __uint_as_float(bw[e2] & 0xFFFF0000u), cf[2 * e2 + 1],
+        rope_pair(__uint_as_float(aw[e2] << 16), __uint_as_float(bw[e2] << 16), rope_chunk_pair(ch, 2 * e2), fb + 2 * e2,
+                  lo0, lo1);
+        rope_pair(__uint_as_float(aw[e2] & 0xFFFF0000u), __uint_as_float(bw[e2] & 0xFFFF0000u), rope_chunk_pair(ch, 2 * e2 + 1),
                   fb + 2 * e2 + 1, hi0, hi1);
         w0[e2] = (uint32_t)lo0 | ((uint32_t)hi0 << 16);
         w1[e2] = (uint32_t)lo1 | ((uint32_t)hi1 << 16);
@@ -403,32 +442,39 @@ __device__ __forceinline__ void rope8(uint4 a, uint4 b, const float4* cf, const 
 // Eight pairs of one query row in fp32, rounded to bf16 (Q feeds the MMA in
 // bf16; its rotation needs no certified rounding).  Rotate-half: a = x0 and
 // b = x1 of pairs j0..j0+7, lo / hi = their outputs.  Interleaved: a = dims
-// 2j0..2j0+7, b = the next eight, outputs in place.  cs: table rows j0..j0+7.
-__device__ __forceinline__ void rope_q8(uint4 a, uint4 b, const float4* cs, bool interleaved, uint4& lo, uint4& hi) {
+// 2j0..2j0+7, b = the next eight, outputs in place.  c, s: cos_hi and sin_hi
+// of pairs j0..j0+7.
+__device__ __forceinline__ void rope_q8(uint4 a, uint4 b, const float (&c)[8], const float (&s)[8], bool interleaved,
+                                        uint4& lo, uint4& hi) {
     const __nv_bfloat16* xa = reinterpret_cast<const __nv_bfloat16*>(&a);
     const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&b);
     uint32_t ylo[4], yhi[4];
     if (!interleaved) {
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
-            const float4 c0 = cs[e], c1 = cs[e + 1];
             const float a0 = __bfloat162float(xa[e]), a1 = __bfloat162float(xa[e + 1]);
             const float b0 = __bfloat162float(xb[e]), b1 = __bfloat162float(xb[e + 1]);
-            ylo[e >> 1] = pack_bf16(a0 * c0.x - b0 * c0.z, a1 * c1.x - b1 * c1.z);
-            yhi[e >> 1] = pack_bf16(b0 * c0.x + a0 * c0.z, b1 * c1.x + a1 * c1.z);
+            ylo[e >> 1] = pack_bf16(a0 * c[e] - b0 * s[e], a1 * c[e + 1] - b1 * s[e + 1]);
+            yhi[e >> 1] = pack_bf16(b0 * c[e] + a0 * s[e], b1 * c[e + 1] + a1 * s[e + 1]);
         }
     } else {
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-            const float4 ca = cs[p], cb = cs[p + 4];
             const float x0 = __bfloat162float(xa[2 * p]), x1 = __bfloat162float(xa[2 * p + 1]);
             const float z0 = __bfloat162float(xb[2 * p]), z1 = __bfloat162float(xb[2 * p + 1]);
-            ylo[p] = pack_bf16(x0 * ca.x - x1 * ca.z, x1 * ca.x + x0 * ca.z);
-            yhi[p] = pack_bf16(z0 * cb.x - z1 * cb.z, z1 * cb.x + z0 * cb.z);
+            ylo[p] = pack_bf16(x0 * c[p] - x1 * s[p], x1 * c[p] + x0 * s[p]);
+            yhi[p] = pack_bf16(z0 * c[p + 4] - z1 * s[p + 4], z1 * c[p + 4] + z0 * s[p + 4]);
         }
     }
     lo = make_uint4(ylo[0], ylo[1], ylo[2], ylo[3]);
     hi = make_uint4(yhi[0], yhi[1], yhi[2], yhi[3]);
+}
+// cos_hi and sin_hi of one table chunk (8 pairs) from global memory.
+__device__ __forceinline__ void load_rope_hi(const float* ch, float (&c)[8], float (&s)[8]) {
+    const float4* v = reinterpret_cast<const float4*>(ch);
+    const float4 c0 = __ldg(v), c1 = __ldg(v + 1), s0 = __ldg(v + 2), s1 = __ldg(v + 3);
+    c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w; c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+    s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w; s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
 }
 
 // ----------------------------------------------------------------------------
@@ -449,7 +495,7 @@ __device__ void run_append(const KParams& P, const int* it, uint8_t* smem, uint3
     const int Hkv = P.Hkv;
     constexpr int HALF = D / 2, C8 = D / 8, H8 = HALF / 8;
     const int row_bytes = Hkv * D * 2;                // one token's K (or V), every kv head
-    const int tok_bytes = 2 * row_bytes + HALF * 16;  // its K, V and fp32 RoPE row
+    const int tok_bytes = 2 * row_bytes + HALF * 16;  // its K, V and fp32 RoPE row (HALF x 4 floats)
     const int tpp = min(cnt, kSmemStages / tok_bytes);
     const uint16_t* kin = reinterpret_cast<const uint16_t*>(P.k);
     uint16_t* kc = reinterpret_cast<uint16_t*>(P.k_cache);
@@ -467,13 +513,13 @@ __device__ void run_append(const KParams& P, const int* it, uint8_t* smem, uint3
                 mbar_expect_tx(bar, 2 * kbytes + rbytes);
                 bulk_load(smem_u32(smem), kin + row0, kbytes, bar);
                 bulk_load(smem_u32(smem + kbytes), P.v + row0, kbytes, bar);
-                bulk_load(smem_u32(smem + 2 * kbytes), P.ropef + (size_t)(R.h + ta) * HALF, rbytes, bar);
+                bulk_load(smem_u32(smem + 2 * kbytes), P.ropef + (size_t)(R.h + ta) * HALF * 4, rbytes, bar);
             }
             if (!mbar_wait_bounded(P, bar, phase & 1, s_abort, 10000 + p0, it)) return;
             ++phase;
             const uint16_t* ks = reinterpret_cast<const uint16_t*>(smem);
             const uint4* vs = reinterpret_cast<const uint4*>(smem + kbytes);
-            const float4* rs = reinterpret_cast<const float4*>(smem + 2 * kbytes);
+            const float* rs = reinterpret_cast<const float*>(smem + 2 * kbytes);
             const int totv = n * Hkv * C8;
             for (int i = tid; i < totv; i += kThreads) {
                 const int c = i % C8, rest = i / C8, g = rest % Hkv, pos = R.h + ta + rest / Hkv;
@@ -493,7 +539,7 @@ __device__ void run_append(const KParams& P, const int* it, uint8_t* smem, uint3
                 }
                 const uint16_t* krow = ks + ((size_t)tl * Hkv + g) * D;
                 uint16_t* drow = kc + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D;
-                const float4* cf = rs + tl * HALF + j8 * 8;
+                const float* cf = rs + (size_t)tl * HALF * 4 + j8 * kRopeChunk;
                 const double2* fb = P.rope + (size_t)pos * HALF + j8 * 8;
                 // pairs 8 j8 .. 8 j8 + 7: dims (j, j + d/2), or (2j, 2j + 1) interleaved
                 const int d0 = IL ? 16 * j8 : 8 * j8;
@@ -609,10 +655,13 @@ constexpr int kPhKFill = 0;    // 4: producer, loads issued into each K stage
 constexpr int kPhVFill = 4;    // 4: producer, loads issued into each V stage
 constexpr int kPhKUse = 8;     // 4: MMA issuer, K loads consumed
 constexpr int kPhVUse = 12;    // 4: MMA issuer, V loads consumed
-constexpr int kPhPFull = 16;   // 2: MMA issuer, P of each Q tile consumed
-constexpr int kPhSUse = 18;    // 2: softmax, S of its Q tile consumed
-constexpr int kPhODone = 20;   // 2: softmax, final P.V of its Q tile
-constexpr int kPhVSeen = 22;   // 4: softmax, V loads into each stage (last-block clean-up)
+constexpr int kPhPFull = 16;   // 2: MMA issuer, P of each buffer consumed
+constexpr int kPhSUse = 18;    // 2: softmax, S of each buffer consumed
+constexpr int kPhOUp = 20;     // 2: softmax, P.V groups of each P buffer waited for
+constexpr int kPhODone = 22;   // 1: softmax, items completed before this one
+constexpr int kPhVSeen = 23;   // 4: softmax, V loads into each stage (last-block clean-up)
+constexpr int kPhSFree = 27;   // 2: QK issuer, S of each buffer loaded by the softmax
+constexpr int kPhQ = 29;       // 1: Q writers, Q tiles loaded
 __device__ __forceinline__ uint32_t ph_get(const PfPhase& ph, int bit) { return (ph.bits >> bit) & 1u; }
 __device__ __forceinline__ void ph_flip(PfPhase& ph, int bit) { ph.bits ^= 1u << bit; }
 
@@ -657,110 +706,143 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 }
 
 // ----------------------------------------------------------------------------
-// PREFILL item on the 5th-generation tensor cores: two Q tiles (A, B) of up to
-// 128 query rows each (token-major, q-head-in-group minor) of one chunk for
-// one kv head, causal over every history page and the chunk
-// ("Sarathi-Serve 完全拆解", §"分块不等于截断上下文").  Both tiles read the
-// same 128-key K/V blocks, so each block's TMA boxes (one per page and
-// 64-column half: 16-token pages allow no larger box in the swizzled layout
-// the tensor cores read) serve 256 query rows.
-//   S_T = Q_T K^T per block: tcgen05.mma (M 128, N 128, K 16 steps), fp32 in
-//       TMEM columns [128 T, 128 T + 128);
-//   softmax (warps 4T..4T+3, thread = query row = TMEM lane): one pass over
-//       the row's 128 scores in two halves of 64 (each half's max from the
+// PREFILL item on the 5th-generation tensor cores: one Q tile of up to 128
+// query rows (token-major, q-head-in-group minor) of one chunk for one kv
+// head, causal over every history page and the chunk ("Sarathi-Serve 完全拆解",
+// §"分块不等于截断上下文").  128-key blocks of K and V stream through shared
+// memory rings; tensor memory holds two score buffers, two P buffers and O:
+//   S(j) = Q K(j)^T: tcgen05.mma (M 128, N 128, K 16 steps, both operands in
+//       shared memory), fp32 into S buffer j & 1 (columns [128 b, 128 b + 128));
+//   softmax (warps 0-3, thread = query row = TMEM lane): one pass over the
+//       row's 128 scores in two halves of 64 (each half's max from the
 //       registers that then give its P), lazy rescale of O (only when the max
-//       grows by more than 2^8), bf16 P written over the first
-//       64 columns of S_T;
-//   O_T += P_T V: tcgen05.mma with A = P from TMEM and V read as an MN-major
-//       operand straight from the TMA-loaded pages; O_T in TMEM columns
-//       256 + T d until the end of the item.
-// MMAs issued by one thread run in order, so when S_T(j+1) is complete the
-// P.V of block j has read P_T and finished with O_T: the softmax needs no
-// other wait before it overwrites S_T or rescales O_T.
-// Roles: warps 8 and 9 are the TMA producers of the K and V rings (sixteen
-// lanes each, one box per lane: the whole 128-key block of a ring in one
-// instruction), warp 10 lane 0 issues the MMAs, warps 0-7 run the two
-// softmaxes and epilogues.  Eleven warps leave room for 168 registers a
-// thread (thirteen capped it at 128 and made the kernel spill).
+//       grows by more than 2^8), bf16 P into P buffer j & 1 (64 columns at
+//       384 + 64 b);
+//   O += P(j) V(j): tcgen05.mma with A = P from tensor memory and V read as an
+//       MN-major operand straight from the TMA-loaded pages; O in columns
+//       [256, 256 + d) until the end of the item.
+// The MMA issuer runs S(j + 2) and P(j).V(j) as soon as the softmax has
+// finished block j, so the tensor pipe holds the next block's scores while
+// the softmax works on this one; P has buffers of its own, so no MMA writes
+// tensor memory that an earlier MMA still reads.  MMAs issued by one thread
+// complete in order: a complete S(j + 2) means P(j).V(j) is done, which is
+// what makes P buffer j & 1 free again for block j + 2.
+// Roles: warps 8 and 9 are the TMA producers of the K and V rings (one box per
+// block when the block's pages are consecutive in the pool, else one box per
+// page and 64-column half), warp 10 lane 0 issues the MMAs, warps 0-3 run the
+// softmax and the epilogue; warps 0-7 and 10 rotate Q at the item's start.
 // ----------------------------------------------------------------------------
 constexpr int kTcKeys = 128;                     // keys per block
-constexpr int kTcTiles = kTilesPerItem;          // Q tiles per prefill item
 static_assert(kTcKeys == kTileRows, "a K/V block and a Q tile have the same shape");
 template <int D>
 struct PfLayout {
-    static constexpr int kTile = kTileRows * D * 2;   // bytes of one Q tile or one K/V block
-    static constexpr int kStages = D == 128 ? 2 : 4;  // depth of the K ring and of the V ring
-    static constexpr int kQ = 0;                      // Q tiles A, B: [d/64][128 rows][128 B] each
-    static constexpr int kK = kTcTiles * kTile;
-    static constexpr int kV = kK + kStages * kTile;
-    static_assert(kV + kStages * kTile <= kSmemStages, "prefill shared memory");
-    static_assert(kStages <= kPfStagesMax, "phase bits");
+    static constexpr int kTile = kTileRows * D * 2;    // bytes of the Q tile or of one K/V block
+    static constexpr int kKStages = D == 128 ? 3 : 4;  // K ring (runs two blocks ahead of V)
+    static constexpr int kVStages = D == 128 ? 2 : 4;  // V ring
+    static constexpr int kQ = 0;                       // Q tile: [d/64][128 rows][128 B]
+    static constexpr int kK = kTile;
+    static constexpr int kV = kK + kKStages * kTile;
+    static_assert(kV + kVStages * kTile <= kSmemStages, "prefill shared memory");
+    static_assert(kKStages <= kPfStagesMax && kVStages <= kPfStagesMax, "phase bits");
 };
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;     // S (then P) of tile T at 128 T
-constexpr uint32_t kTmemO = 256;   // O of tile T at 256 + T d
+constexpr uint32_t kTmemS = 0;     // S of block parity b at 128 b
+constexpr uint32_t kTmemO = 256;   // O
+constexpr uint32_t kTmemP = 384;   // bf16 P of block parity b at 384 + 64 b
 constexpr int kBarKFull = kDecWarps * kDecStages;   // kPfStagesMax
 constexpr int kBarKEmpty = kBarKFull + kPfStagesMax;
 constexpr int kBarVFull = kBarKEmpty + kPfStagesMax;
 constexpr int kBarVEmpty = kBarVFull + kPfStagesMax;
-constexpr int kBarSFull = kBarVEmpty + kPfStagesMax;  // 2 (per Q tile)
-constexpr int kBarPFull = kBarSFull + 2;               // 2 (per Q tile, 128 arrivals each)
-constexpr int kBarODone = kBarPFull + 2;               // 2 (per Q tile)
-constexpr int kBarDrain = kBarODone + 2;               // 1
-constexpr int kBarAppend = kBarDrain + 1;              // 1 (APPEND bulk copies)
-constexpr int kNumBars = kBarAppend + 1;
+constexpr int kBarSFull = kBarVEmpty + kPfStagesMax;  // 2 (per S buffer)
+constexpr int kBarPFull = kBarSFull + 2;               // 2 (per P buffer, 256 arrivals each)
+constexpr int kBarSFree = kBarPFull + 2;               // 2 (per S buffer: loaded by the softmax, 256 arrivals)
+constexpr int kBarOUp = kBarSFree + 2;                 // 2 (per P buffer: its P.V group done)
+constexpr int kBarODone = kBarOUp + 2;                 // 1 (one completion per item: its last P.V)
+constexpr int kBarDrain = kBarODone + 1;               // 2 (one per MMA-issuing thread)
+constexpr int kBarAppend = kBarDrain + 2;              // 1 (APPEND bulk copies)
+constexpr int kBarQ = kBarAppend + 1;                  // 1 (the Q tile's TMA boxes)
+constexpr int kNumBars = kBarQ + 1;
 static_assert(kNumBars * 8 <= 512, "barrier area");
 
 template <int D, bool IL>
-__device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUtensorMap* tmV, const int* it,
-                            uint8_t* smem, int* s_abort, PfPhase& ph, uint32_t tmem) {
+__device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                            const CUtensorMap* tmK5, const CUtensorMap* tmV5, const CUtensorMap* tmQ, const int* it,
+                            uint8_t* smem,
+                            int* s_abort, PfPhase& ph, uint32_t tmem) {
     using L = PfLayout<D>;
     constexpr int HALVES = D / 64;
     constexpr int HALF = D / 2;
-    constexpr int NST = L::kStages;
     constexpr int BLK_HALF = kTcKeys * 128;      // one 64-column half of a 128-key block
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = it[kS], g = it[kG], t0 = it[kStart], cnt = it[kCount];
     const Row R = row_geom(it);
     const int G = P.group;
-    const int tpt = kTileRows / G;               // tokens per Q tile
-    const int cA = min(cnt, tpt), cB = cnt - cA; // tokens of tiles A and B
-    const int ntile = cB > 0 ? 2 : 1;
     const int kv_hi = R.h + t0 + cnt;            // keys [0, kv_hi) are visible to some row
     const int nblk = (kv_hi + kTcKeys - 1) / kTcKeys;
-    const int nblkA = (R.h + t0 + cA + kTcKeys - 1) / kTcKeys;  // blocks tile A reads (a prefix)
     const int pages_hi = (kv_hi + kPage - 1) / kPage;
     const uint32_t bars = smem_u32(smem + kSmemBars);
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
     // The TMA producers (warps 8 and 9) start on the history pages at once; only
     // the blocks holding the chunk's own keys wait for this request's APPENDs.
-    // Meanwhile warps 0-7 and 10 write the Q tiles and meet on named barrier 5.
-    const bool q_writer = warp < 8 || warp == 10;
-    const int qtid = warp == 10 ? 256 + lane : tid;
-    constexpr int kQThreads = 288;
-    constexpr int kQUnits = kTileRows * (HALF / 8);  // per tile
-    // Q rows, RoPE'd in fp32 at their absolute positions, into the swizzled
-    // tiles; one thread rotates 8 consecutive pairs (two 16-byte chunks)
-    for (int i = q_writer ? qtid : ntile * kQUnits; i < ntile * kQUnits; i += kQThreads) {
-        const int T = i / kQUnits, rem = i % kQUnits;
-        const int row = rem / (HALF / 8), c = rem % (HALF / 8);
-        // 16-byte chunks holding pairs 8c..8c+7, and where their outputs go
-        const int c0 = IL ? 2 * c : c, c1 = IL ? 2 * c + 1 : c + HALF / 8;
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-        if (row < (T == 0 ? cA : cB) * G) {
-            const int t = t0 + T * tpt + row / G;
-            const int hq = g * G + row % G;
-            const int pos = R.h + t;
-            const __nv_bfloat16* qr = P.q + ((size_t)(R.qo0 + t) * P.Hq + hq) * D;
-            const uint4* qv = reinterpret_cast<const uint4*>(qr);
-            rope_q8(__ldg(qv + c0), __ldg(qv + c1), P.ropef + (size_t)pos * HALF + c * 8, IL, lo, hi);
-        }
-        uint8_t* qtile = smem + L::kQ + T * L::kTile;
-        *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c0)) = lo;
-        *reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c1)) = hi;
+    // Meanwhile warps 0-7, 10 and 11 write the Q tile and meet on named barrier 5.
+    const bool q_writer = warp < 8 || warp >= 10;
+    const int qtid = warp >= 10 ? 256 + (warp - 10) * 32 + lane : tid;
+    constexpr int kQThreads = 320;
+    constexpr int kQUnits = kTileRows * (HALF / 8);
+    // Q tile: two TMA boxes (one per 64-column half) bring the raw rows
+    // [tokens][heads of the group][d] of the item straight into the swizzled
+    // tile; meanwhile every writer loads the RoPE table values of its units
+    // (all at once), then rotates its 16-byte chunks in place in fp32.  One
+    // memory round trip for the whole tile.
+    if (warp == 11 && lane == 0) {
+        mbar_expect_tx(bar(kBarQ), (uint32_t)(HALVES * (kTileRows / G) * G * 128));
+        for (int hf = 0; hf < HALVES; ++hf)
+            tma_load_3d(smem_u32(smem + L::kQ + hf * kTileRows * 128), tmQ, hf * 64, g * G, R.qo0 + t0, bar(kBarQ));
     }
     if (q_writer) {
+        // units in rounds of two (registers): the first round's table values are
+        // loaded while the boxes fly, the later rounds' are prefetched into L2
+        constexpr int QU = (kQUnits + kQThreads - 1) / kQThreads;
+        const int rows_valid = cnt * G;
+        auto table_row = [&](int i) {
+            const int row = min(i / (HALF / 8), rows_valid - 1);  // rows past the tile's end are zeroed below
+            return P.ropef + (size_t)(R.h + t0 + row / G) * HALF * 4 + (i % (HALF / 8)) * kRopeChunk;
+        };
+#pragma unroll
+        for (int u = 2; u < QU; ++u) {
+            const int i = qtid + u * kQThreads;
+            if (i < kQUnits) asm volatile("prefetch.global.L2 [%0];" ::"l"(table_row(i)));
+        }
+        uint8_t* qtile = smem + L::kQ;
+#pragma unroll
+        for (int u0 = 0; u0 < QU; u0 += 2) {
+            float cs[2][8], sn[2][8];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = qtid + (u0 + u) * kQThreads;
+                if (u0 + u < QU && i < kQUnits) load_rope_hi(table_row(i), cs[u], sn[u]);
+            }
+            if (u0 == 0) {
+                mbar_wait_bounded(P, bar(kBarQ), ph_get(ph, kPhQ), s_abort, 500, it);
+                ph_flip(ph, kPhQ);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = qtid + (u0 + u) * kQThreads;
+                if (u0 + u < QU && i < kQUnits) {
+                    const int row = i / (HALF / 8), c = i % (HALF / 8);
+                    // 16-byte chunks holding pairs 8c..8c+7
+                    const int c0 = IL ? 2 * c : c, c1 = IL ? 2 * c + 1 : c + HALF / 8;
+                    uint4* p0 = reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c0));
+                    uint4* p1 = reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c1));
+                    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+                    if (row < rows_valid) rope_q8(*p0, *p1, cs[u], sn[u], IL, lo, hi);
+                    *p0 = lo;
+                    *p1 = hi;
+                }
+            }
+        }
         fence_proxy_async_shared();  // Q is read by the tensor cores (async proxy)
         tc_fence_before();
         asm volatile("bar.sync 5, %0;" ::"n"(kQThreads) : "memory");
@@ -770,44 +852,57 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
     if (warp == 8 || warp == 9) {
         // ---------------- TMA producers: warp 8 fills the K ring, warp 9 the V ring ----------------
         const bool is_v = warp == 9;
-        // lane 8 hf + q issues the box of page q of the block, column half hf:
-        // the whole block in one instruction
+        const int NST = is_v ? L::kVStages : L::kKStages;
+        // lane 8 hf + q holds the id of page q of the block; when the block's
+        // pages are not consecutive in the pool it issues the box of that page
+        // and column half hf
         const int hf = lane >> 3, pq = lane & 7;
         const bool issuer = hf < HALVES;
-        {
-            const CUtensorMap* map = is_v ? tmV : tmK;
-            const int full0 = is_v ? kBarVFull : kBarKFull;
-            const int empty0 = is_v ? kBarVEmpty : kBarKEmpty;
-            const int fill = is_v ? kPhVFill : kPhKFill;
-            uint8_t* ring = smem + (is_v ? L::kV : L::kK) + hf * BLK_HALF;
-            const int32_t* kvi = P.plan + P.off_kvi + R.kvp0;
-            int id = (issuer && pq < pages_hi) ? it[kIds + pq] : 0;  // block 0's ids come with the item
-            const int j_chunk = R.h / kTcKeys;  // first block with a key of the chunk
-            for (int j = 0; j < nblk; ++j) {
-                if (j == j_chunk) {
-                    // the chunk's K/V must be in the pages: this request's APPENDs
-                    const int need = P.plan[P.off_aux + s];
-                    const int* ctr = &P.ws_int[kHdrInts + s];
-                    if (lane == 0 && ld_acquire(ctr) < need) {
-                        const uint64_t w0 = globaltimer();
-                        while (ld_acquire(ctr) < need) {
-                            if (globaltimer() - w0 > kWaitNs / 2) {  // first to give up: names the cause
-                                raise_error(P, kErrWait, -1 - s, s_abort);
-                                break;
-                            }
-                            __nanosleep(100);
+        const CUtensorMap* map = is_v ? tmV : tmK;
+        const CUtensorMap* map5 = is_v ? tmV5 : tmK5;
+        const int full0 = is_v ? kBarVFull : kBarKFull;
+        const int empty0 = is_v ? kBarVEmpty : kBarKEmpty;
+        const int fill = is_v ? kPhVFill : kPhKFill;
+        uint8_t* ring = smem + (is_v ? L::kV : L::kK);
+        const int32_t* kvi = P.plan + P.off_kvi + R.kvp0;
+        int id = pq < pages_hi ? it[kIds + pq] : 0;  // block 0's ids come with the item
+        const int j_chunk = R.h / kTcKeys;  // first block with a key of the chunk
+        for (int j = 0; j < nblk; ++j) {
+            if (j == j_chunk) {
+                // the chunk's K/V must be in the pages: this request's APPENDs
+                const int need = P.plan[P.off_aux + s];
+                const int* ctr = &P.ws_int[kHdrInts + s];
+                if (lane == 0 && ld_acquire(ctr) < need) {
+                    const uint64_t w0 = globaltimer();
+                    while (ld_acquire(ctr) < need) {
+                        if (globaltimer() - w0 > kWaitNs / 2) {  // first to give up: names the cause
+                            raise_error(P, kErrWait, -1 - s, s_abort);
+                            break;
                         }
+                        __nanosleep(100);
                     }
-                    __syncwarp();
-                    (void)ld_acquire(ctr);      // every issuing lane acquires for itself
-                    fence_proxy_async_global();  // ... and orders the TMA reads after it
                 }
-                if (*(volatile int*)s_abort) break;
-                const int st = j % NST;
-                const int nxt = (issuer && (j + 1) * 8 + pq < pages_hi) ? kvi[(j + 1) * 8 + pq] : 0;
-                const int npg = min(kTcKeys / kPage, pages_hi - j * 8);
-                mbar_wait_bounded(P, bar(empty0 + st), ph_get(ph, fill + st) ^ 1u, s_abort, (is_v ? 2000 : 1000) + j,
-                                  it);
+                __syncwarp();
+                (void)ld_acquire(ctr);      // every issuing lane acquires for itself
+                fence_proxy_async_global();  // ... and orders the TMA reads after it
+            }
+            if (*(volatile int*)s_abort) break;
+            const int st = j % NST;
+            const int nxt = (j + 1) * 8 + pq < pages_hi ? kvi[(j + 1) * 8 + pq] : 0;
+            const int npg = min(kTcKeys / kPage, pages_hi - j * 8);
+            // one box for the whole block when its pages are consecutive and in the pool
+            const int id0 = __shfl_sync(0xffffffffu, id, 0);
+            const bool ok_page = pq >= npg || (id == id0 + pq && id >= 0 && id < P.num_pages);
+            const bool one_box = __all_sync(0xffffffffu, ok_page);
+            mbar_wait_bounded<true>(P, bar(empty0 + st), ph_get(ph, fill + st) ^ 1u, s_abort,
+                                    (is_v ? 2000 : 1000) + j, it);
+            uint8_t* dst = ring + st * L::kTile;
+            if (one_box) {
+                if (lane == 0) {
+                    mbar_expect_tx(bar(full0 + st), (uint32_t)L::kTile);
+                    tma_load_5d(smem_u32(dst), map5, 0, 0, g, id0, 0, bar(full0 + st));
+                }
+            } else {
                 if (lane == 0) mbar_expect_tx(bar(full0 + st), (uint32_t)(npg * HALVES) * kPageHalfBytes);
                 __syncwarp();
                 if (issuer && pq < npg) {
@@ -816,33 +911,33 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                         raise_error(P, kErrBounds, page, s_abort);
                         page = 0;
                     }
-                    tma_load_2d(smem_u32(ring + st * L::kTile + pq * kPageHalfBytes), map, hf * 64,
+                    tma_load_2d(smem_u32(dst + hf * BLK_HALF + pq * kPageHalfBytes), map, hf * 64,
                                 (page * P.Hkv + g) * kPage, bar(full0 + st));
                 }
-                __syncwarp();
-                ph_flip(ph, fill + st);
-                id = nxt;
             }
+            __syncwarp();
+            ph_flip(ph, fill + st);
+            id = nxt;
         }
-    } else if (warp == 10) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == 11) {
+        // ---------------- QK issuer: S(j) = Q K(j)^T into S buffer j & 1 ----------------
+        // S buffer j & 1 is free once the softmax has loaded block j - 2's scores
+        // (P has buffers of its own), so S(j) runs while block j - 2's softmax does
         if (lane == 0) {
             constexpr uint32_t idesc_s = umma_idesc(kTcKeys, false);
-            constexpr uint32_t idesc_o = umma_idesc(D, true);
-            const uint64_t qd0 = umma_desc(smem_u32(smem + L::kQ), 16, 1024);
-            const uint64_t qd1 = umma_desc(smem_u32(smem + L::kQ + L::kTile), 16, 1024);
-            int k_have = -1, v_have = -1;  // last block whose K / V load this thread has waited for
-            auto issue_qk = [&](int T, int j) {
-                const int st = j % NST;
-                if (k_have < j) {
-                    mbar_wait_bounded(P, bar(kBarKFull + st), ph_get(ph, kPhKUse + st), s_abort, 3000 + j, it);
-                    ph_flip(ph, kPhKUse + st);
-                    tc_fence_after();
-                    k_have = j;
+            const uint64_t qd = umma_desc(smem_u32(smem + L::kQ), 16, 1024);
+            for (int j = 0; j < nblk; ++j) {
+                const int b = j & 1;
+                if (j >= 2) {
+                    mbar_wait_bounded<true>(P, bar(kBarSFree + b), ph_get(ph, kPhSFree + b), s_abort, 4000 + j, it);
+                    ph_flip(ph, kPhSFree + b);
                 }
+                const int st = j % L::kKStages;
+                mbar_wait_bounded<true>(P, bar(kBarKFull + st), ph_get(ph, kPhKUse + st), s_abort, 3000 + j, it);
+                ph_flip(ph, kPhKUse + st);
+                tc_fence_after();
                 const uint64_t kd = umma_desc(smem_u32(smem + L::kK + st * L::kTile), 16, 1024);
-                const uint64_t qd = T ? qd1 : qd0;
-                const uint32_t sd = tmem + kTmemS + (uint32_t)(T * kTcKeys);
+                const uint32_t sd = tmem + kTmemS + (uint32_t)(b * kTcKeys);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     // start addresses advance in 16-byte units inside the descriptors
@@ -850,180 +945,188 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                     const uint64_t koff = (uint64_t)(((kk >> 2) * BLK_HALF + (kk & 3) * 32) >> 4);
                     umma_f16(sd, qd + off, kd + koff, idesc_s, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(bar(kBarSFull + T));
-                if (T == ntile - 1) umma_commit(bar(kBarKEmpty + st));  // its last reader
-            };
-            issue_qk(0, 0);
-            if (ntile > 1) issue_qk(1, 0);
+                umma_commit(bar(kBarSFull + b));
+                umma_commit(bar(kBarKEmpty + st));
+            }
+            // the loads of the item's last two blocks were not waited for here
+            for (int j = max(nblk - 2, 0); j < nblk; ++j) ph_flip(ph, kPhSFree + (j & 1));
+        }
+    } else if (warp == 10) {
+        // ---------------- P.V issuer: O += P(j) V(j) ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc_o = umma_idesc(D, true);
             for (int j = 0; j < nblk; ++j) {
-                const int vst = j % NST;
-                for (int T = 0; T < ntile; ++T) {
-                    if (j >= (T == 0 ? nblkA : nblk)) continue;
-                    mbar_wait_bounded(P, bar(kBarPFull + T), ph_get(ph, kPhPFull + T), s_abort, 4000 + j, it);
-                    ph_flip(ph, kPhPFull + T);
-                    if (v_have < j) {
-                        mbar_wait_bounded(P, bar(kBarVFull + vst), ph_get(ph, kPhVUse + vst), s_abort, 5000 + j, it);
-                        ph_flip(ph, kPhVUse + vst);
-                        v_have = j;
-                    }
-                    tc_fence_after();
-                    const uint64_t vd = umma_desc(smem_u32(smem + L::kV + vst * L::kTile), BLK_HALF, 1024);
-                    const uint32_t pa = tmem + kTmemS + (uint32_t)(T * kTcKeys);
+                const int b = j & 1;
+                const int vst = j % L::kVStages;
+                mbar_wait_bounded<true>(P, bar(kBarVFull + vst), ph_get(ph, kPhVUse + vst), s_abort, 5000 + j, it);
+                ph_flip(ph, kPhVUse + vst);
+                mbar_wait_bounded<true>(P, bar(kBarPFull + b), ph_get(ph, kPhPFull + b), s_abort, 4500 + j, it);
+                ph_flip(ph, kPhPFull + b);
+                tc_fence_after();
+                const uint64_t vd = umma_desc(smem_u32(smem + L::kV + vst * L::kTile), BLK_HALF, 1024);
+                const uint32_t pa = tmem + kTmemP + (uint32_t)(b * (kTcKeys / 2));
 #pragma unroll
-                    for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                        // A = P from TMEM (16 keys = 8 columns per step); B = V (MN-major:
-                        // d contiguous, keys as rows) straight from the TMA-loaded pages
-                        umma_f16_ts(tmem + kTmemO + (uint32_t)(T * D), pa + (uint32_t)(kk * 8),
-                                    vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    if (T == ntile - 1) umma_commit(bar(kBarVEmpty + vst));  // its last reader
-                    if (j + 1 < (T == 0 ? nblkA : nblk))
-                        issue_qk(T, j + 1);
-                    else
-                        umma_commit(bar(kBarODone + T));
+                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                    // A = P from TMEM (16 keys = 8 columns per step); B = V (MN-major:
+                    // d contiguous, keys as rows) straight from the TMA-loaded pages
+                    umma_f16_ts(tmem + kTmemO, pa + (uint32_t)(kk * 8), vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                                (j > 0 || kk > 0) ? 1u : 0u);
                 }
+                umma_commit(bar(kBarVEmpty + vst));
+                umma_commit(bar(kBarOUp + b));
+                if (j == nblk - 1) umma_commit(bar(kBarODone));
             }
         }
     } else if (warp < 8) {
-        // ---------------- softmax + epilogue: warps 4T..4T+3 own Q tile T ----------------
-        const int T = warp >> 2;
+        // ---------------- softmax + epilogue: warps q and q + 4 share query rows 32 q .. 32 q + 31 ----------------
+        // (a warp reaches the TMEM lanes of its SM sub-partition, so both see
+        // the same rows); warp q takes keys 0-63 of each block, warp q + 4 keys
+        // 64-127, and the pair agree on the exponent base through shared memory
+        const int hs = warp >> 2;                    // key half of the block (and of P, and of O's columns)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;              // query row = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        // the last block's stale V rows are zeroed by the tile that reads it first
-        const int zero_tile = nblkA == nblk ? 0 : 1;
-        if (T < ntile) {
-            const int cT = T == 0 ? cA : cB;
-            const int rows_valid = cT * G;
-            const int tt = T * tpt + (r < rows_valid ? r / G : cT - 1);  // item-local token of the row
-            const int pos_r = R.h + t0 + tt;
-            const int nT = T == 0 ? nblkA : nblk;
-            const uint32_t s_col = kTmemS + (uint32_t)(T * kTcKeys);
-            const uint32_t o_col = kTmemO + (uint32_t)(T * D);
-            const float sl2 = P.scale_log2;
-            float m_run = -INFINITY, l_run = 0.f;
-            for (int j = 0; j < nT; ++j) {
-                const int kb0 = j * kTcKeys;
-                mbar_wait_bounded(P, bar(kBarSFull + T), ph_get(ph, kPhSUse + T), s_abort, 6000 + j, it);
-                ph_flip(ph, kPhSUse + T);
-                tc_fence_after();
-                // One pass over the row's 128 scores, 64 at a time: each half's max
-                // comes from the registers it is loaded into, and the exponent base
-                // moves only when a half's max exceeds it by more than 2^8 (lazy
-                // rescaling).  When the second half moves it, the first half's P,
-                // already written in bf16, is rescaled in place (warp-wide; rare
-                // after a tile's first block).
-                float2 sum2 = make_float2(0.f, 0.f);
-                const float2 sl2v = make_float2(sl2, sl2);
-                float m_use = m_run;  // exponent base of this block's P
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    float v[64];
-                    tmem_ld32_nw(lane_base + s_col + (uint32_t)(h * 64), v);
-                    tmem_ld32_nw(lane_base + s_col + (uint32_t)(h * 64 + 32), v + 32);
-                    tmem_wait_ld(v);
-                    const int kc = kb0 + h * 64;
-                    if (kc + 63 > pos_r) {
-#pragma unroll
-                        for (int e = 0; e < 64; ++e) v[e] = kc + e <= pos_r ? v[e] : -INFINITY;
-                    }
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < 64; e += 2) mx = fmax3(mx, v[e], v[e + 1]);
-                    const float mxs = mx * sl2;  // raw scores; the scale (> 0) applied to the max
-                    const bool grow = mxs > m_use + 8.f;
-                    if (h == 1 && __any_sync(0xffffffffu, grow)) {
-                        const float a = grow ? exp2f(m_use - mxs) : 1.f;
-                        sum2.x *= a;
-                        sum2.y *= a;
-                        tmem_wait_st();
-#pragma unroll 1
-                        for (int q = 0; q < 2; ++q) {
-                            uint32_t pw[16];
-                            tmem_ld16(lane_base + s_col + (uint32_t)(q * 16), pw);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                pw[i] = pack_bf16(__uint_as_float(pw[i] << 16) * a,
-                                                  __uint_as_float(pw[i] & 0xFFFF0000u) * a);
-                            tmem_st16_nw(lane_base + s_col + (uint32_t)(q * 16), pw);
-                        }
-                    }
-                    if (grow) m_use = mxs;
-                    // P = 2^(s - m) in bf16, two keys per column, over the first 64
-                    // columns of S (half h's columns are written after half h and
-                    // every column below it have been read)
-                    const float2 nmv = make_float2(-m_use, -m_use);
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const float2 x = ffma2(make_float2(v[q * 32 + e], v[q * 32 + e + 1]), sl2v, nmv);
-                            const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                            sum2 = fadd2(sum2, pp);
-                            pk[e >> 1] = pack_bf16(pp.x, pp.y);
-                        }
-                        tmem_st16_nw(lane_base + s_col + (uint32_t)(h * 32 + q * 16), pk);
-                    }
-                }
-                tmem_wait_st();
-                // O and l hold sums with base m_run: bring them to m_use
-                const bool moved = m_use != m_run;
-                const float alpha = moved ? exp2f(m_run - m_use) : 1.f;
-                if (j > 0 && __any_sync(0xffffffffu, moved)) {
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(lane_base + o_col + (uint32_t)(c * 32), o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                        tmem_st32(lane_base + o_col + (uint32_t)(c * 32), o);
-                    }
-                }
-                l_run = l_run * alpha + (sum2.x + sum2.y);
-                m_run = m_use;
-                // last block: V rows past kv_hi hold stale bytes; zero them so 0 x V stays 0
-                if (T == zero_tile && j == nblk - 1 && kb0 + kTcKeys > kv_hi) {
-                    const int vst = j % NST;
-                    mbar_wait_bounded(P, bar(kBarVFull + vst), ph_get(ph, kPhVSeen + vst) ^ (uint32_t)((j / NST) & 1),
-                                      s_abort, 8000 + j, it);
-                    uint8_t* vb = smem + L::kV + vst * L::kTile;
-                    const int first = kv_hi - kb0;
-                    for (int hf = 0; hf < HALVES; ++hf)
-                        for (int i = first * 128 + (tid & 127) * 16; i < kTcKeys * 128; i += 128 * 16)
-                            *reinterpret_cast<uint4*>(vb + hf * BLK_HALF + i) = make_uint4(0, 0, 0, 0);
-                    fence_proxy_async_shared();
-                }
-                tc_fence_before();
-                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull + T)) : "memory");
-            }
-            // epilogue: O / l -> bf16, one row per thread
-            mbar_wait_bounded(P, bar(kBarODone + T), ph_get(ph, kPhODone + T), s_abort, 9000, it);
-            ph_flip(ph, kPhODone + T);
+        const int rows_valid = cnt * G;
+        const int tt = r < rows_valid ? r / G : cnt - 1;  // item-local token of the row
+        const int pos_r = R.h + t0 + tt;
+        const float sl2 = P.scale_log2;
+        // [block parity][key half][row] maxima, then [key half][row] sums
+        float* xmax = reinterpret_cast<float*>(smem + kSmemDecQ);
+        float* xsum = xmax + 2 * 2 * kTileRows;
+        const uint32_t pair_bar = 6u + (uint32_t)quad;   // named barrier of warps q and q + 4
+        constexpr int OCOLS = D / 2;                 // O columns this warp rescales and stores
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int j = 0; j < nblk; ++j) {
+            const int b = j & 1;
+            const int kc = j * kTcKeys + hs * 64;    // first key of this warp's half
+            const uint32_t s_col = kTmemS + (uint32_t)(b * kTcKeys + hs * 64);
+            const uint32_t p_col = kTmemP + (uint32_t)(b * (kTcKeys / 2) + hs * 32);
+            mbar_wait_bounded(P, bar(kBarSFull + b), ph_get(ph, kPhSUse + b), s_abort, 6000 + j, it);
+            ph_flip(ph, kPhSUse + b);
             tc_fence_after();
-            const float inv = 1.f / l_run;
-            __nv_bfloat16* dst =
-                r < rows_valid ? P.out + ((size_t)(R.qo0 + t0 + tt) * P.Hq + g * G + r % G) * D : nullptr;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                tmem_ld32(lane_base + o_col + (uint32_t)(c * 32), o);
-                if (dst) {
+            float v[64];
+            tmem_ld32_nw(lane_base + s_col, v);
+            tmem_ld32_nw(lane_base + s_col + 32u, v + 32);
+            tmem_wait_ld(v);
+            // the scores are in registers: S buffer b may take S(j + 2)
+            tc_fence_before();
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarSFree + b)) : "memory");
+            if (kc + 63 > pos_r) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) =
-                            make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
-                                       pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                                       pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                                       pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+                for (int e = 0; e < 64; ++e) v[e] = kc + e <= pos_r ? v[e] : -INFINITY;
+            }
+            // the half's max in four independent chains
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int e = 0; e < 64; e += 8) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mq[c] = fmax3(mq[c], v[e + 2 * c], v[e + 2 * c + 1]);
+            }
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            xmax[(b * 2 + hs) * kTileRows + r] = mx;
+            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+            const float mxs = fmaxf(mx, xmax[(b * 2 + (hs ^ 1)) * kTileRows + r]) * sl2;  // the scale (> 0) applied to the max
+            // lazy rescaling: the exponent base moves only when the block's max
+            // exceeds it by more than 2^8 (both warps of the pair decide alike)
+            const float m_use = mxs > m_run + 8.f ? mxs : m_run;
+            if (j >= 2) {
+                // P buffer b was read by P(j - 2).V, issued by another thread
+                // than this block's S: wait for it before overwriting
+                mbar_wait_bounded(P, bar(kBarOUp + b), ph_get(ph, kPhOUp + b), s_abort, 6500 + j, it);
+                ph_flip(ph, kPhOUp + b);
+                tc_fence_after();
+            }
+            // P = 2^(s - m) in bf16, two keys per column
+            float2 sum2 = make_float2(0.f, 0.f);
+            const float2 sl2v = make_float2(sl2, sl2);
+            const float2 nmv = make_float2(-m_use, -m_use);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float2 x = ffma2(make_float2(v[q * 32 + e], v[q * 32 + e + 1]), sl2v, nmv);
+                    const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    sum2 = fadd2(sum2, pp);
+                    pk[e >> 1] = pack_bf16(pp.x, pp.y);
                 }
+                tmem_st16_nw(lane_base + p_col + (uint32_t)(q * 16), pk);
+            }
+            tmem_wait_st();
+            // O and l hold sums with base m_run: bring them to m_use.  O holds
+            // the P.V groups of blocks before j; the last of them may still be
+            // running, so wait for it first (rare: only when the base moves).
+            // P(j - 3).V is done (block j - 1 waited for it) and P(j + 1).V is
+            // not issued, so the wait on buffer (j - 1) & 1 is for P(j - 1).V;
+            // block j + 1 waits for the same phase again and counts it.
+            const bool moved = m_use != m_run;
+            const float alpha = moved ? exp2f(m_run - m_use) : 1.f;
+            if (j > 0 && __any_sync(0xffffffffu, moved)) {
+                mbar_wait_bounded(P, bar(kBarOUp + ((j - 1) & 1)), ph_get(ph, kPhOUp + ((j - 1) & 1)), s_abort,
+                                  7000 + j, it);
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < OCOLS / 32; ++c) {
+                    float o[32];
+                    const uint32_t oc = kTmemO + (uint32_t)(hs * OCOLS + c * 32);
+                    tmem_ld32(lane_base + oc, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                    tmem_st32(lane_base + oc, o);
+                }
+            }
+            l_run = l_run * alpha + (sum2.x + sum2.y);
+            m_run = m_use;
+            // last block: V rows past kv_hi hold other bytes; zero them so 0 x V stays 0
+            if (j == nblk - 1 && j * kTcKeys + kTcKeys > kv_hi) {
+                const int vst = j % L::kVStages;
+                mbar_wait_bounded(P, bar(kBarVFull + vst),
+                                  ph_get(ph, kPhVSeen + vst) ^ (uint32_t)((j / L::kVStages) & 1), s_abort, 8000 + j,
+                                  it);
+                uint8_t* vb = smem + L::kV + vst * L::kTile;
+                const int first = kv_hi - j * kTcKeys;
+                for (int hf = 0; hf < HALVES; ++hf)
+                    for (int i = first * 128 + tid * 16; i < kTcKeys * 128; i += 256 * 16)
+                        *reinterpret_cast<uint4*>(vb + hf * BLK_HALF + i) = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_shared();
             }
             tc_fence_before();
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull + b)) : "memory");
         }
-        // every softmax thread keeps count of the item's V loads per stage
+        // epilogue: O / l -> bf16 once the last P.V group is done (a barrier of
+        // its own: when it is waited for, two P.V groups may be outstanding,
+        // which a parity wait on the per-buffer barriers cannot tell apart);
+        // each warp of the pair adds the other's part of l and stores half of
+        // the row's columns
+        mbar_wait_bounded(P, bar(kBarODone), ph_get(ph, kPhODone), s_abort, 9000, it);
+        ph_flip(ph, kPhODone);
+        tc_fence_after();
+        xsum[hs * kTileRows + r] = l_run;
+        asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+        const float inv = 1.f / (l_run + xsum[(hs ^ 1) * kTileRows + r]);
+        __nv_bfloat16* dst =
+            r < rows_valid ? P.out + ((size_t)(R.qo0 + t0 + tt) * P.Hq + g * G + r % G) * D + hs * OCOLS : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < OCOLS / 32; ++c) {
+            float o[32];
+            tmem_ld32(lane_base + kTmemO + (uint32_t)(hs * OCOLS + c * 32), o);
+            if (dst) {
 #pragma unroll
-        for (int st = 0; st < NST; ++st)
-            if (((nblk - st + NST - 1) / NST) & 1) ph_flip(ph, kPhVSeen + st);
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) =
+                        make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                   pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                   pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                   pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+            }
+        }
+        tc_fence_before();
+        // carried across items: the P.V groups not waited for above (the last
+        // two blocks'), and the V loads per stage of this item
+        for (int j = max(nblk - 2, 0); j < nblk; ++j) ph_flip(ph, kPhOUp + (j & 1));
+#pragma unroll
+        for (int st = 0; st < L::kVStages; ++st)
+            if (((nblk - st + L::kVStages - 1) / L::kVStages) & 1) ph_flip(ph, kPhVSeen + st);
     }
 }
 
@@ -1090,7 +1193,9 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if (row < G) {
             const uint4* qv = reinterpret_cast<const uint4*>(P.q + ((size_t)R.qo0 * P.Hq + g * G + row) * D);
-            rope_q8(__ldg(qv + c0), __ldg(qv + c1), P.ropef + (size_t)pos * HALF + c * 8, IL, lo, hi);
+            float cs[8], sn[8];
+            load_rope_hi(P.ropef + (size_t)pos * HALF * 4 + c * kRopeChunk, cs, sn);
+            rope_q8(__ldg(qv + c0), __ldg(qv + c1), cs, sn, IL, lo, hi);
         }
         *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c0)) = lo;
         *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c1)) = hi;
@@ -1107,7 +1212,9 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
             uint16_t y0 = 0, y1 = 0;
             if (ok) {
                 const size_t ti = (size_t)pos * HALF + j;
-                rope_pair(bf16_bits_to_float(kr[i0]), bf16_bits_to_float(kr[i1]), P.ropef[ti], P.rope + ti, y0, y1);
+                rope_pair(bf16_bits_to_float(kr[i0]), bf16_bits_to_float(kr[i1]),
+                          rope_chunk_pair(P.ropef + (size_t)pos * HALF * 4 + (j >> 3) * kRopeChunk, j & 7), P.rope + ti,
+                          y0, y1);
                 reinterpret_cast<uint16_t*>(P.k_cache)[off + i0] = y0;
                 reinterpret_cast<uint16_t*>(P.k_cache)[off + i1] = y1;
             }
@@ -1310,7 +1417,10 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap tmK,
                                                                  const __grid_constant__ CUtensorMap tmV,
                                                                  const __grid_constant__ CUtensorMap tmK3,
-                                                                 const __grid_constant__ CUtensorMap tmV3) {
+                                                                 const __grid_constant__ CUtensorMap tmV3,
+                                                                 const __grid_constant__ CUtensorMap tmK5,
+                                                                 const __grid_constant__ CUtensorMap tmV5,
+                                                                 const __grid_constant__ CUtensorMap tmQ) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(16) int s_item[kItemInts];
@@ -1325,7 +1435,8 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         s_app_phase = 0;
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == kBarPFull || i == kBarPFull + 1) count = 128;  // the tile's softmax threads
+            if (i == kBarPFull || i == kBarPFull + 1 || i == kBarSFree || i == kBarSFree + 1)
+                count = 256;  // the tile's softmax threads
             mbar_init(bars + 8 * i, count);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1386,7 +1497,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
                 tmem_held = true;
                 tmem = s_tmem;
             }
-            run_prefill<D, IL>(P, &tmK, &tmV, it, smem, &s_abort, pf_phase, tmem);
+            run_prefill<D, IL>(P, &tmK, &tmV, &tmK5, &tmV5, &tmQ, it, smem, &s_abort, pf_phase, tmem);
         }
         else
             run_decode<D, IL>(P, &tmK3, &tmV3, it, smem, &s_abort, &s_flag, dec_phase);
@@ -1400,10 +1511,12 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
     }
     if (tmem_held) {
         // no tensor-core work may be in flight when the tensor memory is released
-        if (tid == 10 * 32) {
-            umma_commit(bars + 8 * kBarDrain);
+        // (each MMA-issuing thread's commit covers the MMAs it issued)
+        if (tid == 10 * 32 || tid == 11 * 32) {
+            const uint32_t db = bars + 8 * (kBarDrain + (tid == 11 * 32 ? 1 : 0));
+            umma_commit(db);
             const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(bars + 8 * kBarDrain, 0))
+            while (!mbar_try_wait(db, 0))
                 if (globaltimer() - t0 > kWaitNs) break;
         }
         tc_fence_before();
@@ -1438,7 +1551,7 @@ struct InvFreq {
     double v[64];
 };
 
-__global__ void rope_table_kernel(double2* table, float4* split, int max_pos, int half, const InvFreq f) {
+__global__ void rope_table_kernel(double2* table, float* split, int max_pos, int half, const InvFreq f) {
     const int64_t total = (int64_t)max_pos * half;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int p = (int)(i / half), j = (int)(i % half);
@@ -1447,7 +1560,13 @@ __global__ void rope_table_kernel(double2* table, float4* split, int max_pos, in
         sincos(th, &sn, &cs);
         table[i] = make_double2(cs, sn);
         const float ch = __double2float_rn(cs), sh = __double2float_rn(sn);
-        split[i] = make_float4(ch, __double2float_rn(cs - (double)ch), sh, __double2float_rn(sn - (double)sh));
+        // chunk of pairs 8c..8c+7: cos_hi[8], sin_hi[8], cos_lo[8], sin_lo[8]
+        float* chunk = split + (size_t)p * half * 4 + (j >> 3) * kRopeChunk;
+        const int e = j & 7;
+        chunk[e] = ch;
+        chunk[8 + e] = sh;
+        chunk[16 + e] = __double2float_rn(cs - (double)ch);
+        chunk[24 + e] = __double2float_rn(sn - (double)sh);
     }
 }
 
@@ -1516,6 +1635,49 @@ int32_t make_page_map3(CUtensorMap* m, void* base, int num_pages, int Hkv, int d
     return SARATHI_OK;
 }
 
+// 5-D view of the same pool: {64 columns, 16 slots, H_kv heads, pages, d/64
+// halves} (strides 2 B, d*2, 16*d*2, H_kv*16*d*2 and 128 B).  Box = 64 x 16 x
+// 1 x 8 x d/64: eight consecutive pages of one kv head (a whole 128-key block)
+// in one copy, landing as [half][page][16 rows][128 B] like eight 2-D boxes.
+int32_t make_page_map5(CUtensorMap* m, void* base, int num_pages, int Hkv, int d) {
+    auto enc = encode_fn();
+    if (!enc) return fail(SARATHI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[5] = {64, (cuuint64_t)kPage, (cuuint64_t)Hkv, (cuuint64_t)num_pages, (cuuint64_t)(d / 64)};
+    cuuint64_t strides[4] = {(cuuint64_t)d * 2, (cuuint64_t)kPage * d * 2, (cuuint64_t)Hkv * kPage * d * 2, 128};
+    cuuint32_t box[5] = {64, (cuuint32_t)kPage, 1, (cuuint32_t)(kTileRows / kPage), (cuuint32_t)(d / 64)};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[128];
+        std::snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled (5-D page view) failed (%d)", (int)r);
+        return fail(SARATHI_ERR_CUDA, msg);
+    }
+    return SARATHI_OK;
+}
+
+// 3-D view of the step's queries q[T][H_q][d]: {d, H_q heads, T tokens}.  Box =
+// 64 x G x (128 / G): the rows (token, q head of one GQA group) of one Q tile,
+// token-major, landing as one 64-column half of the swizzled tile.
+int32_t make_q_map(CUtensorMap* m, const void* q, int T, int Hq, int d, int G) {
+    auto enc = encode_fn();
+    if (!enc) return fail(SARATHI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hq, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)Hq * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)tokens_per_tile(G)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[128];
+        std::snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled (query view) failed (%d)", (int)r);
+        return fail(SARATHI_ERR_CUDA, msg);
+    }
+    return SARATHI_OK;
+}
+
 // The step kernel instantiation for a head size and RoPE pairing.
 const void* kernel_for(int d, int rope_style) {
     const bool il = rope_style == SARATHI_ROPE_INTERLEAVED;
@@ -1540,8 +1702,8 @@ using namespace sarathi;
 extern "C" int32_t sarathi_rope_table(double* table, int32_t max_pos, int32_t head_dim, double rope_theta,
                                       void* cuda_stream) {
     if (!table || max_pos <= 0) return fail(SARATHI_ERR_INVALID_ARG, "table NULL or max_pos <= 0");
-    if (head_dim <= 0 || (head_dim & 1) || head_dim / 2 > 64)
-        return fail(SARATHI_ERR_UNSUPPORTED, "head_dim must be even and <= 128");
+    if (head_dim <= 0 || (head_dim & 15) || head_dim / 2 > 64)
+        return fail(SARATHI_ERR_UNSUPPORTED, "head_dim must be a multiple of 16 and <= 128");
     if (!(rope_theta > 0.0)) return fail(SARATHI_ERR_INVALID_ARG, "rope_theta must be positive");
     InvFreq f;
     std::memset(&f, 0, sizeof f);
@@ -1549,7 +1711,7 @@ extern "C" int32_t sarathi_rope_table(double* table, int32_t max_pos, int32_t he
     const int64_t total = (int64_t)max_pos * (head_dim / 2);
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, 8192);
     rope_table_kernel<<<blocks, 256, 0, (cudaStream_t)cuda_stream>>>(
-        reinterpret_cast<double2*>(table), reinterpret_cast<float4*>(table + (size_t)max_pos * head_dim), max_pos,
+        reinterpret_cast<double2*>(table), reinterpret_cast<float*>(table + (size_t)max_pos * head_dim), max_pos,
         head_dim / 2, f);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "rope_table launch");
@@ -1641,6 +1803,14 @@ int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void*
     if (st) return st;
     st = make_page_map(&tmV, a->v_cache, a->num_pages, Hkv, d);
     if (st) return st;
+    CUtensorMap tmQ;
+    st = make_q_map(&tmQ, a->q, in->num_tokens, a->shape.num_heads_q, d, a->shape.num_heads_q / Hkv);
+    if (st) return st;
+    CUtensorMap tmK5, tmV5;
+    st = make_page_map5(&tmK5, a->k_cache, a->num_pages, Hkv, d);
+    if (st) return st;
+    st = make_page_map5(&tmV5, a->v_cache, a->num_pages, Hkv, d);
+    if (st) return st;
     CUtensorMap tmK3 = tmK, tmV3 = tmV;
     if (d == 128) {
         st = make_page_map3(&tmK3, a->k_cache, a->num_pages, Hkv, d);
@@ -1667,7 +1837,7 @@ int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void*
     P.n_first = in->n_first;
     P.n_sched = in->n_sched;
     P.rope = reinterpret_cast<const double2*>(a->rope_table);
-    P.ropef = reinterpret_cast<const float4*>(a->rope_table + (size_t)a->rope_max_pos * d);
+    P.ropef = reinterpret_cast<const float*>(a->rope_table + (size_t)a->rope_max_pos * d);
     P.rope_max_pos = a->rope_max_pos;
     P.ws_int = static_cast<int32_t*>(a->workspace);
     P.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) +
@@ -1707,13 +1877,13 @@ int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void*
     }
     const bool il = a->rope_style == SARATHI_ROPE_INTERLEAVED;
     if (d == 128 && !il)
-        mixed_step_kernel<128, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
+        mixed_step_kernel<128, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ);
     else if (d == 128)
-        mixed_step_kernel<128, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
+        mixed_step_kernel<128, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ);
     else if (!il)
-        mixed_step_kernel<64, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
+        mixed_step_kernel<64, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ);
     else
-        mixed_step_kernel<64, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3);
+        mixed_step_kernel<64, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "mixed_step_kernel launch");
     if (io) {

@@ -74,8 +74,8 @@ int32_t validate_requests(const sarathi_request* reqs, int32_t n_reqs) {
 // at tensor-core speed; a decode split a fixed start plus its pages at an
 // equal share of HBM bandwidth (every SM streaming), or at one SM's own rate
 // while fewer SMs stream than saturate HBM.
-constexpr double kPrefillFixedNs = 8000.0;
-constexpr double kPrefillFlopPerNs = 6000.0;
+constexpr double kPrefillFixedNs = 6500.0;
+constexpr double kPrefillFlopPerNs = 9000.0;
 constexpr double kDecodeFixedNs = 2000.0;
 constexpr double kDecodeBytesPerNs = 40.0;       // a decode split's share of HBM with every SM streaming
 constexpr double kDecodeAloneBytesPerNs = 80.0;  // one SM's own streaming rate when HBM has room

@@ -64,8 +64,7 @@ inline int64_t partial_offset_bytes(int n_sched, int n_merge) {
 inline int64_t partial_slot_floats(int group, int d) { return (int64_t)group * (d + 2); }
 
 inline int tokens_per_tile(int group) { return group >= kTileRows ? 1 : kTileRows / group; }
-// A prefill item holds up to kTilesPerItem Q tiles that share each K/V block.
-constexpr int kTilesPerItem = 2;
-inline int tokens_per_item(int group) { return kTilesPerItem * tokens_per_tile(group); }
+// A prefill item is one Q tile.
+inline int tokens_per_item(int group) { return tokens_per_tile(group); }
 
 }  // namespace sarathi
