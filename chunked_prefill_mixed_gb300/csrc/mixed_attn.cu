@@ -60,7 +60,7 @@ struct KParams {
     int n_items, n_sched;
     int n_first, first_sms;   // the work list's two queues (see the kernel's claim loop)
     const double2* rope;  // [max_pos][d/2] {cos, sin} in fp64
-    const float* ropef;   // [max_pos][d/16][32]: per 8 pairs cos_hi[8], sin_hi[8], cos_lo[8], sin_lo[8] (cos = hi + lo to ~2^-48)
+    const float* ropef;   // [max_pos][4][d/2]: cos_hi, sin_hi, cos_lo, sin_lo rows (cos = hi + lo to ~2^-48)
     int rope_max_pos;
     int32_t* ws_int;      // header, append counters, merge tickets
     float* ws_part;       // split partials
@@ -392,12 +392,12 @@ __device__ __forceinline__ uint16_t rope_bf16(float a, float b, float p_hi, floa
     const double2 c = *pq;  // fp64 {cos, sin}: read only on this rare path
     return bf16_from_double(__dadd_rn(__dmul_rn((double)a, c.x), __dmul_rn((double)b, c.y)));
 }
-// fp32 RoPE table: the 8 pairs 8c..8c+7 of one position form a chunk of 32
-// floats, cos_hi[8], sin_hi[8], cos_lo[8], sin_lo[8], so that a query unit
-// (which needs only the hi parts) loads 64 contiguous bytes.
-constexpr int kRopeChunk = 32;
-__device__ __forceinline__ float4 rope_chunk_pair(const float* ch, int e) {
-    return make_float4(ch[e], ch[16 + e], ch[8 + e], ch[24 + e]);  // {cos_hi, cos_lo, sin_hi, sin_lo}
+// fp32 RoPE table: each position's row holds cos_hi[d/2], sin_hi[d/2],
+// cos_lo[d/2], sin_lo[d/2], so that the hi parts the queries need are the
+// first half of the row (one TMA box fetches them for a whole Q tile).
+template <int HALF>
+__device__ __forceinline__ float4 rope_row_pair(const float* row, int j) {
+    return make_float4(row[j], row[2 * HALF + j], row[HALF + j], row[3 * HALF + j]);  // {cos_hi, cos_lo, sin_hi, sin_lo}
 }
 __device__ __forceinline__ void rope_pair(float x0, float x1, float4 cf, const double2* cs, uint16_t& y0,
                                           uint16_t& y1) {
@@ -406,6 +406,7 @@ __device__ __forceinline__ void rope_pair(float x0, float x1, float4 cf, const d
 }
 // Interleaved pairing: a holds dims 2j0..2j0+7 (pairs j0..j0+3), b the next
 // eight (pairs j0+4..j0+7); the outputs replace them in place.
+template <int HALF>
 __device__ __forceinline__ void rope8_interleaved(uint4 a, uint4 b, const float* ch, const double2* fb, uint4& oa,
                                                   uint4& ob) {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -413,8 +414,8 @@ __device__ __forceinline__ void rope8_interleaved(uint4 a, uint4 b, const float*
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
         uint16_t y0, y1;
-        rope_pair(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xFFFF0000u), rope_chunk_pair(ch, p), fb + p, y0,
-                  y1);
+        rope_pair(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xFFFF0000u), rope_row_pair<HALF>(ch, p), fb + p,
+                  y0, y1);
         o[p] = (uint32_t)y0 | ((uint32_t)y1 << 16);
     }
     oa = make_uint4(o[0], o[1], o[2], o[3]);
@@ -422,15 +423,16 @@ __device__ __forceinline__ void rope8_interleaved(uint4 a, uint4 b, const float*
 }
 // Eight consecutive pairs (x0 = a, x1 = b, 8 bf16 each) of one key row:
 // lo = first-half outputs, hi = second-half outputs.
+template <int HALF>
 __device__ __forceinline__ void rope8(uint4 a, uint4 b, const float* ch, const double2* fb, uint4& lo, uint4& hi) {
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
     uint32_t w0[4], w1[4];
 #pragma unroll
     for (int e2 = 0; e2 < 4; ++e2) {
         uint16_t lo0, lo1, hi0, hi1;
-        rope_pair(__uint_as_float(aw[e2] << 16), __uint_as_float(bw[e2] << 16), rope_chunk_pair(ch, 2 * e2), fb + 2 * e2,
-                  lo0, lo1);
-        rope_pair(__uint_as_float(aw[e2] & 0xFFFF0000u), __uint_as_float(bw[e2] & 0xFFFF0000u), rope_chunk_pair(ch, 2 * e2 + 1),
+        rope_pair(__uint_as_float(aw[e2] << 16), __uint_as_float(bw[e2] << 16), rope_row_pair<HALF>(ch, 2 * e2),
+                  fb + 2 * e2, lo0, lo1);
+        rope_pair(__uint_as_float(aw[e2] & 0xFFFF0000u), __uint_as_float(bw[e2] & 0xFFFF0000u), rope_row_pair<HALF>(ch, 2 * e2 + 1),
                   fb + 2 * e2 + 1, hi0, hi1);
         w0[e2] = (uint32_t)lo0 | ((uint32_t)hi0 << 16);
         w1[e2] = (uint32_t)lo1 | ((uint32_t)hi1 << 16);
@@ -469,10 +471,13 @@ __device__ __forceinline__ void rope_q8(uint4 a, uint4 b, const float (&c)[8], c
     lo = make_uint4(ylo[0], ylo[1], ylo[2], ylo[3]);
     hi = make_uint4(yhi[0], yhi[1], yhi[2], yhi[3]);
 }
-// cos_hi and sin_hi of one table chunk (8 pairs) from global memory.
-__device__ __forceinline__ void load_rope_hi(const float* ch, float (&c)[8], float (&s)[8]) {
-    const float4* v = reinterpret_cast<const float4*>(ch);
-    const float4 c0 = __ldg(v), c1 = __ldg(v + 1), s0 = __ldg(v + 2), s1 = __ldg(v + 3);
+// cos_hi and sin_hi of pairs j0..j0+7 of one table row (global or shared
+// memory; the row's first d/2 floats are cos_hi, the next d/2 sin_hi).
+template <int HALF>
+__device__ __forceinline__ void load_rope_hi(const float* row, int j0, float (&c)[8], float (&s)[8]) {
+    const float4* vc = reinterpret_cast<const float4*>(row + j0);
+    const float4* vs = reinterpret_cast<const float4*>(row + HALF + j0);
+    const float4 c0 = vc[0], c1 = vc[1], s0 = vs[0], s1 = vs[1];
     c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w; c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
     s[0] = s0.x; s[1] = s0.y; s[2] = s0.z; s[3] = s0.w; s[4] = s1.x; s[5] = s1.y; s[6] = s1.z; s[7] = s1.w;
 }
@@ -539,17 +544,17 @@ __device__ void run_append(const KParams& P, const int* it, uint8_t* smem, uint3
                 }
                 const uint16_t* krow = ks + ((size_t)tl * Hkv + g) * D;
                 uint16_t* drow = kc + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D;
-                const float* cf = rs + (size_t)tl * HALF * 4 + j8 * kRopeChunk;
+                const float* cf = rs + (size_t)tl * HALF * 4 + j8 * 8;
                 const double2* fb = P.rope + (size_t)pos * HALF + j8 * 8;
                 // pairs 8 j8 .. 8 j8 + 7: dims (j, j + d/2), or (2j, 2j + 1) interleaved
                 const int d0 = IL ? 16 * j8 : 8 * j8;
                 const int d1 = IL ? 16 * j8 + 8 : HALF + 8 * j8;
                 uint4 lo, hi;
                 if (IL)
-                    rope8_interleaved(*reinterpret_cast<const uint4*>(krow + d0),
+                    rope8_interleaved<HALF>(*reinterpret_cast<const uint4*>(krow + d0),
                                       *reinterpret_cast<const uint4*>(krow + d1), cf, fb, lo, hi);
                 else
-                    rope8(*reinterpret_cast<const uint4*>(krow + d0), *reinterpret_cast<const uint4*>(krow + d1), cf,
+                    rope8<HALF>(*reinterpret_cast<const uint4*>(krow + d0), *reinterpret_cast<const uint4*>(krow + d1), cf,
                           fb, lo, hi);
                 *reinterpret_cast<uint4*>(drow + d0) = lo;
                 *reinterpret_cast<uint4*>(drow + d1) = hi;
@@ -766,7 +771,8 @@ static_assert(kNumBars * 8 <= 512, "barrier area");
 
 template <int D, bool IL>
 __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                            const CUtensorMap* tmK5, const CUtensorMap* tmV5, const CUtensorMap* tmQ, const int* it,
+                            const CUtensorMap* tmK5, const CUtensorMap* tmV5, const CUtensorMap* tmQ,
+                            const CUtensorMap* tmR, const int* it,
                             uint8_t* smem,
                             int* s_abort, PfPhase& ph, uint32_t tmem) {
     using L = PfLayout<D>;
@@ -792,61 +798,47 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
     constexpr int kQUnits = kTileRows * (HALF / 8);
     // Q tile: two TMA boxes (one per 64-column half) bring the raw rows
     // [tokens][heads of the group][d] of the item straight into the swizzled
-    // tile; meanwhile every writer loads the RoPE table values of its units
-    // (all at once), then rotates its 16-byte chunks in place in fp32.  One
-    // memory round trip for the whole tile.
+    // tile, and one more box brings the hi parts (cos_hi, sin_hi) of the RoPE
+    // table rows of the tile's positions into the V ring, still idle then (the
+    // V producer joins the writers' barrier before its first load).  The
+    // writers then rotate their 16-byte chunks in place in fp32: one memory
+    // round trip for the whole tile.
+    constexpr int kQBar = kQThreads + 32;
+    const int tpt = kTileRows / G;
+    const float* rtab = reinterpret_cast<const float*>(smem + L::kV);  // [tpt][cos_hi[d/2], sin_hi[d/2]]
     if (warp == 11 && lane == 0) {
-        mbar_expect_tx(bar(kBarQ), (uint32_t)(HALVES * (kTileRows / G) * G * 128));
+        mbar_expect_tx(bar(kBarQ), (uint32_t)(HALVES * tpt * G * 128 + tpt * HALF * 8));
         for (int hf = 0; hf < HALVES; ++hf)
             tma_load_3d(smem_u32(smem + L::kQ + hf * kTileRows * 128), tmQ, hf * 64, g * G, R.qo0 + t0, bar(kBarQ));
+        tma_load_2d(smem_u32(smem + L::kV), tmR, 0, R.h + t0, bar(kBarQ));
     }
     if (q_writer) {
-        // units in rounds of two (registers): the first round's table values are
-        // loaded while the boxes fly, the later rounds' are prefetched into L2
-        constexpr int QU = (kQUnits + kQThreads - 1) / kQThreads;
         const int rows_valid = cnt * G;
-        auto table_row = [&](int i) {
-            const int row = min(i / (HALF / 8), rows_valid - 1);  // rows past the tile's end are zeroed below
-            return P.ropef + (size_t)(R.h + t0 + row / G) * HALF * 4 + (i % (HALF / 8)) * kRopeChunk;
-        };
-#pragma unroll
-        for (int u = 2; u < QU; ++u) {
-            const int i = qtid + u * kQThreads;
-            if (i < kQUnits) asm volatile("prefetch.global.L2 [%0];" ::"l"(table_row(i)));
-        }
+        mbar_wait_bounded(P, bar(kBarQ), ph_get(ph, kPhQ), s_abort, 500, it);
+        ph_flip(ph, kPhQ);
         uint8_t* qtile = smem + L::kQ;
-#pragma unroll
-        for (int u0 = 0; u0 < QU; u0 += 2) {
-            float cs[2][8], sn[2][8];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int i = qtid + (u0 + u) * kQThreads;
-                if (u0 + u < QU && i < kQUnits) load_rope_hi(table_row(i), cs[u], sn[u]);
+        for (int i = qtid; i < kQUnits; i += kQThreads) {
+            const int row = i / (HALF / 8), c = i % (HALF / 8);
+            // 16-byte chunks holding pairs 8c..8c+7
+            const int c0 = IL ? 2 * c : c, c1 = IL ? 2 * c + 1 : c + HALF / 8;
+            uint4* p0 = reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c0));
+            uint4* p1 = reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c1));
+            uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+            if (row < rows_valid) {
+                float cs[8], sn[8];
+                load_rope_hi<HALF>(rtab + (row / G) * HALF * 2, c * 8, cs, sn);
+                rope_q8(*p0, *p1, cs, sn, IL, lo, hi);
             }
-            if (u0 == 0) {
-                mbar_wait_bounded(P, bar(kBarQ), ph_get(ph, kPhQ), s_abort, 500, it);
-                ph_flip(ph, kPhQ);
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int i = qtid + (u0 + u) * kQThreads;
-                if (u0 + u < QU && i < kQUnits) {
-                    const int row = i / (HALF / 8), c = i % (HALF / 8);
-                    // 16-byte chunks holding pairs 8c..8c+7
-                    const int c0 = IL ? 2 * c : c, c1 = IL ? 2 * c + 1 : c + HALF / 8;
-                    uint4* p0 = reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c0));
-                    uint4* p1 = reinterpret_cast<uint4*>(qtile + sw128_chunk(kTileRows, row, c1));
-                    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-                    if (row < rows_valid) rope_q8(*p0, *p1, cs[u], sn[u], IL, lo, hi);
-                    *p0 = lo;
-                    *p1 = hi;
-                }
-            }
+            *p0 = lo;
+            *p1 = hi;
         }
         fence_proxy_async_shared();  // Q is read by the tensor cores (async proxy)
         tc_fence_before();
-        asm volatile("bar.sync 5, %0;" ::"n"(kQThreads) : "memory");
+        asm volatile("bar.sync 5, %0;" ::"n"(kQBar) : "memory");
         tc_fence_after();
+    } else if (warp == 9) {
+        // the V ring holds the table rows until the Q tile is written
+        asm volatile("bar.sync 5, %0;" ::"n"(kQBar) : "memory");
     }
 
     if (warp == 8 || warp == 9) {
@@ -1194,7 +1186,7 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         if (row < G) {
             const uint4* qv = reinterpret_cast<const uint4*>(P.q + ((size_t)R.qo0 * P.Hq + g * G + row) * D);
             float cs[8], sn[8];
-            load_rope_hi(P.ropef + (size_t)pos * HALF * 4 + c * kRopeChunk, cs, sn);
+            load_rope_hi<HALF>(P.ropef + (size_t)pos * HALF * 4, c * 8, cs, sn);
             rope_q8(__ldg(qv + c0), __ldg(qv + c1), cs, sn, IL, lo, hi);
         }
         *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c0)) = lo;
@@ -1213,7 +1205,7 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
             if (ok) {
                 const size_t ti = (size_t)pos * HALF + j;
                 rope_pair(bf16_bits_to_float(kr[i0]), bf16_bits_to_float(kr[i1]),
-                          rope_chunk_pair(P.ropef + (size_t)pos * HALF * 4 + (j >> 3) * kRopeChunk, j & 7), P.rope + ti,
+                          rope_row_pair<HALF>(P.ropef + (size_t)pos * HALF * 4, j), P.rope + ti,
                           y0, y1);
                 reinterpret_cast<uint16_t*>(P.k_cache)[off + i0] = y0;
                 reinterpret_cast<uint16_t*>(P.k_cache)[off + i1] = y1;
@@ -1420,7 +1412,8 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap tmV3,
                                                                  const __grid_constant__ CUtensorMap tmK5,
                                                                  const __grid_constant__ CUtensorMap tmV5,
-                                                                 const __grid_constant__ CUtensorMap tmQ) {
+                                                                 const __grid_constant__ CUtensorMap tmQ,
+                                                                 const __grid_constant__ CUtensorMap tmR) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(16) int s_item[kItemInts];
@@ -1497,7 +1490,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
                 tmem_held = true;
                 tmem = s_tmem;
             }
-            run_prefill<D, IL>(P, &tmK, &tmV, &tmK5, &tmV5, &tmQ, it, smem, &s_abort, pf_phase, tmem);
+            run_prefill<D, IL>(P, &tmK, &tmV, &tmK5, &tmV5, &tmQ, &tmR, it, smem, &s_abort, pf_phase, tmem);
         }
         else
             run_decode<D, IL>(P, &tmK3, &tmV3, it, smem, &s_abort, &s_flag, dec_phase);
@@ -1560,13 +1553,12 @@ __global__ void rope_table_kernel(double2* table, float* split, int max_pos, int
         sincos(th, &sn, &cs);
         table[i] = make_double2(cs, sn);
         const float ch = __double2float_rn(cs), sh = __double2float_rn(sn);
-        // chunk of pairs 8c..8c+7: cos_hi[8], sin_hi[8], cos_lo[8], sin_lo[8]
-        float* chunk = split + (size_t)p * half * 4 + (j >> 3) * kRopeChunk;
-        const int e = j & 7;
-        chunk[e] = ch;
-        chunk[8 + e] = sh;
-        chunk[16 + e] = __double2float_rn(cs - (double)ch);
-        chunk[24 + e] = __double2float_rn(sn - (double)sh);
+        // row p: cos_hi[half], sin_hi[half], cos_lo[half], sin_lo[half]
+        float* row = split + (size_t)p * half * 4;
+        row[j] = ch;
+        row[half + j] = sh;
+        row[2 * half + j] = __double2float_rn(cs - (double)ch);
+        row[3 * half + j] = __double2float_rn(sn - (double)sh);
     }
 }
 
@@ -1673,6 +1665,27 @@ int32_t make_q_map(CUtensorMap* m, const void* q, int T, int Hq, int d, int G) {
     if (r != CUDA_SUCCESS) {
         char msg[128];
         std::snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled (query view) failed (%d)", (int)r);
+        return fail(SARATHI_ERR_CUDA, msg);
+    }
+    return SARATHI_OK;
+}
+
+// 2-D view of the fp32 RoPE table rows {max_pos rows, 2 d floats each}; box =
+// the rows' first d floats (cos_hi and sin_hi) of 128 / G consecutive
+// positions: the table values one Q tile needs.
+int32_t make_rope_map(CUtensorMap* m, const void* ropef, int max_pos, int d, int G) {
+    auto enc = encode_fn();
+    if (!enc) return fail(SARATHI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)d * 2, (cuuint64_t)max_pos};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 2 * 4};
+    cuuint32_t box[2] = {(cuuint32_t)d, (cuuint32_t)tokens_per_tile(G)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ropef), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[128];
+        std::snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled (RoPE table view) failed (%d)", (int)r);
         return fail(SARATHI_ERR_CUDA, msg);
     }
     return SARATHI_OK;
@@ -1806,6 +1819,10 @@ int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void*
     CUtensorMap tmQ;
     st = make_q_map(&tmQ, a->q, in->num_tokens, a->shape.num_heads_q, d, a->shape.num_heads_q / Hkv);
     if (st) return st;
+    CUtensorMap tmR;
+    st = make_rope_map(&tmR, a->rope_table + (size_t)a->rope_max_pos * d, a->rope_max_pos, d,
+                       a->shape.num_heads_q / Hkv);
+    if (st) return st;
     CUtensorMap tmK5, tmV5;
     st = make_page_map5(&tmK5, a->k_cache, a->num_pages, Hkv, d);
     if (st) return st;
@@ -1877,13 +1894,13 @@ int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void*
     }
     const bool il = a->rope_style == SARATHI_ROPE_INTERLEAVED;
     if (d == 128 && !il)
-        mixed_step_kernel<128, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ);
+        mixed_step_kernel<128, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR);
     else if (d == 128)
-        mixed_step_kernel<128, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ);
+        mixed_step_kernel<128, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR);
     else if (!il)
-        mixed_step_kernel<64, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ);
+        mixed_step_kernel<64, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR);
     else
-        mixed_step_kernel<64, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ);
+        mixed_step_kernel<64, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "mixed_step_kernel launch");
     if (io) {
