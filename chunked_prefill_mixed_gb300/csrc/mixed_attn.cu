@@ -58,6 +58,7 @@ struct KParams {
     const int32_t* plan;
     int off_qo, off_kvp, off_kvi, off_last, off_aux, off_items;
     int n_items, n_sched;
+    int n_flags;              // ready-flag words after the header (merge tickets follow them)
     int n_first, first_sms;   // the work list's two queues (see the kernel's claim loop)
     const double2* rope;  // [max_pos][d/2] {cos, sin} in fp64
     const float* ropef;   // [max_pos][4][d/2]: cos_hi, sin_hi, cos_lo, sin_lo rows (cos = hi + lo to ~2^-48)
@@ -441,6 +442,144 @@ __device__ __forceinline__ void rope8(uint4 a, uint4 b, const float* ch, const d
     hi = make_uint4(w1[0], w1[1], w1[2], w1[3]);
 }
 
+// Key rotation for the APPEND items, branch-free.  For one output y = a p +
+// b q (p, q = cos, sin of the angle, |p|, |q| <= 1) the fp32 value
+// u = fl(fma(a, p_hi, fl(b q_hi))) lies within 3.1 2^-24 (|a| + |b|) of the
+// fp64 evaluation (the lo parts of p and q, the two roundings, and the fp64
+// evaluation's own error, which is below 2^-52 (|a| + |b|)).  bf16 rounding
+// boundaries lie where the low 16 bits of u's fp32 encoding are 0x8000, one
+// fp32 ulp = 2^(E - 150) apart for u's biased exponent E; with E_m the biased
+// exponent of |a| + |b| (so |a| + |b| < 2^(E_m - 126)), the error is below
+// 3.1 2^(E_m - E) ulps.  When the low bits are more than 4 << (E_m - E) from
+// 0x8000, u and the fp64 value round to the same bf16 (to nearest even) -- all
+// but about one output in 10^3; the others are queued and redone by rope_bf16.
+// (E_m - E is clamped to [0, 13]: at 13 the threshold reaches 0x8000 and
+// nothing passes.)
+__device__ __forceinline__ uint32_t exp_bits(float x) { return (__float_as_uint(x) >> 23) & 0xFFu; }
+__device__ __forceinline__ float rope_fast(float a, float b, float p_hi, float q_hi, uint32_t em, bool& sure) {
+    const float u = fmaf(a, p_hi, b * q_hi);
+    const uint32_t ub = __float_as_uint(u);
+    const int dist = abs((int)(ub & 0xFFFFu) - 0x8000);
+    const int de = min(max((int)em - (int)exp_bits(u), 0), 13);
+    sure = dist > (4 << de);
+    return u;
+}
+// Fix-up queue entry: where the output goes (byte offset in shared memory), its
+// pair and token (pair j, output 0 or 1, item-local token), and x0, x1.
+struct RopeFix {
+    uint32_t off;   // kRopeFixNone: a slot of a run that did not fit the queue
+    uint32_t code;  // j | which << 7 | tl << 8 | page of the pair << 15
+    float x0, x1;
+};
+constexpr int kRopeFixCap = 256;            // entries (4 KB)
+constexpr uint32_t kRopeFixNone = 0xFFFFFFFFu;
+
+// Element e (0..7) of eight packed bf16 values.
+__device__ __forceinline__ void set_bf16(uint32_t (&w)[4], int e, uint16_t v) {
+    w[e >> 1] = (e & 1) ? ((w[e >> 1] & 0xFFFFu) | ((uint32_t)v << 16)) : ((w[e >> 1] & 0xFFFF0000u) | v);
+}
+
+// Eight pairs of one key row, rotated and rounded to bf16 exactly as the fp64
+// evaluation is.  Rotate-half (IL false): a = x0 and b = x1 of pairs j0..j0+7,
+// lo / hi = their outputs.  Interleaved: a = dims 2j0..2j0+7, b = the next
+// eight, outputs in place.  hrow: cos_hi and sin_hi of pairs j0..j0+7 (planes
+// HALF floats apart).  The rare uncertain outputs are appended to the fix-up
+// queue (off_lo / off_hi: byte offsets in shared memory where lo / hi will be
+// stored; code_tl: the token and page bits of the entry's code); if the queue
+// is full they are redone here with rope_bf16 (grow: the full fp32 table row at
+// pair j0, fb: its fp64 values).
+template <int HALF, bool IL>
+__device__ __forceinline__ void rope8_key(uint4 a, uint4 b, const float* hrow, int j0, uint32_t off_lo,
+                                          uint32_t off_hi, uint32_t code_tl, RopeFix* fixq, int* fix_n,
+                                          const float* grow, const double2* fb, uint4& lo, uint4& hi) {
+    float ch[8], sh[8];
+    {
+        const float4* vc = reinterpret_cast<const float4*>(hrow);
+        const float4* vs = reinterpret_cast<const float4*>(hrow + HALF);
+        const float4 c0 = vc[0], c1 = vc[1], s0 = vs[0], s1 = vs[1];
+        ch[0] = c0.x; ch[1] = c0.y; ch[2] = c0.z; ch[3] = c0.w; ch[4] = c1.x; ch[5] = c1.y; ch[6] = c1.z; ch[7] = c1.w;
+        sh[0] = s0.x; sh[1] = s0.y; sh[2] = s0.z; sh[3] = s0.w; sh[4] = s1.x; sh[5] = s1.y; sh[6] = s1.z; sh[7] = s1.w;
+    }
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+    float x0[8], x1[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (!IL) {
+            x0[2 * q] = __uint_as_float(aw[q] << 16);
+            x0[2 * q + 1] = __uint_as_float(aw[q] & 0xFFFF0000u);
+            x1[2 * q] = __uint_as_float(bw[q] << 16);
+            x1[2 * q + 1] = __uint_as_float(bw[q] & 0xFFFF0000u);
+        } else {
+            x0[q] = __uint_as_float(aw[q] << 16);
+            x1[q] = __uint_as_float(aw[q] & 0xFFFF0000u);
+            x0[4 + q] = __uint_as_float(bw[q] << 16);
+            x1[4 + q] = __uint_as_float(bw[q] & 0xFFFF0000u);
+        }
+    }
+    float y0[8], y1[8];
+    uint32_t unsure = 0;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const uint32_t em = exp_bits(fabsf(x0[p]) + fabsf(x1[p]));
+        bool s0, s1;
+        y0[p] = rope_fast(x0[p], -x1[p], ch[p], sh[p], em, s0);
+        y1[p] = rope_fast(x1[p], x0[p], ch[p], sh[p], em, s1);
+        unsure |= (s0 ? 0u : 1u << p) | (s1 ? 0u : 0x100u << p);
+    }
+    uint32_t wl[4], wh[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (!IL) {
+            wl[q] = pack_bf16(y0[2 * q], y0[2 * q + 1]);
+            wh[q] = pack_bf16(y1[2 * q], y1[2 * q + 1]);
+        } else {
+            wl[q] = pack_bf16(y0[q], y1[q]);
+            wh[q] = pack_bf16(y0[4 + q], y1[4 + q]);
+        }
+    }
+    if (unsure) {
+        // rare: queue the uncertain outputs (a run of consecutive entries)
+        const int need = __popc(unsure);
+        const int k0 = atomicAdd(fix_n, need);
+        if (k0 + need <= kRopeFixCap) {
+            int k = k0;
+            for (uint32_t m = unsure; m; m &= m - 1, ++k) {
+                const int bit = __ffs(m) - 1;
+                const int p = bit & 7, which = bit >> 3;
+                // where that output sits in lo / hi (two bytes per element)
+                const uint32_t off = IL ? ((p < 4 ? off_lo : off_hi) + (uint32_t)(4 * (p & 3) + 2 * which))
+                                        : ((which ? off_hi : off_lo) + (uint32_t)(2 * p));
+                float px0 = 0.f, px1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (e == p) {
+                        px0 = x0[e];
+                        px1 = x1[e];
+                    }
+                fixq[k] = RopeFix{off, (uint32_t)(j0 + p) | ((uint32_t)which << 7) | code_tl, px0, px1};
+            }
+        } else {
+            // the queue is full (never with ordinary inputs): mark this run's
+            // slots that fit, and redo the outputs here
+            for (int k = k0; k < kRopeFixCap; ++k) fixq[k].off = kRopeFixNone;
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const float4 cf = rope_row_pair<HALF>(grow, p);
+                if (unsure & (1u << p)) {
+                    const uint16_t r = rope_bf16(x0[p], -x1[p], cf.x, cf.y, cf.z, cf.w, fb + p);
+                    if (!IL) set_bf16(wl, p, r); else set_bf16(p < 4 ? wl : wh, 2 * (p & 3), r);
+                }
+                if (unsure & (0x100u << p)) {
+                    const uint16_t r = rope_bf16(x1[p], x0[p], cf.x, cf.y, cf.z, cf.w, fb + p);
+                    if (!IL) set_bf16(wh, p, r); else set_bf16(p < 4 ? wl : wh, 2 * (p & 3) + 1, r);
+                }
+            }
+        }
+    }
+    lo = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    hi = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+}
+
 // Eight pairs of one query row in fp32, rounded to bf16 (Q feeds the MMA in
 // bf16; its rotation needs no certified rounding).  Rotate-half: a = x0 and
 // b = x1 of pairs j0..j0+7, lo / hi = their outputs.  Interleaved: a = dims
@@ -483,96 +622,162 @@ __device__ __forceinline__ void load_rope_hi(const float* row, int j0, float (&c
 }
 
 // ----------------------------------------------------------------------------
-// APPEND: rotate + store the K/V of up to kAppendTokens prefill tokens
+// APPEND: rotate + store the K/V of the prefill tokens of one 128-position
+// block (up to 8 pages), for up to kAppendHeads kv heads
 // ----------------------------------------------------------------------------
-// The item's K and V rows ([token][kv_head][d], contiguous) and the fp32 RoPE
-// rows of its positions (contiguous) come into shared memory with three bulk
-// copies, so a pass costs one memory round trip however loaded HBM is.  A
-// pass holds as many tokens as fit in the stage area: all 16 up to 10 kv heads
-// of d = 128 (two passes for 32 heads).
+// Per page, two TMA boxes bring the K and V rows from k/v's [token][kv head][d]
+// layout as [head][16 tokens][d] -- the order of a page's slots -- and a third
+// the cos_hi / sin_hi planes of the positions' fp32 RoPE rows.  V goes straight
+// back out to the page with one bulk store per head (no thread touches it); K
+// is rotated in place (certified rounding) and stored the same way.
+// kAppendBufs page buffers: later pages' loads fly while a page is rotated, so
+// the item costs about one memory round trip plus its rotations.  The item then sets its ready flag,
+// which the prefill tiles of its kv heads wait for before they load the block.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
 template <int D, bool IL>
-__device__ void run_append(const KParams& P, const int* it, uint8_t* smem, uint32_t bar, uint32_t* s_phase,
-                           int* s_abort) {
+__device__ void run_append(const KParams& P, const CUtensorMap* tmKin, const CUtensorMap* tmVin, const int* it,
+                           uint8_t* smem, uint32_t bar0, uint32_t* s_phase, int* s_abort, int* s_fix) {
     const int tid = threadIdx.x;
-    uint32_t phase = *s_phase;  // passes this CTA has waited for; kept in shared memory, not a loop register
-    const int s = it[kS], t0 = it[kStart], cnt = it[kCount];
+    const int s = it[kS], g0 = it[kG], t0 = it[kStart], cnt = it[kCount];
     const Row R = row_geom(it);
     const int Hkv = P.Hkv;
-    constexpr int HALF = D / 2, C8 = D / 8, H8 = HALF / 8;
-    const int row_bytes = Hkv * D * 2;                // one token's K (or V), every kv head
-    const int tok_bytes = 2 * row_bytes + HALF * 16;  // its K, V and fp32 RoPE row (HALF x 4 floats)
-    const int tpp = min(cnt, kSmemStages / tok_bytes);
-    const uint16_t* kin = reinterpret_cast<const uint16_t*>(P.k);
-    uint16_t* kc = reinterpret_cast<uint16_t*>(P.k_cache);
+    constexpr int HALF = D / 2;
+    constexpr int ROW = D * 2;                           // bytes of one (token, head) row
+    constexpr int BOX = kAppendHeads * kPage * ROW;      // bytes of one tensor's box
+    constexpr int RROW = HALF * 16;                      // bytes of one position's fp32 RoPE row
+    constexpr int BUF = 2 * BOX + kPage * RROW;          // K box, V box, RoPE rows of one page
+    constexpr int NB = kAppendBufs;
+    static_assert(NB * BUF <= kSmemStages && NB % 2 == 0, "APPEND page buffers");
+    const int ng = min(kAppendHeads, Hkv - g0);          // heads of this item
+    const int pos0 = R.h + t0;                           // position of the item's first token
+    const int npg = (pos0 + cnt - 1) / kPage - pos0 / kPage + 1;
     const int32_t* pages = P.plan + P.off_kvi + R.kvp0;
-    if (R.h + t0 + cnt > P.rope_max_pos) {
-        if (tid == 0) raise_error(P, kErrBounds, R.h + t0 + cnt - 1, s_abort);
+    // every page id and the RoPE table bound checked up front (all threads alike)
+    bool ok = pos0 + cnt <= P.rope_max_pos;
+    int bad = pos0 + cnt - 1;
+    for (int k = 0; k < npg && ok; ++k) {
+        bad = pages[pos0 / kPage + k];
+        ok = bad >= 0 && bad < P.num_pages;
+    }
+    uint16_t* kc = reinterpret_cast<uint16_t*>(P.k_cache);
+    uint16_t* vc = reinterpret_cast<uint16_t*>(P.v_cache);
+    // tokens [tk0, tk0 + tkc) of the item lie in its page k
+    auto span = [&](int k, int& tk0, int& tkc) {
+        const int pa = (pos0 / kPage + k) * kPage;
+        tk0 = max(pos0, pa) - pos0;
+        tkc = min(pos0 + cnt, pa + kPage) - pos0 - tk0;
+    };
+    auto issue = [&](int k) {
+        int tk0, tkc;
+        span(k, tk0, tkc);
+        uint8_t* base = smem + (k % NB) * BUF;
+        const uint32_t bar = bar0 + 8u * (uint32_t)(k % NB);
+        mbar_expect_tx(bar, 2u * BOX + (uint32_t)(tkc * RROW));
+        tma_load_3d(smem_u32(base), tmKin, 0, R.qo0 + t0 + tk0, g0, bar);
+        tma_load_3d(smem_u32(base + BOX), tmVin, 0, R.qo0 + t0 + tk0, g0, bar);
+        bulk_load(smem_u32(base + 2 * BOX), P.ropef + (size_t)(pos0 + tk0) * HALF * 4, (uint32_t)(tkc * RROW), bar);
+    };
+    RopeFix* fixq = reinterpret_cast<RopeFix*>(smem + kSmemDecQ);  // idle during APPEND items
+    static_assert(kRopeFixCap * sizeof(RopeFix) <= 2 * kPageHalfBytes, "fix-up queue");
+    uint32_t ph = *s_phase;  // completed-phase parities of the buffers' barriers
+    if (!ok) {
+        if (tid == 0) raise_error(P, kErrBounds, bad, s_abort);
     } else {
-        for (int p0 = 0; p0 < cnt; p0 += tpp) {
-            const int n = min(tpp, cnt - p0);
-            const int ta = t0 + p0;  // first chunk token of this pass
-            const uint32_t kbytes = (uint32_t)(n * row_bytes);
-            if (tid == 0) {
-                const uint32_t rbytes = (uint32_t)(n * HALF * 16);
-                const size_t row0 = (size_t)(R.qo0 + ta) * Hkv * D;
-                mbar_expect_tx(bar, 2 * kbytes + rbytes);
-                bulk_load(smem_u32(smem), kin + row0, kbytes, bar);
-                bulk_load(smem_u32(smem + kbytes), P.v + row0, kbytes, bar);
-                bulk_load(smem_u32(smem + 2 * kbytes), P.ropef + (size_t)(R.h + ta) * HALF * 4, rbytes, bar);
+        if (tid == 0)
+            for (int k = 0; k < NB && k < npg; ++k) issue(k);
+        // pages two at a time: (2i, 2i + 1); the K rows of both, eight pairs per thread
+        for (int i = 0; 2 * i < npg; ++i) {
+            const int kp[2] = {2 * i, 2 * i + 1};
+            const int np2 = min(2, npg - 2 * i);
+            int tk0[2] = {0, 0}, tkc[2] = {0, 0};
+            size_t dst0[2] = {0, 0};
+            for (int q = 0; q < np2; ++q) {
+                const int b = kp[q] % NB;
+                span(kp[q], tk0[q], tkc[q]);
+                if (!mbar_wait_bounded(P, bar0 + 8u * (uint32_t)b, (ph >> b) & 1u, s_abort, 10000 + kp[q], it)) return;
+                ph ^= 1u << b;
+                const int pos = pos0 + tk0[q];
+                dst0[q] = (((size_t)pages[pos / kPage] * Hkv + g0) * kPage + pos % kPage) * D;
+                if (tid == 0)
+                    for (int g = 0; g < ng; ++g)
+                        bulk_store(vc + dst0[q] + (size_t)g * kPage * D,
+                                   smem_u32(smem + b * BUF + BOX + g * kPage * ROW), (uint32_t)(tkc[q] * ROW));
             }
-            if (!mbar_wait_bounded(P, bar, phase & 1, s_abort, 10000 + p0, it)) return;
-            ++phase;
-            const uint16_t* ks = reinterpret_cast<const uint16_t*>(smem);
-            const uint4* vs = reinterpret_cast<const uint4*>(smem + kbytes);
-            const float* rs = reinterpret_cast<const float*>(smem + 2 * kbytes);
-            const int totv = n * Hkv * C8;
-            for (int i = tid; i < totv; i += kThreads) {
-                const int c = i % C8, rest = i / C8, g = rest % Hkv, pos = R.h + ta + rest / Hkv;
-                const int page = __ldg(pages + pos / kPage);
-                if (page < 0 || page >= P.num_pages) continue;  // reported by the K loop below
-                reinterpret_cast<uint4*>(P.v_cache + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D)[c] = vs[i];
-            }
-            const int totk = n * H8 * Hkv;
-            for (int i = tid; i < totk; i += kThreads) {
-                // kv head fastest: neighbouring threads share a RoPE row
-                const int g = i % Hkv, rest = i / Hkv, j8 = rest % H8, tl = rest / H8;
-                const int pos = R.h + ta + tl;
-                const int page = __ldg(pages + pos / kPage);
-                if (page < 0 || page >= P.num_pages) {
-                    raise_error(P, kErrBounds, page, s_abort);
-                    continue;
-                }
-                const uint16_t* krow = ks + ((size_t)tl * Hkv + g) * D;
-                uint16_t* drow = kc + (((size_t)page * Hkv + g) * kPage + pos % kPage) * D;
-                const float* cf = rs + (size_t)tl * HALF * 4 + j8 * 8;
-                const double2* fb = P.rope + (size_t)pos * HALF + j8 * 8;
-                // pairs 8 j8 .. 8 j8 + 7: dims (j, j + d/2), or (2j, 2j + 1) interleaved
-                const int d0 = IL ? 16 * j8 : 8 * j8;
-                const int d1 = IL ? 16 * j8 + 8 : HALF + 8 * j8;
+            int* fix_n = s_fix + (i & 1);  // this pair's queue count (the other pair's is being cleared)
+            const int u0 = ng * tkc[0] * (HALF / 8);
+            const int units = u0 + (np2 > 1 ? ng * tkc[1] * (HALF / 8) : 0);
+            // (scalars, not the arrays: no dynamic indexing in the loop)
+            const int tkcA = tkc[0], tkcB = tkc[1], tk0A = tk0[0], tk0B = tk0[1];
+            uint8_t* baseA = smem + (kp[0] % NB) * BUF;
+            uint8_t* baseB = smem + (kp[1] % NB) * BUF;
+            for (int u = tid; u < units; u += kThreads) {
+                const int q = u < u0 ? 0 : 1;
+                const int i2 = q ? u - u0 : u;
+                const int tkcq = q ? tkcB : tkcA;
+                const int c = i2 % (HALF / 8), rest = i2 / (HALF / 8);
+                const int tl = rest % tkcq, g = rest / tkcq;
+                uint8_t* base = q ? baseB : baseA;
+                uint16_t* krow = reinterpret_cast<uint16_t*>(base + (g * kPage + tl) * ROW);
+                const float* rrow = reinterpret_cast<const float*>(base + 2 * BOX + tl * RROW);
+                const int pos = pos0 + (q ? tk0B : tk0A) + tl;
+                // pairs 8c .. 8c + 7: dims (j, j + d/2), or (2j, 2j + 1) interleaved
+                const int d0 = IL ? 16 * c : 8 * c;
+                const int d1 = IL ? 16 * c + 8 : HALF + 8 * c;
                 uint4 lo, hi;
-                if (IL)
-                    rope8_interleaved<HALF>(*reinterpret_cast<const uint4*>(krow + d0),
-                                      *reinterpret_cast<const uint4*>(krow + d1), cf, fb, lo, hi);
-                else
-                    rope8<HALF>(*reinterpret_cast<const uint4*>(krow + d0), *reinterpret_cast<const uint4*>(krow + d1), cf,
-                          fb, lo, hi);
-                *reinterpret_cast<uint4*>(drow + d0) = lo;
-                *reinterpret_cast<uint4*>(drow + d1) = hi;
+                rope8_key<HALF, IL>(*reinterpret_cast<const uint4*>(krow + d0),
+                                    *reinterpret_cast<const uint4*>(krow + d1), rrow + c * 8, 8 * c,
+                                    smem_u32(krow + d0), smem_u32(krow + d1),
+                                    ((uint32_t)tl << 8) | ((uint32_t)q << 15), fixq, fix_n, rrow + c * 8,
+                                    P.rope + (size_t)pos * HALF + c * 8, lo, hi);
+                *reinterpret_cast<uint4*>(krow + d0) = lo;
+                *reinterpret_cast<uint4*>(krow + d1) = hi;
             }
-            if (p0 + tpp < cnt) {
-                // the next pass's bulk copies overwrite what was just read
-                fence_proxy_async_shared();
-                __syncthreads();
+            __syncthreads();
+            // the queued uncertain outputs, redone in full (about one in 10^3;
+            // the table rows are in shared memory)
+            const int nfix = min(*(volatile int*)fix_n, kRopeFixCap);
+            for (int e = tid; e < nfix; e += kThreads) {
+                const RopeFix f = fixq[e];
+                if (f.off == kRopeFixNone) continue;
+                const int j = (int)(f.code & 127u), which = (int)((f.code >> 7) & 1u);
+                const int tl = (int)((f.code >> 8) & 127u), q = (int)(f.code >> 15);
+                const float* rrow = reinterpret_cast<const float*>((q ? baseB : baseA) + 2 * BOX + tl * RROW);
+                const float4 cf = rope_row_pair<HALF>(rrow, j);
+                const double2* fb = P.rope + (size_t)(pos0 + (q ? tk0B : tk0A) + tl) * HALF + j;
+                const uint16_t r = which ? rope_bf16(f.x1, f.x0, cf.x, cf.y, cf.z, cf.w, fb)
+                                         : rope_bf16(f.x0, -f.x1, cf.x, cf.y, cf.z, cf.w, fb);
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(f.off), "h"(r) : "memory");
+            }
+            fence_proxy_async_shared();  // the rotated rows are read by the bulk stores (async proxy)
+            __syncthreads();
+            if (tid == 0) {
+                *fix_n = 0;  // every thread read it before the barrier; pair i + 2 counts from 0
+                for (int q = 0; q < np2; ++q)
+                    for (int g = 0; g < ng; ++g)
+                        bulk_store(kc + dst0[q] + (size_t)g * kPage * D,
+                                   smem_u32(smem + (kp[q] % NB) * BUF + g * kPage * ROW), (uint32_t)(tkc[q] * ROW));
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                if (i >= 1 && 2 * i + 2 < npg) {
+                    // the previous pair's stores have read its buffers: refill them
+                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    issue(2 * i + 2);
+                    if (2 * i + 3 < npg) issue(2 * i + 3);
+                }
             }
         }
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the pages are written
     }
     // publish: the pages are read next by TMA (async proxy) in other CTAs
     fence_proxy_async_global();
     __threadfence();
     __syncthreads();
     if (tid == 0) {
-        atomicAdd(&P.ws_int[kHdrInts + s], 1);
-        *s_phase = phase;
+        const int blk = pos0 / kTileRows - R.h / kTileRows;
+        atomicExch(&P.ws_int[kHdrInts + P.plan[P.off_aux + s] + blk * kv_groups(Hkv) + g0 / kAppendHeads], 1);
+        *s_phase = ph;
     }
 }
 
@@ -764,8 +969,8 @@ constexpr int kBarSFree = kBarPFull + 2;               // 2 (per S buffer: loade
 constexpr int kBarOUp = kBarSFree + 2;                 // 2 (per P buffer: its P.V group done)
 constexpr int kBarODone = kBarOUp + 2;                 // 1 (one completion per item: its last P.V)
 constexpr int kBarDrain = kBarODone + 1;               // 2 (one per MMA-issuing thread)
-constexpr int kBarAppend = kBarDrain + 2;              // 1 (APPEND bulk copies)
-constexpr int kBarQ = kBarAppend + 1;                  // 1 (the Q tile's TMA boxes)
+constexpr int kBarAppend = kBarDrain + 2;              // kAppendBufs (APPEND page buffers)
+constexpr int kBarQ = kBarAppend + kAppendBufs;        // 1 (the Q tile's TMA boxes)
 constexpr int kNumBars = kBarQ + 1;
 static_assert(kNumBars * 8 <= 512, "barrier area");
 
@@ -860,13 +1065,14 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         int id = pq < pages_hi ? it[kIds + pq] : 0;  // block 0's ids come with the item
         const int j_chunk = R.h / kTcKeys;  // first block with a key of the chunk
         for (int j = 0; j < nblk; ++j) {
-            if (j == j_chunk) {
-                // the chunk's K/V must be in the pages: this request's APPENDs
-                const int need = P.plan[P.off_aux + s];
-                const int* ctr = &P.ws_int[kHdrInts + s];
-                if (lane == 0 && ld_acquire(ctr) < need) {
+            if (j >= j_chunk) {
+                // the block's new K/V must be in the pages: the ready flag its
+                // APPEND item sets for this tile's group of kv heads
+                const int* ctr = &P.ws_int[kHdrInts + P.plan[P.off_aux + s] + (j - j_chunk) * kv_groups(P.Hkv) +
+                                           g / kAppendHeads];
+                if (lane == 0 && ld_acquire(ctr) == 0) {
                     const uint64_t w0 = globaltimer();
-                    while (ld_acquire(ctr) < need) {
+                    while (ld_acquire(ctr) == 0) {
                         if (globaltimer() - w0 > kWaitNs / 2) {  // first to give up: names the cause
                             raise_error(P, kErrWait, -1 - s, s_abort);
                             break;
@@ -1377,7 +1583,7 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     __threadfence();
     __syncthreads();
     if (tid == 0) {
-        const int old = atomicAdd(&P.ws_int[kHdrInts + P.n_sched + merge], 1);
+        const int old = atomicAdd(&P.ws_int[kHdrInts + P.n_flags + merge], 1);
         *s_flag = (old == nsplit - 1);
         if (*s_flag) __threadfence();
     }
@@ -1397,7 +1603,7 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         }
         P.out[((size_t)R.qo0 * P.Hq + g * G + row) * D + col] = __float2bfloat16_rn(acc / L);
     }
-    if (tid == 0) P.ws_int[kHdrInts + P.n_sched + merge] = 0;
+    if (tid == 0) P.ws_int[kHdrInts + P.n_flags + merge] = 0;
 }
 
 // ----------------------------------------------------------------------------
@@ -1413,7 +1619,9 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap tmK5,
                                                                  const __grid_constant__ CUtensorMap tmV5,
                                                                  const __grid_constant__ CUtensorMap tmQ,
-                                                                 const __grid_constant__ CUtensorMap tmR) {
+                                                                 const __grid_constant__ CUtensorMap tmR,
+                                                                 const __grid_constant__ CUtensorMap tmKin,
+                                                                 const __grid_constant__ CUtensorMap tmVin) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(16) int s_item[kItemInts];
@@ -1421,11 +1629,13 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
     __shared__ int s_flag;
     __shared__ uint32_t s_tmem;
     __shared__ uint32_t s_app_phase;
+    __shared__ int s_fix[2];  // entries in the APPEND items' fix-up queue, by page parity
     const int tid = threadIdx.x;
     const uint32_t bars = smem_u32(smem + kSmemBars);
     if (tid == 0) {
         s_abort = 0;
         s_app_phase = 0;
+        s_fix[0] = s_fix[1] = 0;
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
             if (i == kBarPFull || i == kBarPFull + 1 || i == kBarSFree || i == kBarSFree + 1)
@@ -1474,7 +1684,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         const int* it = s_item;  // rewritten only after the end-of-item barrier
         if (it[0] < 0) break;
         if (it[0] == kAppend)
-            run_append<D, IL>(P, it, smem, bars + 8 * kBarAppend, &s_app_phase, &s_abort);
+            run_append<D, IL>(P, &tmKin, &tmVin, it, smem, bars + 8 * kBarAppend, &s_app_phase, &s_abort, s_fix);
         else if (it[0] == kPrefill) {
             if (!tmem_held) {
                 if (tid < 32) {
@@ -1528,7 +1738,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
     }
     __syncthreads();
     if (s_flag) {
-        for (int i = tid; i < P.n_sched; i += kThreads) P.ws_int[kHdrInts + i] = 0;
+        for (int i = tid; i < P.n_flags; i += kThreads) P.ws_int[kHdrInts + i] = 0;
         if (tid == 0) {
             P.ws_int[0] = 0;
             P.ws_int[1] = 0;
@@ -1671,14 +1881,14 @@ int32_t make_q_map(CUtensorMap* m, const void* q, int T, int Hq, int d, int G) {
 }
 
 // 2-D view of the fp32 RoPE table rows {max_pos rows, 2 d floats each}; box =
-// the rows' first d floats (cos_hi and sin_hi) of 128 / G consecutive
-// positions: the table values one Q tile needs.
-int32_t make_rope_map(CUtensorMap* m, const void* ropef, int max_pos, int d, int G) {
+// the rows' first d floats (cos_hi and sin_hi) of `rows` (128 / G)
+// consecutive positions: the table values one Q tile needs.
+int32_t make_rope_map(CUtensorMap* m, const void* ropef, int max_pos, int d, int rows) {
     auto enc = encode_fn();
     if (!enc) return fail(SARATHI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     cuuint64_t dims[2] = {(cuuint64_t)d * 2, (cuuint64_t)max_pos};
     cuuint64_t strides[1] = {(cuuint64_t)d * 2 * 4};
-    cuuint32_t box[2] = {(cuuint32_t)d, (cuuint32_t)tokens_per_tile(G)};
+    cuuint32_t box[2] = {(cuuint32_t)d, (cuuint32_t)rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ropef), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1686,6 +1896,28 @@ int32_t make_rope_map(CUtensorMap* m, const void* ropef, int max_pos, int d, int
     if (r != CUDA_SUCCESS) {
         char msg[128];
         std::snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled (RoPE table view) failed (%d)", (int)r);
+        return fail(SARATHI_ERR_CUDA, msg);
+    }
+    return SARATHI_OK;
+}
+
+// 3-D view of the step's new keys or values k[T][H_kv][d]: {d, T tokens, H_kv
+// heads} (strides H_kv*d*2 and d*2 bytes).  Box = d x 16 x kAppendHeads: the
+// rows of 16 tokens for a group of kv heads, landing head-major ([head][token]
+// [d]) like the slots of a page.
+int32_t make_kv_in_map(CUtensorMap* m, const void* x, int T, int Hkv, int d) {
+    auto enc = encode_fn();
+    if (!enc) return fail(SARATHI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)Hkv};
+    cuuint64_t strides[2] = {(cuuint64_t)Hkv * d * 2, (cuuint64_t)d * 2};
+    cuuint32_t box[3] = {(cuuint32_t)d, (cuuint32_t)kPage, (cuuint32_t)kAppendHeads};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[128];
+        std::snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled (new K/V view) failed (%d)", (int)r);
         return fail(SARATHI_ERR_CUDA, msg);
     }
     return SARATHI_OK;
@@ -1819,9 +2051,14 @@ int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void*
     CUtensorMap tmQ;
     st = make_q_map(&tmQ, a->q, in->num_tokens, a->shape.num_heads_q, d, a->shape.num_heads_q / Hkv);
     if (st) return st;
+    CUtensorMap tmKin, tmVin;
+    st = make_kv_in_map(&tmKin, a->k, in->num_tokens, Hkv, d);
+    if (st) return st;
+    st = make_kv_in_map(&tmVin, a->v, in->num_tokens, Hkv, d);
+    if (st) return st;
     CUtensorMap tmR;
     st = make_rope_map(&tmR, a->rope_table + (size_t)a->rope_max_pos * d, a->rope_max_pos, d,
-                       a->shape.num_heads_q / Hkv);
+                       tokens_per_tile(a->shape.num_heads_q / Hkv));
     if (st) return st;
     CUtensorMap tmK5, tmV5;
     st = make_page_map5(&tmK5, a->k_cache, a->num_pages, Hkv, d);
@@ -1853,12 +2090,13 @@ int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void*
     P.n_items = in->n_items;
     P.n_first = in->n_first;
     P.n_sched = in->n_sched;
+    P.n_flags = (int)flag_ints(in->n_sched, in->num_tokens, Hkv);
     P.rope = reinterpret_cast<const double2*>(a->rope_table);
     P.ropef = reinterpret_cast<const float*>(a->rope_table + (size_t)a->rope_max_pos * d);
     P.rope_max_pos = a->rope_max_pos;
     P.ws_int = static_cast<int32_t*>(a->workspace);
     P.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(a->workspace) +
-                                         partial_offset_bytes(in->n_sched, in->n_merge));
+                                         partial_offset_bytes(in->n_sched, in->n_merge, in->num_tokens, Hkv));
     P.Hq = a->shape.num_heads_q;
     P.Hkv = Hkv;
     P.group = a->shape.num_heads_q / Hkv;
@@ -1894,13 +2132,17 @@ int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void*
     }
     const bool il = a->rope_style == SARATHI_ROPE_INTERLEAVED;
     if (d == 128 && !il)
-        mixed_step_kernel<128, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR);
+        mixed_step_kernel<128, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR, tmKin,
+                                                                                  tmVin);
     else if (d == 128)
-        mixed_step_kernel<128, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR);
+        mixed_step_kernel<128, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR, tmKin,
+                                                                                  tmVin);
     else if (!il)
-        mixed_step_kernel<64, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR);
+        mixed_step_kernel<64, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR, tmKin,
+                                                                                  tmVin);
     else
-        mixed_step_kernel<64, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR);
+        mixed_step_kernel<64, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR, tmKin,
+                                                                                  tmVin);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "mixed_step_kernel launch");
     if (io) {

@@ -49,11 +49,12 @@ extern "C" int32_t sarathi_mixed_attn_noalloc(const sarathi_attn_args* args, voi
     // comes from n_sched and n_merge, so both are checked against the array
     // before anything is enqueued (an inconsistent plan info must not make the
     // memset run past the array).
-    if (in->n_sched <= 0 || in->n_merge < 0 || in->n_partials < 0 || in->n_items < 0)
+    if (in->n_sched <= 0 || in->n_merge < 0 || in->n_partials < 0 || in->n_items < 0 || in->num_tokens < 0)
         return fail(SARATHI_ERR_INVALID_ARG, "inconsistent plan info (n_sched, n_merge, n_partials or n_items)");
     const int32_t st = check_shape(&args->shape);
     if (st) return st;
-    const int64_t clear_bytes = partial_offset_bytes(in->n_sched, in->n_merge);
+    const int64_t clear_bytes =
+        partial_offset_bytes(in->n_sched, in->n_merge, in->num_tokens, args->shape.num_heads_kv);
     const int64_t need = clear_bytes + (int64_t)in->n_partials *
                                            partial_slot_floats(args->shape.num_heads_q / args->shape.num_heads_kv,
                                                                args->shape.head_dim) * 4;

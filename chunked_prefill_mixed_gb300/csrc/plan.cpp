@@ -108,7 +108,9 @@ extern "C" int32_t sarathi_plan_bounds(const sarathi_request* reqs, int32_t n_re
     }
     const int64_t n = n_reqs;
     const int64_t T = n_dec + token_budget;
-    const int64_t appends = T / kAppendTokens + n;
+    // APPEND items: each row's tokens cut where their positions cross a
+    // 128-position boundary, times the groups of kv heads
+    const int64_t appends = (T / kTileRows + 2 * n) * kv_groups((int)Hkv);
     const int64_t tiles = (T / tokens_per_tile(group) + n) * Hkv;
     // decode splits: sum over one-token rows (decodes, and prefill chunks of one
     // token) and kv heads of ceil(np / split) with split >= their page-heads /
@@ -121,7 +123,7 @@ extern "C" int32_t sarathi_plan_bounds(const sarathi_request* reqs, int32_t n_re
     if (host_buf_bytes) *host_buf_bytes = (size_t)ints * 4;
     if (device_workspace_bytes) {
         const int64_t n_merge = n * Hkv;
-        *device_workspace_bytes = (size_t)(partial_offset_bytes((int)n, (int)n_merge) +
+        *device_workspace_bytes = (size_t)(partial_offset_bytes((int)n, (int)n_merge, (int)T, (int)Hkv) +
                                            dec_items * partial_slot_floats(group, shape->head_dim) * 4);
     }
     return SARATHI_OK;
@@ -282,19 +284,26 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     const int64_t target = (int64_t)num_sms * kDecodeItemsPerSm;
     const int64_t split =
         std::max<int64_t>(kDecodeMinSplitPages, ceil_div(std::max<int64_t>(dec_page_heads, 1), target));
-    int32_t n_partials = 0, n_merge = 0;
+    int32_t n_partials = 0, n_merge = 0, n_flags = 0;
     const double kv_page_bytes = 2.0 * kPage * d * 2;
     for (int32_t s = 0; s < ns; ++s) {
         const int32_t n = sched[s].n;
         const int32_t h = hist[s];
         if (n >= 2) {
-            // prefill-like: append items first, then one tile per (kv head, token block)
-            int32_t cnt = 0;
-            for (int32_t t0 = 0; t0 < n; t0 += kAppendTokens) {
-                appends.push_back({kAppend, s, 0, t0, std::min(kAppendTokens, n - t0), -1, -1, 0});
-                ++cnt;
+            // prefill-like: append items first (the row's tokens cut where their
+            // positions cross a 128-position boundary -- a K/V block of the
+            // tiles -- times the groups of kv heads; each sets one ready flag,
+            // the row's flags from aux[s] on), then one tile per (kv head,
+            // token block)
+            aux[s] = n_flags;
+            for (int32_t t0 = 0; t0 < n;) {
+                const int32_t c = std::min<int32_t>(n - t0, kTileRows - (h + t0) % kTileRows);
+                for (int g0 = 0; g0 < Hkv; g0 += kAppendHeads) {
+                    appends.push_back({kAppend, s, g0, t0, c, -1, -1, 0});
+                    ++n_flags;
+                }
+                t0 += c;
             }
-            aux[s] = cnt;
             // one (request, kv head) at a time, costliest item first: the items
             // that read the same history pages run side by side and share L2
             for (int g = 0; g < Hkv; ++g)
@@ -445,7 +454,7 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     info->pairs = pairs;
     info->history_tokens = history;
     info->workspace_bytes =
-        partial_offset_bytes(ns, n_merge) + (int64_t)n_partials * partial_slot_floats(group, d) * 4;
+        partial_offset_bytes(ns, n_merge, (int)T, Hkv) + (int64_t)n_partials * partial_slot_floats(group, d) * 4;
     if (!host_buf || host_buf_bytes < (size_t)off * 4)
         return fail(SARATHI_ERR_CAPACITY, "host_buf too small (info->packed_ints holds the size needed)");
 

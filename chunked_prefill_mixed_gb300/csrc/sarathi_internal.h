@@ -13,7 +13,8 @@ int32_t fail(int32_t code, const char* msg);
 int32_t check_shape(const sarathi_shape* shape);
 
 constexpr int kPage = 16;             // tokens per KV page (the only size built)
-constexpr int kAppendTokens = 16;     // new tokens per APPEND work item
+constexpr int kAppendHeads = 4;       // kv heads per APPEND work item (its tokens: one 128-position block's)
+constexpr int kAppendBufs = 4;        // page buffers an APPEND item cycles through
 constexpr int kTileRows = 128;        // query rows (token x head-in-group) per prefill tile
 constexpr int kMaxGroup = 16;         // q heads per kv head handled by the decode path
 constexpr int kDecodeMinSplitPages = 8;
@@ -45,18 +46,34 @@ enum ItemKind : int32_t { kAppend = 0, kPrefill = 1, kDecode = 2 };
 enum ItemField { kKind = 0, kS, kG, kStart, kCount, kSlot, kMerge, kNSplit, kQo0, kNNew, kKvp0, kNp, kKvLen,
                  kIds = 16 };
 
-// Workspace: an int32 header, then fp32 partial slots from byte kPartialOffset.
+// Workspace: an int32 header, then fp32 partial slots from a 256-byte boundary.
 //   [0] second queue's head   [1] CTAs exited   [2] error word   [3] error detail
 //   [4..11] where a bounded wait ran out   [12] first queue's head
-//   [kHdrInts + s]             append items finished for row s
-//   [kHdrInts + n_sched + m]   arrivals in merge group m
+//   [kHdrInts + f]             ready flags of the chunks' K/V: one word per
+//                              (row, 128-position block holding some of the
+//                              row's new tokens, group of kAppendHeads kv
+//                              heads), set to 1 by the APPEND item that wrote
+//                              it; row s's flags start at its req_aux entry
+//   [kHdrInts + F + m]         arrivals in merge group m (F = flag_ints)
 constexpr int kHdrInts = 16;
 constexpr int kErrWait = 1;     // a bounded wait ran out
 constexpr int kErrBounds = 2;   // a bounds check failed
 
-inline int64_t sync_ints(int n_sched, int n_merge) { return kHdrInts + (int64_t)n_sched + n_merge; }
-inline int64_t partial_offset_bytes(int n_sched, int n_merge) {
-    int64_t b = sync_ints(n_sched, n_merge) * 4;
+#if defined(__CUDACC__)
+#define SARATHI_HD __host__ __device__
+#else
+#define SARATHI_HD
+#endif
+SARATHI_HD inline int kv_groups(int Hkv) { return (Hkv + kAppendHeads - 1) / kAppendHeads; }
+// A row of n new tokens touches at most n / 128 + 2 blocks of 128 positions.
+inline int64_t flag_ints(int n_sched, int num_tokens, int Hkv) {
+    return ((int64_t)num_tokens / kTileRows + 2 * (int64_t)n_sched) * kv_groups(Hkv);
+}
+inline int64_t sync_ints(int n_sched, int n_merge, int num_tokens, int Hkv) {
+    return kHdrInts + flag_ints(n_sched, num_tokens, Hkv) + n_merge;
+}
+inline int64_t partial_offset_bytes(int n_sched, int n_merge, int num_tokens, int Hkv) {
+    int64_t b = sync_ints(n_sched, n_merge, num_tokens, Hkv) * 4;
     return (b + 255) / 256 * 256;
 }
 // One decode split writes, for each q head of its group, o[d] (normalised by

@@ -99,7 +99,7 @@ typedef struct sarathi_plan_info {
     int32_t off_kv_page_indptr; /* [n_sched+1]                                          */
     int32_t off_kv_page_indices;/* [nnz_pages]                                          */
     int32_t off_kv_last_page_len;/* [n_sched] in 1..page_size                            */
-    int32_t off_req_aux;        /* [n_sched] kernel bookkeeping (append items per row)  */
+    int32_t off_req_aux;        /* [n_sched] kernel bookkeeping (first K/V ready flag)  */
     int32_t off_items;          /* [n_items][SARATHI_ITEM_INTS] kernel work list         */
     int32_t packed_ints;        /* int32 elements to copy to the device                  */
     int64_t workspace_bytes;    /* device workspace sarathi_mixed_attn needs             */

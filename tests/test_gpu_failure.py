@@ -37,7 +37,13 @@ def test_wait_that_runs_out_is_reported_and_context_stays_usable():
     gs._k0, gs._v0 = gs.kc_dev.clone(), gs.vc_dev.clone()
     bad = gs.packed.copy()
     s = gs.meta["n_sched"] - 1                     # the prefill row
-    bad[gs.info.off_req_aux + s] += 1              # one APPEND more than will ever run
+    # the row's two APPEND items (positions 64-127 and 128-199): the first is
+    # replaced by a copy of the second, so the first block's ready flag is
+    # never set and the tiles' wait for it runs out
+    items = bad[gs.info.off_items:gs.info.off_items + gs.info.n_items * 24].reshape(-1, 24)
+    app = [i for i in range(len(items)) if items[i, 0] == 0 and items[i, 1] == s]
+    assert len(app) == 2 and items[app[0], 3] < items[app[1], 3]
+    items[app[0]] = items[app[1]]
     gs.plan_dev = gs.runner.upload(bad)
     err = gs.run()
     assert err == 1, f"expected a bounded-wait error, got {err}"

@@ -139,8 +139,11 @@ def _check_work_list(info, m, shape, num_sms=148):
             k = min(8, count)
             assert list(ids[:k]) == list(kvi[kvp[s] + start:kvp[s] + start + k]) and not ids[k:].any()
         if kind == 0:
-            assert nn >= 2
-            appended[qo[s] + start: qo[s] + start + count, :] += 1
+            # up to 4 kv heads, tokens whose positions share one 128-position block
+            assert nn >= 2 and g % 4 == 0 and 0 < count <= 128
+            h = 16 * (np_ - 1) + last[s] - nn
+            assert (h + start) // 128 == (h + start + count - 1) // 128
+            appended[qo[s] + start: qo[s] + start + count, g:g + 4] += 1
         elif kind == 1:
             # one Q tile of up to 128 // G tokens, starting on a tile boundary
             tpi = 128 // G
@@ -172,10 +175,18 @@ def _check_work_list(info, m, shape, num_sms=148):
             pos += c
         assert pos == kvp[s + 1] - kvp[s]
     assert len(seen_slots) == info.n_partials
+    # each prefill row's ready flags (one per 128-position block and group of 4
+    # kv heads) follow the previous row's, from req_aux on
     aux = m["req_aux"]
+    groups = -(-shape.H_kv // 4)
+    nxt = 0
     for s in range(n):
         nn = qo[s + 1] - qo[s]
-        assert aux[s] == (-(-nn // 16) if nn >= 2 else 0)
+        if nn >= 2:
+            h = 16 * (kvp[s + 1] - kvp[s] - 1) + last[s] - nn
+            assert aux[s] == nxt
+            nxt += ((h + nn - 1) // 128 - h // 128 + 1) * groups
+    assert nxt <= (int(qo[-1]) // 128 + 2 * n) * groups if n else True
 
 
 def test_plan_reports_errors_and_warning():
