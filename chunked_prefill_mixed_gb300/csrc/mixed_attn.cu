@@ -991,6 +991,10 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
     const int kv_hi = R.h + t0 + cnt;            // keys [0, kv_hi) are visible to some row
     const int nblk = (kv_hi + kTcKeys - 1) / kTcKeys;
     const int pages_hi = (kv_hi + kPage - 1) / kPage;
+    // a tile split along its keys runs blocks [kb0, kb1) here (j below is
+    // the block, jj its place in this item's pipeline); else every block
+    const int kb0 = it[kB0], kb1 = it[kB1] > 0 ? min(it[kB1], nblk) : nblk;
+    const int nb = kb1 - kb0;
     const uint32_t bars = smem_u32(smem + kSmemBars);
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
 
@@ -1062,9 +1066,10 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         const int fill = is_v ? kPhVFill : kPhKFill;
         uint8_t* ring = smem + (is_v ? L::kV : L::kK);
         const int32_t* kvi = P.plan + P.off_kvi + R.kvp0;
-        int id = pq < pages_hi ? it[kIds + pq] : 0;  // block 0's ids come with the item
+        int id = kb0 * 8 + pq < pages_hi ? it[kIds + pq] : 0;  // the first block's ids come with the item
         const int j_chunk = R.h / kTcKeys;  // first block with a key of the chunk
-        for (int j = 0; j < nblk; ++j) {
+        for (int jj = 0; jj < nb; ++jj) {
+            const int j = kb0 + jj;
             if (j >= j_chunk) {
                 // the block's new K/V must be in the pages: the ready flag its
                 // APPEND item sets for this tile's group of kv heads
@@ -1085,7 +1090,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 fence_proxy_async_global();  // ... and orders the TMA reads after it
             }
             if (*(volatile int*)s_abort) break;
-            const int st = j % NST;
+            const int st = jj % NST;
             const int nxt = (j + 1) * 8 + pq < pages_hi ? kvi[(j + 1) * 8 + pq] : 0;
             const int npg = min(kTcKeys / kPage, pages_hi - j * 8);
             // one box for the whole block when its pages are consecutive and in the pool
@@ -1124,13 +1129,14 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         if (lane == 0) {
             constexpr uint32_t idesc_s = umma_idesc(kTcKeys, false);
             const uint64_t qd = umma_desc(smem_u32(smem + L::kQ), 16, 1024);
-            for (int j = 0; j < nblk; ++j) {
-                const int b = j & 1;
-                if (j >= 2) {
+            for (int jj = 0; jj < nb; ++jj) {
+                const int j = kb0 + jj;
+                const int b = jj & 1;
+                if (jj >= 2) {
                     mbar_wait_bounded<true>(P, bar(kBarSFree + b), ph_get(ph, kPhSFree + b), s_abort, 4000 + j, it);
                     ph_flip(ph, kPhSFree + b);
                 }
-                const int st = j % L::kKStages;
+                const int st = jj % L::kKStages;
                 mbar_wait_bounded<true>(P, bar(kBarKFull + st), ph_get(ph, kPhKUse + st), s_abort, 3000 + j, it);
                 ph_flip(ph, kPhKUse + st);
                 tc_fence_after();
@@ -1147,15 +1153,16 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                 umma_commit(bar(kBarKEmpty + st));
             }
             // the loads of the item's last two blocks were not waited for here
-            for (int j = max(nblk - 2, 0); j < nblk; ++j) ph_flip(ph, kPhSFree + (j & 1));
+            for (int jj = max(nb - 2, 0); jj < nb; ++jj) ph_flip(ph, kPhSFree + (jj & 1));
         }
     } else if (warp == 10) {
         // ---------------- P.V issuer: O += P(j) V(j) ----------------
         if (lane == 0) {
             constexpr uint32_t idesc_o = umma_idesc(D, true);
-            for (int j = 0; j < nblk; ++j) {
-                const int b = j & 1;
-                const int vst = j % L::kVStages;
+            for (int jj = 0; jj < nb; ++jj) {
+                const int j = kb0 + jj;
+                const int b = jj & 1;
+                const int vst = jj % L::kVStages;
                 mbar_wait_bounded<true>(P, bar(kBarVFull + vst), ph_get(ph, kPhVUse + vst), s_abort, 5000 + j, it);
                 ph_flip(ph, kPhVUse + vst);
                 mbar_wait_bounded<true>(P, bar(kBarPFull + b), ph_get(ph, kPhPFull + b), s_abort, 4500 + j, it);
@@ -1168,11 +1175,11 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
                     // A = P from TMEM (16 keys = 8 columns per step); B = V (MN-major:
                     // d contiguous, keys as rows) straight from the TMA-loaded pages
                     umma_f16_ts(tmem + kTmemO, pa + (uint32_t)(kk * 8), vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+                                (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(bar(kBarVEmpty + vst));
                 umma_commit(bar(kBarOUp + b));
-                if (j == nblk - 1) umma_commit(bar(kBarODone));
+                if (jj == nb - 1) umma_commit(bar(kBarODone));
             }
         }
     } else if (warp < 8) {
@@ -1194,8 +1201,9 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         const uint32_t pair_bar = 6u + (uint32_t)quad;   // named barrier of warps q and q + 4
         constexpr int OCOLS = D / 2;                 // O columns this warp rescales and stores
         float m_run = -INFINITY, l_run = 0.f;
-        for (int j = 0; j < nblk; ++j) {
-            const int b = j & 1;
+        for (int jj = 0; jj < nb; ++jj) {
+            const int j = kb0 + jj;
+            const int b = jj & 1;
             const int kc = j * kTcKeys + hs * 64;    // first key of this warp's half
             const uint32_t s_col = kTmemS + (uint32_t)(b * kTcKeys + hs * 64);
             const uint32_t p_col = kTmemP + (uint32_t)(b * (kTcKeys / 2) + hs * 32);
@@ -1227,7 +1235,7 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             // lazy rescaling: the exponent base moves only when the block's max
             // exceeds it by more than 2^8 (both warps of the pair decide alike)
             const float m_use = mxs > m_run + 8.f ? mxs : m_run;
-            if (j >= 2) {
+            if (jj >= 2) {
                 // P buffer b was read by P(j - 2).V, issued by another thread
                 // than this block's S: wait for it before overwriting
                 mbar_wait_bounded(P, bar(kBarOUp + b), ph_get(ph, kPhOUp + b), s_abort, 6500 + j, it);
@@ -1237,7 +1245,9 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             // P = 2^(s - m) in bf16, two keys per column
             float2 sum2 = make_float2(0.f, 0.f);
             const float2 sl2v = make_float2(sl2, sl2);
-            const float2 nmv = make_float2(-m_use, -m_use);
+            // (a row of a later key piece may see no key yet: base 0, P = 0)
+            const float m_exp = m_use == -INFINITY ? 0.f : m_use;
+            const float2 nmv = make_float2(-m_exp, -m_exp);
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 uint32_t pk[16];
@@ -1259,8 +1269,8 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             // block j + 1 waits for the same phase again and counts it.
             const bool moved = m_use != m_run;
             const float alpha = moved ? exp2f(m_run - m_use) : 1.f;
-            if (j > 0 && __any_sync(0xffffffffu, moved)) {
-                mbar_wait_bounded(P, bar(kBarOUp + ((j - 1) & 1)), ph_get(ph, kPhOUp + ((j - 1) & 1)), s_abort,
+            if (jj > 0 && __any_sync(0xffffffffu, moved)) {
+                mbar_wait_bounded(P, bar(kBarOUp + ((jj - 1) & 1)), ph_get(ph, kPhOUp + ((jj - 1) & 1)), s_abort,
                                   7000 + j, it);
                 tc_fence_after();
 #pragma unroll 1
@@ -1277,9 +1287,9 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
             m_run = m_use;
             // last block: V rows past kv_hi hold other bytes; zero them so 0 x V stays 0
             if (j == nblk - 1 && j * kTcKeys + kTcKeys > kv_hi) {
-                const int vst = j % L::kVStages;
+                const int vst = jj % L::kVStages;
                 mbar_wait_bounded(P, bar(kBarVFull + vst),
-                                  ph_get(ph, kPhVSeen + vst) ^ (uint32_t)((j / L::kVStages) & 1), s_abort, 8000 + j,
+                                  ph_get(ph, kPhVSeen + vst) ^ (uint32_t)((jj / L::kVStages) & 1), s_abort, 8000 + j,
                                   it);
                 uint8_t* vb = smem + L::kV + vst * L::kTile;
                 const int first = kv_hi - j * kTcKeys;
@@ -1301,30 +1311,167 @@ __device__ void run_prefill(const KParams& P, const CUtensorMap* tmK, const CUte
         tc_fence_after();
         xsum[hs * kTileRows + r] = l_run;
         asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-        const float inv = 1.f / (l_run + xsum[(hs ^ 1) * kTileRows + r]);
+        const float lt = l_run + xsum[(hs ^ 1) * kTileRows + r];
         __nv_bfloat16* dst =
             r < rows_valid ? P.out + ((size_t)(R.qo0 + t0 + tt) * P.Hq + g * G + r % G) * D + hs * OCOLS : nullptr;
+        const int nsplit = it[kNSplit];
+        if (nsplit <= 1) {
+            const float inv = 1.f / lt;
 #pragma unroll 1
-        for (int c = 0; c < OCOLS / 32; ++c) {
-            float o[32];
-            tmem_ld32(lane_base + kTmemO + (uint32_t)(hs * OCOLS + c * 32), o);
-            if (dst) {
+            for (int c = 0; c < OCOLS / 32; ++c) {
+                float o[32];
+                tmem_ld32(lane_base + kTmemO + (uint32_t)(hs * OCOLS + c * 32), o);
+                if (dst) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) =
-                        make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
-                                   pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                                   pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                                   pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) =
+                            make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                       pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                       pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                       pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+                }
+            }
+        } else {
+            // one key piece of a split tile.  Its partial -- O / l in fp32
+            // ([128 rows][d]), then the rows' base m[128] and sum l[128] -- goes
+            // to global memory through a staging copy in the (now idle) ring
+            // buffers, so that the stores are coalesced; the last piece to
+            // arrive merges: out = sum_k O_k 2^(m_k - M) / sum_k l_k 2^(m_k - M),
+            // its own O straight from TMEM and the others' copied into shared
+            // memory with cp.async.  Shared rows hold 16-byte chunks in
+            // XOR-swizzled order (chunk c of row r at c ^ (r & 7)): the row's
+            // owner and a warp sweeping a row both access it conflict-free.
+            constexpr int F4 = D / 4;              // 16-byte chunks per row
+            constexpr int RPW = 32 / F4;           // rows per warp instruction when sweeping rows
+            const int sub = lane / F4, c4 = lane % F4;
+            const int piece = it[kPiece];
+            const size_t piece_floats = (size_t)pf_piece_slots(G) * P.slot_floats;
+            float* base = P.ws_part + (size_t)it[kSlot] * P.slot_floats;
+            float* part = base + (size_t)piece * piece_floats;
+            float4* stg = reinterpret_cast<float4*>(smem);
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < OCOLS / 32; ++c) {
+                float o[32];
+                tmem_ld32(lane_base + kTmemO + (uint32_t)(hs * OCOLS + c * 32), o);
+                const int lc0 = (hs * OCOLS + c * 32) / 4;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    stg[r * F4 + ((lc0 + q) ^ (r & 7))] =
+                        make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv, o[4 * q + 3] * inv);
+            }
+            if (hs == 0 && r < rows_valid) {
+                __stcg(part + kTileRows * D + r, m_run);
+                __stcg(part + kTileRows * D + kTileRows + r, lt);
+            }
+            __syncwarp();  // bar.sync wants converged warps
+            asm volatile("bar.sync 10, 256;" ::: "memory");
+            for (int rr = warp * RPW + sub; rr < rows_valid; rr += 8 * RPW)
+                __stcg(reinterpret_cast<float4*>(part + (size_t)rr * D) + c4, stg[rr * F4 + (c4 ^ (rr & 7))]);
+            int* s_last = reinterpret_cast<int*>(xsum + 2 * kTileRows);
+            int* ticket = &P.ws_int[kHdrInts + P.n_flags + it[kMerge]];
+            __threadfence();
+            __syncwarp();  // bar.sync wants converged warps
+            asm volatile("bar.sync 10, 256;" ::: "memory");
+            if (tid == 0) {
+                const int old = atomicAdd(ticket, 1);
+                *s_last = old == nsplit - 1;
+                if (old == nsplit - 1) __threadfence();
+            }
+            __syncwarp();  // bar.sync wants converged warps
+            asm volatile("bar.sync 10, 256;" ::: "memory");
+            if (*s_last) {
+                // the other pieces' O / l into shared slots 0.. (the staging
+                // copy is read out), and the m, l of this thread's row of every
+                // piece.  The merge takes the pieces in index order, each from
+                // its O / l (this piece's recomputed from TMEM: the same fp32
+                // products it stored), so its bits do not depend on which
+                // piece arrived last.
+                float mk[kMaxPieces], lk[kMaxPieces];
+#pragma unroll
+                for (int k = 0; k < kMaxPieces; ++k) {
+                    mk[k] = k == piece ? m_run : -INFINITY;
+                    lk[k] = k == piece ? lt : 0.f;
+                    if (k < nsplit && k != piece) {
+                        const float* src = base + (size_t)k * piece_floats;
+                        const uint32_t dsl = smem_u32(stg + (size_t)(k < piece ? k : k - 1) * kTileRows * F4);
+                        for (int rr = warp * RPW + sub; rr < rows_valid; rr += 8 * RPW)
+                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                                             dsl + (uint32_t)(rr * F4 + (c4 ^ (rr & 7))) * 16u),
+                                         "l"(src + (size_t)rr * D + 4 * c4)
+                                         : "memory");
+                        if (r < rows_valid) {
+                            mk[k] = __ldcg(src + kTileRows * D + r);
+                            lk[k] = __ldcg(src + kTileRows * D + kTileRows + r);
+                        }
+                    }
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncwarp();  // bar.sync wants converged warps
+                asm volatile("bar.sync 10, 256;" ::: "memory");
+                {
+                    // every lane runs this (tcgen05.ld is warp-collective); only
+                    // the rows of the tile's tokens are stored
+                    float M = mk[0];
+#pragma unroll
+                    for (int k = 1; k < kMaxPieces; ++k) M = fmaxf(M, mk[k]);
+                    float w[kMaxPieces], L = 0.f;
+#pragma unroll
+                    for (int k = 0; k < kMaxPieces; ++k) {
+                        w[k] = mk[k] == -INFINITY ? 0.f : lk[k] * exp2f(mk[k] - M);
+                        L += w[k];
+                    }
+                    const float invL = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+                    for (int k = 0; k < kMaxPieces; ++k) w[k] *= invL;
+#pragma unroll 1
+                    for (int c = 0; c < OCOLS / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(lane_base + kTmemO + (uint32_t)(hs * OCOLS + c * 32), o);
+                        const int lc0 = (hs * OCOLS + c * 32) / 4;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 own = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv,
+                                                           o[4 * q + 3] * inv);
+                            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int k = 0; k < kMaxPieces; ++k) {
+                                if (k < nsplit) {
+                                    const float4 x =
+                                        k == piece ? own
+                                                   : stg[(size_t)(k < piece ? k : k - 1) * kTileRows * F4 + r * F4 +
+                                                         ((lc0 + q) ^ (r & 7))];
+                                    acc.x += x.x * w[k];
+                                    acc.y += x.y * w[k];
+                                    acc.z += x.z * w[k];
+                                    acc.w += x.w * w[k];
+                                }
+                            }
+                            o[4 * q] = acc.x;
+                            o[4 * q + 1] = acc.y;
+                            o[4 * q + 2] = acc.z;
+                            o[4 * q + 3] = acc.w;
+                        }
+                        if (dst) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                *reinterpret_cast<uint4*>(dst + c * 32 + q * 8) = make_uint4(
+                                    pack_bf16(o[8 * q], o[8 * q + 1]), pack_bf16(o[8 * q + 2], o[8 * q + 3]),
+                                    pack_bf16(o[8 * q + 4], o[8 * q + 5]), pack_bf16(o[8 * q + 6], o[8 * q + 7]));
+                        }
+                    }
+                }
+                if (tid == 0) *ticket = 0;
             }
         }
         tc_fence_before();
         // carried across items: the P.V groups not waited for above (the last
         // two blocks'), and the V loads per stage of this item
-        for (int j = max(nblk - 2, 0); j < nblk; ++j) ph_flip(ph, kPhOUp + (j & 1));
+        for (int jj = max(nb - 2, 0); jj < nb; ++jj) ph_flip(ph, kPhOUp + (jj & 1));
 #pragma unroll
         for (int st = 0; st < L::kVStages; ++st)
-            if (((nblk - st + L::kVStages - 1) / L::kVStages) & 1) ph_flip(ph, kPhVSeen + st);
+            if (((nb - st + L::kVStages - 1) / L::kVStages) & 1) ph_flip(ph, kPhVSeen + st);
     }
 }
 

@@ -11,6 +11,7 @@
 #include <array>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <string>
 #include <vector>
 
@@ -80,6 +81,12 @@ constexpr double kDecodeFixedNs = 2000.0;
 constexpr double kDecodeBytesPerNs = 40.0;       // a decode split's share of HBM with every SM streaming
 constexpr double kDecodeAloneBytesPerNs = 80.0;  // one SM's own streaming rate when HBM has room
 constexpr double kHbmBytesPerNs = 6500.0;        // the whole GPU
+// an APPEND item: per (token, kv head) it rotates and stores
+constexpr double kAppendFixedNs = 1500.0;
+constexpr double kAppendNsPerTokenHead = 45.0;
+// a key piece of a split tile: a tile's fixed start, plus its partial's
+// write and (for the last piece) the merge
+constexpr double kPieceExtraNs = 4500.0;
 
 }  // namespace
 }  // namespace sarathi
@@ -118,13 +125,17 @@ extern "C" int32_t sarathi_plan_bounds(const sarathi_request* reqs, int32_t n_re
     // (rows x kv heads) items
     const int64_t dec_items =
         std::min<int64_t>((pages / kDecodeMinSplitPages + n) * Hkv, (int64_t)num_sms * kDecodeItemsPerSm + n * Hkv);
-    const int64_t items = appends + tiles + dec_items;
+    // key pieces: at most num_sms tiles of a step are split, into at most
+    // kMaxPieces pieces each
+    const int64_t pieces_extra = (int64_t)num_sms * (kMaxPieces - 1);
+    const int64_t items = appends + tiles + dec_items + pieces_extra;
     const int64_t ints = 6 * n + 2 + pages + 8 + items * kItemInts;
     if (host_buf_bytes) *host_buf_bytes = (size_t)ints * 4;
     if (device_workspace_bytes) {
-        const int64_t n_merge = n * Hkv;
+        const int64_t n_merge = n * Hkv + num_sms;
+        const int64_t slots = dec_items + 1 + (int64_t)num_sms * kMaxPieces * pf_piece_slots(group);
         *device_workspace_bytes = (size_t)(partial_offset_bytes((int)n, (int)n_merge, (int)T, (int)Hkv) +
-                                           dec_items * partial_slot_floats(group, shape->head_dim) * 4);
+                                           slots * partial_slot_floats(group, shape->head_dim) * 4);
     }
     return SARATHI_OK;
 }
@@ -158,7 +169,7 @@ struct PlanScratch {
     std::vector<int32_t> np, hist, aux;
     std::vector<ItemHead> appends;
     std::vector<Timed> tiles, decs;
-    std::vector<double> key, pred;
+    std::vector<double> key, pred, heap, snaps;
     std::vector<int64_t> grp;
     std::vector<uint32_t> pf_order, dec_order, bucket;
 };
@@ -420,8 +431,88 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
         first_sms = std::min<int32_t>((lo + hi) / 2, (int32_t)n_tiles);
     }
     const bool apps_first = decs.empty();
-    const int64_t n_first = (int64_t)n_tiles + (apps_first ? (int64_t)appends.size() : 0);
-    const int64_t n_items = (int64_t)n_tiles + (int64_t)appends.size() + (int64_t)decs.size();
+
+    // ---- 3b. key pieces for the last tiles.  Without decodes every CTA takes
+    // the one queue in order (APPENDs, then the tiles), so the step ends with
+    // the list schedule of the queue: each item starts on the CTA that frees
+    // first.  Tiles of similar cost leave a last wave that can hold a few
+    // SMs busy while the rest idle; cutting the last split_k tiles into
+    // split_n pieces along their 128-key blocks (merged by log-sum-exp, like
+    // decode splits) trades a fixed cost per piece for a finer tail.  The
+    // pair comes from simulating that schedule with the cost model.
+    int64_t split_k = 0;
+    int32_t split_n = 1;
+    auto tile_blocks = [&](const ItemHead& t) {
+        return (int32_t)ceil_div((int64_t)hist[t[kS]] + t[kStart] + t[kCount], kTileRows);
+    };
+    if (apps_first && n_tiles >= 2 && num_sms > 1) {
+        std::vector<double>& heap = sc.heap;
+        std::vector<double>& snaps = sc.snaps;
+        auto take_next = [&](double est) {  // the CTA that frees first takes an item; its end
+            std::pop_heap(heap.begin(), heap.end(), std::greater<double>());
+            const double e = heap.back() += est;
+            std::push_heap(heap.begin(), heap.end(), std::greater<double>());
+            return e;
+        };
+        heap.assign((size_t)num_sms, 0.0);
+        for (auto& a : appends)
+            take_next(kAppendFixedNs + kAppendNsPerTokenHead * a[kCount] * std::min<int>(kAppendHeads, Hkv - a[kG]));
+        // candidate split_k: quarters of the SM count, up to all of it
+        constexpr int kCand = 4;
+        int64_t cand[kCand];
+        int n_cand = 0;
+        for (int q = 1; q <= kCand; ++q) {
+            const int64_t k = std::min<int64_t>((int64_t)num_sms * q / 4, (int64_t)n_tiles);
+            if (k > 0 && (n_cand == 0 || k != cand[n_cand - 1])) cand[n_cand++] = k;
+        }
+        snaps.resize((size_t)n_cand * num_sms);
+        for (size_t i = 0; i < n_tiles; ++i) {
+            for (int c = 0; c < n_cand; ++c)
+                if ((int64_t)(n_tiles - i) == cand[c]) std::copy(heap.begin(), heap.end(), snaps.begin() + (size_t)c * num_sms);
+            take_next(tiles[pf_order[i]].ns_est);
+        }
+        double best = *std::max_element(heap.begin(), heap.end());
+        const double unsplit = best;
+        for (int c = 0; c < n_cand; ++c) {
+            for (int32_t n = 2; n <= kMaxPieces; ++n) {
+                heap.assign(snaps.begin() + (size_t)c * num_sms, snaps.begin() + (size_t)(c + 1) * num_sms);
+                double m = *std::max_element(heap.begin(), heap.end());
+                for (size_t i = n_tiles - (size_t)cand[c]; i < n_tiles && m < best; ++i) {
+                    const Timed& t = tiles[pf_order[i]];
+                    const int32_t nb = tile_blocks(t.it);
+                    if (nb < 2 * n) {
+                        m = std::max(m, take_next(t.ns_est));
+                        continue;
+                    }
+                    const double per = (t.ns_est - kPrefillFixedNs) / n + kPrefillFixedNs + kPieceExtraNs;
+                    for (int32_t k = 0; k < n; ++k) m = std::max(m, take_next(per));
+                }
+                if (m < best) {
+                    best = m;
+                    split_k = cand[c];
+                    split_n = n;
+                }
+            }
+        }
+        // keep the plain schedule unless the model gains clearly
+        if (best > unsplit * 0.97) {
+            split_k = 0;
+            split_n = 1;
+        }
+    }
+    int64_t n_pieces_extra = 0;
+    for (size_t i = n_tiles - (size_t)split_k; i < n_tiles; ++i)
+        if (tile_blocks(tiles[pf_order[i]].it) >= 2 * split_n) n_pieces_extra += split_n - 1;
+    const int64_t n_first = (int64_t)n_tiles + n_pieces_extra + (apps_first ? (int64_t)appends.size() : 0);
+    const int64_t n_items = (int64_t)n_tiles + n_pieces_extra + (int64_t)appends.size() + (int64_t)decs.size();
+    // partial slots and merge groups of the pieces (after the decodes')
+    int32_t piece_slot0 = n_partials + ((group & 1) && (n_partials & 1) ? 1 : 0);
+    const int32_t piece_merge0 = n_merge;
+    const int32_t n_split_tiles = (int32_t)(n_pieces_extra / std::max(split_n - 1, 1));
+    if (n_split_tiles > 0) {
+        n_partials = piece_slot0 + n_split_tiles * split_n * pf_piece_slots(group);
+        n_merge += n_split_tiles;
+    }
 
     // ---- 4. packed layout
     int64_t off = 0;
@@ -480,7 +571,7 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     }
     int32_t* items = b + info->off_items;
     int64_t w = 0;
-    auto put = [&](const ItemHead& src) {
+    auto put = [&](const ItemHead& src, int32_t b0 = 0, int32_t b1 = 0, int32_t piece = 0) {
         int32_t* it = items + kItemInts * w++;
         std::memcpy(it, src.data(), sizeof src);
         const int32_t s = it[kS];
@@ -490,11 +581,15 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
         it[kNp] = np[s];
         it[kKvLen] = kPage * (np[s] - 1) + b[info->off_kv_last_page_len + s];
         for (int k = kKvLen + 1; k < kIds; ++k) it[k] = 0;
+        it[kB0] = b0;
+        it[kB1] = b1;
+        it[kPiece] = piece;
         int32_t* ids = it + kIds;
         if (it[kKind] == kDecode) {
             for (int k = 0; k < kItemIds; ++k) ids[k] = k < it[kCount] ? kvi[kvp[s] + it[kStart] + k] : 0;
         } else if (it[kKind] == kPrefill) {
-            for (int k = 0; k < kItemIds; ++k) ids[k] = k < np[s] ? kvi[kvp[s] + k] : 0;
+            const int32_t p0 = b0 * (kTileRows / kPage);  // the pages of the item's first block
+            for (int k = 0; k < kItemIds; ++k) ids[k] = p0 + k < np[s] ? kvi[kvp[s] + p0 + k] : 0;
         } else {
             for (int k = 0; k < kItemIds; ++k) ids[k] = 0;
         }
@@ -502,7 +597,22 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     // the first queue, then the second
     if (apps_first)
         for (auto& a : appends) put(a);
-    for (uint32_t i : pf_order) put(tiles[i].it);
+    for (size_t i = 0; i < n_tiles - (size_t)split_k; ++i) put(tiles[pf_order[i]].it);
+    int32_t mg = piece_merge0;
+    for (size_t i = n_tiles - (size_t)split_k; i < n_tiles; ++i) {
+        const ItemHead& t = tiles[pf_order[i]].it;
+        const int32_t nb = tile_blocks(t);
+        if (nb < 2 * split_n) {
+            put(t);
+            continue;
+        }
+        ItemHead h = t;
+        h[kSlot] = piece_slot0;
+        h[kMerge] = mg++;
+        h[kNSplit] = split_n;
+        for (int32_t k = 0; k < split_n; ++k) put(h, (int32_t)((int64_t)nb * k / split_n), (int32_t)((int64_t)nb * (k + 1) / split_n), k);
+        piece_slot0 += split_n * pf_piece_slots(group);
+    }
     if (!apps_first)
         for (auto& a : appends) put(a);
     for (uint32_t i : dec_order) put(decs[i].it);

@@ -39,12 +39,15 @@ enum ItemKind : int32_t { kAppend = 0, kPrefill = 1, kDecode = 2 };
 //   [8..12]      row s: qo_indptr[s], new tokens, kv_page_indptr[s], pages,
 //                kv length -- copies of the metadata, so that an item needs
 //                one load before its first page can be fetched
-//   [13..15]     zero
+//   [13..15]     prefill: the item's 128-key blocks [b0, b1) and its piece
+//                index when its tile is split along the keys (then [5..7] are
+//                the tile's first partial slot, merge group and piece count,
+//                as for decode splits); 0, 0, 0: the whole tile
 //   [16..23]     decode: the page id of page start + w for decode warp w (0
-//                past the item's pages); prefill: the ids of the request's
-//                pages 0..7 (0 past its pages); append: zero
+//                past the item's pages); prefill: the ids of the pages of its
+//                first block (0 past the request's pages); append: zero
 enum ItemField { kKind = 0, kS, kG, kStart, kCount, kSlot, kMerge, kNSplit, kQo0, kNNew, kKvp0, kNp, kKvLen,
-                 kIds = 16 };
+                 kB0, kB1, kPiece, kIds = 16 };
 
 // Workspace: an int32 header, then fp32 partial slots from a 256-byte boundary.
 //   [0] second queue's head   [1] CTAs exited   [2] error word   [3] error detail
@@ -81,6 +84,16 @@ inline int64_t partial_offset_bytes(int n_sched, int n_merge, int num_tokens, in
 inline int64_t partial_slot_floats(int group, int d) { return (int64_t)group * (d + 2); }
 
 inline int tokens_per_tile(int group) { return group >= kTileRows ? 1 : kTileRows / group; }
+// A prefill tile split along its keys runs as 2..kMaxPieces pieces; each
+// piece's partial ([128][d] fp32 O / l, then m[128], l[128]) takes
+// pf_piece_slots(group) partial slots: an even count when the group is odd,
+// so that every piece's partial starts on a 16-byte boundary (the first slot
+// of a split tile is even too).
+constexpr int kMaxPieces = 4;
+SARATHI_HD inline int pf_piece_slots(int group) {
+    const int n = (kTileRows + group - 1) / group;
+    return (group & 1) ? (n + 1) / 2 * 2 : n;
+}
 // A prefill item is one Q tile.
 inline int tokens_per_item(int group) { return tokens_per_tile(group); }
 

@@ -95,7 +95,9 @@ def _check_work_list(info, m, shape, num_sms=148):
     once per kv head; decode splits tile each decode's pages; the first queue
     holds the prefill tiles and the second the decode splits; the appends lead
     the second queue (the first when there are no decodes), so a CTA that waits
-    on one never holds up the CTAs that take them."""
+    on one never holds up the CTAs that take them.  A tile split along its keys
+    comes as pieces whose 128-key block ranges tile [0, nblk) in order, with
+    partial slots of their own."""
     G = shape.H_q // shape.H_kv
     n = m["n_sched"]
     qo, kvp = m["qo_indptr"], m["kv_page_indptr"]
@@ -105,6 +107,9 @@ def _check_work_list(info, m, shape, num_sms=148):
     appended = np.zeros((T, shape.H_kv), np.int32)
     seen_slots = set()
     pages_cov = {}
+    pieces = {}
+    spt = -(-128 // G)
+    spt += spt & (G & 1)
     kvi, last = m["kv_page_indices"], m["kv_last_page_len"]
     kinds = items[:, 0] if len(items) else np.zeros(0, np.int32)
     nf = info.n_first
@@ -128,13 +133,16 @@ def _check_work_list(info, m, shape, num_sms=148):
         np_ = kvp[s + 1] - kvp[s]
         # the row's metadata copied into the item, and the page ids it carries
         assert list(it[8:13]) == [qo[s], nn, kvp[s], np_, 16 * (np_ - 1) + last[s]]
-        assert not it[13:16].any()
+        b0, b1, piece = (int(x) for x in it[13:16])
+        if kind != 1 or nsplit == 1:
+            assert b0 == b1 == piece == 0
         ids = it[16:24]
         if kind == 0:
             assert not ids.any()
         elif kind == 1:
-            k = min(8, np_)
-            assert list(ids[:k]) == list(kvi[kvp[s]:kvp[s] + k]) and not ids[k:].any()
+            p0 = 8 * b0
+            k = max(min(8, np_ - p0), 0)
+            assert list(ids[:k]) == list(kvi[kvp[s] + p0:kvp[s] + p0 + k]) and not ids[k:].any()
         else:
             k = min(8, count)
             assert list(ids[:k]) == list(kvi[kvp[s] + start:kvp[s] + start + k]) and not ids[k:].any()
@@ -148,6 +156,19 @@ def _check_work_list(info, m, shape, num_sms=148):
             # one Q tile of up to 128 // G tokens, starting on a tile boundary
             tpi = 128 // G
             assert 0 < count <= tpi and start % tpi == 0 and start + count <= nn
+            if nsplit > 1:
+                h = 16 * (np_ - 1) + last[s] - nn
+                nblk = -(-(h + start + count) // 128)
+                assert 2 <= nsplit <= 4 and 0 <= b0 < b1 <= nblk and 0 <= piece < nsplit
+                assert 0 <= merge < info.n_merge and slot >= 0 and (slot % 2 == 0 or G % 2 == 0)
+                pieces.setdefault((slot, merge), []).append((piece, b0, b1, nblk, nsplit, s, g, start))
+                for q in range(spt):
+                    assert slot + piece * spt + q not in seen_slots
+                    seen_slots.add(slot + piece * spt + q)
+                if piece != 0:
+                    continue
+            else:
+                assert slot == -1 and merge == -1
             for t in range(start, start + count):
                 covered[qo[s] + t, g * G:(g + 1) * G] += 1
         else:
@@ -174,7 +195,14 @@ def _check_work_list(info, m, shape, num_sms=148):
             assert a == pos and c > 0
             pos += c
         assert pos == kvp[s + 1] - kvp[s]
-    assert len(seen_slots) == info.n_partials
+    for key, ps in pieces.items():
+        ps.sort()
+        assert [p[0] for p in ps] == list(range(ps[0][4]))
+        assert len({p[3:] for p in ps}) == 1
+        assert ps[0][1] == 0 and ps[-1][2] == ps[0][3]
+        assert all(ps[i][2] == ps[i + 1][1] for i in range(len(ps) - 1))
+    assert len(seen_slots) <= info.n_partials and (not seen_slots or max(seen_slots) < info.n_partials)
+    assert info.n_partials - len(seen_slots) <= 1
     # each prefill row's ready flags (one per 128-position block and group of 4
     # kv heads) follow the previous row's, from req_aux on
     aux = m["req_aux"]
