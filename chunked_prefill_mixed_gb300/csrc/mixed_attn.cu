@@ -445,25 +445,23 @@ __device__ __forceinline__ void rope8(uint4 a, uint4 b, const float* ch, const d
 // Key rotation for the APPEND items, branch-free.  For one output y = a p +
 // b q (p, q = cos, sin of the angle, |p|, |q| <= 1) the fp32 value
 // u = fl(fma(a, p_hi, fl(b q_hi))) lies within 3.1 2^-24 (|a| + |b|) of the
-// fp64 evaluation (the lo parts of p and q, the two roundings, and the fp64
-// evaluation's own error, which is below 2^-52 (|a| + |b|)).  bf16 rounding
-// boundaries lie where the low 16 bits of u's fp32 encoding are 0x8000, one
-// fp32 ulp = 2^(E - 150) apart for u's biased exponent E; with E_m the biased
-// exponent of |a| + |b| (so |a| + |b| < 2^(E_m - 126)), the error is below
-// 3.1 2^(E_m - E) ulps.  When the low bits are more than 4 << (E_m - E) from
-// 0x8000, u and the fp64 value round to the same bf16 (to nearest even) -- all
-// but about one output in 10^3; the others are queued and redone by rope_bf16.
-// (E_m - E is clamped to [0, 13]: at 13 the threshold reaches 0x8000 and
-// nothing passes.)
-__device__ __forceinline__ uint32_t exp_bits(float x) { return (__float_as_uint(x) >> 23) & 0xFFu; }
-__device__ __forceinline__ float rope_fast(float a, float b, float p_hi, float q_hi, uint32_t em, bool& sure) {
+// fp64 evaluation v (the lo parts of p and q, the two roundings, and the fp64
+// evaluation's own error, which is below 2^-52 (|a| + |b|)); eb = 3.25 2^-24
+// (|a| + |b|) in fp32 bounds it strictly.  Rounding to nearest even changes
+// bf16 value only at the midpoints between bf16 numbers.  m, u's fp32 encoding
+// with its low 16 bits set to 0x8000, is the midpoint inside u's bf16 interval
+// (u - m is exact: same sign and exponent); the neighbouring intervals'
+// midpoints lie at least a quarter bf16 ulp of u, so at least |u| 2^-10, from
+// u.  Hence |u - m| > eb and |u| >= 1024 eb mean that no midpoint lies between
+// u and v: both round to the same bf16 -- all but about one output in 10^3;
+// the others are queued and redone by rope_bf16.
+__device__ __forceinline__ float rope_fast(float a, float b, float p_hi, float q_hi, float eb, float ebk, bool& sure) {
     const float u = fmaf(a, p_hi, b * q_hi);
-    const uint32_t ub = __float_as_uint(u);
-    const int dist = abs((int)(ub & 0xFFFFu) - 0x8000);
-    const int de = min(max((int)em - (int)exp_bits(u), 0), 13);
-    sure = dist > (4 << de);
+    const float m = __uint_as_float((__float_as_uint(u) & 0xFFFF0000u) | 0x8000u);
+    sure = (fabsf(u - m) > eb) & (fabsf(u) >= ebk);
     return u;
 }
+constexpr float kRopeErrScale = 3.25f / 16777216.f;  // 3.25 2^-24
 // Fix-up queue entry: where the output goes (byte offset in shared memory), its
 // pair and token (pair j, output 0 or 1, item-local token), and x0, x1.
 struct RopeFix {
@@ -520,10 +518,10 @@ __device__ __forceinline__ void rope8_key(uint4 a, uint4 b, const float* hrow, i
     uint32_t unsure = 0;
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-        const uint32_t em = exp_bits(fabsf(x0[p]) + fabsf(x1[p]));
+        const float eb = (fabsf(x0[p]) + fabsf(x1[p])) * kRopeErrScale, ebk = eb * 1024.f;
         bool s0, s1;
-        y0[p] = rope_fast(x0[p], -x1[p], ch[p], sh[p], em, s0);
-        y1[p] = rope_fast(x1[p], x0[p], ch[p], sh[p], em, s1);
+        y0[p] = rope_fast(x0[p], -x1[p], ch[p], sh[p], eb, ebk, s0);
+        y1[p] = rope_fast(x1[p], x0[p], ch[p], sh[p], eb, ebk, s1);
         unsure |= (s0 ? 0u : 1u << p) | (s1 ? 0u : 0x100u << p);
     }
     uint32_t wl[4], wh[4];
@@ -625,150 +623,136 @@ __device__ __forceinline__ void load_rope_hi(const float* row, int j0, float (&c
 // APPEND: rotate + store the K/V of the prefill tokens of one 128-position
 // block (up to 8 pages), for up to kAppendHeads kv heads
 // ----------------------------------------------------------------------------
-// Per page, two TMA boxes bring the K and V rows from k/v's [token][kv head][d]
-// layout as [head][16 tokens][d] -- the order of a page's slots -- and a third
-// the cos_hi / sin_hi planes of the positions' fp32 RoPE rows.  V goes straight
-// back out to the page with one bulk store per head (no thread touches it); K
-// is rotated in place (certified rounding) and stored the same way.
-// kAppendBufs page buffers: later pages' loads fly while a page is rotated, so
-// the item costs about one memory round trip plus its rotations.  The item then sets its ready flag,
-// which the prefill tiles of its kv heads wait for before they load the block.
+// Every page's K rows arrive at once: per page, lane k of warp 0 issues one TMA
+// box that brings them from k's [token][kv head][d] layout as [head][16
+// tokens][d] -- the order of a page's slots -- and another with the cos_hi /
+// sin_hi planes of the page's positions (one mbarrier per page).  The threads
+// rotate the K rows in place as their pages land (certified rounding, the rare
+// uncertain outputs redone from a queue), lane k stores page k's row runs with
+// bulk copies, and once they have been read out it loads page k's V rows into
+// the same buffer (the barrier's next phase) and stores them the same way.
+// The item then sets its ready flag, which the prefill tiles of its kv heads
+// wait for before they load the block.
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
                  : "memory");
 }
 template <int D, bool IL>
-__device__ void run_append(const KParams& P, const CUtensorMap* tmKin, const CUtensorMap* tmVin, const int* it,
-                           uint8_t* smem, uint32_t bar0, uint32_t* s_phase, int* s_abort, int* s_fix) {
+__device__ void run_append(const KParams& P, const CUtensorMap* tmKin, const CUtensorMap* tmVin,
+                           const CUtensorMap* tmRA, const int* it, uint8_t* smem, uint32_t bar0, uint32_t* s_phase,
+                           int* s_abort, int* s_fix) {
     const int tid = threadIdx.x;
     const int s = it[kS], g0 = it[kG], t0 = it[kStart], cnt = it[kCount];
     const Row R = row_geom(it);
     const int Hkv = P.Hkv;
     constexpr int HALF = D / 2;
     constexpr int ROW = D * 2;                           // bytes of one (token, head) row
-    constexpr int BOX = kAppendHeads * kPage * ROW;      // bytes of one tensor's box
-    constexpr int RROW = HALF * 16;                      // bytes of one position's fp32 RoPE row
-    constexpr int BUF = 2 * BOX + kPage * RROW;          // K box, V box, RoPE rows of one page
-    constexpr int NB = kAppendBufs;
-    static_assert(NB * BUF <= kSmemStages && NB % 2 == 0, "APPEND page buffers");
+    constexpr int KBOX = kAppendHeads * kPage * ROW;     // one page's K (or V) rows, [head][slot][d]
+    constexpr int TROW = D * 4;                          // cos_hi, sin_hi of one position
+    constexpr int TBOX = kPage * TROW;                   // ... of one page's positions
+    constexpr int kMaxPg = kTileRows / kPage;            // pages of a 128-position block
+    constexpr int TBASE = kMaxPg * KBOX;
+    static_assert(TBASE + kMaxPg * TBOX <= kSmemStages && kAppendBufs >= kMaxPg && kMaxPg <= 32,
+                  "APPEND shared memory");
     const int ng = min(kAppendHeads, Hkv - g0);          // heads of this item
     const int pos0 = R.h + t0;                           // position of the item's first token
-    const int npg = (pos0 + cnt - 1) / kPage - pos0 / kPage + 1;
+    const int pg0 = pos0 / kPage;
+    const int npg = (pos0 + cnt - 1) / kPage - pg0 + 1;
     const int32_t* pages = P.plan + P.off_kvi + R.kvp0;
     // every page id and the RoPE table bound checked up front (all threads alike)
     bool ok = pos0 + cnt <= P.rope_max_pos;
     int bad = pos0 + cnt - 1;
     for (int k = 0; k < npg && ok; ++k) {
-        bad = pages[pos0 / kPage + k];
+        bad = pages[pg0 + k];
         ok = bad >= 0 && bad < P.num_pages;
     }
-    uint16_t* kc = reinterpret_cast<uint16_t*>(P.k_cache);
-    uint16_t* vc = reinterpret_cast<uint16_t*>(P.v_cache);
-    // tokens [tk0, tk0 + tkc) of the item lie in its page k
-    auto span = [&](int k, int& tk0, int& tkc) {
-        const int pa = (pos0 / kPage + k) * kPage;
-        tk0 = max(pos0, pa) - pos0;
-        tkc = min(pos0 + cnt, pa + kPage) - pos0 - tk0;
-    };
-    auto issue = [&](int k) {
-        int tk0, tkc;
-        span(k, tk0, tkc);
-        uint8_t* base = smem + (k % NB) * BUF;
-        const uint32_t bar = bar0 + 8u * (uint32_t)(k % NB);
-        mbar_expect_tx(bar, 2u * BOX + (uint32_t)(tkc * RROW));
-        tma_load_3d(smem_u32(base), tmKin, 0, R.qo0 + t0 + tk0, g0, bar);
-        tma_load_3d(smem_u32(base + BOX), tmVin, 0, R.qo0 + t0 + tk0, g0, bar);
-        bulk_load(smem_u32(base + 2 * BOX), P.ropef + (size_t)(pos0 + tk0) * HALF * 4, (uint32_t)(tkc * RROW), bar);
-    };
     RopeFix* fixq = reinterpret_cast<RopeFix*>(smem + kSmemDecQ);  // idle during APPEND items
     static_assert(kRopeFixCap * sizeof(RopeFix) <= 2 * kPageHalfBytes, "fix-up queue");
-    uint32_t ph = *s_phase;  // completed-phase parities of the buffers' barriers
+    // completed-phase parities of the pages' barriers: each completes two
+    // phases per item (K and table rows, then V rows)
+    const uint32_t ph = *s_phase;
+    // lane k of warp 0 runs page k's copies: its slots' positions [lo, hi)
+    const int lane_pg = tid < 32 ? tid : 0;
+    const int pa = (pg0 + lane_pg) * kPage;
+    const int lo_pos = max(pos0, pa), hi_pos = min(pos0 + cnt, pa + kPage);
+    const uint32_t pbar = bar0 + 8u * (uint32_t)lane_pg;
+    uint8_t* pbuf = smem + lane_pg * KBOX;
+    const bool copier = ok && tid < npg;
     if (!ok) {
         if (tid == 0) raise_error(P, kErrBounds, bad, s_abort);
     } else {
-        if (tid == 0)
-            for (int k = 0; k < NB && k < npg; ++k) issue(k);
-        // pages two at a time: (2i, 2i + 1); the K rows of both, eight pairs per thread
-        for (int i = 0; 2 * i < npg; ++i) {
-            const int kp[2] = {2 * i, 2 * i + 1};
-            const int np2 = min(2, npg - 2 * i);
-            int tk0[2] = {0, 0}, tkc[2] = {0, 0};
-            size_t dst0[2] = {0, 0};
-            for (int q = 0; q < np2; ++q) {
-                const int b = kp[q] % NB;
-                span(kp[q], tk0[q], tkc[q]);
-                if (!mbar_wait_bounded(P, bar0 + 8u * (uint32_t)b, (ph >> b) & 1u, s_abort, 10000 + kp[q], it)) return;
-                ph ^= 1u << b;
-                const int pos = pos0 + tk0[q];
-                dst0[q] = (((size_t)pages[pos / kPage] * Hkv + g0) * kPage + pos % kPage) * D;
-                if (tid == 0)
-                    for (int g = 0; g < ng; ++g)
-                        bulk_store(vc + dst0[q] + (size_t)g * kPage * D,
-                                   smem_u32(smem + b * BUF + BOX + g * kPage * ROW), (uint32_t)(tkc[q] * ROW));
+        if (copier) {
+            // the page's 16 slots: the box starts at the slot of the page's
+            // first position (rows outside the item are loaded, not used)
+            mbar_expect_tx(pbar, (uint32_t)(KBOX + TBOX));
+            tma_load_3d(smem_u32(pbuf), tmKin, 0, R.qo0 + t0 + (pa - pos0), g0, pbar);
+            tma_load_2d(smem_u32(smem + TBASE + lane_pg * TBOX), tmRA, 0, pa, pbar);
+        }
+        // K: eight pairs of one (token, head) row per unit, in token order
+        int* fix_n = s_fix;
+        const int units = cnt * ng * (HALF / 8);
+        int seen = -1;  // pages whose loads this thread has waited for: 0..seen
+        for (int u = tid; u < units; u += kThreads) {
+            const int c = u % (HALF / 8), h = (u / (HALF / 8)) % ng, tl = u / (ng * (HALF / 8));
+            const int pos = pos0 + tl;
+            const int k = pos / kPage - pg0, slot = pos % kPage;
+            while (seen < k) {
+                ++seen;
+                if (!mbar_wait_bounded(P, bar0 + 8u * (uint32_t)seen, (ph >> seen) & 1u, s_abort, 10000 + seen, it))
+                    break;
             }
-            int* fix_n = s_fix + (i & 1);  // this pair's queue count (the other pair's is being cleared)
-            const int u0 = ng * tkc[0] * (HALF / 8);
-            const int units = u0 + (np2 > 1 ? ng * tkc[1] * (HALF / 8) : 0);
-            // (scalars, not the arrays: no dynamic indexing in the loop)
-            const int tkcA = tkc[0], tkcB = tkc[1], tk0A = tk0[0], tk0B = tk0[1];
-            uint8_t* baseA = smem + (kp[0] % NB) * BUF;
-            uint8_t* baseB = smem + (kp[1] % NB) * BUF;
-            for (int u = tid; u < units; u += kThreads) {
-                const int q = u < u0 ? 0 : 1;
-                const int i2 = q ? u - u0 : u;
-                const int tkcq = q ? tkcB : tkcA;
-                const int c = i2 % (HALF / 8), rest = i2 / (HALF / 8);
-                const int tl = rest % tkcq, g = rest / tkcq;
-                uint8_t* base = q ? baseB : baseA;
-                uint16_t* krow = reinterpret_cast<uint16_t*>(base + (g * kPage + tl) * ROW);
-                const float* rrow = reinterpret_cast<const float*>(base + 2 * BOX + tl * RROW);
-                const int pos = pos0 + (q ? tk0B : tk0A) + tl;
-                // pairs 8c .. 8c + 7: dims (j, j + d/2), or (2j, 2j + 1) interleaved
-                const int d0 = IL ? 16 * c : 8 * c;
-                const int d1 = IL ? 16 * c + 8 : HALF + 8 * c;
-                uint4 lo, hi;
-                rope8_key<HALF, IL>(*reinterpret_cast<const uint4*>(krow + d0),
-                                    *reinterpret_cast<const uint4*>(krow + d1), rrow + c * 8, 8 * c,
-                                    smem_u32(krow + d0), smem_u32(krow + d1),
-                                    ((uint32_t)tl << 8) | ((uint32_t)q << 15), fixq, fix_n, rrow + c * 8,
-                                    P.rope + (size_t)pos * HALF + c * 8, lo, hi);
-                *reinterpret_cast<uint4*>(krow + d0) = lo;
-                *reinterpret_cast<uint4*>(krow + d1) = hi;
-            }
-            __syncthreads();
-            // the queued uncertain outputs, redone in full (about one in 10^3;
-            // the table rows are in shared memory)
+            if (*(volatile int*)s_abort) break;
+            uint16_t* krow = reinterpret_cast<uint16_t*>(smem + k * KBOX + (h * kPage + slot) * ROW);
+            const float* trow = reinterpret_cast<const float*>(smem + TBASE + k * TBOX + slot * TROW);
+            const float* grow = P.ropef + (size_t)pos * 4 * HALF;  // the full fp32 row (rare path)
+            // pairs 8c .. 8c + 7: dims (j, j + d/2), or (2j, 2j + 1) interleaved
+            const int d0 = IL ? 16 * c : 8 * c;
+            const int d1 = IL ? 16 * c + 8 : HALF + 8 * c;
+            uint4 lo, hi;
+            rope8_key<HALF, IL>(*reinterpret_cast<const uint4*>(krow + d0), *reinterpret_cast<const uint4*>(krow + d1),
+                                trow + c * 8, 8 * c, smem_u32(krow + d0), smem_u32(krow + d1), (uint32_t)tl << 8,
+                                fixq, fix_n, grow + c * 8, P.rope + (size_t)pos * HALF + c * 8, lo, hi);
+            *reinterpret_cast<uint4*>(krow + d0) = lo;
+            *reinterpret_cast<uint4*>(krow + d1) = hi;
+        }
+        __syncthreads();
+        if (!*(volatile int*)s_abort) {
+            // the queued uncertain outputs, redone in full (about one in 10^3);
+            // the row's four values load together
             const int nfix = min(*(volatile int*)fix_n, kRopeFixCap);
             for (int e = tid; e < nfix; e += kThreads) {
                 const RopeFix f = fixq[e];
                 if (f.off == kRopeFixNone) continue;
                 const int j = (int)(f.code & 127u), which = (int)((f.code >> 7) & 1u);
-                const int tl = (int)((f.code >> 8) & 127u), q = (int)(f.code >> 15);
-                const float* rrow = reinterpret_cast<const float*>((q ? baseB : baseA) + 2 * BOX + tl * RROW);
-                const float4 cf = rope_row_pair<HALF>(rrow, j);
-                const double2* fb = P.rope + (size_t)(pos0 + (q ? tk0B : tk0A) + tl) * HALF + j;
+                const int pos = pos0 + (int)((f.code >> 8) & 127u);
+                const float4 cf = rope_row_pair<HALF>(P.ropef + (size_t)pos * 4 * HALF, j);
+                const double2* fb = P.rope + (size_t)pos * HALF + j;
                 const uint16_t r = which ? rope_bf16(f.x1, f.x0, cf.x, cf.y, cf.z, cf.w, fb)
                                          : rope_bf16(f.x0, -f.x1, cf.x, cf.y, cf.z, cf.w, fb);
                 asm volatile("st.shared.u16 [%0], %1;" ::"r"(f.off), "h"(r) : "memory");
             }
-            fence_proxy_async_shared();  // the rotated rows are read by the bulk stores (async proxy)
-            __syncthreads();
-            if (tid == 0) {
-                *fix_n = 0;  // every thread read it before the barrier; pair i + 2 counts from 0
-                for (int q = 0; q < np2; ++q)
-                    for (int g = 0; g < ng; ++g)
-                        bulk_store(kc + dst0[q] + (size_t)g * kPage * D,
-                                   smem_u32(smem + (kp[q] % NB) * BUF + g * kPage * ROW), (uint32_t)(tkc[q] * ROW));
-                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                if (i >= 1 && 2 * i + 2 < npg) {
-                    // the previous pair's stores have read its buffers: refill them
-                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                    issue(2 * i + 2);
-                    if (2 * i + 3 < npg) issue(2 * i + 3);
-                }
-            }
         }
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the pages are written
+        fence_proxy_async_shared();  // the rotated rows are read by the bulk stores (async proxy)
+        __syncthreads();
+        if (tid == 0) *fix_n = 0;    // every thread read it before the barrier
+        if (copier && !*(volatile int*)s_abort) {
+            const size_t dst = (((size_t)pages[pg0 + lane_pg] * Hkv + g0) * kPage + lo_pos % kPage) * D;
+            const uint32_t src = smem_u32(pbuf + (lo_pos % kPage) * ROW);
+            const uint32_t bytes = (uint32_t)((hi_pos - lo_pos) * ROW);
+            for (int g = 0; g < ng; ++g)
+                bulk_store(P.k_cache + dst + (size_t)g * kPage * D, src + (uint32_t)(g * kPage * ROW), bytes);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            // the K rows have been read out: the buffer takes the page's V rows
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            mbar_expect_tx(pbar, (uint32_t)KBOX);
+            tma_load_3d(smem_u32(pbuf), tmVin, 0, R.qo0 + t0 + (pa - pos0), g0, pbar);
+            if (mbar_wait_bounded(P, pbar, ((ph >> lane_pg) & 1u) ^ 1u, s_abort, 11000 + lane_pg, it)) {
+                for (int g = 0; g < ng; ++g)
+                    bulk_store(P.v_cache + dst + (size_t)g * kPage * D, src + (uint32_t)(g * kPage * ROW), bytes);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the page's K and V are written
+        }
     }
     // publish: the pages are read next by TMA (async proxy) in other CTAs
     fence_proxy_async_global();
@@ -777,8 +761,9 @@ __device__ void run_append(const KParams& P, const CUtensorMap* tmKin, const CUt
     if (tid == 0) {
         const int blk = pos0 / kTileRows - R.h / kTileRows;
         atomicExch(&P.ws_int[kHdrInts + P.plan[P.off_aux + s] + blk * kv_groups(Hkv) + g0 / kAppendHeads], 1);
-        *s_phase = ph;
     }
+    // each page's barrier completed two phases, so *s_phase stands (a thread
+    // that gave up on a wait has flagged the CTA, which stops taking items)
 }
 
 // ----------------------------------------------------------------------------
@@ -1768,7 +1753,8 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap tmQ,
                                                                  const __grid_constant__ CUtensorMap tmR,
                                                                  const __grid_constant__ CUtensorMap tmKin,
-                                                                 const __grid_constant__ CUtensorMap tmVin) {
+                                                                 const __grid_constant__ CUtensorMap tmVin,
+                                                                 const __grid_constant__ CUtensorMap tmRA) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(16) int s_item[kItemInts];
@@ -1776,7 +1762,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
     __shared__ int s_flag;
     __shared__ uint32_t s_tmem;
     __shared__ uint32_t s_app_phase;
-    __shared__ int s_fix[2];  // entries in the APPEND items' fix-up queue, by page parity
+    __shared__ int s_fix[2];  // entries in the APPEND items' fix-up queue ([0]; [1] unused)
     const int tid = threadIdx.x;
     const uint32_t bars = smem_u32(smem + kSmemBars);
     if (tid == 0) {
@@ -1831,7 +1817,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
         const int* it = s_item;  // rewritten only after the end-of-item barrier
         if (it[0] < 0) break;
         if (it[0] == kAppend)
-            run_append<D, IL>(P, &tmKin, &tmVin, it, smem, bars + 8 * kBarAppend, &s_app_phase, &s_abort, s_fix);
+            run_append<D, IL>(P, &tmKin, &tmVin, &tmRA, it, smem, bars + 8 * kBarAppend, &s_app_phase, &s_abort, s_fix);
         else if (it[0] == kPrefill) {
             if (!tmem_held) {
                 if (tid < 32) {
@@ -2198,10 +2184,12 @@ int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void*
     CUtensorMap tmQ;
     st = make_q_map(&tmQ, a->q, in->num_tokens, a->shape.num_heads_q, d, a->shape.num_heads_q / Hkv);
     if (st) return st;
-    CUtensorMap tmKin, tmVin;
+    CUtensorMap tmKin, tmVin, tmRA;
     st = make_kv_in_map(&tmKin, a->k, in->num_tokens, Hkv, d);
     if (st) return st;
     st = make_kv_in_map(&tmVin, a->v, in->num_tokens, Hkv, d);
+    if (st) return st;
+    st = make_rope_map(&tmRA, a->rope_table + (size_t)a->rope_max_pos * d, a->rope_max_pos, d, kPage);
     if (st) return st;
     CUtensorMap tmR;
     st = make_rope_map(&tmR, a->rope_table + (size_t)a->rope_max_pos * d, a->rope_max_pos, d,
@@ -2280,16 +2268,16 @@ int32_t launch_step(const sarathi_attn_args* a, const sarathi_host_io* io, void*
     const bool il = a->rope_style == SARATHI_ROPE_INTERLEAVED;
     if (d == 128 && !il)
         mixed_step_kernel<128, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR, tmKin,
-                                                                                  tmVin);
+                                                                                  tmVin, tmRA);
     else if (d == 128)
         mixed_step_kernel<128, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR, tmKin,
-                                                                                  tmVin);
+                                                                                  tmVin, tmRA);
     else if (!il)
         mixed_step_kernel<64, false><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR, tmKin,
-                                                                                  tmVin);
+                                                                                  tmVin, tmRA);
     else
         mixed_step_kernel<64, true><<<grid, kThreads, kSmemAlloc, stream>>>(P, tmK, tmV, tmK3, tmV3, tmK5, tmV5, tmQ, tmR, tmKin,
-                                                                                  tmVin);
+                                                                                  tmVin, tmRA);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "mixed_step_kernel launch");
     if (io) {
