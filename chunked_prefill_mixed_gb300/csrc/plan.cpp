@@ -85,8 +85,10 @@ constexpr double kHbmBytesPerNs = 6500.0;        // the whole GPU
 constexpr double kAppendFixedNs = 1500.0;
 constexpr double kAppendNsPerTokenHead = 45.0;
 // a key piece of a split tile: a tile's fixed start, plus its partial's
-// write and (for the last piece) the merge
-constexpr double kPieceExtraNs = 4500.0;
+// write, the merge (by the last piece) and the slower blocks of pieces that
+// share fewer pages with the tiles running beside them (fitted to step times
+// of prefill-only steps cut at 512, 1024 and 2048 tokens)
+constexpr double kPieceExtraNs = 8000.0;
 
 }  // namespace
 }  // namespace sarathi
