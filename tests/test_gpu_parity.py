@@ -120,12 +120,12 @@ def test_work_queues_planned_for_another_sm_count(make, num_sms):
 
 
 def _plan_with_pieces(wl, sh, want_split):
-    """The first SM count (of a few small ones) for which the planner cuts
-    some tiles of the step into want_split key pieces."""
+    """The first SM count for which the planner cuts some tiles of the step
+    into want_split key pieces."""
     import chunked_prefill_mixed_gb300 as S
     reqs, keep = S.make_requests(*wl.arrays())
     shp = S.Shape(sh.H_q, sh.H_kv, sh.d, 16)
-    for nsm in range(6, 64):
+    for nsm in range(2, 152):
         st, info, packed = S.sarathi_plan(reqs, len(wl.requests), wl.budget, shp, nsm)
         items = packed[info.off_items:info.off_items + info.n_items * 24].reshape(-1, 24)
         if want_split in set(items[(items[:, 0] == 1), 7].tolist()):
@@ -133,21 +133,23 @@ def _plan_with_pieces(wl, sh, want_split):
     return None
 
 
-@pytest.mark.parametrize("H_q,H_kv,d,nsplit", [(32, 8, 128, 3), (56, 8, 128, 2), (32, 32, 128, 2), (8, 1, 64, 3),
-                                               (7, 1, 128, 4)])
-def test_key_pieces_of_split_tiles_all_rows(H_q, H_kv, d, nsplit):
-    """A 300-token chunk after 2300 tokens of history, alone in the step, so
-    every tile runs ~20 key blocks: planned for a small SM count the last
+@pytest.mark.parametrize("H_q,H_kv,d,hist,chunk,nsplit", [
+    (32, 8, 128, 2300, 300, 3), (56, 8, 128, 2300, 300, 4), (32, 32, 128, 2300, 300, 3), (8, 1, 64, 4300, 400, 3),
+    (7, 1, 128, 2300, 300, 2), (7, 1, 128, 2300, 300, 4)])
+def test_key_pieces_of_split_tiles_all_rows(H_q, H_kv, d, hist, chunk, nsplit):
+    """A chunk after thousands of tokens of history, alone in the step, so
+    every tile runs ~20-40 key blocks: planned for a small SM count the last
     tiles come as 2-4 key pieces that write fp32 partials and are merged by
     the last piece to finish (odd groups place their partials on an even
     slot; d = 64 and 128).  Every output row matches the oracle and the pages
     match bit for bit."""
     from chunked_prefill_mixed_gb300.runner import StepRunner
     sh = W.Shape(H_q, H_kv, d)
-    wl = _custom(sh, [(W.PREFILL_RUNNING, 2600, 2300, 2600)], 300, name=f"pieces{H_q}x{H_kv}x{d}")
+    L = hist + chunk
+    wl = _custom(sh, [(W.PREFILL_RUNNING, L, hist, L)], chunk, name=f"pieces{H_q}x{H_kv}x{d}")
     num_sms = _plan_with_pieces(wl, sh, nsplit)
     assert num_sms is not None, f"no SM count gives {nsplit} pieces"
-    runner = StepRunner(sh.H_q, sh.H_kv, sh.d, 2600 + 16, device="cuda", rope_theta=sh.rope_base)
+    runner = StepRunner(sh.H_q, sh.H_kv, sh.d, L + 16, device="cuda", rope_theta=sh.rope_base)
     runner.num_sms = num_sms
     gs = GpuStep(wl, runner=runner)
     items = gs.packed[gs.info.off_items:gs.info.off_items + gs.info.n_items * 24].reshape(-1, 24)
