@@ -209,8 +209,9 @@ int32_t sarathi_advance(sarathi_request* reqs, int32_t n_reqs, const sarathi_pla
  * values split into float pairs (hi + lo) for the kernel's fp32 fast path.
  * table: device pointer to 2*max_pos*head_dim doubles (16*max_pos*head_dim
  * bytes): double[max_pos][head_dim/2][2] {cos, sin}, then
- * float[max_pos][head_dim/16][32]: for each run of 8 pairs, cos_hi[8],
- * sin_hi[8], cos_lo[8], sin_lo[8] (cos = cos_hi + cos_lo, likewise sin).
+ * float[max_pos][4][head_dim/2]: per position the planes cos_hi, sin_hi,
+ * cos_lo, sin_lo over the pairs (cos = cos_hi + cos_lo, likewise sin; the
+ * hi planes first, so that one tensor-map box fetches them for many rows).
  * head_dim must be a multiple of 16 (UNSUPPORTED otherwise).
  * Asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy default stream). */
 int32_t sarathi_rope_table(double* table, int32_t max_pos, int32_t head_dim, double rope_theta,
