@@ -623,16 +623,15 @@ __device__ __forceinline__ void load_rope_hi(const float* row, int j0, float (&c
 // APPEND: rotate + store the K/V of the prefill tokens of one 128-position
 // block (up to 8 pages), for up to kAppendHeads kv heads
 // ----------------------------------------------------------------------------
-// Every page's K rows arrive at once: per page, lane k of warp 0 issues one TMA
-// box that brings them from k's [token][kv head][d] layout as [head][16
-// tokens][d] -- the order of a page's slots -- and another with the cos_hi /
-// sin_hi planes of the page's positions (one mbarrier per page).  The threads
-// rotate the K rows in place as their pages land (certified rounding, the rare
-// uncertain outputs redone from a queue), lane k stores page k's row runs with
-// bulk copies, and once they have been read out it loads page k's V rows into
-// the same buffer (the barrier's next phase) and stores them the same way.
-// The item then sets its ready flag, which the prefill tiles of its kv heads
-// wait for before they load the block.
+// Every page's rows arrive at once: per page, lane k of warp 0 issues three TMA
+// boxes -- the page's K rows and V rows from k's and v's [token][kv head][d]
+// layout as [head][16 tokens][d] (the order of a page's slots), and the cos_hi /
+// sin_hi planes of the page's positions -- on one mbarrier per page, and stores
+// the V rows to the page as soon as they land.  The threads rotate the K rows in
+// place as their pages land (certified rounding, the rare uncertain outputs
+// redone from a queue), then lane k stores page k's K rows.  The item then sets
+// its ready flag, which the prefill tiles of its kv heads wait for before they
+// load the block.
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
                  : "memory");
@@ -651,7 +650,8 @@ __device__ void run_append(const KParams& P, const CUtensorMap* tmKin, const CUt
     constexpr int TROW = D * 4;                          // cos_hi, sin_hi of one position
     constexpr int TBOX = kPage * TROW;                   // ... of one page's positions
     constexpr int kMaxPg = kTileRows / kPage;            // pages of a 128-position block
-    constexpr int TBASE = kMaxPg * KBOX;
+    constexpr int VBASE = kMaxPg * KBOX;
+    constexpr int TBASE = 2 * kMaxPg * KBOX;
     static_assert(TBASE + kMaxPg * TBOX <= kSmemStages && kAppendBufs >= kMaxPg && kMaxPg <= 32,
                   "APPEND shared memory");
     const int ng = min(kAppendHeads, Hkv - g0);          // heads of this item
@@ -668,25 +668,32 @@ __device__ void run_append(const KParams& P, const CUtensorMap* tmKin, const CUt
     }
     RopeFix* fixq = reinterpret_cast<RopeFix*>(smem + kSmemDecQ);  // idle during APPEND items
     static_assert(kRopeFixCap * sizeof(RopeFix) <= 2 * kPageHalfBytes, "fix-up queue");
-    // completed-phase parities of the pages' barriers: each completes two
-    // phases per item (K and table rows, then V rows)
-    const uint32_t ph = *s_phase;
+    const uint32_t ph = *s_phase;  // completed-phase parities of the pages' barriers
     // lane k of warp 0 runs page k's copies: its slots' positions [lo, hi)
     const int lane_pg = tid < 32 ? tid : 0;
     const int pa = (pg0 + lane_pg) * kPage;
     const int lo_pos = max(pos0, pa), hi_pos = min(pos0 + cnt, pa + kPage);
     const uint32_t pbar = bar0 + 8u * (uint32_t)lane_pg;
-    uint8_t* pbuf = smem + lane_pg * KBOX;
     const bool copier = ok && tid < npg;
+    const size_t pdst = (((size_t)pages[pg0 + (copier ? lane_pg : 0)] * Hkv + g0) * kPage + lo_pos % kPage) * D;
+    const uint32_t prow = (uint32_t)((lo_pos % kPage) * ROW), pbytes = (uint32_t)((hi_pos - lo_pos) * ROW);
     if (!ok) {
         if (tid == 0) raise_error(P, kErrBounds, bad, s_abort);
     } else {
         if (copier) {
-            // the page's 16 slots: the box starts at the slot of the page's
+            // the page's 16 slots: the boxes start at the slot of the page's
             // first position (rows outside the item are loaded, not used)
-            mbar_expect_tx(pbar, (uint32_t)(KBOX + TBOX));
-            tma_load_3d(smem_u32(pbuf), tmKin, 0, R.qo0 + t0 + (pa - pos0), g0, pbar);
+            mbar_expect_tx(pbar, (uint32_t)(2 * KBOX + TBOX));
+            tma_load_3d(smem_u32(smem + lane_pg * KBOX), tmKin, 0, R.qo0 + t0 + (pa - pos0), g0, pbar);
+            tma_load_3d(smem_u32(smem + VBASE + lane_pg * KBOX), tmVin, 0, R.qo0 + t0 + (pa - pos0), g0, pbar);
             tma_load_2d(smem_u32(smem + TBASE + lane_pg * TBOX), tmRA, 0, pa, pbar);
+            // V goes straight back out to the page
+            if (mbar_wait_bounded(P, pbar, (ph >> lane_pg) & 1u, s_abort, 11000 + lane_pg, it)) {
+                const uint32_t src = smem_u32(smem + VBASE + lane_pg * KBOX) + prow;
+                for (int g = 0; g < ng; ++g)
+                    bulk_store(P.v_cache + pdst + (size_t)g * kPage * D, src + (uint32_t)(g * kPage * ROW), pbytes);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
         }
         // K: eight pairs of one (token, head) row per unit, in token order
         int* fix_n = s_fix;
@@ -736,23 +743,12 @@ __device__ void run_append(const KParams& P, const CUtensorMap* tmKin, const CUt
         __syncthreads();
         if (tid == 0) *fix_n = 0;    // every thread read it before the barrier
         if (copier && !*(volatile int*)s_abort) {
-            const size_t dst = (((size_t)pages[pg0 + lane_pg] * Hkv + g0) * kPage + lo_pos % kPage) * D;
-            const uint32_t src = smem_u32(pbuf + (lo_pos % kPage) * ROW);
-            const uint32_t bytes = (uint32_t)((hi_pos - lo_pos) * ROW);
+            const uint32_t src = smem_u32(smem + lane_pg * KBOX) + prow;
             for (int g = 0; g < ng; ++g)
-                bulk_store(P.k_cache + dst + (size_t)g * kPage * D, src + (uint32_t)(g * kPage * ROW), bytes);
+                bulk_store(P.k_cache + pdst + (size_t)g * kPage * D, src + (uint32_t)(g * kPage * ROW), pbytes);
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            // the K rows have been read out: the buffer takes the page's V rows
-            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            mbar_expect_tx(pbar, (uint32_t)KBOX);
-            tma_load_3d(smem_u32(pbuf), tmVin, 0, R.qo0 + t0 + (pa - pos0), g0, pbar);
-            if (mbar_wait_bounded(P, pbar, ((ph >> lane_pg) & 1u) ^ 1u, s_abort, 11000 + lane_pg, it)) {
-                for (int g = 0; g < ng; ++g)
-                    bulk_store(P.v_cache + dst + (size_t)g * kPage * D, src + (uint32_t)(g * kPage * ROW), bytes);
-                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            }
-            asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the page's K and V are written
         }
+        if (copier) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the page's V and K are written
     }
     // publish: the pages are read next by TMA (async proxy) in other CTAs
     fence_proxy_async_global();
@@ -761,9 +757,10 @@ __device__ void run_append(const KParams& P, const CUtensorMap* tmKin, const CUt
     if (tid == 0) {
         const int blk = pos0 / kTileRows - R.h / kTileRows;
         atomicExch(&P.ws_int[kHdrInts + P.plan[P.off_aux + s] + blk * kv_groups(Hkv) + g0 / kAppendHeads], 1);
+        // each page's barrier completed one phase (a thread that gave up on a
+        // wait has flagged the CTA, which stops taking items)
+        if (ok) *s_phase = ph ^ ((1u << npg) - 1u);
     }
-    // each page's barrier completed two phases, so *s_phase stands (a thread
-    // that gave up on a wait has flagged the CTA, which stops taking items)
 }
 
 // ----------------------------------------------------------------------------

@@ -13,7 +13,7 @@ int32_t fail(int32_t code, const char* msg);
 int32_t check_shape(const sarathi_shape* shape);
 
 constexpr int kPage = 16;             // tokens per KV page (the only size built)
-constexpr int kAppendHeads = 4;       // kv heads per APPEND work item (its tokens: one 128-position block's)
+constexpr int kAppendHeads = 2;       // kv heads per APPEND work item (its tokens: one 128-position block's)
 constexpr int kAppendBufs = 8;        // mbarriers of an APPEND item (one per page)
 constexpr int kTileRows = 128;        // query rows (token x head-in-group) per prefill tile
 constexpr int kMaxGroup = 16;         // q heads per kv head handled by the decode path

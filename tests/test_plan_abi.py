@@ -147,11 +147,11 @@ def _check_work_list(info, m, shape, num_sms=148):
             k = min(8, count)
             assert list(ids[:k]) == list(kvi[kvp[s] + start:kvp[s] + start + k]) and not ids[k:].any()
         if kind == 0:
-            # up to 4 kv heads, tokens whose positions share one 128-position block
-            assert nn >= 2 and g % 4 == 0 and 0 < count <= 128
+            # up to 2 kv heads, tokens whose positions share one 128-position block
+            assert nn >= 2 and g % 2 == 0 and 0 < count <= 128
             h = 16 * (np_ - 1) + last[s] - nn
             assert (h + start) // 128 == (h + start + count - 1) // 128
-            appended[qo[s] + start: qo[s] + start + count, g:g + 4] += 1
+            appended[qo[s] + start: qo[s] + start + count, g:g + 2] += 1
         elif kind == 1:
             # one Q tile of up to 128 // G tokens, starting on a tile boundary
             tpi = 128 // G
@@ -203,10 +203,10 @@ def _check_work_list(info, m, shape, num_sms=148):
         assert all(ps[i][2] == ps[i + 1][1] for i in range(len(ps) - 1))
     assert len(seen_slots) <= info.n_partials and (not seen_slots or max(seen_slots) < info.n_partials)
     assert info.n_partials - len(seen_slots) <= 1
-    # each prefill row's ready flags (one per 128-position block and group of 4
+    # each prefill row's ready flags (one per 128-position block and group of 2
     # kv heads) follow the previous row's, from req_aux on
     aux = m["req_aux"]
-    groups = -(-shape.H_kv // 4)
+    groups = -(-shape.H_kv // 2)
     nxt = 0
     for s in range(n):
         nn = qo[s + 1] - qo[s]
