@@ -5,19 +5,24 @@
 // 把两类注意力强行做成同一个形状": one ragged batch, attention split back per
 // request through qo_indptr / kv_page_indptr / kv_page_indices /
 // kv_last_page_len).  CTAs pull work items from the planner's two queues
-// (prefill tiles; decode splits) through an atomic head counter each, longest
-// items first; CTAs below first_sms start on the first queue, the others on
-// the second, and each moves to the other queue once its own is empty:
+// (prefill tiles; APPEND items and decode splits) through an atomic head
+// counter each, longest items first; CTAs below first_sms start on the first
+// queue, the others on the second, and each moves to the other queue once its
+// own is empty:
 //
-//   APPEND   new prefill tokens: K rotated at its ABSOLUTE position in fp64 and
-//            rounded once to bf16, V copied, both into the page that holds the
-//            position ("Sarathi-Serve 完全拆解", §"分块不等于截断上下文": RoPE never
-//            restarts per chunk; the chunk's K/V land in the paged cache).
+//   APPEND   new prefill tokens of one 128-position block, 2 kv heads: K rotated
+//            at its ABSOLUTE position and rounded once to bf16 as from the fp64
+//            value, V copied, both into the pages that hold the positions
+//            ("Sarathi-Serve 完全拆解", §"分块不等于截断上下文": RoPE never restarts
+//            per chunk; the chunk's K/V land in the paged cache); then a ready
+//            flag for the block.
 //   PREFILL  one tile of up to 128 query rows (token x q-head of one GQA group)
 //            of a chunk: causal attention over every history page plus the
-//            chunk's own keys (ibid.: o_i = sum_{j<=i} softmax(q_i.k_j/sqrt d) v_j).
-//            Waits (bounded) until the request's APPEND items are done, then
-//            streams 64-key blocks of pages into shared memory with TMA.
+//            chunk's own keys (ibid.: o_i = sum_{j<=i} softmax(q_i.k_j/sqrt d) v_j),
+//            128-key blocks streamed into shared memory with TMA; a block of the
+//            chunk's own keys waits (bounded) for its ready flag.  The last tiles
+//            of a step without decodes may come as key pieces, merged by
+//            log-sum-exp by the last piece to arrive.
 //   DECODE   one split of a decode's pages for one kv head: per-warp TMA page
 //            pipelines, warp-level MMA for the GQA group, online softmax,
 //            in-CTA merge, and across splits a log-sum-exp merge done by the
@@ -25,9 +30,10 @@
 //            owns the last page also appends the decode token's K/V.
 //
 // No CTA waits on a CTA that took a later item, and the only cross-CTA wait
-// (PREFILL on its request's APPENDs, which lead the second queue, or the first
-// when there are no decodes, and which some CTA starts on at launch) is
-// bounded by a timer; a wait that runs out sets an error word in the workspace.
+// (a PREFILL block on its APPEND item's ready flag; the APPEND items lead the
+// second queue, or the first when there are no decodes, and some CTA starts on
+// them at launch) is bounded by a timer; a wait that runs out sets an error
+// word in the workspace.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -901,28 +907,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 // PREFILL item on the 5th-generation tensor cores: one Q tile of up to 128
 // query rows (token-major, q-head-in-group minor) of one chunk for one kv
 // head, causal over every history page and the chunk ("Sarathi-Serve 完全拆解",
-// §"分块不等于截断上下文").  128-key blocks of K and V stream through shared
+// §"分块不等于截断上下文"), over all its 128-key blocks or, for a key piece of a
+// split tile, over a range of them.  K and V blocks stream through shared
 // memory rings; tensor memory holds two score buffers, two P buffers and O:
 //   S(j) = Q K(j)^T: tcgen05.mma (M 128, N 128, K 16 steps, both operands in
 //       shared memory), fp32 into S buffer j & 1 (columns [128 b, 128 b + 128));
-//   softmax (warps 0-3, thread = query row = TMEM lane): one pass over the
-//       row's 128 scores in two halves of 64 (each half's max from the
-//       registers that then give its P), lazy rescale of O (only when the max
-//       grows by more than 2^8), bf16 P into P buffer j & 1 (64 columns at
-//       384 + 64 b);
+//   softmax (warps 0-7: warps q and q + 4 hold rows 32 q .. 32 q + 31, the TMEM
+//       lanes of their SM sub-partition, one thread a row, each warp one half
+//       of the block's keys; the pair agrees on the block's max through shared
+//       memory), lazy rescale of O (only when the max grows by more than 2^8),
+//       bf16 P into P buffer j & 1 (64 columns at 384 + 64 b);
 //   O += P(j) V(j): tcgen05.mma with A = P from tensor memory and V read as an
 //       MN-major operand straight from the TMA-loaded pages; O in columns
 //       [256, 256 + d) until the end of the item.
-// The MMA issuer runs S(j + 2) and P(j).V(j) as soon as the softmax has
-// finished block j, so the tensor pipe holds the next block's scores while
-// the softmax works on this one; P has buffers of its own, so no MMA writes
-// tensor memory that an earlier MMA still reads.  MMAs issued by one thread
-// complete in order: a complete S(j + 2) means P(j).V(j) is done, which is
-// what makes P buffer j & 1 free again for block j + 2.
+// Two threads issue the MMAs: warp 11 runs S(j) as soon as the softmax has
+// loaded S(j - 2) (so the tensor pipe holds the next block's scores while the
+// softmax works), warp 10 runs P(j).V(j) once all eight softmax warps have
+// stored P(j).  The groups of different issuers do not complete in a known
+// order, so each P.V group signals its P buffer's barrier, which the softmax
+// waits for before it overwrites that buffer or rescales O.
 // Roles: warps 8 and 9 are the TMA producers of the K and V rings (one box per
 // block when the block's pages are consecutive in the pool, else one box per
-// page and 64-column half), warp 10 lane 0 issues the MMAs, warps 0-3 run the
-// softmax and the epilogue; warps 0-7 and 10 rotate Q at the item's start.
+// page and 64-column half), warps 0-7 run the softmax and the epilogue, warps
+// 0-7, 10 and 11 rotate Q at the item's start.
 // ----------------------------------------------------------------------------
 constexpr int kTcKeys = 128;                     // keys per block
 static_assert(kTcKeys == kTileRows, "a K/V block and a Q tile have the same shape");
@@ -951,7 +958,7 @@ constexpr int kBarSFree = kBarPFull + 2;               // 2 (per S buffer: loade
 constexpr int kBarOUp = kBarSFree + 2;                 // 2 (per P buffer: its P.V group done)
 constexpr int kBarODone = kBarOUp + 2;                 // 1 (one completion per item: its last P.V)
 constexpr int kBarDrain = kBarODone + 1;               // 2 (one per MMA-issuing thread)
-constexpr int kBarAppend = kBarDrain + 2;              // kAppendBufs (APPEND page buffers)
+constexpr int kBarAppend = kBarDrain + 2;              // kAppendBufs (one per page of an APPEND item)
 constexpr int kBarQ = kBarAppend + kAppendBufs;        // 1 (the Q tile's TMA boxes)
 constexpr int kNumBars = kBarQ + 1;
 static_assert(kNumBars * 8 <= 512, "barrier area");

@@ -29,13 +29,15 @@ enum ItemKind : int32_t { kAppend = 0, kPrefill = 1, kDecode = 2 };
 //   [1] s        scheduled row (request) index
 //   [2] g        kv head (prefill / decode)
 //   [3] start    append: first token (request-local); prefill: first token of the
-//                item's first Q tile (request-local); decode: first page (request-local)
+//                item's Q tile (request-local); decode: first page (request-local)
 //   [4] count    tokens (append / prefill) or pages (decode)
 //   [5] slot     decode: first partial slot of its merge group (the group's
 //                splits own consecutive slots; split k = start / ceil(pages /
-//                nsplit) owns slot + k); -1 when the item is the only split
-//   [6] merge    decode: merge group, -1 when the item is the only split
-//   [7] nsplit   decode: splits in the merge group
+//                nsplit) owns slot + k); prefill key piece: the tile's first
+//                slot (piece k owns pf_piece_slots slots from slot + k times
+//                that); -1 when the item is the only split
+//   [6] merge    decode / key piece: merge group, -1 when the item is the only split
+//   [7] nsplit   decode / key piece: splits in the merge group
 //   [8..12]      row s: qo_indptr[s], new tokens, kv_page_indptr[s], pages,
 //                kv length -- copies of the metadata, so that an item needs
 //                one load before its first page can be fetched
