@@ -27,7 +27,8 @@ ITEM_INTS = 24    # SARATHI_ITEM_INTS
 EXPORTED = ("sarathi_plan_bounds", "sarathi_plan", "sarathi_plan_ex", "sarathi_advance", "sarathi_split_metadata",
             "sarathi_rope_table", "sarathi_qkv_proj",
             "sarathi_mixed_attn", "sarathi_mixed_attn_host",
-            "sarathi_mixed_attn_noalloc", "sarathi_workspace_status", "sarathi_last_error", "sarathi_abi_version")
+            "sarathi_mixed_attn_noalloc", "sarathi_noalloc_status", "sarathi_workspace_status", "sarathi_last_error",
+            "sarathi_abi_version")
 
 
 class SarathiError(RuntimeError):
@@ -136,6 +137,8 @@ def load(build_if_missing: bool = True):
     lib.sarathi_mixed_attn_host.argtypes = [ctypes.POINTER(AttnArgs), ctypes.POINTER(HostIO), ctypes.c_void_p]
     lib.sarathi_mixed_attn_noalloc.restype = ctypes.c_int32
     lib.sarathi_mixed_attn_noalloc.argtypes = [ctypes.POINTER(AttnArgs), ctypes.c_void_p]
+    lib.sarathi_noalloc_status.restype = ctypes.c_int32
+    lib.sarathi_noalloc_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.sarathi_workspace_status.restype = ctypes.c_int32
     lib.sarathi_workspace_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
     lib.sarathi_last_error.restype = ctypes.c_char_p
@@ -370,6 +373,16 @@ def sarathi_qkv_proj(x, w, q, k, v, shape: Shape, workspace, stream=None) -> Non
     a.shape = shape
     a.workspace = workspace.data_ptr()
     _check(load().sarathi_qkv_proj(ctypes.byref(a), _stream_ptr(stream)), "sarathi_qkv_proj")
+
+
+def sarathi_noalloc_status(stream=None) -> int:
+    """Synchronise, read and clear the error word of the built-in scratch array
+    of sarathi_mixed_attn_noalloc on the current device (0 = fine)."""
+    err = ctypes.c_int32(0)
+    st = load().sarathi_noalloc_status(_stream_ptr(stream), ctypes.byref(err))
+    if st not in (OK, ERR_DEVICE_CHECK):
+        _check(st, "sarathi_noalloc_status")
+    return int(err.value)
 
 
 def sarathi_workspace_status(workspace, stream=None) -> int:

@@ -28,6 +28,27 @@ static __device__ __align__(256) unsigned char g_step_scratch[kStaticScratchByte
 std::mutex g_scratch_mu;
 void* g_scratch_dev[128] = {};  // device address of g_step_scratch, per device index
 
+// The array's device address on the current device, looked up once per device.
+int32_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(SARATHI_ERR_CUDA, cudaGetErrorString(e));
+    if (dev < 0 || dev >= 128) return fail(SARATHI_ERR_UNSUPPORTED, "device index >= 128");
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_dev[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_step_scratch);
+        if (e != cudaSuccess || !p) {
+            char msg[200];
+            std::snprintf(msg, sizeof msg, "cudaGetSymbolAddress of the scratch array: %s", cudaGetErrorString(e));
+            return fail(SARATHI_ERR_CUDA, msg);
+        }
+        g_scratch_dev[dev] = p;
+    }
+    *out = g_scratch_dev[dev];
+    return SARATHI_OK;
+}
+
 }  // namespace
 }  // namespace sarathi
 
@@ -60,34 +81,24 @@ extern "C" int32_t sarathi_mixed_attn_noalloc(const sarathi_attn_args* args, voi
                                                                args->shape.head_dim) * 4;
     if (need > in->workspace_bytes)
         return fail(SARATHI_ERR_INVALID_ARG, "inconsistent plan info (counters and partials exceed its workspace_bytes)");
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail(SARATHI_ERR_CUDA, cudaGetErrorString(e));
-    if (dev < 0 || dev >= 128) return fail(SARATHI_ERR_UNSUPPORTED, "device index >= 128");
     void* scratch = nullptr;
-    {
-        // once per device, with that device current
-        std::lock_guard<std::mutex> lk(g_scratch_mu);
-        if (!g_scratch_dev[dev]) {
-            void* p = nullptr;
-            e = cudaGetSymbolAddress(&p, g_step_scratch);
-            if (e != cudaSuccess || !p) {
-                char msg[200];
-                std::snprintf(msg, sizeof msg, "cudaGetSymbolAddress of the scratch array: %s",
-                              cudaGetErrorString(e));
-                return fail(SARATHI_ERR_CUDA, msg);
-            }
-            g_scratch_dev[dev] = p;
-        }
-        scratch = g_scratch_dev[dev];
-    }
+    const int32_t sa = scratch_address(&scratch);
+    if (sa) return sa;
     // The array keeps whatever the previous call left.  The counters, tickets
     // and error word must start at zero; the partial slots are always written
     // before they are read.
-    e = cudaMemsetAsync(scratch, 0, (size_t)clear_bytes, (cudaStream_t)cuda_stream);
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)clear_bytes, (cudaStream_t)cuda_stream);
     if (e != cudaSuccess) return fail(SARATHI_ERR_CUDA, cudaGetErrorString(e));
     sarathi_attn_args a = *args;
     a.workspace = scratch;
     a.workspace_bytes = (int64_t)kStaticScratchBytes;
     return sarathi_mixed_attn(&a, cuda_stream);
+}
+
+extern "C" int32_t sarathi_noalloc_status(void* cuda_stream, int32_t* device_error) {
+    if (!device_error) return fail(SARATHI_ERR_INVALID_ARG, "NULL pointer");
+    void* scratch = nullptr;
+    const int32_t sa = scratch_address(&scratch);
+    if (sa) return sa;
+    return sarathi_workspace_status(scratch, cuda_stream, device_error);
 }

@@ -315,15 +315,23 @@ int32_t sarathi_mixed_attn_host(const sarathi_attn_args* args, const sarathi_hos
  * this call after cudaDeviceReset on that device.  All calls share the one
  * array, so calls whose work overlaps on the GPU (other streams, other
  * threads) race and give wrong results.  The device error word lives in the
- * shared array and is not reported: a bounded wait that runs out or a page id
- * outside the pool leaves the outputs and pages partly written while the call
- * still returned SARATHI_OK; use sarathi_mixed_attn with a workspace (and
- * sarathi_workspace_status) when such failures must be detected.
+ * shared array: a bounded wait that runs out or a page id outside the pool
+ * leaves the outputs and pages partly written while the call still returned
+ * SARATHI_OK; read the word with sarathi_noalloc_status (the next call clears
+ * the array's counters itself).
  * Errors, all before anything is enqueued: CAPACITY when
  * info->workspace_bytes exceeds the array; INVALID_ARG when the plan info is
  * inconsistent (n_sched <= 0, negative counts, or counters and partial slots
  * larger than info->workspace_bytes); then as sarathi_mixed_attn. */
 int32_t sarathi_mixed_attn_noalloc(const sarathi_attn_args* args, void* cuda_stream);
+
+/* sarathi_workspace_status for the built-in array of sarathi_mixed_attn_noalloc
+ * on the current device: synchronise `cuda_stream`, then read and clear the
+ * device error word of the last call there.  Allocates nothing.  Returns
+ * SARATHI_OK, SARATHI_ERR_DEVICE_CHECK when the word was nonzero
+ * (*device_error: 1 a bounded wait ran out, 2 a bounds check failed), or
+ * SARATHI_ERR_CUDA / INVALID_ARG. */
+int32_t sarathi_noalloc_status(void* cuda_stream, int32_t* device_error);
 
 /* The Q/K/V projection of a step's tokens as ONE GEMM over the concatenated
  * ragged batch ([SA] §"Decode-maximal batching：顺车的账本": the linear layers of

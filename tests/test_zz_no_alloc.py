@@ -74,3 +74,43 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         assert np.array_equal(to_u16(gs.kc_dev), ref_k), f"call {call}: K pages differ"
         assert np.array_equal(to_u16(gs.vc_dev), ref_v), f"call {call}: V pages differ"
         assert_close(oracle.bf16_to_double(to_u16(out)), ref_out, f"no-alloc call {call}")
+
+
+@pytest.mark.gpu
+def test_noalloc_error_word_is_reported_and_the_next_call_is_clean():
+    """A bounded wait that runs out inside a no-allocation step sets the error
+    word of the built-in array; sarathi_noalloc_status reports it (and clears
+    it), and the next call on a correct plan gives the oracle's pages and
+    outputs.  The failure is made in the metadata (a row's first APPEND item
+    replaced by a copy of its second, so the first block's ready flag is never
+    set), as in the workspace entry point's failure test."""
+    import torch
+    from gpu_helpers import GpuStep, assert_close, to_u16
+    shape = W.Shape(8, 2, 64)
+    specs = [(W.DECODE, 0, 40, 41), (W.DECODE, 0, 70, 71), (W.PREFILL_RUNNING, 200, 64, 200)]
+    gs = GpuStep(W._build("noalloc_fail", shape, 100, specs, 9, spare_pages=2))
+    k0, v0 = gs.kc_dev.clone(), gs.vc_dev.clone()
+    r = gs.runner
+    bad = gs.packed.copy()
+    s = gs.meta["n_sched"] - 1
+    items = bad[gs.info.off_items:gs.info.off_items + gs.info.n_items * 24].reshape(-1, 24)
+    app = [i for i in range(len(items)) if items[i, 0] == 0 and items[i, 1] == s]
+    assert len(app) >= 2 and items[app[0], 3] < items[app[-1], 3]
+    items[app[0]] = items[app[-1]]
+    out = torch.full_like(gs.out, float("nan"))
+    plan_bad = r.upload(bad)  # (the runner's stream waits for the work above)
+    S.sarathi_mixed_attn_noalloc(gs.q_dev, gs.k_dev, gs.v_dev, gs.kc_dev, gs.vc_dev, out, plan_bad, gs.info,
+                                 r.rope, r.max_pos, r.shape, r.sm_scale, r.stream)
+    assert S.sarathi_noalloc_status(r.stream) == 1
+    assert S.sarathi_noalloc_status(r.stream) == 0   # read once, then cleared
+    gs.kc_dev.copy_(k0)
+    gs.vc_dev.copy_(v0)
+    out = torch.full_like(gs.out, float("nan"))
+    plan_ok = r.upload(gs.packed)
+    S.sarathi_mixed_attn_noalloc(gs.q_dev, gs.k_dev, gs.v_dev, gs.kc_dev, gs.vc_dev, out, plan_ok, gs.info,
+                                 r.rope, r.max_pos, r.shape, r.sm_scale, r.stream)
+    assert S.sarathi_noalloc_status(r.stream) == 0
+    kc, vc = gs.oracle_caches()
+    assert np.array_equal(to_u16(gs.kc_dev), kc) and np.array_equal(to_u16(gs.vc_dev), vc)
+    ref, rt, rh = gs.oracle_rows(kc, vc)
+    assert_close(oracle.bf16_to_double(to_u16(out))[rt, rh], ref, "no-alloc call after an error")
