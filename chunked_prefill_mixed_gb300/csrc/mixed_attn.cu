@@ -83,8 +83,8 @@ constexpr int kPageHalfBytes = kPage * 128;                    // 16 rows x 64 b
 constexpr int kDecStageBytes = 2 * 2 * kPageHalfBytes;         // K+V page-head, d=128
 constexpr int kSmemStages = kDecWarps * kDecStages * kDecStageBytes;  // 192 KB
 constexpr int kSmemDecQ = kSmemStages;                         // 16 x 128 bf16
-constexpr int kSmemStash = kSmemDecQ + 2 * kPageHalfBytes;     // new K/V (2 x 128 bf16)
-constexpr int kSmemBars = kSmemStash + 512;                   // mbarriers, initialised once
+constexpr int kSmemStash = kSmemDecQ + 8192;                   // new K/V of a decode item's heads
+constexpr int kSmemBars = kSmemStash + 1024;                  // mbarriers, initialised once
 constexpr int kDecBar0 = 0;                                    // [warp][stage] decode rings
 constexpr int kSmemBytes = kSmemBars + 512;
 constexpr int kSmemAlloc = kSmemBytes + 1024;                  // + alignment slack
@@ -1481,17 +1481,27 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     const int G = P.group;
     const int pos = R.kv_len - 1;   // the decode token's absolute position
     const bool last_owner = (p0 + pc == R.np);
-    uint8_t* qtile = smem + kSmemDecQ;
-    uint16_t* stash = reinterpret_cast<uint16_t*>(smem + kSmemStash);
+    // the item's kv heads g .. g + ng - 1: warps WPH h .. WPH h + WPH - 1 stream
+    // the pages of head g + h (warp place wq: pages p0 + wq, p0 + wq + WPH, ...)
+    const int ng = min(kDecodeHeads, P.Hkv - g);
+    constexpr int WPH = kDecWarps / kDecodeHeads;
+    const int hw = warp / WPH, wq = warp % WPH;
+    const bool streams = warp < kDecWarps && hw < ng;
+    const int gh = g + (streams ? hw : 0);         // this warp's kv head
+    constexpr int QBYTES = 16 * D * 2;              // one head's Q rows
+    static_assert(kDecodeHeads * QBYTES <= kSmemStash - kSmemDecQ && kDecodeHeads * 2 * D * 2 <= kSmemBars - kSmemStash,
+                  "decode Q tiles and stash");
+    uint8_t* qtile = smem + kSmemDecQ + (streams ? hw : 0) * QBYTES;
+    uint16_t* stash = reinterpret_cast<uint16_t*>(smem + kSmemStash) + (streams ? hw : 0) * 2 * D;
     uint8_t* wst = smem + warp * kDecStages * kDecStageBytes;
     const uint32_t wbar = smem_u32(smem + kSmemBars) + 8 * (kDecBar0 + kDecStages * warp);
-    const int my_pages = (warp < kDecWarps && pc > warp) ? (pc - warp + kDecWarps - 1) / kDecWarps : 0;
+    const int my_pages = (streams && pc > wq) ? (pc - wq + WPH - 1) / WPH : 0;
 
     // lane l holds the page id of this warp's page (32*window + l), so that
     // lane 0 never waits on a global load right before a TMA issue
     auto load_ids = [&](int base) -> int {
         const int k = base + lane;
-        return k < my_pages ? page_id(P, R, p0 + warp + kDecWarps * k, s_abort) : 0;
+        return k < my_pages ? page_id(P, R, p0 + wq + WPH * k, s_abort) : 0;
     };
     int ids = load_ids(0);
     auto issue = [&](int k, int page) {
@@ -1499,7 +1509,7 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         const uint32_t dst = smem_u32(wst + stg * kDecStageBytes);
         const uint32_t bar = wbar + 8 * stg;
         mbar_expect_tx(bar, STAGE);
-        const int y = (page * P.Hkv + g) * kPage;
+        const int y = (page * P.Hkv + gh) * kPage;
         if (HALVES == 2) {
             // one box per page-head: {64 columns, 16 rows, 2 halves} lands as
             // [half][16 rows][128 B], the same swizzled image as two 2-D boxes
@@ -1511,7 +1521,7 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         }
     };
     // the first page id of every warp comes with the item: no load before it
-    if (my_pages > 0 && lane == 0) issue(0, checked_page(P, it[kIds + warp], s_abort));
+    if (my_pages > 0 && lane == 0) issue(0, checked_page(P, it[kIds + wq], s_abort));
     for (int k = 1; k < my_pages && k < kDecStages; ++k) {
         const int pid = __shfl_sync(0xffffffffu, ids, k);
         if (lane == 0) issue(k, pid);
@@ -1520,28 +1530,31 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     // Q rows of the group, RoPE'd in fp32, rows >= G zero: threads [0, QU) each
     // rotate 8 consecutive pairs (one round trip for the whole tile).
     constexpr int QU = 16 * (HALF / 8);
-    static_assert(QU <= kThreads, "decode prologue threads");
-    if (tid < QU) {
-        const int row = tid / (HALF / 8), c = tid % (HALF / 8);
+    static_assert(kDecodeHeads * QU <= kThreads, "decode prologue threads");
+    if (tid < ng * QU) {
+        const int h = tid / QU, t2 = tid % QU;
+        const int row = t2 / (HALF / 8), c = t2 % (HALF / 8);
         const int c0 = IL ? 2 * c : c, c1 = IL ? 2 * c + 1 : c + HALF / 8;
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
         if (row < G) {
-            const uint4* qv = reinterpret_cast<const uint4*>(P.q + ((size_t)R.qo0 * P.Hq + g * G + row) * D);
+            const uint4* qv = reinterpret_cast<const uint4*>(P.q + ((size_t)R.qo0 * P.Hq + (g + h) * G + row) * D);
             float cs[8], sn[8];
             load_rope_hi<HALF>(P.ropef + (size_t)pos * HALF * 4, c * 8, cs, sn);
             rope_q8(__ldg(qv + c0), __ldg(qv + c1), cs, sn, IL, lo, hi);
         }
-        *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c0)) = lo;
-        *reinterpret_cast<uint4*>(qtile + sw128_chunk(16, row, c1)) = hi;
+        uint8_t* qt = smem + kSmemDecQ + h * QBYTES;
+        *reinterpret_cast<uint4*>(qt + sw128_chunk(16, row, c0)) = lo;
+        *reinterpret_cast<uint4*>(qt + sw128_chunk(16, row, c1)) = hi;
     }
     // the decode token's own K (fp64 RoPE, one rounding) and V: stash + page
     if (last_owner) {
         const int page = P.plan[P.off_kvi + R.kvp0 + pos / kPage];
         const bool ok = page >= 0 && page < P.num_pages && pos < P.rope_max_pos;
-        const size_t off = (((size_t)(ok ? page : 0) * P.Hkv + g) * kPage + pos % kPage) * D;
-        const uint16_t* kr = reinterpret_cast<const uint16_t*>(P.k) + ((size_t)R.qo0 * P.Hkv + g) * D;
-        const uint16_t* vr = reinterpret_cast<const uint16_t*>(P.v) + ((size_t)R.qo0 * P.Hkv + g) * D;
-        for (int j = tid; j < HALF; j += kThreads) {
+        uint16_t* stash0 = reinterpret_cast<uint16_t*>(smem + kSmemStash);
+        for (int jh = tid; jh < ng * HALF; jh += kThreads) {
+            const int h = jh / HALF, j = jh % HALF;
+            const size_t off = (((size_t)(ok ? page : 0) * P.Hkv + g + h) * kPage + pos % kPage) * D;
+            const uint16_t* kr = reinterpret_cast<const uint16_t*>(P.k) + ((size_t)R.qo0 * P.Hkv + g + h) * D;
             const int i0 = IL ? 2 * j : j, i1 = IL ? 2 * j + 1 : j + HALF;
             uint16_t y0 = 0, y1 = 0;
             if (ok) {
@@ -1552,12 +1565,14 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
                 reinterpret_cast<uint16_t*>(P.k_cache)[off + i0] = y0;
                 reinterpret_cast<uint16_t*>(P.k_cache)[off + i1] = y1;
             }
-            stash[i0] = y0;
-            stash[i1] = y1;
+            stash0[h * 2 * D + i0] = y0;
+            stash0[h * 2 * D + i1] = y1;
         }
-        for (int e = tid; e < D; e += kThreads) {
-            const uint16_t vv = vr[e];
-            stash[D + e] = vv;
+        for (int eh = tid; eh < ng * D; eh += kThreads) {
+            const int h = eh / D, e = eh % D;
+            const size_t off = (((size_t)(ok ? page : 0) * P.Hkv + g + h) * kPage + pos % kPage) * D;
+            const uint16_t vv = reinterpret_cast<const uint16_t*>(P.v)[((size_t)R.qo0 * P.Hkv + g + h) * D + e];
+            stash0[h * 2 * D + D + e] = vv;
             if (ok) reinterpret_cast<uint16_t*>(P.v_cache)[off + e] = vv;
         }
         if (!ok && tid == 0) raise_error(P, kErrBounds, page, s_abort);
@@ -1583,7 +1598,7 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         phase ^= 1u << stg;
         uint8_t* kb = wst + stg * kDecStageBytes;
         uint8_t* vb = kb + KPAGE;
-        const int lp = p0 + warp + kDecWarps * k;
+        const int lp = p0 + wq + WPH * k;
         const int key0 = lp * kPage;
         if (lp == R.np - 1) {
             // last page: put the new token in its slot, zero the slots past it
@@ -1690,13 +1705,14 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     __syncthreads();
     const bool single = slot_first < 0;
     const int ksplit = single ? 0 : p0 / ((R.np + nsplit - 1) / nsplit);
-    float* part = single ? nullptr : P.ws_part + (size_t)(slot_first + ksplit) * P.slot_floats;
-    for (int i = tid; i < G * D; i += kThreads) {
-        const int row = i / D, col = i % D;
+    // head h's streaming warps are WPH h .. WPH h + WPH - 1; split k of the
+    // group writes head h's partial to slot slot_first + k ng + h
+    for (int i = tid; i < ng * G * D; i += kThreads) {
+        const int h = i / (G * D), row = (i / D) % G, col = i % D;
         float M = -INFINITY;
-        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm[w * 16 + row]);
+        for (int w = h * WPH; w < (h + 1) * WPH; ++w) M = fmaxf(M, sm[w * 16 + row]);
         float L = 0.f, acc = 0.f;
-        for (int w = 0; w < kDecWarps; ++w) {
+        for (int w = h * WPH; w < (h + 1) * WPH; ++w) {
             const float mw = sm[w * 16 + row];
             if (mw == -INFINITY) continue;
             const float sc = exp2f(mw - M);
@@ -1705,8 +1721,9 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
         }
         const float val = acc / L;
         if (single) {
-            P.out[((size_t)R.qo0 * P.Hq + g * G + row) * D + col] = __float2bfloat16_rn(val);
+            P.out[((size_t)R.qo0 * P.Hq + (g + h) * G + row) * D + col] = __float2bfloat16_rn(val);
         } else {
+            float* part = P.ws_part + (size_t)(slot_first + ksplit * ng + h) * P.slot_floats;
             part[row * (D + 2) + col] = val;
             if (col == 0) {
                 part[row * (D + 2) + D] = M;
@@ -1725,19 +1742,20 @@ __device__ void run_decode(const KParams& P, const CUtensorMap* tmK, const CUten
     }
     __syncthreads();
     if (!*s_flag) return;
-    const float* base = P.ws_part + (size_t)slot_first * P.slot_floats;
-    for (int i = tid; i < G * D; i += kThreads) {
-        const int row = i / D, col = i % D;
+    for (int i = tid; i < ng * G * D; i += kThreads) {
+        const int h = i / (G * D), row = (i / D) % G, col = i % D;
+        const float* base = P.ws_part + (size_t)(slot_first + h) * P.slot_floats;
+        const size_t kstride = (size_t)ng * P.slot_floats;
         float M = -INFINITY;
-        for (int k = 0; k < nsplit; ++k) M = fmaxf(M, __ldcg(base + (size_t)k * P.slot_floats + row * (D + 2) + D));
+        for (int k = 0; k < nsplit; ++k) M = fmaxf(M, __ldcg(base + k * kstride + row * (D + 2) + D));
         float L = 0.f, acc = 0.f;
         for (int k = 0; k < nsplit; ++k) {
-            const float* pk = base + (size_t)k * P.slot_floats + row * (D + 2);
+            const float* pk = base + k * kstride + row * (D + 2);
             const float w = __ldcg(pk + D + 1) * exp2f(__ldcg(pk + D) - M);
             L += w;
             acc += __ldcg(pk + col) * w;
         }
-        P.out[((size_t)R.qo0 * P.Hq + g * G + row) * D + col] = __float2bfloat16_rn(acc / L);
+        P.out[((size_t)R.qo0 * P.Hq + (g + h) * G + row) * D + col] = __float2bfloat16_rn(acc / L);
     }
     if (tid == 0) P.ws_int[kHdrInts + P.n_flags + merge] = 0;
 }

@@ -328,19 +328,21 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
                         {kPrefillFixedNs + flops / kPrefillFlopPerNs, {kPrefill, s, g, t0, c, -1, -1, 0}});
                 }
         } else {
-            // decode-like: split the pages; the item holding the last page also
-            // appends the new token's K/V for its head.
+            // decode-like: split the pages; an item covers up to kDecodeHeads kv
+            // heads (sharing its start-up over them); the item holding the last
+            // page also appends the new token's K/V for its heads.
             // (nsplit-1)*per < np always holds, so no split is empty.
             const int64_t nsplit = ceil_div(np[s], split);
             const int64_t per = ceil_div(np[s], nsplit);
-            for (int g = 0; g < Hkv; ++g) {
+            for (int g = 0; g < Hkv; g += kDecodeHeads) {
+                const int ngh = std::min(kDecodeHeads, Hkv - g);
                 int32_t merge = nsplit > 1 ? n_merge++ : -1;
                 int32_t first = nsplit > 1 ? n_partials : -1;
-                if (nsplit > 1) n_partials += (int32_t)nsplit;
+                if (nsplit > 1) n_partials += (int32_t)(nsplit * ngh);
                 for (int64_t k = 0; k < nsplit; ++k) {
                     int32_t p0 = (int32_t)(k * per);
                     int32_t pc = (int32_t)std::min<int64_t>(per, np[s] - p0);
-                    decs.push_back({kDecodeFixedNs + pc * kv_page_bytes / kDecodeBytesPerNs,
+                    decs.push_back({kDecodeFixedNs + pc * ngh * kv_page_bytes / kDecodeBytesPerNs,
                                     {kDecode, s, g, p0, pc, first, merge, (int32_t)nsplit}});
                 }
             }
@@ -403,7 +405,7 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
             wp += t.ns_est;
             maxp = std::max(maxp, t.ns_est);
         }
-        for (auto& t : decs) dec_bytes += t.it[kCount] * kv_page_bytes;
+        for (auto& t : decs) dec_bytes += t.it[kCount] * std::min(kDecodeHeads, Hkv - t.it[kG]) * kv_page_bytes;
         // Fluid model of the step with k CTAs on the first queue (more than
         // n_tiles act as n_tiles: the rest find it empty and move on): the
         // tiles take wp / k; the decodes stream from the other SMs at

@@ -19,6 +19,7 @@ constexpr int kTileRows = 128;        // query rows (token x head-in-group) per 
 constexpr int kMaxGroup = 16;         // q heads per kv head handled by the decode path
 constexpr int kDecodeMinSplitPages = 8;
 constexpr int kDecodeItemsPerSm = 2;  // target split-KV items per SM for the decode phase
+constexpr int kDecodeHeads = 2;       // kv heads per decode item (4 streaming warps each)
 constexpr int kItemInts = 24;
 constexpr int kItemIds = 8;           // page ids carried in an item (one per decode warp)
 
@@ -27,13 +28,15 @@ enum ItemKind : int32_t { kAppend = 0, kPrefill = 1, kDecode = 2 };
 // Work item, kItemInts int32 (96 bytes, 16-byte aligned):
 //   [0] kind
 //   [1] s        scheduled row (request) index
-//   [2] g        kv head (prefill / decode)
+//   [2] g        kv head (prefill); first of the item's kv heads (append: up to
+//                kAppendHeads, decode: up to kDecodeHeads)
 //   [3] start    append: first token (request-local); prefill: first token of the
 //                item's Q tile (request-local); decode: first page (request-local)
 //   [4] count    tokens (append / prefill) or pages (decode)
 //   [5] slot     decode: first partial slot of its merge group (the group's
 //                splits own consecutive slots; split k = start / ceil(pages /
-//                nsplit) owns slot + k); prefill key piece: the tile's first
+//                nsplit) owns slots slot + k h .. + h - 1 for its h kv heads,
+//                one per head); prefill key piece: the tile's first
 //                slot (piece k owns pf_piece_slots slots from slot + k times
 //                that); -1 when the item is the only split
 //   [6] merge    decode / key piece: merge group, -1 when the item is the only split

@@ -172,17 +172,21 @@ def _check_work_list(info, m, shape, num_sms=148):
             for t in range(start, start + count):
                 covered[qo[s] + t, g * G:(g + 1) * G] += 1
         else:
-            assert nn == 1
+            # a page range of one decode for up to 2 kv heads
+            assert nn == 1 and g % 2 == 0
+            ngh = min(2, shape.H_kv - g)
             per = -(-np_ // nsplit)
-            pages_cov.setdefault((s, g), []).append((start, count))
+            for h in range(ngh):
+                pages_cov.setdefault((s, g + h), []).append((start, count))
             if start + count == np_:
-                appended[qo[s], g] += 1
-                covered[qo[s], g * G:(g + 1) * G] += 1
+                appended[qo[s], g:g + ngh] += 1
+                covered[qo[s], g * G:(g + ngh) * G] += 1
             if nsplit > 1:
                 k = start // per
                 assert start == k * per
-                assert (slot + k) not in seen_slots
-                seen_slots.add(slot + k)
+                for h in range(ngh):
+                    assert (slot + k * ngh + h) not in seen_slots
+                    seen_slots.add(slot + k * ngh + h)
                 assert 0 <= merge < info.n_merge
             else:
                 assert slot == -1 and merge == -1
