@@ -86,10 +86,39 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def kernel_source_sha() -> str:
+def _code_only(src: str) -> str:
+    """C++ source without comments or blank lines, so that a profile stays keyed to
+    the code that ran when only the comments change.  String literals are kept as
+    they are."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(l.rstrip() for l in "".join(out).splitlines() if l.strip())
+
+
+def kernel_source_sha(read=None) -> str:
+    """Hash of the code (comments stripped) of the three sources that make the
+    step kernel and its plan."""
     h = hashlib.sha256()
     for f in ("mixed_attn.cu", "sarathi_internal.h", "plan.cpp"):
-        h.update(open(os.path.join(ROOT, "chunked_prefill_mixed_gb300", "csrc", f), "rb").read())
+        rel = os.path.join("chunked_prefill_mixed_gb300", "csrc", f)
+        src = read(rel) if read else open(os.path.join(ROOT, rel)).read()
+        h.update(_code_only(src).encode())
     return h.hexdigest()[:16]
 
 

@@ -23,11 +23,12 @@
 //            chunk's own keys waits (bounded) for its ready flag.  The last tiles
 //            of a step without decodes may come as key pieces, merged by
 //            log-sum-exp by the last piece to arrive.
-//   DECODE   one split of a decode's pages for one kv head: per-warp TMA page
-//            pipelines, warp-level MMA for the GQA group, online softmax,
-//            in-CTA merge, and across splits a log-sum-exp merge done by the
-//            last split to arrive (atomic ticket, no spinning).  The split that
-//            owns the last page also appends the decode token's K/V.
+//   DECODE   one split of a decode's pages for two kv heads (four warps a
+//            head): per-warp TMA page pipelines, warp-level MMA for the GQA
+//            group, online softmax, in-CTA merge per head, and across splits a
+//            log-sum-exp merge done by the last split to arrive (atomic ticket,
+//            no spinning).  The split that owns the last page also appends the
+//            decode token's K/V.
 //
 // No CTA waits on a CTA that took a later item, and the only cross-CTA wait
 // (a PREFILL block on its APPEND item's ready flag; the APPEND items lead the
