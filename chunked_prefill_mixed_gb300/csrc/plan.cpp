@@ -76,6 +76,7 @@ int32_t validate_requests(const sarathi_request* reqs, int32_t n_reqs) {
 // equal share of HBM bandwidth (every SM streaming), or at one SM's own rate
 // while fewer SMs stream than saturate HBM.
 constexpr double kPrefillFixedNs = 6500.0;
+constexpr double kPrefillPreNs = 3000.0;  // the part of the fixed start before the first block (Q fill)
 constexpr double kPrefillFlopPerNs = 9000.0;
 constexpr double kDecodeFixedNs = 2000.0;
 constexpr double kDecodeBytesPerNs = 40.0;       // a decode split's share of HBM with every SM streaming
@@ -171,7 +172,7 @@ struct PlanScratch {
     std::vector<int32_t> np, hist, aux;
     std::vector<ItemHead> appends;
     std::vector<Timed> tiles, decs;
-    std::vector<double> key, pred, heap, snaps;
+    std::vector<double> key, pred, heap, snaps, flag, flag_pm;
     std::vector<int64_t> grp;
     std::vector<uint32_t> pf_order, dec_order, bucket;
 };
@@ -359,8 +360,8 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     // decodes would stream from a few SMs meanwhile); first_sms comes from a
     // fluid model of the two sides (below).  APPEND items lead
     // the second queue (they never wait, so the streaming CTAs take them first
-    // and the tiles that wait for them are not held up), or the first when
-    // there are no decodes.  (The sorts move 4-byte indices, not the items.)
+    // and the tiles that wait for them are not held up); in a step without
+    // decodes they lead the one queue, or make up the second (3b).  (The sorts move 4-byte indices, not the items.)
     const size_t n_tiles = tiles.size();
     std::vector<double>& key = sc.key;
     std::vector<int64_t>& grp = sc.grp;
@@ -434,76 +435,204 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
             }
         first_sms = std::min<int32_t>((lo + hi) / 2, (int32_t)n_tiles);
     }
-    const bool apps_first = decs.empty();
-
-    // ---- 3b. key pieces for the last tiles.  Without decodes every CTA takes
-    // the one queue in order (APPENDs, then the tiles), so the step ends with
-    // the list schedule of the queue: each item starts on the CTA that frees
-    // first.  Tiles of similar cost leave a last wave that can hold a few
-    // SMs busy while the rest idle; cutting the last split_k tiles into
-    // split_n pieces along their 128-key blocks (merged by log-sum-exp, like
-    // decode splits) trades a fixed cost per piece for a finer tail.  The
-    // pair comes from simulating that schedule with the cost model.
+    // ---- 3b. prefill-only steps (no decodes): where the APPEND items run, and
+    // key pieces for the last tiles.  Two layouts are simulated with the cost
+    // model.  (A) One queue, the APPEND items first: every CTA appends, then
+    // takes tiles.  (B) The tiles on the first queue and the APPEND items on the
+    // second, which app_sms CTAs start on (they never wait, so the tiles that
+    // wait for a ready flag are not held up): the tiles stream their history
+    // blocks while the chunk's new K/V is appended beside them, and wait only
+    // if they reach a chunk block before its APPEND item is done.  Either way
+    // the APPEND items never wait, so they are list-scheduled first on the CTAs
+    // that take them, and their ends are the ready-flag times; the tiles then
+    // start on the CTA that frees first and wait at each chunk block for its
+    // flag.  Tiles of similar cost leave a last wave that can hold a few SMs
+    // busy while the rest idle; cutting the last split_k tiles into split_n
+    // pieces along their 128-key blocks (merged by log-sum-exp, like decode
+    // splits) trades a fixed cost per piece for a finer tail.  Layout B is
+    // kept only where the model gains clearly over A.
+    bool apps_first = decs.empty();
+    int32_t app_sms = 0;
     int64_t split_k = 0;
     int32_t split_n = 1;
     auto tile_blocks = [&](const ItemHead& t) {
         return (int32_t)ceil_div((int64_t)hist[t[kS]] + t[kStart] + t[kCount], kTileRows);
     };
-    if (apps_first && n_tiles >= 2 && num_sms > 1) {
+    if (decs.empty() && n_tiles >= 1 && num_sms > 1) {
         std::vector<double>& heap = sc.heap;
         std::vector<double>& snaps = sc.snaps;
-        auto take_next = [&](double est) {  // the CTA that frees first takes an item; its end
-            std::pop_heap(heap.begin(), heap.end(), std::greater<double>());
-            const double e = heap.back() += est;
-            std::push_heap(heap.begin(), heap.end(), std::greater<double>());
+        std::vector<double>& flag = sc.flag;
+        std::vector<double>& flag_pm = sc.flag_pm;
+        flag.resize(appends.size());
+        flag_pm.resize(appends.size());
+        // every tile block costs the same (an M = 128 tile of 128 keys)
+        const double blk = 4.0 * d * kTileRows * kTileRows / kPrefillFlopPerNs;
+        // a min-heap of the CTAs' free times: the CTA that frees first takes
+        // the next item.  Its new free time replaces the top: the hole moves
+        // down along the smaller children to a leaf (a fixed trip count, no
+        // data-dependent branch but the child pick), then the new time rises
+        // to its place -- a step or two, as it is usually among the latest.
+        auto replace_top = [&](double e) {
+            const size_t n = heap.size();
+            double* h = heap.data();
+            size_t i = 0;
+            for (size_t c = 1; c < n; c = 2 * i + 1) {
+                c += (c + 1 < n) & (h[c + 1 < n ? c + 1 : c] < h[c]);
+                h[i] = h[c];
+                i = c;
+            }
+            while (i > 0) {
+                const size_t q = (i - 1) / 2;
+                if (h[q] <= e) break;
+                h[i] = h[q];
+                i = q;
+            }
+            h[i] = e;
             return e;
         };
-        heap.assign((size_t)num_sms, 0.0);
-        for (auto& a : appends)
-            take_next(kAppendFixedNs + kAppendNsPerTokenHead * a[kCount] * std::min<int>(kAppendHeads, Hkv - a[kG]));
-        // candidate split_k: quarters of the SM count, up to all of it
-        constexpr int kCand = 4;
+        // the end of a tile's key blocks [b0, b1) started at t: block j of the
+        // chunk's own keys (j >= jc) starts once the one before has ended and
+        // its flag f_j is set, so the blocks end at
+        // max(t_jc + (b1 - jc) blk, max_j (f_j + (b1 - j) blk)), t_jc the end of
+        // the history blocks.  flag_pm holds the running max of f_j - j blk
+        // over a (row, kv-head group)'s blocks, for whole tiles (b0 = 0).
+        const int32_t fs = kv_groups(Hkv);
+        auto tile_end = [&](const Timed& t, int32_t b0, int32_t b1, double start, double extra) {
+            const int32_t s = t.it[kS];
+            const int32_t jc = hist[s] / kTileRows;
+            double e = start + kPrefillPreNs + blk * std::max(0, std::min(b1, jc) - b0);
+            const int64_t f0 = aux[s] + t.it[kG] / kAppendHeads - (int64_t)jc * fs;
+            if (b0 == 0 && b1 > jc)
+                e = std::max(e + blk * (b1 - jc), flag_pm[f0 + (int64_t)(b1 - 1) * fs] + blk * b1);
+            else
+                for (int32_t j = std::max(b0, jc); j < b1; ++j) e = std::max(e, flag[f0 + (int64_t)j * fs]) + blk;
+            return e + (kPrefillFixedNs - kPrefillPreNs) + extra;
+        };
+        // candidate split_k: a quarter and a half of the SM count (more
+        // measured no better)
+        constexpr int kCand = 2;
         int64_t cand[kCand];
         int n_cand = 0;
         for (int q = 1; q <= kCand; ++q) {
             const int64_t k = std::min<int64_t>((int64_t)num_sms * q / 4, (int64_t)n_tiles);
             if (k > 0 && (n_cand == 0 || k != cand[n_cand - 1])) cand[n_cand++] = k;
         }
-        snaps.resize((size_t)n_cand * num_sms);
-        for (size_t i = 0; i < n_tiles; ++i) {
-            for (int c = 0; c < n_cand; ++c)
-                if ((int64_t)(n_tiles - i) == cand[c]) std::copy(heap.begin(), heap.end(), snaps.begin() + (size_t)c * num_sms);
-            take_next(tiles[pf_order[i]].ns_est);
-        }
-        double best = *std::max_element(heap.begin(), heap.end());
-        const double unsplit = best;
-        for (int c = 0; c < n_cand; ++c) {
-            for (int32_t n = 2; n <= kMaxPieces; ++n) {
-                heap.assign(snaps.begin() + (size_t)c * num_sms, snaps.begin() + (size_t)(c + 1) * num_sms);
-                double m = *std::max_element(heap.begin(), heap.end());
-                for (size_t i = n_tiles - (size_t)cand[c]; i < n_tiles && m < best; ++i) {
-                    const Timed& t = tiles[pf_order[i]];
-                    const int32_t nb = tile_blocks(t.it);
-                    if (nb < 2 * n) {
-                        m = std::max(m, take_next(t.ns_est));
-                        continue;
+        // one layout (k APPEND CTAs, 0 = layout A); with_pieces also searches
+        // the tail split.  Returns the step's predicted end.
+        auto simulate = [&](int32_t k, bool with_pieces, int64_t* sk, int32_t* sn) {
+            heap.assign((size_t)(k > 0 ? k : num_sms), 0.0);
+            for (size_t i = 0; i < appends.size(); ++i) {
+                const ItemHead& a = appends[i];
+                flag[i] = replace_top(heap[0] + kAppendFixedNs +
+                                      kAppendNsPerTokenHead * a[kCount] * std::min<int>(kAppendHeads, Hkv - a[kG]));
+            }
+            for (int32_t s = 0; s < ns; ++s) {
+                if (sched[s].n < 2) continue;
+                const int32_t jc = hist[s] / kTileRows;
+                const int32_t nbk = (int32_t)ceil_div((int64_t)hist[s] + sched[s].n, kTileRows) - jc;
+                for (int32_t gg = 0; gg < fs; ++gg) {
+                    double m = -1e300;
+                    for (int32_t j = 0; j < nbk; ++j) {
+                        const int64_t i = aux[s] + (int64_t)j * fs + gg;
+                        m = std::max(m, flag[i] - blk * (jc + j));
+                        flag_pm[i] = m;
                     }
-                    const double per = (t.ns_est - kPrefillFixedNs) / n + kPrefillFixedNs + kPieceExtraNs;
-                    for (int32_t k = 0; k < n; ++k) m = std::max(m, take_next(per));
                 }
-                if (m < best) {
-                    best = m;
-                    split_k = cand[c];
-                    split_n = n;
+            }
+            heap.resize((size_t)num_sms, 0.0);
+            std::make_heap(heap.begin(), heap.end(), std::greater<double>());
+            if (with_pieces) snaps.resize((size_t)n_cand * num_sms);
+            for (size_t i = 0; i < n_tiles; ++i) {
+                if (with_pieces)
+                    for (int c = 0; c < n_cand; ++c)
+                        if ((int64_t)(n_tiles - i) == cand[c])
+                            std::copy(heap.begin(), heap.end(), snaps.begin() + (size_t)c * num_sms);
+                const Timed& t = tiles[pf_order[i]];
+                replace_top(tile_end(t, 0, tile_blocks(t.it), heap[0], 0.0));
+            }
+            double best = *std::max_element(heap.begin(), heap.end());
+            *sk = 0;
+            *sn = 1;
+            if (!with_pieces) return best;
+            const double unsplit = best;
+            for (int c = 0; c < n_cand; ++c) {
+                for (int32_t n = 2; n <= kMaxPieces; ++n) {
+                    heap.assign(snaps.begin() + (size_t)c * num_sms, snaps.begin() + (size_t)(c + 1) * num_sms);
+                    double m = *std::max_element(heap.begin(), heap.end());
+                    for (size_t i = n_tiles - (size_t)cand[c]; i < n_tiles && m < best; ++i) {
+                        const Timed& t = tiles[pf_order[i]];
+                        const int32_t nb = tile_blocks(t.it);
+                        if (nb < 2 * n) {
+                            m = std::max(m, replace_top(tile_end(t, 0, nb, heap[0], 0.0)));
+                            continue;
+                        }
+                        for (int32_t q = 0; q < n; ++q)
+                            m = std::max(m, replace_top(tile_end(t, (int32_t)((int64_t)nb * q / n),
+                                                                 (int32_t)((int64_t)nb * (q + 1) / n), heap[0],
+                                                                 kPieceExtraNs)));
+                    }
+                    if (m < best) {
+                        best = m;
+                        *sk = cand[c];
+                        *sn = n;
+                    }
+                }
+            }
+            // keep the plain schedule unless the model gains clearly
+            if (best > unsplit * 0.97) {
+                *sk = 0;
+                *sn = 1;
+                return unsplit;
+            }
+            return best;
+        };
+        const double t_a = simulate(0, n_tiles >= 2, &split_k, &split_n);
+        // layout B can only gain where some tile streams history for longer
+        // than an APPEND item takes before it needs a ready flag
+        int32_t max_jc = 0;
+        for (int32_t s = 0; s < ns; ++s)
+            if (sched[s].n >= 2) max_jc = std::max(max_jc, hist[s] / kTileRows);
+        const double app_full = kAppendFixedNs + kAppendNsPerTokenHead * kTileRows * std::min(kAppendHeads, Hkv);
+        if (!appends.empty() && n_tiles >= 2 && kPrefillPreNs + max_jc * blk > app_full) {
+            // layout B's candidates: the CTAs left over by w full waves of
+            // tiles, a quarter and a half of the SMs; at most half the SMs and
+            // at most one CTA per APPEND item
+            const int64_t kmax = std::min<int64_t>(num_sms / 2, (int64_t)appends.size());
+            int32_t kc[6];
+            int n_kc = 0;
+            auto add = [&](int64_t k) {
+                k = std::max<int64_t>(k, (int64_t)num_sms - (int64_t)n_tiles);  // tile CTAs <= tiles
+                if (k < 1 || k > kmax) return;
+                for (int i = 0; i < n_kc; ++i)
+                    if (kc[i] == k) return;
+                kc[n_kc++] = (int32_t)k;
+            };
+            for (int64_t w = 1; w <= 4; ++w) add((int64_t)num_sms - ceil_div((int64_t)n_tiles, w));
+            add(num_sms / 4);
+            add(num_sms / 2);
+            int64_t sk;
+            int32_t sn;
+            double t_b = 0;
+            int32_t k_b = 0;
+            for (int i = 0; i < n_kc; ++i) {
+                const double t = simulate(kc[i], false, &sk, &sn);
+                if (!k_b || t < t_b) {
+                    t_b = t;
+                    k_b = kc[i];
+                }
+            }
+            if (k_b) {
+                t_b = simulate(k_b, true, &sk, &sn);
+                if (t_b < t_a * 0.98) {
+                    app_sms = k_b;
+                    apps_first = false;
+                    split_k = sk;
+                    split_n = sn;
                 }
             }
         }
-        // keep the plain schedule unless the model gains clearly
-        if (best > unsplit * 0.97) {
-            split_k = 0;
-            split_n = 1;
-        }
     }
+    if (app_sms > 0) first_sms = num_sms - app_sms;
     int64_t n_pieces_extra = 0;
     for (size_t i = n_tiles - (size_t)split_k; i < n_tiles; ++i)
         if (tile_blocks(tiles[pf_order[i]].it) >= 2 * split_n) n_pieces_extra += split_n - 1;

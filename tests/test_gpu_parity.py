@@ -164,6 +164,48 @@ def test_key_pieces_of_split_tiles_all_rows(H_q, H_kv, d, hist, chunk, nsplit):
         assert np.array_equal(to_u16(gs.out), first)
 
 
+def _plan_where(wl, sh, pred):
+    """The first SM count whose plan of the step satisfies pred(info, items)."""
+    import chunked_prefill_mixed_gb300 as S
+    reqs, keep = S.make_requests(*wl.arrays())
+    shp = S.Shape(sh.H_q, sh.H_kv, sh.d, 16)
+    for nsm in range(2, 153):
+        st, info, packed = S.sarathi_plan(reqs, len(wl.requests), wl.budget, shp, nsm)
+        items = packed[info.off_items:info.off_items + info.n_items * 24].reshape(-1, 24)
+        if pred(info, items):
+            return nsm
+    return None
+
+
+@pytest.mark.parametrize("H_q,H_kv,d,hist,chunk,pieces", [
+    (32, 8, 128, 4000, 300, 3), (8, 1, 64, 6000, 500, 4), (7, 1, 128, 4000, 300, 2), (32, 32, 128, 3000, 300, 0),
+    (56, 8, 128, 3840, 256, 0)])
+def test_appends_on_a_second_queue_beside_the_tiles(H_q, H_kv, d, hist, chunk, pieces):
+    """A chunk after thousands of tokens of history, alone in the step, planned
+    for an SM count where the APPEND items make up a second queue that a few
+    CTAs start on while the others take the tiles (which wait at the chunk's
+    blocks for the ready flags); with key pieces of the last tiles where
+    pieces > 0.  Every output row matches the oracle and the pages match bit
+    for bit."""
+    from chunked_prefill_mixed_gb300.runner import StepRunner
+    sh = W.Shape(H_q, H_kv, d)
+    L = hist + chunk
+    wl = _custom(sh, [(W.PREFILL_RUNNING, L, hist, L)], chunk, name=f"appq{H_q}x{H_kv}x{d}")
+
+    def second_queue(info, items):
+        split = set(items[items[:, 0] == 1, 7].tolist())
+        return (info.n_first < info.n_items and (items[info.n_first:, 0] == 0).all()
+                and (pieces in split if pieces else not (split - {0, 1})))
+    num_sms = _plan_where(wl, sh, second_queue)
+    assert num_sms is not None, "no SM count gives that layout"
+    runner = StepRunner(sh.H_q, sh.H_kv, sh.d, L + 16, device="cuda", rope_theta=sh.rope_base)
+    runner.num_sms = num_sms
+    gs = GpuStep(wl, runner=runner)
+    items = gs.packed[gs.info.off_items:gs.info.off_items + gs.info.n_items * 24].reshape(-1, 24)
+    assert second_queue(gs.info, items)
+    _check_step(gs)
+
+
 def test_llama70b_budget_1536_sampled():
     _check_step(GpuStep(W.llama70b()), rows="sample")
 

@@ -94,7 +94,7 @@ def _check_work_list(info, m, shape, num_sms=148):
     """Every (row, q head) is produced once; every new token's K/V is appended
     once per kv head; decode splits tile each decode's pages; the first queue
     holds the prefill tiles and the second the decode splits; the appends lead
-    the second queue (the first when there are no decodes), so a CTA that waits
+    the second queue (the first when it holds everything), so a CTA that waits
     on one never holds up the CTAs that take them.  A tile split along its keys
     comes as pieces whose 128-key block ranges tile [0, nblk) in order, with
     partial slots of their own."""
@@ -116,7 +116,8 @@ def _check_work_list(info, m, shape, num_sms=148):
     assert 0 <= nf <= info.n_items == len(items)
     has_dec = bool((kinds == 2).any())
     assert not (kinds[:nf] == 2).any() and not (kinds[nf:] == 1).any()
-    app_q = kinds[nf:] if has_dec else kinds[:nf]
+    # the APPEND items lead the second queue when it holds items, else the first
+    app_q = kinds[nf:] if nf < info.n_items else kinds[:nf]
     n_app = int((kinds == 0).sum())
     assert (app_q[:n_app] == 0).all() and not (app_q[n_app:] == 0).any()
     if nf == 0:
@@ -383,3 +384,24 @@ def test_sm_partition_lies_in_the_measured_flat_range(wl, lo, hi):
     16-80 (133-135 us; 138 at 40, 148 at 120)."""
     st, info, mp = _product_plan(*wl.arrays(), wl.budget, wl.shape, num_sms=152)
     assert lo <= info.first_sms <= hi, info.first_sms
+
+
+def test_prefill_only_steps_choose_where_the_appends_run():
+    """In a step without decodes the planner starts the APPEND items on a
+    second queue (a few CTAs append while the tiles stream their history)
+    where every tile has more history to read than an APPEND item takes, and
+    keeps them at the head of the one queue where the tiles need the new keys
+    at once.  Last 512-token chunk of an 8192-token prompt on 152 SMs: 128
+    tiles on the first queue, the 64 APPEND items on the second, 24 CTAs
+    starting there; the one-shot prompt (no history): one queue."""
+    wl = W.llama7b_prefill_only(512, 15)
+    st, info, mp = _product_plan(*wl.arrays(), wl.budget, wl.shape, num_sms=152)
+    kinds = mp["items"][:, 0]
+    assert info.n_first == int((kinds == 1).sum()) == 128 and (kinds[info.n_first:] == 0).all()
+    assert info.first_sms == 128
+    _check_work_list(info, mp, wl.shape, 152)
+    wl = W.llama7b_prefill_only(8192, 0)
+    st, info, mp = _product_plan(*wl.arrays(), wl.budget, wl.shape, num_sms=152)
+    kinds = mp["items"][:, 0]
+    assert info.n_first == info.n_items and info.first_sms == 152
+    assert (kinds[:int((kinds == 0).sum())] == 0).all()
