@@ -76,7 +76,6 @@ int32_t validate_requests(const sarathi_request* reqs, int32_t n_reqs) {
 // equal share of HBM bandwidth (every SM streaming), or at one SM's own rate
 // while fewer SMs stream than saturate HBM.
 constexpr double kPrefillFixedNs = 6500.0;
-constexpr double kPrefillPreNs = 3000.0;  // the part of the fixed start before the first block (Q fill)
 constexpr double kPrefillFlopPerNs = 9000.0;
 constexpr double kDecodeFixedNs = 2000.0;
 constexpr double kDecodeBytesPerNs = 40.0;       // a decode split's share of HBM with every SM streaming
@@ -90,6 +89,21 @@ constexpr double kAppendNsPerTokenHead = 45.0;
 // share fewer pages with the tiles running beside them (fitted to step times
 // of prefill-only steps cut at 512, 1024 and 2048 tokens)
 constexpr double kPieceExtraNs = 8000.0;
+// The simulation of a step without decodes has a fit of its own, to item
+// times (per-CTA timelines) and step times of prefill-only steps on GB300 --
+// chunks of 512, 1024 and 2048 tokens after 6144-7680 tokens of history, the
+// APPEND items on the one queue or beside the tiles, with and without key
+// pieces: a 128-key block of a tile (d = 128; in proportion to d), the
+// tile's start before its first block and its end after the last, the
+// APPEND item's time as a factor of its estimate above when every CTA
+// appends at the start of the step (A) and when a few append beside the
+// tiles (B), and the extra cost of a key piece.
+constexpr double kSoloBlockNs = 790.0;
+constexpr double kSoloPreNs = 4000.0;
+constexpr double kSoloPostNs = 3000.0;
+constexpr double kSoloAppendA = 1.09;
+constexpr double kSoloAppendB = 0.92;
+constexpr double kSoloPieceExtraNs = 5000.0;
 
 }  // namespace
 }  // namespace sarathi
@@ -466,7 +480,7 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
         flag.resize(appends.size());
         flag_pm.resize(appends.size());
         // every tile block costs the same (an M = 128 tile of 128 keys)
-        const double blk = 4.0 * d * kTileRows * kTileRows / kPrefillFlopPerNs;
+        const double blk = kSoloBlockNs * d / 128.0;
         // a min-heap of the CTAs' free times: the CTA that frees first takes
         // the next item.  Its new free time replaces the top: the hole moves
         // down along the smaller children to a leaf (a fixed trip count, no
@@ -500,13 +514,13 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
         auto tile_end = [&](const Timed& t, int32_t b0, int32_t b1, double start, double extra) {
             const int32_t s = t.it[kS];
             const int32_t jc = hist[s] / kTileRows;
-            double e = start + kPrefillPreNs + blk * std::max(0, std::min(b1, jc) - b0);
+            double e = start + kSoloPreNs + blk * std::max(0, std::min(b1, jc) - b0);
             const int64_t f0 = aux[s] + t.it[kG] / kAppendHeads - (int64_t)jc * fs;
             if (b0 == 0 && b1 > jc)
                 e = std::max(e + blk * (b1 - jc), flag_pm[f0 + (int64_t)(b1 - 1) * fs] + blk * b1);
             else
                 for (int32_t j = std::max(b0, jc); j < b1; ++j) e = std::max(e, flag[f0 + (int64_t)j * fs]) + blk;
-            return e + (kPrefillFixedNs - kPrefillPreNs) + extra;
+            return e + kSoloPostNs + extra;
         };
         // candidate split_k: a quarter and a half of the SM count (more
         // measured no better)
@@ -523,8 +537,9 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
             heap.assign((size_t)(k > 0 ? k : num_sms), 0.0);
             for (size_t i = 0; i < appends.size(); ++i) {
                 const ItemHead& a = appends[i];
-                flag[i] = replace_top(heap[0] + kAppendFixedNs +
-                                      kAppendNsPerTokenHead * a[kCount] * std::min<int>(kAppendHeads, Hkv - a[kG]));
+                flag[i] = replace_top(heap[0] + (k > 0 ? kSoloAppendB : kSoloAppendA) *
+                                                    (kAppendFixedNs + kAppendNsPerTokenHead * a[kCount] *
+                                                                          std::min<int>(kAppendHeads, Hkv - a[kG])));
             }
             for (int32_t s = 0; s < ns; ++s) {
                 if (sched[s].n < 2) continue;
@@ -569,7 +584,7 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
                         for (int32_t q = 0; q < n; ++q)
                             m = std::max(m, replace_top(tile_end(t, (int32_t)((int64_t)nb * q / n),
                                                                  (int32_t)((int64_t)nb * (q + 1) / n), heap[0],
-                                                                 kPieceExtraNs)));
+                                                                 kSoloPieceExtraNs)));
                     }
                     if (m < best) {
                         best = m;
@@ -593,7 +608,7 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
         for (int32_t s = 0; s < ns; ++s)
             if (sched[s].n >= 2) max_jc = std::max(max_jc, hist[s] / kTileRows);
         const double app_full = kAppendFixedNs + kAppendNsPerTokenHead * kTileRows * std::min(kAppendHeads, Hkv);
-        if (!appends.empty() && n_tiles >= 2 && kPrefillPreNs + max_jc * blk > app_full) {
+        if (!appends.empty() && n_tiles >= 2 && kSoloPreNs + max_jc * blk > kSoloAppendB * app_full) {
             // layout B's candidates: the CTAs left over by w full waves of
             // tiles, a quarter and a half of the SMs; at most half the SMs and
             // at most one CTA per APPEND item
