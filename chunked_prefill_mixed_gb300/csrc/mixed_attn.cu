@@ -1812,17 +1812,29 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
     // [0, n_first), head in header word 12) before the second (the rest, head
     // in word 0); the others the other way round.  A queue's head runs past its
     // end once it is empty; the last CTA out resets both.
+    // The first round needs no atomic: CTA b takes item b of the queue it
+    // prefers (b - first_sms of the second), and the heads count the claims
+    // after those.
     const bool first_pref = (int)blockIdx.x < P.first_sms;
+    const int n_second = P.n_items - P.n_first;
+    const int stat1 = min(P.first_sms, P.n_first);                   // items of the first queue taken so
+    const int stat2 = min((int)gridDim.x - P.first_sms, n_second);   // ... and of the second
+    bool first_round = true;
     for (;;) {
         if (tid == 0) {
             int idx = -1;
+            if (first_round) {
+                const int b = (int)blockIdx.x;
+                if (first_pref && b < P.n_first) idx = b;
+                if (!first_pref && b - P.first_sms < n_second) idx = P.n_first + (b - P.first_sms);
+            }
             for (int q = 0; q < 2 && idx < 0; ++q) {
                 if ((q == 0) == first_pref) {
-                    const int k = atomicAdd(&P.ws_int[12], 1);
+                    const int k = stat1 + atomicAdd(&P.ws_int[12], 1);
                     if (k < P.n_first) idx = k;
                 } else {
-                    const int k = atomicAdd(&P.ws_int[0], 1);
-                    if (k < P.n_items - P.n_first) idx = P.n_first + k;
+                    const int k = stat2 + atomicAdd(&P.ws_int[0], 1);
+                    if (k < n_second) idx = P.n_first + k;
                 }
             }
             if (idx >= 0) {
@@ -1837,6 +1849,7 @@ __global__ void __launch_bounds__(kThreads, 1) mixed_step_kernel(const __grid_co
             }
         }
         __syncthreads();
+        first_round = false;
         const int* it = s_item;  // rewritten only after the end-of-item barrier
         if (it[0] < 0) break;
         if (it[0] == kAppend)
