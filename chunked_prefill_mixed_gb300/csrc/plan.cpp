@@ -463,8 +463,8 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
     // flag.  Tiles of similar cost leave a last wave that can hold a few SMs
     // busy while the rest idle; cutting the last split_k tiles into split_n
     // pieces along their 128-key blocks (merged by log-sum-exp, like decode
-    // splits) trades a fixed cost per piece for a finer tail.  Layout B is
-    // kept only where the model gains clearly over A.
+    // splits) trades a fixed cost per piece for a finer tail (in layout A
+    // only).  Layout B is kept only where the model gains clearly over A.
     bool apps_first = decs.empty();
     int32_t app_sms = 0;
     int64_t split_k = 0;
@@ -636,14 +636,13 @@ extern "C" int32_t sarathi_plan_ex(const sarathi_request* reqs, int32_t n_reqs, 
                     k_b = kc[i];
                 }
             }
-            if (k_b) {
-                t_b = simulate(k_b, true, &sk, &sn);
-                if (t_b < t_a * 0.98) {
-                    app_sms = k_b;
-                    apps_first = false;
-                    split_k = sk;
-                    split_n = sn;
-                }
+            // layout B runs without key pieces: with the APPEND items beside
+            // the tiles, pieces measured slower than the plain tail
+            if (k_b && t_b < t_a * 0.98) {
+                app_sms = k_b;
+                apps_first = false;
+                split_k = 0;
+                split_n = 1;
             }
         }
     }
