@@ -405,3 +405,21 @@ def test_prefill_only_steps_choose_where_the_appends_run():
     kinds = mp["items"][:, 0]
     assert info.n_first == info.n_items and info.first_sms == 152
     assert (kinds[:int((kinds == 0).sum())] == 0).all()
+
+
+@pytest.mark.parametrize("chunk,app_sms,pieces", [(512, 24, 0), (1024, 38, 0), (2048, 76, 0), (8192, 0, 0)])
+def test_prefill_only_layout_is_the_measured_best(chunk, app_sms, pieces):
+    """The last chunk of an 8192-token prompt on 152 SMs gets the layout that
+    timed fastest on GB300 among those tried: APPEND items on a second queue
+    started by 24 CTAs at 512 tokens (70.4 us; 81.8 with them at the head of
+    the one queue), 38 at 1024 (125.6; 24: 131.7, 57: 144.0, 76: 142.0, one
+    queue with 38 x 2 key pieces: 137.9), 76 at 2048 (223.9; 66: 224.9, 49:
+    228.5, one queue with 76 x 2 pieces: 228.0), and one queue without
+    pieces for the one-shot prompt, whose tiles need the new keys at once."""
+    wl = W.llama7b_prefill_only(chunk, 8192 // chunk - 1)
+    st, info, mp = _product_plan(*wl.arrays(), wl.budget, wl.shape, num_sms=152)
+    kinds = mp["items"][:, 0]
+    assert info.first_sms == 152 - app_sms
+    assert (info.n_first < info.n_items) == (app_sms > 0)
+    assert int(((kinds == 1) & (mp["items"][:, 7] > 1)).sum()) == pieces
+    _check_work_list(info, mp, wl.shape, 152)
