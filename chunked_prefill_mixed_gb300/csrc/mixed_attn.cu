@@ -32,9 +32,9 @@
 //
 // No CTA waits on a CTA that took a later item, and the only cross-CTA wait
 // (a PREFILL block on its APPEND item's ready flag; the APPEND items lead the
-// second queue, or the first when there are no decodes, and some CTA starts on
-// them at launch) is bounded by a timer; a wait that runs out sets an error
-// word in the workspace.
+// second queue, or, in a step without decodes, the one queue or all of the
+// second, and some CTA starts on them at launch) is bounded by a timer; a wait
+// that runs out sets an error word in the workspace.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
